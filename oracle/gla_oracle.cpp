@@ -1,0 +1,255 @@
+// Simple GLA mixer: plain fp64 CPU oracle.  TEST INFRASTRUCTURE ONLY.
+//
+// Only the tests, the package's smoke check and the benchmark's CPU-baseline leg load this
+// file.  The GPU library shares no code, header or constant with it, and it never calls the
+// GPU library.  Everything here is written for a reader checking it against the source by eye:
+// straight loops over tokens, fp64 throughout, no blocking and no reordering beyond what the
+// definitions state.
+//
+// Source: "Beyond the KV cache: Training and serving i14's Laplace 3B linear attention model
+// on AWS Trainium2 with native PyTorch" (AWS blog post and its Spanish and Chinese copies),
+//   - section "i14 and the Laplace 3B architecture", paragraph "GLA mixer": each head keeps a
+//     d_k x d_v state S_t, decayed by the fixed per-head factor lambda_h and written with the
+//     rank-1 outer product k_t v_t^T ("GLA recurrent-state update equation"); the readout
+//     queries the state ("GLA state-readout equation").  The equation images are missing from
+//     the text; the readings used are
+//         S_t = lambda_h * S_{t-1} + k_t v_t^T,        o_t = S_t^T (scale * q_t),
+//     with the readout taken after the update, S_0 = h0 (zeros when absent), hT = S_T.
+//   - section "Challenge 1: Using native PyTorch on Trainium for GLA": the chunked form
+//     (intra-chunk masked linear attention plus the running state, state advanced with the
+//     decay compounded over the chunk).  Its equation images are missing too; the chunked
+//     function below is derived from the recurrence and used only to show chunk-size
+//     invariance of the definition.
+//   - section "Challenge 3" (backward through the sequential state updates): the page only says
+//     that autograd differentiates the 16 sequential updates; the backward below is the adjoint
+//     of the recurrence above.  lambda is fixed, not learned, so there is no lambda gradient.
+//
+// Layouts (all C order): q, k [T_total, H, dk]; v, o, dO [T_total, H, dv];
+// h0, hT, dhT, dh0 [n_seq, H, dk, dv]; sequence n owns tokens cu_seqlens[n] .. cu_seqlens[n+1]-1.
+// Inputs are fp32 arrays (bf16 inputs arrive as their exact fp32 values); results are fp64.
+// log_lambda is the natural log of lambda_h, one fp32 per head; lambda_h = exp(log_lambda[h])
+// evaluated in double.
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <thread>
+#include <vector>
+
+namespace {
+
+// Runs body(n, h) for every (sequence, head) pair on `nthreads` threads (0 = all cores).
+void for_each_unit(int n_seq, int H, int nthreads, const std::function<void(int, int)>& body) {
+  const long total = (long)n_seq * H;
+  if (nthreads <= 0) nthreads = (int)std::thread::hardware_concurrency();
+  if (nthreads <= 0) nthreads = 1;
+  if (nthreads > total) nthreads = (int)(total > 0 ? total : 1);
+  std::atomic<long> next(0);
+  auto worker = [&]() {
+    for (long u = next.fetch_add(1); u < total; u = next.fetch_add(1)) body((int)(u / H), (int)(u % H));
+  };
+  if (nthreads == 1) { worker(); return; }
+  std::vector<std::thread> pool;
+  for (int i = 0; i < nthreads; ++i) pool.emplace_back(worker);
+  for (auto& t : pool) t.join();
+}
+
+int check_common(const int32_t* cu_seqlens, int n_seq, int H, int dk, int dv) {
+  if (!cu_seqlens || n_seq < 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+  if (cu_seqlens[0] != 0) return -2;
+  for (int n = 0; n < n_seq; ++n)
+    if (cu_seqlens[n + 1] < cu_seqlens[n]) return -2;
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int oracle_hardware_threads(void) { return (int)std::thread::hardware_concurrency(); }
+
+// Forward: the per-token recurrence, read literally.
+int oracle_fwd(const float* q, const float* k, const float* v, const float* log_lambda,
+               const float* h0, double scale, const int32_t* cu_seqlens, int n_seq, int H,
+               int dk, int dv, double* o, double* hT, int nthreads) {
+  int rc = check_common(cu_seqlens, n_seq, H, dk, dv);
+  if (rc) return rc;
+  for_each_unit(n_seq, H, nthreads, [&](int n, int h) {
+    const double lam = std::exp((double)log_lambda[h]);
+    std::vector<double> S((size_t)dk * dv, 0.0);
+    if (h0) {
+      const float* src = h0 + ((size_t)n * H + h) * dk * dv;
+      for (size_t e = 0; e < S.size(); ++e) S[e] = (double)src[e];
+    }
+    std::vector<double> sq(dk);
+    for (int t = cu_seqlens[n]; t < cu_seqlens[n + 1]; ++t) {
+      const float* kt = k + ((size_t)t * H + h) * dk;
+      const float* vt = v + ((size_t)t * H + h) * dv;
+      const float* qt = q + ((size_t)t * H + h) * dk;
+      // S_t = lambda * S_{t-1} + k_t v_t^T
+      for (int a = 0; a < dk; ++a)
+        for (int b = 0; b < dv; ++b)
+          S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];
+      // o_t = S_t^T (scale * q_t)
+      for (int a = 0; a < dk; ++a) sq[a] = scale * (double)qt[a];
+      double* ot = o + ((size_t)t * H + h) * dv;
+      for (int b = 0; b < dv; ++b) {
+        double acc = 0.0;
+        for (int a = 0; a < dk; ++a) acc += S[(size_t)a * dv + b] * sq[a];
+        ot[b] = acc;
+      }
+    }
+    if (hT) std::memcpy(hT + ((size_t)n * H + h) * dk * dv, S.data(), S.size() * sizeof(double));
+  });
+  return 0;
+}
+
+// Forward in chunks of C tokens, fp64.  Used only to show that the chunked decomposition the
+// GPU path uses reaches the recurrence's result for any chunk size.  Within a chunk of L
+// tokens (local index i, j = 0..L-1; the state before the chunk is S):
+//   o_i   = scale * lambda^(i+1) * S^T q_i + scale * sum_{j<=i} lambda^(i-j) (q_i . k_j) v_j
+//   S_new = lambda^L * S + sum_j lambda^(L-1-j) k_j v_j^T
+int oracle_fwd_chunked(const float* q, const float* k, const float* v, const float* log_lambda,
+                       const float* h0, double scale, const int32_t* cu_seqlens, int n_seq, int H,
+                       int dk, int dv, int C, double* o, double* hT, int nthreads) {
+  int rc = check_common(cu_seqlens, n_seq, H, dk, dv);
+  if (rc) return rc;
+  if (C <= 0) return -1;
+  for_each_unit(n_seq, H, nthreads, [&](int n, int h) {
+    const double lam = std::exp((double)log_lambda[h]);
+    std::vector<double> S((size_t)dk * dv, 0.0), Snew((size_t)dk * dv);
+    if (h0) {
+      const float* src = h0 + ((size_t)n * H + h) * dk * dv;
+      for (size_t e = 0; e < S.size(); ++e) S[e] = (double)src[e];
+    }
+    for (int t0 = cu_seqlens[n]; t0 < cu_seqlens[n + 1]; t0 += C) {
+      const int L = std::min(C, cu_seqlens[n + 1] - t0);
+      auto Q = [&](int i, int a) { return (double)q[((size_t)(t0 + i) * H + h) * dk + a]; };
+      auto K = [&](int i, int a) { return (double)k[((size_t)(t0 + i) * H + h) * dk + a]; };
+      auto V = [&](int i, int b) { return (double)v[((size_t)(t0 + i) * H + h) * dv + b]; };
+      for (int i = 0; i < L; ++i) {
+        double* oi = o + ((size_t)(t0 + i) * H + h) * dv;
+        const double inter = scale * std::pow(lam, i + 1);
+        for (int b = 0; b < dv; ++b) {
+          double acc = 0.0;
+          for (int a = 0; a < dk; ++a) acc += Q(i, a) * S[(size_t)a * dv + b];
+          oi[b] = inter * acc;
+        }
+        for (int j = 0; j <= i; ++j) {
+          double qk = 0.0;
+          for (int a = 0; a < dk; ++a) qk += Q(i, a) * K(j, a);
+          const double w = scale * std::pow(lam, i - j) * qk;
+          for (int b = 0; b < dv; ++b) oi[b] += w * V(j, b);
+        }
+      }
+      const double lamL = std::pow(lam, L);
+      for (int a = 0; a < dk; ++a)
+        for (int b = 0; b < dv; ++b) {
+          double acc = lamL * S[(size_t)a * dv + b];
+          for (int j = 0; j < L; ++j) acc += std::pow(lam, L - 1 - j) * K(j, a) * V(j, b);
+          Snew[(size_t)a * dv + b] = acc;
+        }
+      S.swap(Snew);
+    }
+    if (hT) std::memcpy(hT + ((size_t)n * H + h) * dk * dv, S.data(), S.size() * sizeof(double));
+  });
+  return 0;
+}
+
+// One decode step for N independent states, in place: S <- lambda S + k v^T; o = S^T (scale q).
+// q, k [N, H, dk]; v [N, H, dv]; state [N, H, dk, dv] (fp64, updated); o [N, H, dv].
+int oracle_decode_step(const float* q, const float* k, const float* v, const float* log_lambda,
+                       double scale, double* state, double* o, int N, int H, int dk, int dv,
+                       int nthreads) {
+  if (N < 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+  for_each_unit(N, H, nthreads, [&](int n, int h) {
+    const double lam = std::exp((double)log_lambda[h]);
+    double* S = state + ((size_t)n * H + h) * dk * dv;
+    const float* kt = k + ((size_t)n * H + h) * dk;
+    const float* vt = v + ((size_t)n * H + h) * dv;
+    const float* qt = q + ((size_t)n * H + h) * dk;
+    for (int a = 0; a < dk; ++a)
+      for (int b = 0; b < dv; ++b)
+        S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];
+    double* ot = o + ((size_t)n * H + h) * dv;
+    for (int b = 0; b < dv; ++b) {
+      double acc = 0.0;
+      for (int a = 0; a < dk; ++a) acc += S[(size_t)a * dv + b] * (scale * (double)qt[a]);
+      ot[b] = acc;
+    }
+  });
+  return 0;
+}
+
+// Backward of oracle_fwd (the adjoint of the recurrence), given dO = dL/do and dhT = dL/dhT.
+// With G_t = dL/dS_t (all later uses included) and R_t = lambda * G_{t+1} (R_T = dhT):
+//   G_t  = R_t + scale * q_t dO_t^T
+//   dq_t = scale * S_t dO_t            (S_t is the forward state after token t)
+//   dk_t = G_t v_t,   dv_t = G_t^T k_t
+//   dh0  = lambda * G_1               (= dhT for an empty sequence)
+// dhT and h0 may be null (zeros); dh0 may be null (not written).
+int oracle_bwd(const float* q, const float* k, const float* v, const float* log_lambda,
+               const float* h0, double scale, const float* dO, const float* dhT,
+               const int32_t* cu_seqlens, int n_seq, int H, int dk, int dv, double* dq,
+               double* dk_out, double* dv_out, double* dh0, int nthreads) {
+  int rc = check_common(cu_seqlens, n_seq, H, dk, dv);
+  if (rc) return rc;
+  for_each_unit(n_seq, H, nthreads, [&](int n, int h) {
+    const double lam = std::exp((double)log_lambda[h]);
+    const size_t DS = (size_t)dk * dv;
+    // Pass 1, forward in time: rebuild S_t and read dq_t off it.
+    std::vector<double> S(DS, 0.0);
+    if (h0) {
+      const float* src = h0 + ((size_t)n * H + h) * DS;
+      for (size_t e = 0; e < DS; ++e) S[e] = (double)src[e];
+    }
+    for (int t = cu_seqlens[n]; t < cu_seqlens[n + 1]; ++t) {
+      const float* kt = k + ((size_t)t * H + h) * dk;
+      const float* vt = v + ((size_t)t * H + h) * dv;
+      const float* gt = dO + ((size_t)t * H + h) * dv;
+      for (int a = 0; a < dk; ++a)
+        for (int b = 0; b < dv; ++b)
+          S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];
+      double* dqt = dq + ((size_t)t * H + h) * dk;
+      for (int a = 0; a < dk; ++a) {
+        double acc = 0.0;
+        for (int b = 0; b < dv; ++b) acc += S[(size_t)a * dv + b] * (double)gt[b];
+        dqt[a] = scale * acc;
+      }
+    }
+    // Pass 2, backward in time: carry R = lambda * G_{t+1}.
+    std::vector<double> R(DS, 0.0), G(DS);
+    if (dhT) {
+      const float* src = dhT + ((size_t)n * H + h) * DS;
+      for (size_t e = 0; e < DS; ++e) R[e] = (double)src[e];
+    }
+    for (int t = cu_seqlens[n + 1] - 1; t >= cu_seqlens[n]; --t) {
+      const float* qt = q + ((size_t)t * H + h) * dk;
+      const float* kt = k + ((size_t)t * H + h) * dk;
+      const float* vt = v + ((size_t)t * H + h) * dv;
+      const float* gt = dO + ((size_t)t * H + h) * dv;
+      for (int a = 0; a < dk; ++a)
+        for (int b = 0; b < dv; ++b)
+          G[(size_t)a * dv + b] = R[(size_t)a * dv + b] + scale * (double)qt[a] * (double)gt[b];
+      double* dkt = dk_out + ((size_t)t * H + h) * dk;
+      for (int a = 0; a < dk; ++a) {
+        double acc = 0.0;
+        for (int b = 0; b < dv; ++b) acc += G[(size_t)a * dv + b] * (double)vt[b];
+        dkt[a] = acc;
+      }
+      double* dvt = dv_out + ((size_t)t * H + h) * dv;
+      for (int b = 0; b < dv; ++b) {
+        double acc = 0.0;
+        for (int a = 0; a < dk; ++a) acc += G[(size_t)a * dv + b] * (double)kt[a];
+        dvt[b] = acc;
+      }
+      for (size_t e = 0; e < DS; ++e) R[e] = lam * G[e];
+    }
+    if (dh0) std::memcpy(dh0 + ((size_t)n * H + h) * DS, R.data(), DS * sizeof(double));
+  });
+  return 0;
+}
+
+}  // extern "C"

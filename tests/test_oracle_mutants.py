@@ -1,0 +1,100 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins catch every one.
+
+Each mutant is the oracle source with one edit (a dropped term, a wrong sign or index, a
+transposed operand, a missing factor), compiled on the CPU into a temporary library.  The pin
+tests of ``test_oracle_pins.py`` then run against it, and at least one of them must fail.  The
+oracle itself is never modified.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+# (name, text to replace, replacement, which occurrence: 0 = first)
+MUTANTS = [
+    ("fwd: decay dropped",
+     "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];",
+     "S[(size_t)a * dv + b] = S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];", 0),
+    ("fwd: wrong sign of the write",
+     "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];",
+     "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] - (double)kt[a] * (double)vt[b];", 0),
+    ("fwd: k and v swapped in the write (dk == dv case only hides it)",
+     "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];",
+     "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[b % dk] * (double)vt[a % dv];", 0),
+    ("fwd: scale dropped", "sq[a] = scale * (double)qt[a];", "sq[a] = (double)qt[a];", 0),
+    ("fwd: readout column index reversed",
+     "for (int a = 0; a < dk; ++a) acc += S[(size_t)a * dv + b] * sq[a];",
+     "for (int a = 0; a < dk; ++a) acc += S[(size_t)a * dv + (dv - 1 - b)] * sq[a];", 0),
+    ("fwd: readout row index reversed",
+     "for (int a = 0; a < dk; ++a) acc += S[(size_t)a * dv + b] * sq[a];",
+     "for (int a = 0; a < dk; ++a) acc += S[(size_t)a * dv + b] * sq[dk - 1 - a];", 0),
+    ("fwd: h0 ignored", "    if (h0) {\n      const float* src = h0",
+     "    if (false && h0) {\n      const float* src = h0", 0),
+    ("fwd: readout before the update (off by one token)",
+     "      // o_t = S_t^T (scale * q_t)\n",
+     "      // o_t = S_t^T (scale * q_t)\n      for (size_t e = 0; e < S.size(); ++e) S[e] -= 0.0 * e;\n"
+     "      for (int a = 0; a < dk; ++a) for (int b = 0; b < dv; ++b)"
+     " S[(size_t)a * dv + b] -= (double)kt[a] * (double)vt[b];\n", 0),
+    ("chunked: inter-chunk decay off by one", "const double inter = scale * std::pow(lam, i + 1);",
+     "const double inter = scale * std::pow(lam, i);", 0),
+    ("chunked: state decay uses L-j", "acc += std::pow(lam, L - 1 - j) * K(j, a) * V(j, b);",
+     "acc += std::pow(lam, L - j) * K(j, a) * V(j, b);", 0),
+    ("decode: decay dropped",
+     "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];",
+     "S[(size_t)a * dv + b] = S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];", 1),
+    ("bwd: dq scale dropped", "dqt[a] = scale * acc;", "dqt[a] = acc;", 0),
+    ("bwd: dk contracts with dO instead of v",
+     "for (int b = 0; b < dv; ++b) acc += G[(size_t)a * dv + b] * (double)vt[b];",
+     "for (int b = 0; b < dv; ++b) acc += G[(size_t)a * dv + b] * (double)gt[b];", 0),
+    ("bwd: carry not decayed", "for (size_t e = 0; e < DS; ++e) R[e] = lam * G[e];",
+     "for (size_t e = 0; e < DS; ++e) R[e] = G[e];", 0),
+    ("bwd: dhT ignored", "    if (dhT) {", "    if (false && dhT) {", 0),
+    ("bwd: forward state missing its decay",
+     "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];",
+     "S[(size_t)a * dv + b] = S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];", 2),
+]
+
+PIN_TESTS = [
+    lambda o: pins.test_fwd_matches_quadratic_and_closed_form(o, 17, True),
+    lambda o: pins.test_fwd_matches_quadratic_and_closed_form(o, 1, False),
+    pins.test_exact_rational_worked_example,
+    pins.test_lambda_one_is_causal_linear_attention,
+    pins.test_lambda_zero_keeps_only_current_token,
+    lambda o: pins.test_chunk_size_invariance(o, 7),
+    pins.test_decode_steps_equal_prefill,
+    lambda o: pins.test_backward_matches_finite_differences(o, [6]),
+    pins.test_backward_lambda_one_closed_form,
+]
+
+
+def _replace_nth(src, old, new, n):
+    idx = -1
+    for _ in range(n + 1):
+        idx = src.find(old, idx + 1)
+        if idx < 0:
+            raise AssertionError(f"mutation anchor not found (occurrence {n}): {old!r}")
+    return src[:idx] + new + src[idx + len(old):]
+
+
+@pytest.mark.parametrize("name,old,new,occ", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new, occ):
+    src = open(oracle.source_path()).read()
+    mutated = _replace_nth(src, old, new, occ)
+    assert mutated != src
+    cpp = os.path.join(tmp_path, "mutant.cpp")
+    so = os.path.join(tmp_path, "libmutant.so")
+    with open(cpp, "w") as f:
+        f.write(mutated)
+    subprocess.check_call(["g++", "-O1", "-std=c++17", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-pthread", cpp, "-o", so])
+    variant = oracle.Variant(so)
+    caught = []
+    for pin in PIN_TESTS:
+        try:
+            pin(variant)
+        except AssertionError:
+            caught.append(pin)
+    assert caught, f"no pin caught the planted mistake: {name}"

@@ -1,0 +1,300 @@
+"""Pins of the fp64 oracle against facts fixed by the mathematics, not by the oracle's own code.
+
+The oracle computes the per-token recurrence S_t = lambda S_{t-1} + k_t v_t^T, o_t = S_t^T(s q_t)
+("Beyond the KV cache" blog post on Laplace 3B, section "i14 and the Laplace 3B architecture",
+GLA mixer update and readout equations).  Each test below checks it against an independent
+formulation: the closed-form sum, the O(T^2) decay-masked attention form, exact rational
+arithmetic, the lambda = 1 and lambda = 0 reductions, chunk-size invariance, resume and varlen
+invariance, linearity, and for the backward, finite differences of the forward.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import glasynth as gs
+
+
+def _rand(seed, tid, shape, sigma=1.0):
+    return gs.normal(seed, tid, shape, sigma)
+
+
+def _case(seed, T, H=2, dk=5, dv=7, with_h0=True):
+    q = _rand(seed, 1, (T, H, dk))
+    k = _rand(seed, 2, (T, H, dk))
+    v = _rand(seed, 3, (T, H, dv))
+    h0 = _rand(seed, 4, (1, H, dk, dv), 0.5) if with_h0 else None
+    ll = np.log(np.array([0.9, 0.6, 0.99, 0.3][:H], np.float32)).astype(np.float32)
+    return q, k, v, h0, ll
+
+
+def _f64(x):
+    return None if x is None else np.asarray(x, np.float64)
+
+
+def _closed_form(q, k, v, ll, s, h0):
+    """o_t = s sum_{j<=t} lam^(t-j) (q_t.k_j) v_j + s lam^(t+1) h0^T q_t (0-based t);
+    hT = lam^T h0 + sum_j lam^(T-1-j) k_j v_j^T.  Written as sums, not as a recurrence."""
+    q, k, v, h0 = _f64(q), _f64(k), _f64(v), _f64(h0)
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    lam = np.exp(ll.astype(np.float64))
+    t = np.arange(T)
+    o = np.zeros((T, H, dv))
+    hT = np.zeros((1, H, dk, dv))
+    for h in range(H):
+        diff = t[:, None] - t[None, :]
+        D = np.where(diff >= 0, lam[h] ** np.maximum(diff, 0), 0.0)
+        A = (q[:, h] @ k[:, h].T) * D
+        o[:, h] = s * A @ v[:, h]
+        w = lam[h] ** (T - 1 - t)
+        hT[0, h] = np.einsum("j,ja,jb->ab", w, k[:, h], v[:, h])
+        if h0 is not None:
+            o[:, h] += s * (lam[h] ** (t + 1))[:, None] * (q[:, h] @ h0[0, h])
+            hT[0, h] += lam[h] ** T * h0[0, h]
+    return o, hT
+
+
+def _relerr(x, ref):
+    ref = np.asarray(ref)
+    return np.max(np.abs(np.asarray(x) - ref)) / max(np.sqrt(np.mean(ref ** 2)), 1e-300)
+
+
+@pytest.mark.parametrize("T", [1, 2, 17, 64])
+@pytest.mark.parametrize("with_h0", [False, True])
+def test_fwd_matches_quadratic_and_closed_form(oracle_mod, T, with_h0):
+    q, k, v, h0, ll = _case(10 + T, T, with_h0=with_h0)
+    s = 0.37
+    o, hT = oracle_mod.fwd(q, k, v, ll, s, h0=h0)
+    o_ref, hT_ref = _closed_form(q, k, v, ll, s, h0)
+    assert _relerr(o, o_ref) < 1e-12
+    assert _relerr(hT, hT_ref) < 1e-12
+
+
+def test_exact_rational_worked_example(oracle_mod):
+    """T=3, H=1, dk=dv=2, lambda=1/2, s=1/2: every value is a dyadic rational, so the exact
+    answer of the closed form (Fraction arithmetic) must be met to the last bit."""
+    q = np.array([[1, 2], [0, 1], [3, -1]], np.float32)[:, None, :]
+    k = np.array([[1, 0], [2, 1], [-1, 1]], np.float32)[:, None, :]
+    v = np.array([[1, 1], [0, 2], [4, -3]], np.float32)[:, None, :]
+    h0 = np.array([[1, 0], [0, 2]], np.float32)[None, None]
+    lam, s = Fraction(1, 2), Fraction(1, 2)
+    T = 3
+    o_exact = [[Fraction(0)] * 2 for _ in range(T)]
+    for t in range(T):
+        for b in range(2):
+            acc = Fraction(0)
+            for j in range(t + 1):
+                qk = sum(Fraction(int(q[t, 0, a])) * Fraction(int(k[j, 0, a])) for a in range(2))
+                acc += s * lam ** (t - j) * qk * Fraction(int(v[j, 0, b]))
+            acc += s * lam ** (t + 1) * sum(Fraction(int(h0[0, 0, a, b])) * Fraction(int(q[t, 0, a]))
+                                            for a in range(2))
+            o_exact[t][b] = acc
+    hT_exact = [[lam ** T * Fraction(int(h0[0, 0, a, b])) +
+                 sum(lam ** (T - 1 - j) * Fraction(int(k[j, 0, a])) * Fraction(int(v[j, 0, b]))
+                     for j in range(T)) for b in range(2)] for a in range(2)]
+    ll = np.array([np.log(0.5)], np.float32)
+    assert np.exp(np.float64(ll[0])) == 0.5 or abs(np.exp(np.float64(ll[0])) - 0.5) < 1e-7
+    o, hT = oracle_mod.fwd(q, k, v, ll, 0.5, h0=h0)
+    # lambda is exp(fp32(log 0.5)) in double: not exactly 1/2, so allow its 1e-7 relative offset.
+    lam64 = np.exp(np.float64(ll[0]))
+    tol = 1e-6 if lam64 != 0.5 else 0.0
+    for t in range(T):
+        for b in range(2):
+            assert abs(o[t, 0, b] - float(o_exact[t][b])) <= tol * max(1.0, abs(float(o_exact[t][b])))
+    for a in range(2):
+        for b in range(2):
+            assert abs(hT[0, 0, a, b] - float(hT_exact[a][b])) <= tol * max(1.0, abs(float(hT_exact[a][b])))
+    # A value worked by hand: lam*h0 = [[.5, 0], [0, 1]], k_1 v_1^T = [[1, 1], [0, 0]], so
+    # S_1 = [[1.5, 1], [0, 1]] and o_1 = s * S_1^T q_1 = 0.5 * [1.5*1 + 0*2, 1*1 + 1*2] = [0.75, 1.5].
+    assert abs(o[0, 0, 0] - 0.75) <= 1e-6 and abs(o[0, 0, 1] - 1.5) <= 1e-6
+
+
+def test_lambda_one_is_causal_linear_attention(oracle_mod):
+    T, H, dk, dv = 40, 1, 6, 5
+    q, k, v = _rand(1, 1, (T, H, dk)), _rand(1, 2, (T, H, dk)), _rand(1, 3, (T, H, dv))
+    s = 0.25
+    o, hT = oracle_mod.fwd(q, k, v, np.zeros(1, np.float32), s)
+    kv = np.einsum("ta,tb->tab", _f64(k[:, 0]), _f64(v[:, 0]))
+    S = np.cumsum(kv, axis=0)
+    o_ref = s * np.einsum("tab,ta->tb", S, _f64(q[:, 0]))
+    assert _relerr(o[:, 0], o_ref) < 1e-12
+    assert _relerr(hT[0, 0], S[-1]) < 1e-12
+
+
+def test_lambda_zero_keeps_only_current_token(oracle_mod):
+    T, H, dk, dv = 9, 1, 4, 3
+    q, k, v = _rand(2, 1, (T, H, dk)), _rand(2, 2, (T, H, dk)), _rand(2, 3, (T, H, dv))
+    h0 = _rand(2, 4, (1, H, dk, dv))
+    s = 1.5
+    o, hT = oracle_mod.fwd(q, k, v, np.array([-np.inf], np.float32), s, h0=h0)
+    qk = np.sum(_f64(q[:, 0]) * _f64(k[:, 0]), axis=1)
+    assert _relerr(o[:, 0], s * qk[:, None] * _f64(v[:, 0])) < 1e-14
+    assert _relerr(hT[0, 0], np.outer(_f64(k[-1, 0]), _f64(v[-1, 0]))) < 1e-14
+
+
+def test_single_token(oracle_mod):
+    q, k, v, h0, ll = _case(3, 1, H=2)
+    s = 0.8
+    o, hT = oracle_mod.fwd(q, k, v, ll, s, h0=h0)
+    lam = np.exp(ll.astype(np.float64))
+    for h in range(2):
+        S1 = lam[h] * _f64(h0[0, h]) + np.outer(_f64(k[0, h]), _f64(v[0, h]))
+        assert _relerr(hT[0, h], S1) < 1e-15
+        assert _relerr(o[0, h], s * S1.T @ _f64(q[0, h])) < 1e-14
+
+
+def test_linear_in_v_and_h0(oracle_mod):
+    q, k, v1, h1, ll = _case(4, 23)
+    _, _, v2, h2, _ = _case(5, 23)
+    s = 0.3
+    a, b = 2.0, -0.5
+    o1, s1 = oracle_mod.fwd(q, k, v1, ll, s, h0=h1)
+    o2, s2 = oracle_mod.fwd(q, k, v2, ll, s, h0=h2)
+    # The combined inputs are rounded to fp32 on the way in, hence the 1e-6 bound.
+    o3, s3 = oracle_mod.fwd(q, k, a * v1 + b * v2, ll, s, h0=a * h1 + b * h2)
+    assert _relerr(o3, a * o1 + b * o2) < 1e-6
+    assert _relerr(s3, a * s1 + b * s2) < 1e-6
+
+
+def test_resume_from_final_state(oracle_mod):
+    q, k, v, h0, ll = _case(6, 50)
+    s = 0.5
+    o, hT = oracle_mod.fwd(q, k, v, ll, s, h0=h0)
+    oa, ha = oracle_mod.fwd(q[:19], k[:19], v[:19], ll, s, h0=h0)
+    ob, hb = oracle_mod.fwd(q[19:], k[19:], v[19:], ll, s, h0=ha)
+    # ha is fp64; the second call takes fp32 h0, so compare with that rounding in mind.
+    assert _relerr(np.concatenate([oa, ob]), o) < 1e-6
+    assert _relerr(hb, hT) < 1e-6
+    assert _relerr(oa, o[:19]) < 1e-15
+
+
+@pytest.mark.parametrize("C", [1, 7, 64, 128, 200])
+def test_chunk_size_invariance(oracle_mod, C):
+    q, k, v, h0, ll = _case(7, 200, dk=6, dv=4)
+    s = 0.41
+    o, hT = oracle_mod.fwd(q, k, v, ll, s, h0=h0)
+    oc, hc = oracle_mod.fwd_chunked(q, k, v, ll, s, C, h0=h0)
+    assert _relerr(oc, o) < 1e-12
+    assert _relerr(hc, hT) < 1e-12
+
+
+def test_chunked_form_small_decay_does_not_overflow(oracle_mod):
+    """lambda = 0.5 (the pages' head 0): lambda^127 is tiny but the chunked form never divides."""
+    T = 300
+    q, k, v = _rand(8, 1, (T, 1, 4)), _rand(8, 2, (T, 1, 4)), _rand(8, 3, (T, 1, 3))
+    ll = np.array([np.log(0.5)], np.float32)
+    o, hT = oracle_mod.fwd(q, k, v, ll, 1.0)
+    oc, hc = oracle_mod.fwd_chunked(q, k, v, ll, 1.0, 128)
+    assert np.all(np.isfinite(oc)) and _relerr(oc, o) < 1e-12 and _relerr(hc, hT) < 1e-12
+
+
+def test_varlen_equals_separate_sequences(oracle_mod):
+    lens = [5, 0, 33, 1, 128, 129]
+    cu = gs.cu_seqlens_of(lens)
+    T = int(cu[-1])
+    H, dk, dv = 2, 4, 6
+    q, k, v = _rand(9, 1, (T, H, dk)), _rand(9, 2, (T, H, dk)), _rand(9, 3, (T, H, dv))
+    h0 = _rand(9, 4, (len(lens), H, dk, dv), 0.1)
+    ll = np.log(np.array([0.97, 0.5], np.float32))
+    o, hT = oracle_mod.fwd(q, k, v, ll, 0.3, h0=h0, cu_seqlens=cu)
+    for n in range(len(lens)):
+        a, b = cu[n], cu[n + 1]
+        on, hn = oracle_mod.fwd(q[a:b], k[a:b], v[a:b], ll, 0.3, h0=h0[n:n + 1])
+        assert np.array_equal(o[a:b], on)
+        assert np.array_equal(hT[n], hn[0])
+    # An empty sequence hands its initial state through unchanged.
+    assert np.array_equal(hT[1], h0[1].astype(np.float64))
+
+
+def test_decode_steps_equal_prefill(oracle_mod):
+    T, N, H, dk, dv = 12, 3, 2, 5, 4
+    q, k, v = _rand(11, 1, (T, N, H, dk)), _rand(11, 2, (T, N, H, dk)), _rand(11, 3, (T, N, H, dv))
+    h0 = _rand(11, 4, (N, H, dk, dv), 0.1)
+    ll = np.log(np.array([0.9, 0.8], np.float32))
+    state = h0.astype(np.float64).copy()
+    outs = [oracle_mod.decode_step(q[t], k[t], v[t], ll, 0.7, state) for t in range(T)]
+    for n in range(N):
+        o, hT = oracle_mod.fwd(q[:, n], k[:, n], v[:, n], ll, 0.7, h0=h0[n:n + 1])
+        assert _relerr(np.stack([x[n] for x in outs]), o) < 1e-13
+        assert _relerr(state[n], hT[0]) < 1e-13
+
+
+def test_pages_decay_schedule_endpoints():
+    """Half-life schedule from 1 to 2,048 tokens: head 0 decays by one half per token and head 15
+    keeps about 0.9997 (section "Decay schedule's reach")."""
+    lam = np.exp(gs.halflife_log_lambda().astype(np.float64))
+    assert abs(lam[0] - 0.5) < 1e-7
+    assert abs(lam[15] - 0.9997) < 1e-4
+    lam_w = np.exp(gs.laplace_log_lambda().astype(np.float64))
+    assert abs(lam_w[0] - 0.96875) < 1e-7 and abs(lam_w[15] - (1 - 2.0 ** -12)) < 1e-7
+
+
+# ---------------------------------------------------------------------------------------------
+# Backward: the adjoint of the recurrence, pinned by finite differences of the forward.
+# Each scalar input enters the forward linearly, so a central difference in one coordinate is
+# exact up to rounding.
+# ---------------------------------------------------------------------------------------------
+def _loss(oracle_mod, q, k, v, ll, s, h0, dO, dhT, cu=None):
+    o, hT = oracle_mod.fwd(q, k, v, ll, s, h0=h0, cu_seqlens=cu)
+    return float(np.sum(o * dO) + np.sum(hT * dhT))
+
+
+@pytest.mark.parametrize("lens", [[6], [3, 0, 5]])
+def test_backward_matches_finite_differences(oracle_mod, lens):
+    cu = gs.cu_seqlens_of(lens)
+    T, H, dk, dv = int(cu[-1]), 2, 3, 4
+    n = len(lens)
+    rng = np.random.default_rng(0)
+    # Dyadic inputs (multiples of 1/8) make the forward nearly exact in fp64.
+    q = (rng.integers(-8, 9, (T, H, dk)) / 8).astype(np.float32)
+    k = (rng.integers(-8, 9, (T, H, dk)) / 8).astype(np.float32)
+    v = (rng.integers(-8, 9, (T, H, dv)) / 8).astype(np.float32)
+    h0 = (rng.integers(-8, 9, (n, H, dk, dv)) / 8).astype(np.float32)
+    dO = (rng.integers(-8, 9, (T, H, dv)) / 8).astype(np.float32)
+    dhT = (rng.integers(-8, 9, (n, H, dk, dv)) / 8).astype(np.float32)
+    ll = np.log(np.array([0.75, 0.5], np.float32))
+    s = 0.5
+    dq, dk_, dv_, dh0 = oracle_mod.bwd(q, k, v, ll, s, dO, h0=h0, dhT=dhT, cu_seqlens=cu)
+    eps = 0.125
+    for name, x, g in (("q", q, dq), ("k", k, dk_), ("v", v, dv_), ("h0", h0, dh0)):
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args = dict(q=q, k=k, v=v, h0=h0)
+            args[name] = xp
+            lp = _loss(oracle_mod, args["q"], args["k"], args["v"], ll, s, args["h0"], dO, dhT, cu)
+            args[name] = xm
+            lm = _loss(oracle_mod, args["q"], args["k"], args["v"], ll, s, args["h0"], dO, dhT, cu)
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - g[idx]) <= 1e-9 * max(1.0, abs(fd)), (name, idx, fd, g[idx])
+
+
+def test_backward_lambda_one_closed_form(oracle_mod):
+    """lambda = 1: G_t = dhT + s sum_{u>=t} q_u dO_u^T, so dk_t = G_t v_t and dv_t = G_t^T k_t;
+    dq_t = s (h0 + sum_{j<=t} k_j v_j^T) dO_t."""
+    T, H, dk, dv = 15, 1, 4, 6
+    q, k, v = _rand(12, 1, (T, H, dk)), _rand(12, 2, (T, H, dk)), _rand(12, 3, (T, H, dv))
+    dO, dhT = _rand(12, 5, (T, H, dv)), _rand(12, 6, (1, H, dk, dv))
+    h0 = _rand(12, 4, (1, H, dk, dv))
+    s = 0.6
+    dq, dk_, dv_, dh0 = oracle_mod.bwd(q, k, v, np.zeros(1, np.float32), s, dO, h0=h0, dhT=dhT)
+    q64, k64, v64, g64 = _f64(q[:, 0]), _f64(k[:, 0]), _f64(v[:, 0]), _f64(dO[:, 0])
+    qg = s * np.einsum("ta,tb->tab", q64, g64)
+    G = _f64(dhT[0, 0])[None] + np.cumsum(qg[::-1], axis=0)[::-1]
+    assert _relerr(dk_[:, 0], np.einsum("tab,tb->ta", G, v64)) < 1e-12
+    assert _relerr(dv_[:, 0], np.einsum("tab,ta->tb", G, k64)) < 1e-12
+    assert _relerr(dh0[0, 0], G[0]) < 1e-12
+    S = _f64(h0[0, 0])[None] + np.cumsum(np.einsum("ta,tb->tab", k64, v64), axis=0)
+    assert _relerr(dq[:, 0], s * np.einsum("tab,tb->ta", S, g64)) < 1e-12
+
+
+def test_backward_empty_sequence_passes_dhT(oracle_mod):
+    cu = gs.cu_seqlens_of([0, 4])
+    H, dk, dv = 1, 2, 3
+    q, k, v = _rand(13, 1, (4, H, dk)), _rand(13, 2, (4, H, dk)), _rand(13, 3, (4, H, dv))
+    dO, dhT = _rand(13, 5, (4, H, dv)), _rand(13, 6, (2, H, dk, dv))
+    _, _, _, dh0 = oracle_mod.bwd(q, k, v, np.log(np.array([0.9], np.float32)), 1.0, dO, dhT=dhT,
+                                  cu_seqlens=cu)
+    assert np.array_equal(dh0[0], dhT[0].astype(np.float64))
