@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 Simple GLA mixer (one JSON line on rank 0).
+
+Headline: chunked-forward tokens/s on the Laplace-layer workload (B=8, T=2048, H=16, d_k=96,
+d_v=192, bf16 operands, fp32 state), inputs resident in HBM.  The same line carries the other
+hot-path rows measured the same way: decode tokens/s at 1,280 sequences x 24 layers (64 steps),
+the chunked backward, and the packed varlen forward; each with its roofline against the measured
+GB300 peaks.  `e2e` repeats the headline through host buffers (copies inside the timed region),
+`cpu_baseline` times the fp64 oracle on the host cores.  `--impl reference` times the oracle alone.
+
+Multi-GPU: every rank runs the same workload on its own GPU (independent replicas, no
+collective on the data path; scaling "weak"); values are summed over ranks, times are the max.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GLA chunked-fwd tokens/s (H16,dk96,dv192); decode tok/s at 1280 seqs"
+DK, DV, H = 96, 192, 16
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for_smi(torch):
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        first = vis.split(",")[0] if vis else str(torch.cuda.current_device())
+        return first
+
+
+# ------------------------------------------------------------------------------------------
+# timing
+# ------------------------------------------------------------------------------------------
+class Dist:
+    def __init__(self, torch):
+        self.torch = torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x):
+        if not self.pg:
+            return x
+        t = self.torch.tensor([x], dtype=self.torch.float64,
+                              device="cuda" if self.torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def timed(torch, dist, fn, steps, warmup):
+    """W untimed calls, then exactly K calls between a barrier + synchronize on both sides.
+    Returns (ms per step over the region, mean ms per call from per-call events)."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    dist.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    region = start.elapsed_time(end) / steps
+    per_call = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return region, per_call
+
+
+def roofline(bytes_, flops, secs, peaks, bound="hbm"):
+    if bound == "hbm":
+        ach = bytes_ / secs / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                "algorithmic_bytes": int(bytes_), "flops": int(flops),
+                "tensor_frac": round(flops / secs / 1e12 / peaks["bf16_tflops"], 4),
+                "peak_source": peaks["source"]}
+    ach = flops / secs / 1e12
+    return {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": None}
+
+
+def fwd_bytes(tokens, n_seq, with_h0):
+    io = tokens * H * (2 * DK * 2 + 2 * DV * 2)
+    return io + n_seq * H * DK * DV * 4 * (2 if with_h0 else 1)
+
+
+def fwd_flops(tokens):
+    return tokens * H * 2 * (128 * DK + 128 * DV + 2 * DK * DV)
+
+
+# ------------------------------------------------------------------------------------------
+# rows
+# ------------------------------------------------------------------------------------------
+def bench_fwd(torch, gla, wl, dist, args, peaks):
+    w = wl.layer()
+    g = w.device_inputs()
+    o = torch.empty_like(g["v"])
+    hT = torch.empty((w.n_seq, H, DK, DV), dtype=torch.float32, device="cuda")
+    fn = lambda: gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], w.scale, o=o, hT=hT)
+    region, per_call = timed(torch, dist, fn, args.steps, args.warmup)
+    region = dist.max(region)
+    per_call = dist.max(per_call)
+    tokens = w.tokens
+    res = {
+        "workload": w.name, "tokens": tokens, "ms_per_step": region,
+        "value": tokens * dist.world / (region / 1e3),
+        "roofline": roofline(fwd_bytes(tokens, w.n_seq, False), fwd_flops(tokens), per_call / 1e3,
+                             peaks),
+        "kernel_ms": per_call, "launches_per_step": 1,
+    }
+    # e2e through the public call with host buffers: H2D of q, k, v and D2H of o, hT per step
+    hq, hk, hv = (x.cpu().pin_memory() for x in (g["q"], g["k"], g["v"]))
+    ho, hh = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(hT, device="cpu").pin_memory()
+    dq_, dk_, dv_ = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
+
+    def e2e():
+        dq_.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        gla.gla_chunk_fwd(dq_, dk_, dv_, g["log_lambda"], w.scale, o=o, hT=hT)
+        ho.copy_(o, non_blocking=True)
+        hh.copy_(hT, non_blocking=True)
+    e_region, _ = timed(torch, dist, e2e, args.steps, args.warmup)
+    e_region = dist.max(e_region)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hh.numel() * hh.element_size()
+    res["e2e"] = {"value": tokens * dist.world / (e_region / 1e3), "unit": "tokens/s",
+                  "ms_per_step": e_region, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del g, o, hT, hq, hk, hv, ho, hh, dq_, dk_, dv_
+    return res
+
+
+def bench_varlen(torch, gla, wl, dist, args, peaks):
+    w = wl.varlen()
+    g = w.device_inputs()
+    o = torch.empty_like(g["v"])
+    hT = torch.empty((w.n_seq, H, DK, DV), dtype=torch.float32, device="cuda")
+    ws = torch.empty(gla.gla_workspace_bytes(w.n_seq, H), dtype=torch.uint8, device="cuda")
+    fn = lambda: gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], w.scale, h0=g["h0"],
+                                   cu_seqlens=g["cu_seqlens"], o=o, hT=hT, workspace=ws)
+    region, per_call = timed(torch, dist, fn, args.steps, args.warmup)
+    region, per_call = dist.max(region), dist.max(per_call)
+    res = {"workload": w.name, "tokens": w.tokens, "ms_per_step": region,
+           "value": w.tokens * dist.world / (region / 1e3), "unit": "tokens/s",
+           "roofline": roofline(fwd_bytes(w.tokens, w.n_seq, True), fwd_flops(w.tokens),
+                                per_call / 1e3, peaks),
+           "launches_per_step": 2}
+    del g, o, hT
+    return res
+
+
+def bench_bwd(torch, gla, wl, dist, args, peaks):
+    w = wl.layer(with_grad=True)
+    g = w.device_inputs()
+    fn = lambda: gla.gla_chunk_bwd(g["q"], g["k"], g["v"], g["log_lambda"], g["dO"], w.scale,
+                                   dhT=g["dhT"])
+    region, per_call = timed(torch, dist, fn, args.steps, args.warmup)
+    region, per_call = dist.max(region), dist.max(per_call)
+    tokens = w.tokens
+    byts = tokens * H * (4 * DK * 2 + 4 * DV * 2) + 2 * w.n_seq * H * DK * DV * 4
+    flops = tokens * H * 2 * (128 * DV + 128 * DK + 2 * DK * DV      # dq scan
+                              + 128 * DV + 128 * DK + 128 * DK + 128 * DV + 4 * DK * DV)  # dk, dv scan
+    res = {"workload": w.name, "tokens": tokens, "ms_per_step": region,
+           "value": tokens * dist.world / (region / 1e3), "unit": "tokens/s",
+           "roofline": roofline(byts, flops, per_call / 1e3, peaks), "launches_per_step": 3}
+    del g
+    return res
+
+
+def bench_decode(torch, gla, wl, dist, args, peaks):
+    w = wl.DecodeWorkload()
+    state = w.device_state()
+    ll = torch.from_numpy(w.log_lambda).cuda()
+    steps = [w.device_step(s) for s in range(min(w.steps, 4))]  # 4 distinct token sets, cycled
+    o = torch.empty((w.N, H, DV), dtype=torch.bfloat16, device="cuda")
+    it = [0]
+
+    def fn():
+        b = steps[it[0] % len(steps)]
+        it[0] += 1
+        gla.gla_decode_step(b["q"], b["k"], b["v"], ll, state, w.scale, o=o)
+    n = w.steps
+    region, per_call = timed(torch, dist, fn, n, max(args.warmup, 3))
+    region, per_call = dist.max(region), dist.max(per_call)
+    state_bytes = 2 * w.N * H * DK * DV * 4
+    io_bytes = w.N * H * (2 * DK * 2 + 2 * DV * 2)
+    res = {"workload": w.name, "steps": n, "ms_per_step": region,
+           "value": w.seqs * dist.world / (region / 1e3), "unit": "tokens/s",
+           "token": "one new token per sequence through all 24 layers",
+           "roofline": roofline(state_bytes, 2 * 2 * w.N * H * DK * DV, per_call / 1e3, peaks),
+           "io_bytes_outside_roofline": io_bytes, "launches_per_step": 1}
+    res["roofline"]["algorithmic_bytes_note"] = "fp32 state read + write per step"
+    del state, steps, o
+    return res
+
+
+def cpu_baseline_fwd(seconds_budget=20.0):
+    """The oracle as it stands on the host cores: whole sequences of the B=8, T=2048, H=16
+    workload (all 16 heads each), as many as fit the time budget."""
+    import numpy as np
+
+    import oracle
+    from glasynth import workloads as wl
+    oracle.build()
+    w = wl.layer()
+    cores = oracle.hardware_threads()
+    done_tokens, t_total, seqs = 0, 0.0, 0
+    for n in range(w.n_seq):
+        units = [w.host_unit(n, h) for h in range(H)]
+        q = np.concatenate([u["q"] for u in units], axis=1)
+        k = np.concatenate([u["k"] for u in units], axis=1)
+        v = np.concatenate([u["v"] for u in units], axis=1)
+        t0 = time.perf_counter()
+        oracle.fwd(q, k, v, w.log_lambda, w.scale, nthreads=0)
+        t_total += time.perf_counter() - t0
+        done_tokens += w.lengths[n]
+        seqs += 1
+        if t_total > seconds_budget:
+            break
+    return {"value": done_tokens / t_total, "unit": "tokens/s", "cores": min(cores, H),
+            "kind": "oracle",
+            "sample": f"{seqs} of 8 sequences (T=2048, all 16 heads) of the B=8 T=2048 H=16 "
+                      f"forward workload, fp64 per-token recurrence, {min(cores, H)} threads "
+                      f"(one per head), {t_total:.1f} s"}
+
+
+def run_reference(args):
+    """`--impl reference`: the fp64 oracle timed on the host cores, one sequence per step."""
+    import numpy as np
+
+    import oracle
+    from glasynth import workloads as wl
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    oracle.build()
+    w = wl.layer()
+    units = [w.host_unit(0, h) for h in range(H)]
+    q = np.concatenate([u["q"] for u in units], axis=1)
+    k = np.concatenate([u["k"] for u in units], axis=1)
+    v = np.concatenate([u["v"] for u in units], axis=1)
+    step = lambda: oracle.fwd(q, k, v, w.log_lambda, w.scale, nthreads=0)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    cores = min(oracle.hardware_threads(), H)
+    value = w.lengths[0] / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": 8, "T": 2048, "H": H, "dk": DK, "dv": DV,
+                       "sample_per_step": "sequence 0 (2048 tokens, 16 heads)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": "one T=2048 sequence (16 heads) of the B=8 workload per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--rows", default="fwd,bwd,varlen,decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    import linear_attention_recurrence_simple_gb300 as gla
+    from glasynth import workloads as wl
+    dist = Dist(torch)
+    torch.cuda.set_device(dist.local)
+    dist.init("nccl")
+    gla.load_library()
+    peaks = load_peaks()
+    rows = args.rows.split(",")
+    out = {}
+    sampler = ClockSampler(gpu_id_for_smi(torch))
+    with sampler:
+        if "fwd" in rows:
+            out["fwd"] = bench_fwd(torch, gla, wl, dist, args, peaks)
+        if "varlen" in rows:
+            out["varlen"] = bench_varlen(torch, gla, wl, dist, args, peaks)
+        if "bwd" in rows:
+            out["bwd"] = bench_bwd(torch, gla, wl, dist, args, peaks)
+        if "decode" in rows:
+            out["decode"] = bench_decode(torch, gla, wl, dist, args, peaks)
+    err = gla.gla_get_device_error()
+    clocks = sampler.summary()
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_fwd()
+    if dist.rank == 0:
+        f = out.get("fwd", {})
+        line = {
+            "metric": METRIC, "value": f.get("value"), "unit": "tokens/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": f.get("ms_per_step"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded SplitMix64 / Irwin-Hall(4) normal inputs, no dataset",
+            "config": {"workload": f.get("workload"), "B": 8, "T": 2048, "H": H, "dk": DK, "dv": DV,
+                       "chunk": 128, "accumulate": "fp32 state and accumulation",
+                       "l2": "no flush: inputs of each call (201 MB) exceed the 129 MB L2",
+                       "parallelism": f"replicas x{dist.world} (no collective)"},
+            "roofline": f.get("roofline"), "e2e": f.get("e2e"),
+            "gpu_launches": args.steps * f.get("launches_per_step", 1),
+            "clocks": clocks, "cpu_baseline": cpu, "device_error": err,
+            "rows": {k: v for k, v in out.items() if k != "fwd"},
+        }
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -58,12 +58,17 @@ def _mix64(z: np.ndarray) -> np.ndarray:
     return z ^ (z >> np.uint64(31))
 
 
-def u64(seed: int, tid: int, count: int, start: int = 0) -> np.ndarray:
-    """Outputs ``start .. start+count-1`` of the SplitMix64 stream of (seed, tid)."""
+def u64_at(seed: int, tid: int, idx: np.ndarray) -> np.ndarray:
+    """Outputs number ``idx`` (any array of non-negative ints) of the stream of (seed, tid)."""
     key = np.uint64(stream_key(seed, tid))
-    i = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    i = np.asarray(idx, dtype=np.uint64) + np.uint64(1)
     with np.errstate(over="ignore"):
         return _mix64(key + i * np.uint64(GAMMA))
+
+
+def u64(seed: int, tid: int, count: int, start: int = 0) -> np.ndarray:
+    """Outputs ``start .. start+count-1`` of the SplitMix64 stream of (seed, tid)."""
+    return u64_at(seed, tid, np.arange(start, start + count, dtype=np.uint64))
 
 
 def ih4_scale(sigma: float) -> np.float32:
@@ -71,15 +76,17 @@ def ih4_scale(sigma: float) -> np.float32:
     return np.float32(sigma / IH4_SD)
 
 
-def normal(seed: int, tid: int, shape, sigma: float = 1.0, start: int = 0) -> np.ndarray:
-    """fp32 approximate-normal variates, elements ``start ..`` of the stream, in C order."""
-    count = int(np.prod(shape, dtype=np.int64))
-    x = u64(seed, tid, count, start)
+def _ih4(x: np.ndarray, sigma: float) -> np.ndarray:
     m = np.uint64(0xFFFF)
     s = ((x & m) + ((x >> np.uint64(16)) & m) + ((x >> np.uint64(32)) & m)
          + ((x >> np.uint64(48)) & m))
-    f = (s.astype(np.float32) - np.float32(IH4_MEAN)) * ih4_scale(sigma)
-    return f.astype(np.float32).reshape(shape)
+    return ((s.astype(np.float32) - np.float32(IH4_MEAN)) * ih4_scale(sigma)).astype(np.float32)
+
+
+def normal(seed: int, tid: int, shape, sigma: float = 1.0, start: int = 0) -> np.ndarray:
+    """fp32 approximate-normal variates, elements ``start ..`` of the stream, in C order."""
+    count = int(np.prod(shape, dtype=np.int64))
+    return _ih4(u64(seed, tid, count, start), sigma).reshape(shape)
 
 
 def normal_rows(seed: int, tid: int, row_shape, rows, sigma: float = 1.0) -> np.ndarray:
@@ -87,10 +94,9 @@ def normal_rows(seed: int, tid: int, row_shape, rows, sigma: float = 1.0) -> np.
 
     Lets a test regenerate a sampled slice of a device-generated tensor without the rest."""
     row_len = int(np.prod(row_shape, dtype=np.int64))
-    out = np.empty((len(rows),) + tuple(row_shape), np.float32)
-    for n, r in enumerate(rows):
-        out[n] = normal(seed, tid, tuple(row_shape), sigma, start=int(r) * row_len)
-    return out
+    rows = np.asarray(rows, dtype=np.uint64)
+    idx = rows[:, None] * np.uint64(row_len) + np.arange(row_len, dtype=np.uint64)[None, :]
+    return _ih4(u64_at(seed, tid, idx), sigma).reshape((len(rows),) + tuple(row_shape))
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:

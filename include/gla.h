@@ -1,0 +1,140 @@
+/* gla.h - C ABI of the GB300 Simple GLA mixer library (libgla.so).
+ *
+ * What it computes.  Source: "Beyond the KV cache: Training and serving i14's Laplace 3B linear
+ * attention model on AWS Trainium2 with native PyTorch" (AWS blog post; Spanish and Chinese
+ * copies carry the later sections and the figure captions).
+ *   - Section "i14 and the Laplace 3B architecture", paragraph "GLA mixer": every head h keeps a
+ *     d_k x d_v = 96 x 192 matrix state, decayed by a fixed per-head factor lambda_h and written
+ *     with the rank-1 outer product of the current key and value; the readout queries the state.
+ *     The equation images are missing from the text; this library computes
+ *         S_t = lambda_h * S_{t-1} + k_t v_t^T ,      o_t = S_t^T (scale * q_t)
+ *     with the readout after the update, S_0 = h0 (zeros when h0 is NULL) and hT = S_T.
+ *   - Section "Challenge 1: Using native PyTorch on Trainium for GLA": the chunked form with
+ *     128-token chunks (intra-chunk masked linear attention plus the carried state; the state
+ *     advances with lambda^C, the decay compounded over the chunk).  gla_chunk_fwd computes that
+ *     form; its result equals the recurrence above up to rounding.
+ *   - Section "Challenge 3" (backward through the sequential state updates): gla_chunk_bwd is the
+ *     adjoint of the recurrence.  lambda is fixed at initialisation, not learned ("Decay
+ *     schedule"), so there is no gradient for it.
+ *   - Section "Optimizing inference on Trainium2" (a wrapper reads and writes each sequence's
+ *     recurrent state in a pool, one fixed page per sequence): gla_decode_step advances a pool of
+ *     states by one token in place.
+ *
+ * Conventions shared by every entry point.
+ *   - Sizes: only d_k = 96 and d_v = 192 are implemented; other values return
+ *     GLA_ERR_UNSUPPORTED.  H >= 1.  Chunk size is 128 tokens (GLA_CHUNK).
+ *   - Pointers are DEVICE pointers owned by the caller, 16-byte aligned (else GLA_ERR_ALIGN),
+ *     except where a comment says "host".  The library never allocates, frees or keeps them.
+ *   - Layouts are dense, C order, token-major:
+ *       q, k     [n_seq, T, H, 96]   (or packed [T_total, H, 96] with cu_seqlens)
+ *       v, o, dO [n_seq, T, H, 192]  (or packed [T_total, H, 192])
+ *       h0, hT, dhT, dh0, state  [n_seq (or pool rows), H, 96, 192], always fp32
+ *       log_lambda [H] fp32: natural log of lambda_h, <= 0 (-inf allowed: lambda = 0)
+ *   - dtype (gla_dtype) is the type of q, k, v, o, dO, dq, dk, dv.  GLA_BF16 runs the tensor-core
+ *     kernels (bf16 operands, fp32 accumulation and fp32 state); results are rounded to bf16
+ *     nearest-even.  GLA_F32 runs the all-fp32 CUDA-core kernels.
+ *   - scale multiplies q (1/sqrt(96) in the Laplace 3B configuration).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     Argument errors are detected on the host before anything is launched and return a negative
+ *     gla_status; nothing aborts the process.  Faults found while a kernel runs (a bounded wait
+ *     that timed out, a pool slot out of range) set a sticky per-device error word that
+ *     gla_get_device_error() reports.
+ *   - Empty work is valid: n_seq = 0, T = 0 or sequences of length 0 launch nothing for them;
+ *     a length-0 sequence gives hT = h0 (zeros if h0 is NULL) and dh0 = dhT.
+ */
+#ifndef GLA_H_
+#define GLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gla_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  GLA_OK = 0,
+  GLA_ERR_NULL = -1,        /* a required pointer is NULL */
+  GLA_ERR_SHAPE = -2,       /* negative size, bad cu_seqlens, pool slot out of range */
+  GLA_ERR_DTYPE = -3,       /* dtype is not a gla_dtype */
+  GLA_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned */
+  GLA_ERR_UNSUPPORTED = -5, /* d_k != 96, d_v != 192, or no sm_103 device current */
+  GLA_ERR_WORKSPACE = -6,   /* workspace missing or smaller than gla_workspace_bytes() */
+  GLA_ERR_LAUNCH = -7,      /* the CUDA runtime refused a launch */
+  GLA_ERR_TIMEOUT = -8      /* a bounded device-side wait gave up (kernel returned early) */
+} gla_status;
+
+typedef enum { GLA_BF16 = 0, GLA_F32 = 1 } gla_dtype;
+
+#define GLA_DK 96
+#define GLA_DV 192
+#define GLA_CHUNK 128
+
+/* Bytes of device workspace that gla_chunk_fwd / gla_chunk_bwd need for `n_seq` packed
+ * (cu_seqlens) sequences of H heads.  The workspace holds the longest-first schedule of the
+ * (sequence, head) work.  Calls without cu_seqlens need none (pass NULL, 0). */
+size_t gla_workspace_bytes(int n_seq, int H);
+
+/* Chunked forward.
+ *   q, k, v      inputs (layouts above), dtype `dtype`.
+ *   log_lambda   [H] fp32 device.
+ *   h0           [n_seq, H, 96, 192] fp32, or NULL for zero initial states.
+ *   scale        multiplies q.
+ *   o            output, same dtype and layout as v.
+ *   hT           [n_seq, H, 96, 192] fp32 final states, or NULL to skip.
+ *   cu_seqlens   NULL: n_seq sequences of T tokens each, layout [n_seq, T, H, d].
+ *                else: [n_seq + 1] int32 device array of packed offsets, cu_seqlens[0] = 0,
+ *                non-decreasing, cu_seqlens[n_seq] = T (the packed total); its values are read on
+ *                the device only (no host synchronisation), so the caller guarantees them.
+ *   workspace    >= gla_workspace_bytes(n_seq, H) bytes when cu_seqlens != NULL, else unused.
+ * Returns GLA_OK once the work is queued on `stream`. */
+int gla_chunk_fwd(const void* q, const void* k, const void* v, const float* log_lambda,
+                  const float* h0, float scale, void* o, float* hT, const int32_t* cu_seqlens,
+                  int n_seq, int T, int H, int dk, int dv, int dtype, void* workspace,
+                  size_t ws_bytes, gla_stream_t stream);
+
+/* Chunked backward: gradients of L(o, hT) given dO = dL/do and dhT = dL/dhT.
+ *   q, k, v, log_lambda, h0, scale, cu_seqlens, n_seq, T, H, dtype: as in gla_chunk_fwd
+ *                (h0 NULL = zeros).
+ *   dO           same dtype and layout as v.
+ *   dhT          [n_seq, H, 96, 192] fp32, or NULL for zero.
+ *   dq, dk       outputs, layout of q; dv output, layout of v; all of dtype `dtype`.
+ *   dh0          [n_seq, H, 96, 192] fp32 output, or NULL to skip.
+ * The forward state is recomputed on chip; nothing from gla_chunk_fwd is needed. */
+int gla_chunk_bwd(const void* q, const void* k, const void* v, const float* log_lambda,
+                  const float* h0, float scale, const void* dO, const float* dhT, void* dq,
+                  void* dk, void* dv, float* dh0, const int32_t* cu_seqlens, int n_seq, int T,
+                  int H, int dk_size, int dv_size, int dtype, void* workspace, size_t ws_bytes,
+                  gla_stream_t stream);
+
+/* One decode step for N sequences, in place on a state pool.
+ *   q, k         [N, H, 96]; v, o [N, H, 192]; dtype `dtype`.
+ *   state        [pool_rows, H, 96, 192] fp32, updated in place: S <- lambda S + k v^T.
+ *   slot         [N] int32 device array: sequence n uses pool row slot[n]; NULL = row n
+ *                (then pool_rows >= N is required).  Rows must be distinct.  A slot outside
+ *                [0, pool_rows) skips that sequence (state and o untouched) and records
+ *                GLA_ERR_SHAPE in the device error word.
+ *   o            readout o = S^T (scale q), taken after the update. */
+int gla_decode_step(const void* q, const void* k, const void* v, const float* log_lambda,
+                    float scale, float* state, const int32_t* slot, int pool_rows, void* o, int N,
+                    int H, int dk, int dv, int dtype, gla_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the current device's sticky error word:
+ * GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_SHAPE; GLA_ERR_LAUNCH if the stream itself failed. */
+int gla_get_device_error(gla_stream_t stream);
+
+/* Upper bound, in nanoseconds, of every device-side wait on an mbarrier (default 2e9).  A wait
+ * that exceeds it records GLA_ERR_TIMEOUT, drains the copies its CTA has in flight, releases
+ * tensor memory and returns.  Meant for tests of that path; applies to the current device. */
+int gla_set_wait_limit_ns(unsigned long long ns);
+
+/* Human-readable name of a gla_status value. */
+const char* gla_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GLA_H_ */

@@ -1,0 +1,260 @@
+"""GB300 (sm_103a) Simple GLA mixer: a thin binding over the C ABI of ``libgla.so``.
+
+The functions keep the C names (``include/gla.h``) and only marshal arguments: they check
+torch tensors, allocate outputs with torch, and pass raw device pointers and the current CUDA
+stream to the library.  Every step of the computation runs in the library's CUDA kernels; there
+is no other code path, and a missing library raises instead of falling back.
+
+Layouts (see ``include/gla.h``): q, k ``[B, T, H, 96]``; v ``[B, T, H, 192]``; packed inputs
+``[T_total, H, d]`` (or ``[1, T_total, H, d]``) with ``cu_seqlens``; states ``[B, H, 96, 192]`` fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "GlaError", "load_library", "library_path", "gla_workspace_bytes", "gla_chunk_fwd",
+    "gla_chunk_bwd", "gla_decode_step", "gla_get_device_error", "gla_set_wait_limit_ns",
+    "gla_status_string", "DK", "DV", "CHUNK", "EXPORTS",
+]
+
+DK, DV, CHUNK = 96, 192, 128
+GLA_BF16, GLA_F32 = 0, 1
+EXPORTS = ("gla_workspace_bytes", "gla_chunk_fwd", "gla_chunk_bwd", "gla_decode_step",
+           "gla_get_device_error", "gla_set_wait_limit_ns", "gla_status_string")
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libgla.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class GlaError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {gla_status_string(status)} ({status})" if where else
+                         f"{gla_status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(build: bool = True):
+    """Loads libgla.so (building it first if missing and ``build``); raises if it cannot."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build:
+            from . import _build
+            _build.build()
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libgla.so is missing ({_LIB_PATH}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, F, Z, U = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
+                         ctypes.c_ulonglong)
+        lib.gla_workspace_bytes.argtypes = [I, I]
+        lib.gla_workspace_bytes.restype = Z
+        lib.gla_chunk_fwd.argtypes = [P, P, P, P, P, F, P, P, P, I, I, I, I, I, I, P, Z, P]
+        lib.gla_chunk_fwd.restype = I
+        lib.gla_chunk_bwd.argtypes = [P, P, P, P, P, F, P, P, P, P, P, P, P, I, I, I, I, I, I, P, Z, P]
+        lib.gla_chunk_bwd.restype = I
+        lib.gla_decode_step.argtypes = [P, P, P, P, F, P, P, I, P, I, I, I, I, I, P]
+        lib.gla_decode_step.restype = I
+        lib.gla_get_device_error.argtypes = [P]
+        lib.gla_get_device_error.restype = I
+        lib.gla_set_wait_limit_ns.argtypes = [U]
+        lib.gla_set_wait_limit_ns.restype = I
+        lib.gla_status_string.argtypes = [I]
+        lib.gla_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def gla_status_string(status: int) -> str:
+    return load_library().gla_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise GlaError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return GLA_BF16
+    if t.dtype == torch.float32:
+        return GLA_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _layout(q, k, v, cu_seqlens):
+    """Returns (n_seq, T, H, packed_shape_prefix) for fixed-length or packed inputs."""
+    if cu_seqlens is None:
+        if q.dim() != 4:
+            raise ValueError("without cu_seqlens, q must be [B, T, H, 96]")
+        B, T, H, dk = q.shape
+        n_seq = B
+    else:
+        if q.dim() == 4:
+            if q.shape[0] != 1:
+                raise ValueError("packed inputs must be [T_total, H, d] or [1, T_total, H, d]")
+            T, H, dk = q.shape[1:]
+        elif q.dim() == 3:
+            T, H, dk = q.shape
+        else:
+            raise ValueError("packed q must be [T_total, H, 96]")
+        n_seq = cu_seqlens.numel() - 1
+    if dk != DK or k.shape != q.shape or v.shape[:-1] != q.shape[:-1] or v.shape[-1] != DV:
+        raise ValueError("expected q, k [..., H, 96] and v [..., H, 192] with matching leading dims")
+    return n_seq, T, H
+
+
+def gla_workspace_bytes(n_seq: int, H: int) -> int:
+    return int(load_library().gla_workspace_bytes(int(n_seq), int(H)))
+
+
+def _workspace(cu_seqlens, n_seq, H, device, workspace):
+    if cu_seqlens is None:
+        return None, 0
+    need = gla_workspace_bytes(n_seq, H)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def gla_chunk_fwd(q, k, v, log_lambda, scale=None, h0=None, cu_seqlens=None,
+                  output_final_state: bool = True, o=None, hT=None, workspace=None):
+    """Chunked forward.  Returns ``(o, hT)`` (``hT`` is None if not requested)."""
+    lib = load_library()
+    dev = q.device
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, q.dtype, dev)
+    _need(log_lambda, "log_lambda", torch.float32, dev)
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    n_seq, T, H = _layout(q, k, v, cu_seqlens)
+    if log_lambda.numel() != H:
+        raise ValueError("log_lambda must have H entries")
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, dev)
+        if h0.shape != (n_seq, H, DK, DV):
+            raise ValueError("h0 must be [n_seq, H, 96, 192]")
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    _need(o, "o", v.dtype, dev)
+    if output_final_state and hT is None:
+        hT = torch.empty((n_seq, H, DK, DV), dtype=torch.float32, device=dev)
+    if hT is not None:
+        _need(hT, "hT", torch.float32, dev)
+    ws, ws_bytes = _workspace(cu_seqlens, n_seq, H, dev, workspace)
+    s = float(DK ** -0.5) if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        rc = lib.gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), s, _ptr(o),
+                               _ptr(hT), _ptr(cu_seqlens), n_seq, T, H, DK, DV, dt, _ptr(ws),
+                               ws_bytes, _stream(dev))
+    _check(rc, "gla_chunk_fwd")
+    return o, hT
+
+
+def gla_chunk_bwd(q, k, v, log_lambda, dO, scale=None, h0=None, dhT=None, cu_seqlens=None,
+                  need_dh0: bool = True, workspace=None):
+    """Chunked backward.  Returns ``(dq, dk, dv, dh0)`` (``dh0`` None if not requested)."""
+    lib = load_library()
+    dev = q.device
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("dO", dO)):
+        _need(t, name, q.dtype, dev)
+    _need(log_lambda, "log_lambda", torch.float32, dev)
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    n_seq, T, H = _layout(q, k, v, cu_seqlens)
+    if dO.shape != v.shape:
+        raise ValueError("dO must have the shape of v")
+    for name, t in (("h0", h0), ("dhT", dhT)):
+        if t is not None:
+            _need(t, name, torch.float32, dev)
+            if t.shape != (n_seq, H, DK, DV):
+                raise ValueError(f"{name} must be [n_seq, H, 96, 192]")
+    dq = torch.empty(q.shape, dtype=q.dtype, device=dev)
+    dk = torch.empty(k.shape, dtype=k.dtype, device=dev)
+    dv = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    dh0 = torch.empty((n_seq, H, DK, DV), dtype=torch.float32, device=dev) if need_dh0 else None
+    ws, ws_bytes = _workspace(cu_seqlens, n_seq, H, dev, workspace)
+    s = float(DK ** -0.5) if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        rc = lib.gla_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), s, _ptr(dO),
+                               _ptr(dhT), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dh0), _ptr(cu_seqlens),
+                               n_seq, T, H, DK, DV, dt, _ptr(ws), ws_bytes, _stream(dev))
+    _check(rc, "gla_chunk_bwd")
+    return dq, dk, dv, dh0
+
+
+def gla_decode_step(q, k, v, log_lambda, state, scale=None, slot=None, o=None):
+    """One decode step on the state pool ``state [P, H, 96, 192]`` (updated in place).
+
+    q, k ``[N, H, 96]``; v ``[N, H, 192]``; ``slot`` ``[N]`` int32 pool rows or None (row n).
+    Returns ``o [N, H, 192]``."""
+    lib = load_library()
+    dev = q.device
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, q.dtype, dev)
+    _need(log_lambda, "log_lambda", torch.float32, dev)
+    _need(state, "state", torch.float32, dev)
+    if q.dim() != 3 or q.shape[2] != DK or k.shape != q.shape or v.shape != (*q.shape[:2], DV):
+        raise ValueError("expected q, k [N, H, 96] and v [N, H, 192]")
+    N, H = q.shape[:2]
+    if state.dim() != 4 or state.shape[1:] != (H, DK, DV):
+        raise ValueError("state must be [P, H, 96, 192]")
+    if slot is not None:
+        _need(slot, "slot", torch.int32, dev)
+        if slot.shape != (N,):
+            raise ValueError("slot must be [N]")
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    _need(o, "o", v.dtype, dev)
+    s = float(DK ** -0.5) if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        rc = lib.gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), s, _ptr(state),
+                                 _ptr(slot), state.shape[0], _ptr(o), N, H, DK, DV, dt, _stream(dev))
+    _check(rc, "gla_decode_step")
+    return o
+
+
+def gla_get_device_error(device=None) -> int:
+    """Synchronises the current stream; returns and clears the device's sticky error status."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(load_library().gla_get_device_error(_stream(dev)))
+
+
+def gla_set_wait_limit_ns(ns: int) -> None:
+    _check(load_library().gla_set_wait_limit_ns(int(ns)), "gla_set_wait_limit_ns")

@@ -1,0 +1,136 @@
+// Device-side helpers shared by the GLA kernels: element conversion, the sticky error word,
+// bounded waits, and the argument block every chunked kernel receives.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gla {
+
+constexpr int DK = 96;
+constexpr int DV = 192;
+constexpr int CHUNK = 128;
+
+// Positive codes stored in the device error word (the host negates them into gla_status).
+constexpr unsigned ERR_SHAPE = 2;
+constexpr unsigned ERR_TIMEOUT = 8;
+
+// Everything a chunked forward or backward kernel needs; passed by value.
+struct ChunkArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dO;          // backward only
+  const float* log_lambda;
+  const float* h0;         // may be null
+  const float* dhT;        // backward only; may be null
+  void* o;                 // forward output (or dq in the backward)
+  void* dk;                // backward only
+  void* dv;                // backward only
+  float* hT;               // forward final state / backward dh0; may be null
+  const int32_t* cu_seqlens;  // null: fixed length T
+  const int32_t* order;       // longest-first sequence order (packed calls), or null
+  float scale;
+  int n_seq;
+  int T;                   // per-sequence length (fixed) or packed total
+  int H;
+  unsigned* err;           // device error word
+  unsigned long long wait_ns;  // limit of every bounded wait
+};
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <class T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ void raise_error(unsigned* word, unsigned code) {
+  atomicCAS(word, 0u, code);
+}
+
+// Token range [begin, end) of sequence n.
+__device__ __forceinline__ void seq_range(const ChunkArgs& a, int n, long long& begin, long long& end) {
+  if (a.cu_seqlens) {
+    begin = a.cu_seqlens[n];
+    end = a.cu_seqlens[n + 1];
+  } else {
+    begin = (long long)n * a.T;
+    end = begin + a.T;
+  }
+}
+
+// Splits a 1-D block index into (sequence, head, tile) with the sequence slowest, so that with
+// a longest-first order the longest sequences start first.
+__device__ __forceinline__ void unit_of_block(const ChunkArgs& a, int tiles, int& n, int& h, int& tile) {
+  const long long b = blockIdx.x;
+  const long long per_seq = (long long)a.H * tiles;
+  const int rank = (int)(b / per_seq);
+  const int rem = (int)(b % per_seq);
+  h = rem / tiles;
+  tile = rem % tiles;
+  n = a.order ? a.order[rank] : rank;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------------------------------
+// mbarrier helpers (shared::cta).  Every wait is bounded: it polls try_wait, reads the global
+// timer every 64 polls, and gives up after `limit_ns` (or as soon as *abort is set), raising
+// ERR_TIMEOUT.  Returns true when the phase completed.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns,
+                                          volatile int* abort_flag, unsigned* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
+        if (abort_flag) *abort_flag = 1;
+        raise_error(err, ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+}  // namespace gla

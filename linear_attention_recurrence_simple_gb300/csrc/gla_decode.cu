@@ -1,0 +1,130 @@
+// One-token decode step over a pool of fp32 GLA states, in place.
+//
+// "Beyond the KV cache" (Laplace 3B on Trainium2), section "i14 and the Laplace 3B
+// architecture", GLA mixer: S <- lambda_h S + k v^T (rank-1 write of the current key/value,
+// fixed per-head decay), then the readout o = S^T (scale q) queries the updated state.  Section
+// "Optimizing inference on Trainium2": the serving wrapper keeps one fixed page of recurrent state
+// per sequence in a pool, which `slot` indexes here.
+//
+// The step is a pure stream over the 72 KB state of each (sequence, head): read once, update,
+// write once.  One CTA of 576 threads owns one state; thread (r, c), r < 12, c < 48, holds
+// columns 4c..4c+3 (one 16-byte vector) of the 8 rows r, r+12, ..., r+84, so consecutive lanes
+// touch consecutive 16-byte pieces of a row.  All eight loads are issued before any arithmetic.  The readout's sum over d_k runs
+// in registers, then over the 12 row groups through shared memory.  Loads and stores carry
+// the streaming cache hint, since each state is touched once per step.
+#include "gla_common.cuh"
+
+namespace gla {
+namespace {
+
+constexpr int DEC_THREADS = 576;              // 48 column groups x 12 row groups
+constexpr int DEC_COLS = DV / 4;              // 48 float4 per state row
+constexpr int DEC_RGROUPS = DEC_THREADS / DEC_COLS;  // 12
+constexpr int DEC_ROWS = DK / DEC_RGROUPS;    // 8 rows per thread
+
+struct Bf16x4 { __nv_bfloat162 a, b; };
+
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ void store4(float* p, float4 x) { *reinterpret_cast<float4*>(p) = x; }
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 x) {
+  Bf16x4 r;
+  r.a = __floats2bfloat162_rn(x.x, x.y);
+  r.b = __floats2bfloat162_rn(x.z, x.w);
+  *reinterpret_cast<Bf16x4*>(p) = r;
+}
+
+template <class T>
+__global__ void __launch_bounds__(DEC_THREADS, 2)
+decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                   const float* __restrict__ log_lambda, float scale, float* __restrict__ state,
+                   const int32_t* __restrict__ slot, int pool_rows, T* __restrict__ o, int H,
+                   unsigned* err) {
+  __shared__ float s_q[DK];
+  __shared__ float s_k[DK];
+  __shared__ float4 s_part[DEC_RGROUPS][DEC_COLS];
+
+  const long long nh = blockIdx.x;  // n * H + h
+  const int n = (int)(nh / H);
+  const int h = (int)(nh % H);
+  const int tid = threadIdx.x;
+  const int c = tid % DEC_COLS;
+  const int r = tid / DEC_COLS;
+
+  const int row = slot ? slot[n] : n;
+  if (row < 0 || row >= pool_rows) {
+    if (tid == 0) raise_error(err, ERR_SHAPE);
+    return;
+  }
+  float4* S = reinterpret_cast<float4*>(state + ((long long)row * H + h) * (DK * DV));
+
+  float4 s[DEC_ROWS];
+#pragma unroll
+  for (int i = 0; i < DEC_ROWS; ++i) s[i] = __ldcs(S + (r + DEC_RGROUPS * i) * DEC_COLS + c);
+
+  if (tid < DK) {
+    s_q[tid] = scale * to_f(q[nh * DK + tid]);
+    s_k[tid] = to_f(k[nh * DK + tid]);
+  }
+  const float4 vv = load4(v + nh * DV + 4 * c);
+  const float lam = expf(log_lambda[h]);
+  __syncthreads();
+
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < DEC_ROWS; ++i) {
+    const int a = r + DEC_RGROUPS * i;
+    const float ka = s_k[a], qa = s_q[a];
+    float4 x = s[i];
+    x.x = fmaf(lam, x.x, ka * vv.x);
+    x.y = fmaf(lam, x.y, ka * vv.y);
+    x.z = fmaf(lam, x.z, ka * vv.z);
+    x.w = fmaf(lam, x.w, ka * vv.w);
+    __stcs(S + a * DEC_COLS + c, x);
+    acc.x = fmaf(qa, x.x, acc.x);
+    acc.y = fmaf(qa, x.y, acc.y);
+    acc.z = fmaf(qa, x.z, acc.z);
+    acc.w = fmaf(qa, x.w, acc.w);
+  }
+  s_part[r][c] = acc;
+  __syncthreads();
+  if (tid < DEC_COLS) {
+    float4 t = s_part[0][tid];
+#pragma unroll
+    for (int g = 1; g < DEC_RGROUPS; ++g) {
+      const float4 p = s_part[g][tid];
+      t.x += p.x;
+      t.y += p.y;
+      t.z += p.z;
+      t.w += p.w;
+    }
+    store4(o + nh * DV + 4 * tid, t);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_step(int dtype_f32, const void* q, const void* k, const void* v,
+                               const float* log_lambda, float scale, float* state,
+                               const int32_t* slot, int pool_rows, void* o, int N, int H,
+                               unsigned* err, cudaStream_t stream) {
+  const long long blocks = (long long)N * H;
+  if (blocks == 0) return cudaSuccess;
+  if (dtype_f32) {
+    decode_step_kernel<float><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
+        (const float*)q, (const float*)k, (const float*)v, log_lambda, scale, state, slot,
+        pool_rows, (float*)o, H, err);
+  } else {
+    decode_step_kernel<__nv_bfloat16><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
+        (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, log_lambda,
+        scale, state, slot, pool_rows, (__nv_bfloat16*)o, H, err);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gla

@@ -1,0 +1,63 @@
+"""Shared pieces of the GPU parity tests: inputs built on the host (so the oracle sees exactly
+the same values), the error metric, and per-sequence comparison."""
+import numpy as np
+
+import glasynth as gs
+
+BF16_TOL = 2e-2   # max |gpu - oracle| / rms(oracle), bf16 operands, fp32 state and accumulation
+F32_TOL = 1e-4    # same metric, all-fp32 mode
+
+
+def rel_err(x, ref):
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = np.sqrt(np.mean(ref ** 2)) if ref.size else 0.0
+    if ref.size == 0:
+        return 0.0
+    return float(np.max(np.abs(x - ref)) / max(rms, 1e-30))
+
+
+def host_chunk_inputs(seed, lengths, H, bf16, with_h0, packed, log_lambda=None, grad=False,
+                      qk_sigma=1 / np.sqrt(96), v_sigma=1.0):
+    """Numpy inputs in oracle layout ([T_total, H, d], cu_seqlens) plus the GPU layout shape."""
+    cu = gs.cu_seqlens_of(lengths)
+    Tt = int(cu[-1])
+    rnd = gs.bf16_round if bf16 else (lambda x: x)
+    d = {
+        "q": rnd(gs.normal(seed, 1, (Tt, H, 96), qk_sigma)),
+        "k": rnd(gs.normal(seed, 2, (Tt, H, 96), qk_sigma)),
+        "v": rnd(gs.normal(seed, 3, (Tt, H, 192), v_sigma)),
+        "h0": gs.normal(seed, 4, (len(lengths), H, 96, 192), 0.1) if with_h0 else None,
+        "log_lambda": gs.laplace_log_lambda(H) if log_lambda is None else
+        np.asarray(log_lambda, np.float32),
+        "cu": cu,
+    }
+    if grad:
+        d["dO"] = rnd(gs.normal(seed, 5, (Tt, H, 192)))
+        d["dhT"] = gs.normal(seed, 6, (len(lengths), H, 96, 192), 0.01)
+    if not packed:
+        assert len(set(lengths)) == 1
+    d["gpu_prefix"] = (Tt,) if packed else (len(lengths), lengths[0])
+    return d
+
+
+def to_device(d, bf16, packed):
+    import torch
+    dt = torch.bfloat16 if bf16 else torch.float32
+    out = {}
+    for name in ("q", "k", "v", "dO"):
+        if name in d:
+            x = torch.from_numpy(np.ascontiguousarray(d[name]))
+            x = x.reshape(d["gpu_prefix"] + tuple(d[name].shape[1:]))
+            out[name] = x.to("cuda").to(dt).contiguous()
+    for name in ("h0", "dhT"):
+        out[name] = None if d.get(name) is None else torch.from_numpy(d[name]).cuda()
+    out["log_lambda"] = torch.from_numpy(d["log_lambda"]).cuda()
+    out["cu_seqlens"] = torch.from_numpy(d["cu"]).cuda() if packed else None
+    return out
+
+
+def flat(t, packed):
+    """GPU tensor -> numpy [T_total, H, d] (fp64)."""
+    x = t.float().cpu().numpy().astype(np.float64)
+    return x if packed else x.reshape((-1,) + x.shape[2:])

@@ -1,0 +1,147 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports exactly what
+include/gla.h declares, and rejects bad arguments with the documented status before launching
+anything.  None of these calls touches a GPU (validation runs before any CUDA call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import linear_attention_recurrence_simple_gb300 as gla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gla.h")
+
+OK, NULL, SHAPE, DTYPE, ALIGN, UNSUP, WS = 0, -1, -2, -3, -4, -5, -6
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gla_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return gla.load_library()
+
+
+def test_header_declarations_match_binding():
+    assert _declared() == sorted(gla.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", gla.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (gla_[a-z_0-9]+)\b", out))
+    for name in _declared():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+    # nothing else with the gla_ prefix leaks out of the library
+    assert exported == set(_declared())
+
+
+def test_library_needs_no_cuda_runtime_soname():
+    out = subprocess.run(["readelf", "-d", gla.library_path()], capture_output=True, text=True,
+                         check=True).stdout
+    assert "libcudart" not in out  # static runtime: loads on hosts without a CUDA driver
+
+
+def test_status_strings(lib):
+    for code in (OK, NULL, SHAPE, DTYPE, ALIGN, UNSUP, WS, -7, -8):
+        s = gla.gla_status_string(code)
+        assert s.startswith("GLA_")
+    assert gla.gla_status_string(123) == "unknown gla_status"
+
+
+def test_workspace_bytes(lib):
+    assert gla.gla_workspace_bytes(0, 16) == 256
+    assert gla.gla_workspace_bytes(32, 16) == 512
+    assert gla.gla_workspace_bytes(65, 16) == 256 + 512
+    assert lib.gla_workspace_bytes(-1, 16) == 0
+
+
+# Fake, never-dereferenced device addresses: validation must reject before any use.
+A = 0x10000          # 16-byte aligned
+MIS = 0x10004        # misaligned
+
+
+def _fwd(lib, q=A, k=A, v=A, ll=A, h0=None, o=A, hT=None, cu=None, n=2, T=8, H=2, dk=96, dv=192,
+         dt=0, ws=None, wsb=0):
+    P = ctypes.c_void_p
+    return lib.gla_chunk_fwd(P(q), P(k), P(v), P(ll), P(h0), 0.1, P(o), P(hT), P(cu), n, T, H, dk,
+                             dv, dt, P(ws), wsb, None)
+
+
+def test_fwd_argument_errors(lib):
+    assert _fwd(lib, dt=7) == DTYPE
+    assert _fwd(lib, dk=64) == UNSUP
+    assert _fwd(lib, dv=128) == UNSUP
+    assert _fwd(lib, n=-1) == SHAPE
+    assert _fwd(lib, T=-3) == SHAPE
+    assert _fwd(lib, H=0) == SHAPE
+    assert _fwd(lib, q=None) == NULL
+    assert _fwd(lib, ll=None) == NULL
+    assert _fwd(lib, o=None) == NULL
+    assert _fwd(lib, k=MIS) == ALIGN
+    assert _fwd(lib, h0=MIS) == ALIGN
+    assert _fwd(lib, hT=MIS) == ALIGN
+    # packed calls need a big enough, aligned workspace
+    assert _fwd(lib, cu=A, n=3, T=20) == WS
+    assert _fwd(lib, cu=A, n=3, T=20, ws=A, wsb=16) == WS
+    assert _fwd(lib, cu=A, n=3, T=20, ws=MIS, wsb=4096) == ALIGN
+    assert _fwd(lib, cu=A + 2, n=3, T=20, ws=A, wsb=4096) == ALIGN
+    # empty work is accepted without touching a device
+    assert _fwd(lib, n=0) == OK
+    assert _fwd(lib, n=0, q=None, k=None, v=None, o=None, ll=None) == OK
+
+
+def test_bwd_argument_errors(lib):
+    P = ctypes.c_void_p
+
+    def bwd(q=A, dO=A, dq=A, dh0=None, dt=0, dk=96, n=2, cu=None, ws=None, wsb=0):
+        return lib.gla_chunk_bwd(P(q), P(A), P(A), P(A), None, 0.1, P(dO), None, P(dq), P(A), P(A),
+                                 P(dh0), P(cu), n, 8, 2, dk, 192, dt, P(ws), wsb, None)
+    assert bwd(dt=2) == DTYPE
+    assert bwd(dk=95) == UNSUP
+    assert bwd(n=-5) == SHAPE
+    assert bwd(dO=None) == NULL
+    assert bwd(dq=None) == NULL
+    assert bwd(dh0=MIS) == ALIGN
+    assert bwd(cu=A) == WS
+    assert bwd(n=0) == OK
+
+
+def test_decode_argument_errors(lib):
+    P = ctypes.c_void_p
+
+    def dec(q=A, state=A, slot=None, pool=4, N=4, H=2, dk=96, dt=0, o=A):
+        return lib.gla_decode_step(P(q), P(A), P(A), P(A), 0.1, P(state), P(slot), pool, P(o), N, H,
+                                   dk, 192, dt, None)
+    assert dec(dt=3) == DTYPE
+    assert dec(dk=32) == UNSUP
+    assert dec(N=-1) == SHAPE
+    assert dec(pool=3) == SHAPE          # identity slots need pool_rows >= N
+    assert dec(H=0) == SHAPE
+    assert dec(state=None) == NULL
+    assert dec(o=None) == NULL
+    assert dec(q=MIS) == ALIGN
+    assert dec(slot=A + 2) == ALIGN
+    assert dec(N=0) == OK
+
+
+def test_no_device_is_reported_not_faulted(lib):
+    """With valid arguments on a host without a usable sm_103 device, the call fails cleanly."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    assert _fwd(lib) == UNSUP
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 8, 2, 96)
+    v = torch.zeros(1, 8, 2, 192)
+    with pytest.raises(ValueError):
+        gla.gla_chunk_fwd(q, q, v, torch.zeros(2))

@@ -1,0 +1,217 @@
+"""GPU parity of gla_chunk_fwd / gla_chunk_bwd against the fp64 oracle, element by element.
+
+Small cases are compared in full, per sequence (each sequence against the oracle run on its own
+inputs); the full-size workloads are compared on sampled (sequence, head) units that the oracle
+computes one by one.  Bar: max |gpu - oracle| / rms(oracle) per output tensor <= 2e-2 in bf16
+mode (bf16 operands, fp32 accumulation and state), <= 1e-4 in fp32 mode."""
+import numpy as np
+import pytest
+
+import glasynth as gs
+import linear_attention_recurrence_simple_gb300 as gla
+import oracle
+from glasynth import workloads as wl
+from tests.gpu_helpers import BF16_TOL, F32_TOL, flat, host_chunk_inputs, rel_err, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    gla.load_library()
+    yield
+    assert gla.gla_get_device_error() == 0
+
+
+def _check_fwd(d, o_gpu, hT_gpu, packed, tol):
+    o_ref, hT_ref = oracle.fwd(d["q"], d["k"], d["v"], d["log_lambda"], d["scale"], h0=d["h0"],
+                               cu_seqlens=d["cu"])
+    o = flat(o_gpu, packed)
+    assert np.all(np.isfinite(o))
+    cu = d["cu"]
+    for n in range(len(cu) - 1):
+        a, b = cu[n], cu[n + 1]
+        if b > a:
+            e = rel_err(o[a:b], o_ref[a:b])
+            assert e <= tol, f"o of sequence {n} (len {b - a}): {e:.3e}"
+        if hT_gpu is not None:
+            e = rel_err(hT_gpu[n].cpu().numpy(), hT_ref[n])
+            assert e <= tol, f"hT of sequence {n}: {e:.3e}"
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 127, 128, 129, 255, 300])
+def test_fwd_fixed_length(bf16, T):
+    B, H = 2, 3
+    d = host_chunk_inputs(100 + T, [T] * B, H, bf16, with_h0=(T % 2 == 1), packed=False)
+    d["scale"] = float(gs.SCALE)
+    g = to_device(d, bf16, packed=False)
+    o, hT = gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], d["scale"], h0=g["h0"])
+    _check_fwd(d, o, hT, False, BF16_TOL if bf16 else F32_TOL)
+
+
+def test_fwd_tiny_workload_fp32():
+    """The tiny fp32 workload (B=1, T=256, H=2, lambda in {0.97, 0.999}, seed 0), all outputs."""
+    w = wl.tiny()
+    import torch
+    g = w.device_inputs()
+    o, hT = gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], w.scale)
+    torch.cuda.synchronize()
+    for h in range(w.H):
+        u = w.host_unit(0, h)
+        o_ref, hT_ref = oracle.fwd(u["q"], u["k"], u["v"], u["log_lambda"], w.scale)
+        assert rel_err(o[0, :, h].cpu().numpy(), o_ref[:, 0]) <= F32_TOL
+        assert rel_err(hT[0, h].cpu().numpy(), hT_ref[0, 0]) <= F32_TOL
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+@pytest.mark.parametrize("lens", [[5, 0, 200, 1, 128, 129, 77], [300], [0, 0], [1000, 3, 257]])
+def test_fwd_varlen_per_sequence(bf16, lens):
+    H = 2
+    d = host_chunk_inputs(7 + len(lens), lens, H, bf16, with_h0=True, packed=True)
+    d["scale"] = float(gs.SCALE)
+    g = to_device(d, bf16, packed=True)
+    o, hT = gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], d["scale"], h0=g["h0"],
+                              cu_seqlens=g["cu_seqlens"])
+    _check_fwd(d, o, hT, True, BF16_TOL if bf16 else F32_TOL)
+    # a length-0 sequence passes h0 through unchanged
+    for n, L in enumerate(lens):
+        if L == 0:
+            assert np.array_equal(hT[n].cpu().numpy(), d["h0"][n])
+
+
+def test_fwd_varlen_equals_fixed_bitwise():
+    """The same kernel on a packed batch of equal lengths and on the [B, T] layout gives the same
+    bits: the schedule changes which CTA runs when, never the arithmetic."""
+    import torch
+    lens = [200] * 4
+    d = host_chunk_inputs(5, lens, 2, True, with_h0=True, packed=True)
+    g = to_device(d, True, packed=True)
+    o1, h1 = gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], 0.1, h0=g["h0"],
+                               cu_seqlens=g["cu_seqlens"])
+    o2, h2 = gla.gla_chunk_fwd(g["q"].view(4, 200, 2, 96), g["k"].view(4, 200, 2, 96),
+                               g["v"].view(4, 200, 2, 192), g["log_lambda"], 0.1, h0=g["h0"])
+    assert torch.equal(o1.view(4, 200, 2, 192), o2) and torch.equal(h1, h2)
+
+
+def test_fwd_pages_decay_schedule_no_overflow():
+    """Half-life schedule 1..2048 tokens: head 0 has lambda = 0.5, so lambda^127 is 2^-127."""
+    H = 16
+    d = host_chunk_inputs(9, [384] * 2, H, True, with_h0=True, packed=False,
+                          log_lambda=gs.halflife_log_lambda(H))
+    d["scale"] = float(gs.SCALE)
+    g = to_device(d, True, packed=False)
+    o, hT = gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], d["scale"], h0=g["h0"])
+    _check_fwd(d, o, hT, False, BF16_TOL)
+
+
+def test_fwd_empty_and_degenerate():
+    import torch
+    ll = torch.zeros(2, device="cuda")
+    q = torch.zeros(3, 0, 2, 96, device="cuda", dtype=torch.bfloat16)
+    v = torch.zeros(3, 0, 2, 192, device="cuda", dtype=torch.bfloat16)
+    h0 = torch.randn(3, 2, 96, 192, device="cuda")
+    o, hT = gla.gla_chunk_fwd(q, q, v, ll, 0.1, h0=h0)
+    assert o.numel() == 0 and torch.equal(hT, h0)
+    o, hT = gla.gla_chunk_fwd(q, q, v, ll, 0.1)
+    assert torch.count_nonzero(hT) == 0
+    q = torch.zeros(0, 4, 2, 96, device="cuda", dtype=torch.bfloat16)
+    v = torch.zeros(0, 4, 2, 192, device="cuda", dtype=torch.bfloat16)
+    o, hT = gla.gla_chunk_fwd(q, q, v, ll, 0.1)
+    assert hT.shape == (0, 2, 96, 192)
+
+
+def _sampled_units(w, units, o, hT, tol):
+    import torch
+    torch.cuda.synchronize()
+    for n, h in units:
+        u = w.host_unit(n, h)
+        o_ref, hT_ref = oracle.fwd(u["q"], u["k"], u["v"], u["log_lambda"], w.scale, h0=u["h0"])
+        a, b = int(w.cu[n]), int(w.cu[n + 1])
+        og = (o[a:b, h] if w.packed else o[n, :, h]).float().cpu().numpy()
+        assert np.all(np.isfinite(og))
+        assert rel_err(og, o_ref[:, 0]) <= tol, (n, h)
+        assert rel_err(hT[n, h].cpu().numpy(), hT_ref[0, 0]) <= tol, (n, h)
+
+
+def test_fwd_layer_workload_sampled():
+    """B=8, T=2048, H=16 bf16 (the benchmark's forward launch), 6 sampled (sequence, head) units."""
+    w = wl.layer()
+    g = w.device_inputs()
+    o, hT = gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], w.scale)
+    _sampled_units(w, [(0, 0), (7, 15), (3, 5), (5, 10), (1, 1), (6, 14)], o, hT, BF16_TOL)
+
+
+def test_fwd_varlen_workload_sampled():
+    """32 packed sequences, lengths U[128, 16384], h0 ~ N(0, 0.1): longest, shortest, others."""
+    w = wl.varlen()
+    g = w.device_inputs()
+    o, hT = gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], w.scale, h0=g["h0"],
+                              cu_seqlens=g["cu_seqlens"])
+    lens = np.array(w.lengths)
+    units = [(int(lens.argmax()), 15), (int(lens.argmin()), 0), (0, 7), (31, 3), (17, 11)]
+    _sampled_units(w, units, o, hT, BF16_TOL)
+
+
+# ------------------------------------------------------------------------------------------
+# Backward
+# ------------------------------------------------------------------------------------------
+def _check_bwd(d, res, packed, tol):
+    dq, dk, dv, dh0 = res
+    ref = oracle.bwd(d["q"], d["k"], d["v"], d["log_lambda"], d["scale"], d["dO"], h0=d["h0"],
+                     dhT=d["dhT"], cu_seqlens=d["cu"])
+    cu = d["cu"]
+    got = [flat(dq, packed), flat(dk, packed), flat(dv, packed)]
+    for name, x, r in zip(("dq", "dk", "dv"), got, ref[:3]):
+        assert np.all(np.isfinite(x)), name
+        for n in range(len(cu) - 1):
+            a, b = cu[n], cu[n + 1]
+            if b > a:
+                e = rel_err(x[a:b], r[a:b])
+                assert e <= tol, f"{name} of sequence {n}: {e:.3e}"
+    for n in range(len(cu) - 1):
+        e = rel_err(dh0[n].cpu().numpy(), ref[3][n])
+        assert e <= tol, f"dh0 of sequence {n}: {e:.3e}"
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+@pytest.mark.parametrize("T", [1, 64, 129, 300])
+def test_bwd_fixed_length(bf16, T):
+    d = host_chunk_inputs(200 + T, [T] * 2, 2, bf16, with_h0=True, packed=False, grad=True)
+    d["scale"] = float(gs.SCALE)
+    g = to_device(d, bf16, packed=False)
+    res = gla.gla_chunk_bwd(g["q"], g["k"], g["v"], g["log_lambda"], g["dO"], d["scale"], h0=g["h0"],
+                            dhT=g["dhT"])
+    _check_bwd(d, res, False, BF16_TOL if bf16 else F32_TOL)
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_bwd_varlen_per_sequence(bf16):
+    lens = [70, 0, 1, 200, 128]
+    d = host_chunk_inputs(31, lens, 2, bf16, with_h0=True, packed=True, grad=True)
+    d["scale"] = float(gs.SCALE)
+    g = to_device(d, bf16, packed=True)
+    res = gla.gla_chunk_bwd(g["q"], g["k"], g["v"], g["log_lambda"], g["dO"], d["scale"], h0=g["h0"],
+                            dhT=g["dhT"], cu_seqlens=g["cu_seqlens"])
+    _check_bwd(d, res, True, BF16_TOL if bf16 else F32_TOL)
+    assert np.array_equal(res[3][1].cpu().numpy(), d["dhT"][1])
+
+
+def test_bwd_layer_workload_sampled():
+    """Backward at B=8, T=2048, H=16 bf16 with dO ~ N(0,1), dhT ~ N(0, 0.01); sampled units."""
+    import torch
+    w = wl.layer(with_grad=True)
+    g = w.device_inputs()
+    dq, dk, dv, dh0 = gla.gla_chunk_bwd(g["q"], g["k"], g["v"], g["log_lambda"], g["dO"], w.scale,
+                                        dhT=g["dhT"])
+    torch.cuda.synchronize()
+    for n, h in [(0, 0), (7, 15), (4, 8)]:
+        u = w.host_unit(n, h)
+        ref = oracle.bwd(u["q"], u["k"], u["v"], u["log_lambda"], w.scale, u["dO"], dhT=u["dhT"])
+        for x, r in zip((dq, dk, dv), ref[:3]):
+            xs = x[n, :, h].float().cpu().numpy()
+            assert np.all(np.isfinite(xs))
+            assert rel_err(xs, r[:, 0]) <= BF16_TOL, (n, h)
+        assert rel_err(dh0[n, h].cpu().numpy(), ref[3][0, 0]) <= BF16_TOL, (n, h)
