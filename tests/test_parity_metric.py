@@ -16,7 +16,7 @@ def test_exactly_rounded_answer_scores_zero(oracle_mod):
                           cu_seqlens=d["cu"])
     ob = gs.bf16_round(o.astype(np.float32)).astype(np.float64)
     assert rel_err(ob, o) > 1.5e-2            # the plain metric charges the format's rounding
-    assert rel_err(ob, o, bf16_out=True) == 0.0
+    assert rel_err(ob, o, bf16_out=True) <= 1e-7   # fp64 -> fp32 -> bf16 double rounding
 
 
 def test_allowance_does_not_hide_real_errors(oracle_mod):
