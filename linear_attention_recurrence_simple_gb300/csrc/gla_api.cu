@@ -10,8 +10,9 @@ cudaError_t launch_decode_step(int dtype_f32, const void* q, const void* k, cons
                                const float* log_lambda, float scale, float* state,
                                const int32_t* slot, int pool_rows, void* o, int N, int H,
                                unsigned* err, cudaStream_t stream);
-cudaError_t launch_simt_fwd(int dtype_f32, const ChunkArgs& a, cudaStream_t stream);
+cudaError_t launch_simt_fwd(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_simt_bwd(int dtype_f32, const ChunkArgs& a, cudaStream_t stream);
+cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream);
 }  // namespace gla
 
 namespace {
@@ -142,8 +143,8 @@ int gla_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
     if (cudaGetLastError() != cudaSuccess) return GLA_ERR_LAUNCH;
     a.order = order;
   }
-  if (dtype == GLA_F32) return to_status(gla::launch_simt_fwd(1, a, s));
-  return to_status(gla::launch_simt_fwd(0, a, s));
+  if (dtype == GLA_F32) return to_status(gla::launch_simt_fwd(a, s));
+  return to_status(gla::launch_tc_fwd(a, s));
 }
 
 int gla_chunk_bwd(const void* q, const void* k, const void* v, const float* log_lambda,

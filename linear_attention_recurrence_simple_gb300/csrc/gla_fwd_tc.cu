@@ -1,0 +1,528 @@
+// Chunked GLA forward on the 5th-generation tensor cores (bf16 operands, fp32 accumulation and
+// state): TMA -> shared memory -> tcgen05.mma -> tensor memory -> register epilogue.
+//
+// "Beyond the KV cache" (Laplace 3B on Trainium2), section "Challenge 1: Using native PyTorch on
+// Trainium for GLA": within each 128-token chunk the output is decay-masked linear attention plus
+// the contribution of the state carried from earlier chunks; the state then advances with the
+// decay compounded over the chunk, and only that advance is sequential.  Per chunk of L tokens
+// (local i, j; S = state before the chunk, s = scale):
+//     A   = Q K^T                                   (MMA1: 128 x 128 x 96)
+//     P   = s * lambda^(i-j) * A  for j <= i, else 0  (decay-mask warps, bf16)
+//     O   = P V  +  diag(s lambda^(i+1)) (Q S)       (MMA2: 128 x 64 x 128, MMA3: 128 x 64 x 96)
+//     S'  = lambda^L S + K^T Vt,  Vt_j = lambda^(L-1-j) v_j   (MMA4: 128(96) x 64 x 128)
+// The decay is never split into lambda^i * lambda^-j, so lambda = 0.5 cannot overflow.
+//
+// Work split: one CTA per (sequence, head, 64-column tile of d_v); the three tiles of a head
+// repeat the cheap Q K^T but share nothing else, which triples the CTA count for the 152 SMs.
+// Warp roles (384 threads, 1 CTA per SM):
+//   warp 0      TMA producer: Q, K, V chunk tiles into a 2-stage ring (72 KB per stage).
+//   warp 1      allocates 448 of 512 tensor-memory columns; one lane issues all tcgen05.mma.
+//   warps 2-3   scale the V tile rows by lambda^(L-1-j) (zero past the sequence end) into Vt.
+//   warps 4-7   decay mask: A (TMEM) -> P (bf16, shared memory, 128B-swizzled K-major).
+//   warps 8-11  epilogue: U (TMEM) -> S = lambda^L S + U in fp32 registers -> bf16 copy of S for
+//               the next chunk's Q S; O (TMEM, intra and inter parts) -> o (bf16, global).
+// Tensor memory: A cols [0,128), O double-buffered [128,256) and [256,384) (intra | inter),
+// U [384,448).  Every mbarrier wait is bounded (see gla_common.cuh); on a timeout the CTA
+// records GLA_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and returns.
+#include <cuda.h>
+
+#include "gla_common.cuh"
+
+namespace gla {
+namespace {
+
+constexpr int TN = 64;             // d_v columns per CTA
+constexpr int NTILE = DV / TN;     // 3
+constexpr int NTHREADS = 384;
+
+// ---- shared memory map (byte offsets from a 1024-byte aligned base) -------------------------
+constexpr uint32_t SZ_Q0 = 128 * 128;        // d_k 0..63, K-major, 128B swizzle
+constexpr uint32_t SZ_Q1 = 128 * 64;         // d_k 64..95, K-major, 64B swizzle
+constexpr uint32_t SZ_K = 2 * 128 * 128;     // d_k 0..63 | 64..127 (96..127 zero-filled by TMA)
+constexpr uint32_t SZ_V = 128 * 128;         // 64 d_v columns, 128B swizzle
+constexpr uint32_t ST_Q0 = 0;
+constexpr uint32_t ST_K = ST_Q0 + SZ_Q0;
+constexpr uint32_t ST_V = ST_K + SZ_K;
+constexpr uint32_t ST_Q1 = ST_V + SZ_V;
+constexpr uint32_t SZ_STAGE = ST_Q1 + SZ_Q1;  // 73728
+constexpr uint32_t OFF_VT = 2 * SZ_STAGE;
+constexpr uint32_t OFF_P = OFF_VT + SZ_V;
+constexpr uint32_t SZ_P = 2 * 128 * 128;
+constexpr uint32_t OFF_SP = OFF_P + SZ_P;
+constexpr uint32_t SZ_SP = 96 * 128;         // bf16 S tile: 96 rows (d_k) x 64 columns
+constexpr uint32_t OFF_PW = OFF_SP + 2 * SZ_SP;
+constexpr uint32_t OFF_BAR = OFF_PW + 2 * 129 * 4 + 8;
+enum {
+  B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
+  B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY = B_SP_FULL + 2, B_O_FULL = B_SP_EMPTY + 2,
+  B_O_EMPTY = B_O_FULL + 2, B_DRAIN = B_O_EMPTY + 2, NBAR
+};
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// ---- tensor memory columns ------------------------------------------------------------------
+constexpr uint32_t TM_A = 0, TM_O = 128, TM_U = 384, TMEM_COLS = 512;
+
+constexpr unsigned long long DRAIN_NS = 1000000000ull;  // drain waits on the exit path
+
+// ---- tcgen05 descriptors --------------------------------------------------------------------
+// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16 (bits 7-9, 10-12 = 1),
+// A/B major-ness (bit 15/16: 0 K-major, 1 MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+constexpr uint32_t LAYOUT_SW128 = 2, LAYOUT_SW64 = 4;
+
+// Shared-memory matrix descriptor: start address, leading / stride byte offsets (>> 4), fixed
+// version bits 46-47 = 1, swizzle layout in bits 61-63.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
+         ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
+}
+
+// K-major operand made of 128-row, 128B-swizzled panels of 64 bf16 along K: step kk (16 along K).
+__device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t base, int kk) {
+  return sdesc(base + (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u, 16, 1024, LAYOUT_SW128);
+}
+// Q: panel 0 (128B swizzle) for d_k 0..63, panel 1 (64B swizzle) for d_k 64..95.
+__device__ __forceinline__ uint64_t desc_q(uint32_t stage, int kk) {
+  if (kk < 4) return sdesc(stage + ST_Q0 + (uint32_t)kk * 32u, 16, 1024, LAYOUT_SW128);
+  return sdesc(stage + ST_Q1 + (uint32_t)(kk - 4) * 32u, 16, 512, LAYOUT_SW64);
+}
+// MN-major operand: rows along K (8-row groups 1024 B apart), 64-element MN blocks `lbo` apart.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t base, int kk, uint32_t lbo) {
+  return sdesc(base + (uint32_t)kk * 2048u, lbo, 1024, LAYOUT_SW128);
+}
+
+// ---- PTX wrappers ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+#define GLA_R8(b) "=r"(r[b]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), "=r"(r[b + 4]), "=r"(r[b + 5]), \
+                  "=r"(r[b + 6]), "=r"(r[b + 7])
+// 64 consecutive fp32 columns of this thread's tensor-memory lane (two 32-column loads, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : GLA_R8(0), GLA_R8(8), GLA_R8(16), GLA_R8(24), GLA_R8(32), GLA_R8(40), GLA_R8(48), GLA_R8(56)
+      : "r"(taddr), "r"(taddr + 32)
+      : "memory");
+}
+// 32 columns at each of two tensor-memory addresses of this thread's lane (one wait).
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : GLA_R8(0), GLA_R8(8), GLA_R8(16), GLA_R8(24), GLA_R8(32), GLA_R8(40), GLA_R8(48), GLA_R8(56)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+#undef GLA_R8
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Warp-uniform bounded wait: every lane waits (and so acquires), then the warp agrees.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const ChunkArgs& a, volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, a.wait_ns, abort_flag, a.err);
+  return __all_sync(0xffffffffu, ok);
+}
+
+struct TmaMaps {
+  CUtensorMap q0, q1, k, v;
+};
+
+__global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_constant__ TmaMaps maps, const ChunkArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (sbase - raw_u32);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
+  float* pw = reinterpret_cast<float*>(sm + OFF_PW);  // lambda^d, d = 0..128
+  float* pws = pw + 129;                               // scale * lambda^d
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int n, h, tile;
+  unit_of_block(a, NTILE, n, h, tile);
+  long long tb, te;
+  seq_range(a, n, tb, te);
+  const int len = (int)(te - tb);
+  const int nc = (len + CHUNK - 1) / CHUNK;
+  const int col0 = tile * TN;
+
+  if (threadIdx.x == 0) {
+    const uint32_t counts[NBAR] = {1, 1, 1, 1, 64, 1, 1, 128, 128, 1, 1, 128, 128, 128, 1, 1, 1, 1, 128, 128, 1};
+    for (int i = 0; i < NBAR; ++i) mbar_init(&bars[i], counts[i]);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_async_smem();
+  }
+  if (threadIdx.x < 129) {
+    const float ll = a.log_lambda[h];
+    const float p = threadIdx.x == 0 ? 1.f : expf((float)threadIdx.x * ll);
+    pw[threadIdx.x] = p;
+    pws[threadIdx.x] = a.scale * p;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.q0) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.q1) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.k) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&maps.v) : "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued[2] = {0, 0};
+      for (int c = 0; c < nc; ++c) {
+        const int s = c & 1;
+        const uint32_t ph = (uint32_t)(c >> 1) & 1u;
+        if (!mbar_wait(&bars[B_EMPTY + s], ph ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+        const uint32_t st = sbase + (uint32_t)s * SZ_STAGE;
+        uint64_t* full = &bars[B_FULL + s];
+        mbar_expect_tx(full, SZ_STAGE);
+        const int tok = (int)(tb + (long long)c * CHUNK);
+        tma_load_3d(st + ST_Q0, &maps.q0, full, 0, h, tok);
+        tma_load_3d(st + ST_Q1, &maps.q1, full, 64, h, tok);
+        tma_load_3d(st + ST_K, &maps.k, full, 0, h, tok);
+        tma_load_3d(st + ST_K + 16384u, &maps.k, full, 64, h, tok);
+        tma_load_3d(st + ST_V, &maps.v, full, col0, h, tok);
+        ++issued[s];
+      }
+      // Never leave a copy in flight into shared memory that is about to be released.
+      for (int s = 0; s < 2; ++s)
+        if (issued[s]) mbar_wait(&bars[B_FULL + s], (uint32_t)(issued[s] - 1) & 1u, DRAIN_NS, nullptr, a.err);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_QK = idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t ID_KV = idesc_bf16(128, TN, 1, 1);
+      constexpr uint32_t ID_O = idesc_bf16(128, TN, 0, 1);
+      const uint32_t vt = sbase + OFF_VT, pb = sbase + OFF_P;
+      for (int c = 0; c < nc; ++c) {
+        const int s = c & 1;
+        const uint32_t ph = (uint32_t)(c >> 1) & 1u, pc = (uint32_t)c & 1u;
+        const uint32_t st = sbase + (uint32_t)s * SZ_STAGE;
+        const int b = c & 1;  // S_prev buffer and O buffer of this chunk
+        const uint32_t fb = (uint32_t)(c >> 1) & 1u;
+        const uint32_t ocol = TM_O + (uint32_t)b * 128u;
+        if (!mbar_wait(&bars[B_FULL + s], ph, a.wait_ns, abort_flag, a.err)) break;
+        if (!mbar_wait(&bars[B_A_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+        tc_fence_after();
+        // MMA1  A = Q K^T
+        for (int kk = 0; kk < 6; ++kk)
+          umma(tmem + TM_A, desc_q(st, kk), desc_kmajor_sw128(st + ST_K, kk), ID_QK, kk > 0);
+        umma_commit(&bars[B_A_FULL]);
+        // MMA4  U = K^T Vt
+        if (!mbar_wait(&bars[B_VT_FULL], pc, a.wait_ns, abort_flag, a.err)) break;
+        if (!mbar_wait(&bars[B_U_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+        tc_fence_after();
+        for (int kk = 0; kk < 8; ++kk)
+          umma(tmem + TM_U, desc_mn_sw128(st + ST_K, kk, 16384), desc_mn_sw128(vt, kk, 8192), ID_KV, kk > 0);
+        umma_commit(&bars[B_U_FULL]);
+        umma_commit(&bars[B_VT_EMPTY]);
+        // MMA3  O_inter = Q S_prev
+        if (!mbar_wait(&bars[B_SP_FULL + b], fb, a.wait_ns, abort_flag, a.err)) break;
+        if (!mbar_wait(&bars[B_O_EMPTY + b], fb ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+        tc_fence_after();
+        const uint32_t spb = sbase + OFF_SP + (uint32_t)b * SZ_SP;
+        for (int kk = 0; kk < 6; ++kk)
+          umma(tmem + ocol + TN, desc_q(st, kk), desc_mn_sw128(spb, kk, 8192), ID_O, kk > 0);
+        umma_commit(&bars[B_SP_EMPTY + b]);
+        // MMA2  O_intra = P V
+        if (!mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag, a.err)) break;
+        tc_fence_after();
+        for (int kk = 0; kk < 8; ++kk)
+          umma(tmem + ocol, desc_kmajor_sw128(pb, kk), desc_mn_sw128(st + ST_V, kk, 8192), ID_O, kk > 0);
+        umma_commit(&bars[B_O_FULL + b]);
+        umma_commit(&bars[B_P_EMPTY]);
+        umma_commit(&bars[B_EMPTY + s]);
+      }
+      // All MMAs (and their barrier arrivals) finish before tensor memory is released.
+      umma_commit(&bars[B_DRAIN]);
+      mbar_wait(&bars[B_DRAIN], 0, DRAIN_NS, nullptr, a.err);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ Vt = lambda^(L-1-j) V
+    const int t = threadIdx.x - 64;  // 0..63
+    for (int c = 0; c < nc; ++c) {
+      const int s = c & 1;
+      const uint32_t ph = (uint32_t)(c >> 1) & 1u, pc = (uint32_t)c & 1u;
+      const int L = min(CHUNK, len - c * CHUNK);
+      if (!warp_wait(&bars[B_FULL + s], ph, a, abort_flag)) break;
+      if (!warp_wait(&bars[B_VT_EMPTY], pc ^ 1u, a, abort_flag)) break;
+      const uint8_t* vsrc = sm + s * SZ_STAGE + ST_V;
+      uint8_t* vdst = sm + OFF_VT;
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int j = t + 64 * rr;
+        const float f = j < L ? pw[L - 1 - j] : 0.f;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const int off = j * 128 + ((p ^ (j & 7)) << 4);
+          uint4 x = *reinterpret_cast<const uint4*>(vsrc + off);
+          uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 fv = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[e]));
+            w[e] = pack_bf16(fv.x * f, fv.y * f);
+          }
+          *reinterpret_cast<uint4*>(vdst + off) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(&bars[B_VT_FULL]);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ decay mask A -> P
+    const int i = ((warp & 3) << 5) + lane;  // query row = tensor-memory lane
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
+    const uint32_t pb = sbase + OFF_P;
+    for (int c = 0; c < nc; ++c) {
+      const uint32_t pc = (uint32_t)c & 1u;
+      const int L = min(CHUNK, len - c * CHUNK);
+      if (!warp_wait(&bars[B_A_FULL], pc, a, abort_flag)) break;
+      tc_fence_after();
+      if (!warp_wait(&bars[B_P_EMPTY], pc ^ 1u, a, abort_flag)) break;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[64];
+        tmem_ld64(lane_addr + TM_A + 64u * half, r);
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(&bars[B_A_EMPTY]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float pv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int jj = cc * 8 + e * 2 + u;
+              const int j = half * 64 + jj;
+              const int d = i - j;
+              const float f = (d >= 0 && i < L) ? pws[d >= 0 ? d : 0] : 0.f;
+              pv[u] = f * __uint_as_float(r[jj]);
+            }
+            w[e] = pack_bf16(pv[0], pv[1]);
+          }
+          st_shared_v4(pb + (uint32_t)half * 16384u + (uint32_t)i * 128u + (uint32_t)((cc ^ (i & 7)) << 4), w[0],
+                       w[1], w[2], w[3]);
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(&bars[B_P_FULL]);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const int r_ = ((warp & 3) << 5) + lane;  // d_k row of S and U; query row of O
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
+    const long long sbase_g = (((long long)n * a.H + h) * DK + r_) * DV + col0;
+    float S[TN];
+#pragma unroll
+    for (int x = 0; x < TN; ++x) S[x] = 0.f;
+    if (a.h0 && r_ < DK) {
+      const float4* src = reinterpret_cast<const float4*>(a.h0 + sbase_g);
+#pragma unroll
+      for (int x = 0; x < TN / 4; ++x) {
+        const float4 v4 = src[x];
+        S[4 * x] = v4.x;
+        S[4 * x + 1] = v4.y;
+        S[4 * x + 2] = v4.z;
+        S[4 * x + 3] = v4.w;
+      }
+    }
+    auto write_sprev = [&](int buf) {
+      if (r_ < DK) {
+        const uint32_t row = sbase + OFF_SP + (uint32_t)buf * SZ_SP + (uint32_t)r_ * 128u;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          st_shared_v4(row + (uint32_t)((cc ^ (r_ & 7)) << 4), pack_bf16(S[8 * cc], S[8 * cc + 1]),
+                       pack_bf16(S[8 * cc + 2], S[8 * cc + 3]), pack_bf16(S[8 * cc + 4], S[8 * cc + 5]),
+                       pack_bf16(S[8 * cc + 6], S[8 * cc + 7]));
+      }
+      fence_async_smem();
+      mbar_arrive(&bars[B_SP_FULL + buf]);
+    };
+    write_sprev(0);
+    bool aborted = false;
+    for (int c = 0; c < nc; ++c) {
+      const uint32_t pc = (uint32_t)c & 1u;
+      const int b = c & 1;
+      const uint32_t fb = (uint32_t)(c >> 1) & 1u;
+      const int L = min(CHUNK, len - c * CHUNK);
+      // S <- lambda^L S + U
+      if (!warp_wait(&bars[B_U_FULL], pc, a, abort_flag)) { aborted = true; break; }
+      tc_fence_after();
+      {
+        uint32_t u[64];
+        tmem_ld64(lane_addr + TM_U, u);
+        tc_fence_before();
+        mbar_arrive(&bars[B_U_EMPTY]);
+        const float lamL = pw[L];
+#pragma unroll
+        for (int x = 0; x < TN; ++x) S[x] = fmaf(lamL, S[x], __uint_as_float(u[x]));
+      }
+      if (c + 1 < nc) {
+        const int b2 = (c + 1) & 1;
+        const uint32_t f2 = (uint32_t)((c + 1) >> 1) & 1u;
+        if (!warp_wait(&bars[B_SP_EMPTY + b2], f2 ^ 1u, a, abort_flag)) { aborted = true; break; }
+        write_sprev(b2);
+      }
+      // o = O_intra + s lambda^(i+1) O_inter
+      if (!warp_wait(&bars[B_O_FULL + b], fb, a, abort_flag)) { aborted = true; break; }
+      tc_fence_after();
+      const uint32_t ocol = TM_O + (uint32_t)b * 128u;
+      const float f = pws[r_ < CHUNK - 1 ? r_ + 1 : CHUNK];
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
+                                            ((tb + (long long)c * CHUNK + r_) * a.H + h) * (long long)DV + col0);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t ov[64];  // [0, 32): intra columns, [32, 64): inter columns of this half
+        tmem_ld32x2(lane_addr + ocol + 32u * half, lane_addr + ocol + TN + 32u * half, ov);
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(&bars[B_O_EMPTY + b]);
+        }
+        if (r_ < L) {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int x = cc * 8 + e * 2;
+              w[e] = pack_bf16(fmaf(f, __uint_as_float(ov[32 + x]), __uint_as_float(ov[x])),
+                               fmaf(f, __uint_as_float(ov[33 + x]), __uint_as_float(ov[x + 1])));
+            }
+            dst[half * 4 + cc] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+    if (!aborted && a.hT && r_ < DK) {
+      float4* dst = reinterpret_cast<float4*>(a.hT + sbase_g);
+#pragma unroll
+      for (int x = 0; x < TN / 4; ++x) dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+  }
+}
+
+// ---- host side ------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 3-D view [T_total, H, d] of a token-major bf16 tensor; box = (box_x columns, 1 head, 128 tokens).
+bool make_map(CUtensorMap* m, const void* base, int d, int H, long long T, int box_x, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)CHUNK};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream) {
+  const long long blocks = (long long)a.n_seq * a.H * NTILE;
+  if (blocks == 0) return cudaSuccess;
+  const long long T_total = a.cu_seqlens ? (long long)a.T : (long long)a.n_seq * a.T;
+  TmaMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  if (T_total > 0) {
+    if (!make_map(&maps.q0, a.q, DK, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&maps.q1, a.q, DK, a.H, T_total, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map(&maps.k, a.k, DK, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&maps.v, a.v, DV, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  tc_fwd_kernel<<<(unsigned)blocks, NTHREADS, SMEM_BYTES, stream>>>(maps, a);
+  return cudaGetLastError();
+}
+
+}  // namespace gla

@@ -1,4 +1,4 @@
-// All-fp32 chunked GLA kernels on the CUDA cores (the GLA_F32 mode).
+// Chunked GLA kernels on the CUDA cores: the all-fp32 forward (GLA_F32 mode) and the backward.
 //
 // "Beyond the KV cache" (Laplace 3B on Trainium2), section "Challenge 1: Using native PyTorch on
 // Trainium for GLA": inside a chunk the output is masked linear attention plus the contribution
@@ -420,9 +420,8 @@ cudaError_t launch(K kernel, int tiles, size_t smem, const ChunkArgs& a, cudaStr
 
 }  // namespace
 
-cudaError_t launch_simt_fwd(int dtype_f32, const ChunkArgs& a, cudaStream_t stream) {
-  return dtype_f32 ? launch(simt_fwd_kernel<float>, FWD_TILES, FWD_SMEM, a, stream)
-                   : launch(simt_fwd_kernel<__nv_bfloat16>, FWD_TILES, FWD_SMEM, a, stream);
+cudaError_t launch_simt_fwd(const ChunkArgs& a, cudaStream_t stream) {
+  return launch(simt_fwd_kernel<float>, FWD_TILES, FWD_SMEM, a, stream);
 }
 
 cudaError_t launch_simt_bwd(int dtype_f32, const ChunkArgs& a, cudaStream_t stream) {
