@@ -7,22 +7,27 @@
 // decay compounded over the chunk, and only that advance is sequential.  Per chunk of L tokens
 // (local i, j; S = state before the chunk, s = scale):
 //     A   = Q K^T                                   (MMA1: 128 x 128 x 96)
-//     P   = s * lambda^(i-j) * A  for j <= i, else 0  (decay-mask warps, bf16)
+//     P   = s * lambda^(i-j) * A  for j <= i, else 0  (decay-mask warps, bf16, kept in TMEM)
 //     O   = P V  +  diag(s lambda^(i+1)) (Q S)       (MMA2: 128 x 64 x 128, MMA3: 128 x 64 x 96)
 //     S'  = lambda^L S + K^T Vt,  Vt_j = lambda^(L-1-j) v_j   (MMA4: 128(96) x 64 x 128)
 // The decay is never split into lambda^i * lambda^-j, so lambda = 0.5 cannot overflow.
+// Operands that carry the state are split into two bf16 terms, x = hi + lo with hi = bf16(x),
+// lo = bf16(x - hi), and multiplied twice into the same fp32 accumulator: the state copy S in
+// MMA3 and the decayed values Vt in MMA4.  That keeps about 16 significant bits on the state
+// path; only P is a single bf16 rounding.
 //
 // Work split: one CTA per (sequence, head, 64-column tile of d_v); the three tiles of a head
 // repeat the cheap Q K^T but share nothing else, which triples the CTA count for the 152 SMs.
 // Warp roles (384 threads, 1 CTA per SM):
 //   warp 0      TMA producer: Q, K, V chunk tiles into a 2-stage ring (72 KB per stage).
 //   warp 1      allocates 448 of 512 tensor-memory columns; one lane issues all tcgen05.mma.
-//   warps 2-3   scale the V tile rows by lambda^(L-1-j) (zero past the sequence end) into Vt.
-//   warps 4-7   decay mask: A (TMEM) -> P (bf16, shared memory, 128B-swizzled K-major).
-//   warps 8-11  epilogue: U (TMEM) -> S = lambda^L S + U in fp32 registers -> bf16 copy of S for
-//               the next chunk's Q S; O (TMEM, intra and inter parts) -> o (bf16, global).
+//   warps 2-3   scale the V tile rows by lambda^(L-1-j) (zero past the sequence end) into Vt
+//               (hi and lo parts).
+//   warps 4-7   decay mask: A (TMEM) -> P (bf16, back into TMEM as the A operand of MMA2).
+//   warps 8-11  epilogue: U (TMEM) -> S = lambda^L S + U in fp32 registers -> bf16 hi/lo copy of
+//               S for the next chunk's Q S; O (TMEM, intra and inter parts) -> o (bf16, global).
 // Tensor memory: A cols [0,128), O double-buffered [128,256) and [256,384) (intra | inter),
-// U [384,448).  Every mbarrier wait is bounded (see gla_common.cuh); on a timeout the CTA
+// U [384,448), P [448,512) (bf16 pairs).  Every mbarrier wait is bounded (see gla_common.cuh); on a timeout the CTA
 // records GLA_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and returns.
 #include <cuda.h>
 
@@ -45,11 +50,10 @@ constexpr uint32_t ST_K = ST_Q0 + SZ_Q0;
 constexpr uint32_t ST_V = ST_K + SZ_K;
 constexpr uint32_t ST_Q1 = ST_V + SZ_V;
 constexpr uint32_t SZ_STAGE = ST_Q1 + SZ_Q1;  // 73728
-constexpr uint32_t OFF_VT = 2 * SZ_STAGE;
-constexpr uint32_t OFF_P = OFF_VT + SZ_V;
-constexpr uint32_t SZ_P = 2 * 128 * 128;
-constexpr uint32_t OFF_SP = OFF_P + SZ_P;
-constexpr uint32_t SZ_SP = 96 * 128;         // bf16 S tile: 96 rows (d_k) x 64 columns
+constexpr uint32_t OFF_VT = 2 * SZ_STAGE;    // Vt hi, then Vt lo (SZ_V each)
+constexpr uint32_t OFF_SP = OFF_VT + 2 * SZ_V;
+constexpr uint32_t SZ_SPH = 96 * 128;        // bf16 S tile: 96 rows (d_k) x 64 columns
+constexpr uint32_t SZ_SP = 2 * SZ_SPH;       // one buffer: hi then lo
 constexpr uint32_t OFF_PW = OFF_SP + 2 * SZ_SP;
 constexpr uint32_t OFF_BAR = OFF_PW + 2 * 129 * 4 + 8;
 enum {
@@ -62,7 +66,7 @@ constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // ---- tensor memory columns ------------------------------------------------------------------
-constexpr uint32_t TM_A = 0, TM_O = 128, TM_U = 384, TMEM_COLS = 512;
+constexpr uint32_t TM_A = 0, TM_O = 128, TM_U = 384, TM_P = 448, TMEM_COLS = 512;
 
 constexpr unsigned long long DRAIN_NS = 1000000000ull;  // drain waits on the exit path
 
@@ -113,6 +117,14 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
       "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// Same, with the A operand (M lanes x K/2 columns of bf16 pairs) read from tensor memory.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -150,9 +162,29 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (
 }
 #undef GLA_R8
 
+// 32 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// x ~ hi + lo with hi = bf16(x), lo = bf16(x - hi); returns the two packed pairs.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = pack_bf16(x0 - hf.x, x1 - hf.y);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -248,7 +280,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_consta
       constexpr uint32_t ID_QK = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t ID_KV = idesc_bf16(128, TN, 1, 1);
       constexpr uint32_t ID_O = idesc_bf16(128, TN, 0, 1);
-      const uint32_t vt = sbase + OFF_VT, pb = sbase + OFF_P;
+      const uint32_t vt = sbase + OFF_VT;
       for (int c = 0; c < nc; ++c) {
         const int s = c & 1;
         const uint32_t ph = (uint32_t)(c >> 1) & 1u, pc = (uint32_t)c & 1u;
@@ -263,27 +295,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_consta
         for (int kk = 0; kk < 6; ++kk)
           umma(tmem + TM_A, desc_q(st, kk), desc_kmajor_sw128(st + ST_K, kk), ID_QK, kk > 0);
         umma_commit(&bars[B_A_FULL]);
-        // MMA4  U = K^T Vt
+        // MMA4  U = K^T Vt_hi + K^T Vt_lo
         if (!mbar_wait(&bars[B_VT_FULL], pc, a.wait_ns, abort_flag, a.err)) break;
         if (!mbar_wait(&bars[B_U_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
         tc_fence_after();
-        for (int kk = 0; kk < 8; ++kk)
-          umma(tmem + TM_U, desc_mn_sw128(st + ST_K, kk, 16384), desc_mn_sw128(vt, kk, 8192), ID_KV, kk > 0);
+        for (int part = 0; part < 2; ++part)
+          for (int kk = 0; kk < 8; ++kk)
+            umma(tmem + TM_U, desc_mn_sw128(st + ST_K, kk, 16384), desc_mn_sw128(vt + part * SZ_V, kk, 8192), ID_KV,
+                 part + kk > 0);
         umma_commit(&bars[B_U_FULL]);
         umma_commit(&bars[B_VT_EMPTY]);
-        // MMA3  O_inter = Q S_prev
+        // MMA3  O_inter = Q S_hi + Q S_lo
         if (!mbar_wait(&bars[B_SP_FULL + b], fb, a.wait_ns, abort_flag, a.err)) break;
         if (!mbar_wait(&bars[B_O_EMPTY + b], fb ^ 1u, a.wait_ns, abort_flag, a.err)) break;
         tc_fence_after();
         const uint32_t spb = sbase + OFF_SP + (uint32_t)b * SZ_SP;
-        for (int kk = 0; kk < 6; ++kk)
-          umma(tmem + ocol + TN, desc_q(st, kk), desc_mn_sw128(spb, kk, 8192), ID_O, kk > 0);
+        for (int part = 0; part < 2; ++part)
+          for (int kk = 0; kk < 6; ++kk)
+            umma(tmem + ocol + TN, desc_q(st, kk), desc_mn_sw128(spb + part * SZ_SPH, kk, 8192), ID_O, part + kk > 0);
         umma_commit(&bars[B_SP_EMPTY + b]);
-        // MMA2  O_intra = P V
+        // MMA2  O_intra = P V   (P from tensor memory: 8 columns of bf16 pairs per 16-wide K step)
         if (!mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag, a.err)) break;
         tc_fence_after();
         for (int kk = 0; kk < 8; ++kk)
-          umma(tmem + ocol, desc_kmajor_sw128(pb, kk), desc_mn_sw128(st + ST_V, kk, 8192), ID_O, kk > 0);
+          umma_ts(tmem + ocol, tmem + TM_P + 8u * kk, desc_mn_sw128(st + ST_V, kk, 8192), ID_O, kk > 0);
         umma_commit(&bars[B_O_FULL + b]);
         umma_commit(&bars[B_P_EMPTY]);
         umma_commit(&bars[B_EMPTY + s]);
@@ -303,7 +338,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_consta
       if (!warp_wait(&bars[B_FULL + s], ph, a, abort_flag)) break;
       if (!warp_wait(&bars[B_VT_EMPTY], pc ^ 1u, a, abort_flag)) break;
       const uint8_t* vsrc = sm + s * SZ_STAGE + ST_V;
-      uint8_t* vdst = sm + OFF_VT;
+      uint8_t* vhi = sm + OFF_VT;
+      uint8_t* vlo = sm + OFF_VT + SZ_V;
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         const int j = t + 64 * rr;
@@ -312,13 +348,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_consta
         for (int p = 0; p < 8; ++p) {
           const int off = j * 128 + ((p ^ (j & 7)) << 4);
           uint4 x = *reinterpret_cast<const uint4*>(vsrc + off);
-          uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          uint32_t w[4] = {x.x, x.y, x.z, x.w}, hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             float2 fv = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[e]));
-            w[e] = pack_bf16(fv.x * f, fv.y * f);
+            split_bf16x2(fv.x * f, fv.y * f, hi[e], lo[e]);
           }
-          *reinterpret_cast<uint4*>(vdst + off) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(vhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(vlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
       fence_async_smem();
@@ -328,7 +365,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_consta
     // ------------------------------------------------------------------ decay mask A -> P
     const int i = ((warp & 3) << 5) + lane;  // query row = tensor-memory lane
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
-    const uint32_t pb = sbase + OFF_P;
     for (int c = 0; c < nc; ++c) {
       const uint32_t pc = (uint32_t)c & 1u;
       const int L = min(CHUNK, len - c * CHUNK);
@@ -343,27 +379,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_consta
           tc_fence_before();
           mbar_arrive(&bars[B_A_EMPTY]);
         }
+        uint32_t w[32];
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint32_t w[4];
+        for (int e = 0; e < 32; ++e) {
+          float pv[2];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float pv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int jj = cc * 8 + e * 2 + u;
-              const int j = half * 64 + jj;
-              const int d = i - j;
-              const float f = (d >= 0 && i < L) ? pws[d >= 0 ? d : 0] : 0.f;
-              pv[u] = f * __uint_as_float(r[jj]);
-            }
-            w[e] = pack_bf16(pv[0], pv[1]);
+          for (int u = 0; u < 2; ++u) {
+            const int jj = 2 * e + u;
+            const int d = i - (half * 64 + jj);
+            const float f = (d >= 0 && i < L) ? pws[d >= 0 ? d : 0] : 0.f;
+            pv[u] = f * __uint_as_float(r[jj]);
           }
-          st_shared_v4(pb + (uint32_t)half * 16384u + (uint32_t)i * 128u + (uint32_t)((cc ^ (i & 7)) << 4), w[0],
-                       w[1], w[2], w[3]);
+          w[e] = pack_bf16(pv[0], pv[1]);
         }
+        tmem_st32(lane_addr + TM_P + 32u * half, w);
       }
-      fence_async_smem();
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
       mbar_arrive(&bars[B_P_FULL]);
     }
   } else {
@@ -389,10 +421,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_consta
       if (r_ < DK) {
         const uint32_t row = sbase + OFF_SP + (uint32_t)buf * SZ_SP + (uint32_t)r_ * 128u;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          st_shared_v4(row + (uint32_t)((cc ^ (r_ & 7)) << 4), pack_bf16(S[8 * cc], S[8 * cc + 1]),
-                       pack_bf16(S[8 * cc + 2], S[8 * cc + 3]), pack_bf16(S[8 * cc + 4], S[8 * cc + 5]),
-                       pack_bf16(S[8 * cc + 6], S[8 * cc + 7]));
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split_bf16x2(S[8 * cc + 2 * e], S[8 * cc + 2 * e + 1], hi[e], lo[e]);
+          const uint32_t off = (uint32_t)((cc ^ (r_ & 7)) << 4);
+          st_shared_v4(row + off, hi[0], hi[1], hi[2], hi[3]);
+          st_shared_v4(row + SZ_SPH + off, lo[0], lo[1], lo[2], lo[3]);
+        }
       }
       fence_async_smem();
       mbar_arrive(&bars[B_SP_FULL + buf]);
