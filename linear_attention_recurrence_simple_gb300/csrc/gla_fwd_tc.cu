@@ -18,17 +18,23 @@
 //
 // Work split: one CTA per (sequence, head, 64-column tile of d_v); the three tiles of a head
 // repeat the cheap Q K^T but share nothing else, which triples the CTA count for the 152 SMs.
+// Each tcgen05.mma costs about 100 cycles to issue regardless of N <= 128, so the kernel keeps
+// the instruction count low (28 per chunk: the hi/lo halves ride in one N = 128 MMA) and issues
+// from three threads in parallel, one per independent accumulator chain.
 // Warp roles (384 threads, 1 CTA per SM):
 //   warp 0      TMA producer: Q, K, V chunk tiles into a 2-stage ring (72 KB per stage).
-//   warp 1      allocates 448 of 512 tensor-memory columns; one lane issues all tcgen05.mma.
-//   warps 2-3   scale the V tile rows by lambda^(L-1-j) (zero past the sequence end) into Vt
-//               (hi and lo parts).
-//   warps 4-7   decay mask: A (TMEM) -> P (bf16, back into TMEM as the A operand of MMA2).
+//   warp 1      allocates tensor memory; one lane issues MMA1 (Q K^T).
+//   warp 2      one lane issues MMA4 (K^T [Vt_hi | Vt_lo]) and MMA3 (Q [S_hi | S_lo]).
+//   warp 3      one lane issues MMA2 (P V, P read from tensor memory).
+//   warps 4-7   per chunk: Vt = lambda^(L-1-j) V (hi and lo, zero past the sequence end), then
+//               the decay mask A (TMEM) -> P (bf16 pairs, back into TMEM).  A is released as
+//               soon as it is in registers, so the next chunk's Q K^T overlaps this one's P.
 //   warps 8-11  epilogue: U (TMEM) -> S = lambda^L S + U in fp32 registers -> bf16 hi/lo copy of
-//               S for the next chunk's Q S; O (TMEM, intra and inter parts) -> o (bf16, global).
-// Tensor memory: A cols [0,128), O double-buffered [128,256) and [256,384) (intra | inter),
-// U [384,448), P [448,512) (bf16 pairs).  Every mbarrier wait is bounded (see gla_common.cuh); on a timeout the CTA
-// records GLA_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and returns.
+//               S for the next chunk's Q S; O (TMEM: intra, inter hi, inter lo) -> o (bf16).
+// Tensor memory (512 columns): A [0,128), P [128,192), O_intra [192,256), O_inter hi|lo
+// [256,384), U hi|lo [384,512).  Every mbarrier wait is bounded (see gla_common.cuh); on a
+// timeout the CTA records GLA_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and
+// returns.
 #include <cuda.h>
 
 #include "gla_common.cuh"
@@ -58,15 +64,15 @@ constexpr uint32_t OFF_PW = OFF_SP + 2 * SZ_SP;
 constexpr uint32_t OFF_BAR = OFF_PW + 2 * 129 * 4 + 8;
 enum {
   B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
-  B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY = B_SP_FULL + 2, B_O_FULL = B_SP_EMPTY + 2,
-  B_O_EMPTY = B_O_FULL + 2, B_DRAIN = B_O_EMPTY + 2, NBAR
+  B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY = B_SP_FULL + 2, B_O_FULL = B_SP_EMPTY + 2, B_O_EMPTY,
+  B_DRAIN, NBAR = B_DRAIN + 3
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // ---- tensor memory columns ------------------------------------------------------------------
-constexpr uint32_t TM_A = 0, TM_O = 128, TM_U = 384, TM_P = 448, TMEM_COLS = 512;
+constexpr uint32_t TM_A = 0, TM_P = 128, TM_OI = 192, TM_OE = 256, TM_U = 384, TMEM_COLS = 512;
 
 constexpr unsigned long long DRAIN_NS = 1000000000ull;  // drain waits on the exit path
 
@@ -136,41 +142,46 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 
 #define GLA_R8(b) "=r"(r[b]), "=r"(r[b + 1]), "=r"(r[b + 2]), "=r"(r[b + 3]), "=r"(r[b + 4]), "=r"(r[b + 5]), \
                   "=r"(r[b + 6]), "=r"(r[b + 7])
-// 64 consecutive fp32 columns of this thread's tensor-memory lane (two 32-column loads, one wait).
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+// 16 columns at each of three tensor-memory addresses of this thread's lane (one wait).
+__device__ __forceinline__ void tmem_ld16x3(uint32_t ta, uint32_t tb, uint32_t tc, uint32_t (&r)[48]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%48];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%49];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%50];\n"
       "tcgen05.wait::ld.sync.aligned;"
-      : GLA_R8(0), GLA_R8(8), GLA_R8(16), GLA_R8(24), GLA_R8(32), GLA_R8(40), GLA_R8(48), GLA_R8(56)
-      : "r"(taddr), "r"(taddr + 32)
+      : GLA_R8(0), GLA_R8(8), GLA_R8(16), GLA_R8(24), GLA_R8(32), GLA_R8(40)
+      : "r"(ta), "r"(tb), "r"(tc)
       : "memory");
 }
-// 32 columns at each of two tensor-memory addresses of this thread's lane (one wait).
-__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (&r)[64]) {
+// 16 columns at each of two tensor-memory addresses of this thread's lane (one wait).
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : GLA_R8(0), GLA_R8(8), GLA_R8(16), GLA_R8(24)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+// 32 columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
       "tcgen05.wait::ld.sync.aligned;"
-      : GLA_R8(0), GLA_R8(8), GLA_R8(16), GLA_R8(24), GLA_R8(32), GLA_R8(40), GLA_R8(48), GLA_R8(56)
-      : "r"(ta), "r"(tb)
+      : GLA_R8(0), GLA_R8(8), GLA_R8(16), GLA_R8(24)
+      : "r"(ta)
       : "memory");
 }
 #undef GLA_R8
 
-// 32 consecutive 32-bit columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+// 16 consecutive 32-bit columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
-      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 
@@ -179,12 +190,45 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Packed two-wide fp32 arithmetic (one instruction for both lanes of a float2).
+__device__ __forceinline__ uint64_t f2u(float2 v) {
+  return (uint64_t)__float_as_uint(v.x) | ((uint64_t)__float_as_uint(v.y) << 32);
+}
+__device__ __forceinline__ float2 u2f(uint64_t u) {
+  return make_float2(__uint_as_float((uint32_t)u), __uint_as_float((uint32_t)(u >> 32)));
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2u(a)), "l"(f2u(b)));
+  return u2f(r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2u(a)), "l"(f2u(b)));
+  return u2f(r);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2u(a)), "l"(f2u(b)));
+  return u2f(r);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2u(a)), "l"(f2u(b)), "l"(f2u(c)));
+  return u2f(r);
+}
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ float2 ld_f2(const uint32_t* r, int x) {
+  return make_float2(__uint_as_float(r[x]), __uint_as_float(r[x + 1]));
+}
+
 // x ~ hi + lo with hi = bf16(x), lo = bf16(x - hi); returns the two packed pairs.
-__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = pack_bf16(x0 - hf.x, x1 - hf.y);
+__device__ __forceinline__ void split_bf16x2(float2 x, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x.x, x.y);
+  const float2 r = sub2(x, bf2_to_f2(hi));
+  lo = pack_bf16(r.x, r.y);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -222,8 +266,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_consta
   const int col0 = tile * TN;
 
   if (threadIdx.x == 0) {
-    const uint32_t counts[NBAR] = {1, 1, 1, 1, 64, 1, 1, 128, 128, 1, 1, 128, 128, 128, 1, 1, 1, 1, 128, 128, 1};
-    for (int i = 0; i < NBAR; ++i) mbar_init(&bars[i], counts[i]);
+    for (int i = 0; i < NBAR; ++i) {
+      uint32_t cnt = 1;
+      if (i == B_EMPTY || i == B_EMPTY + 1) cnt = 3;
+      if (i == B_O_FULL) cnt = 2;
+      if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_U_EMPTY || i == B_SP_FULL ||
+          i == B_SP_FULL + 1 || i == B_O_EMPTY)
+        cnt = 128;
+      mbar_init(&bars[i], cnt);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
@@ -274,125 +325,137 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_consta
         if (issued[s]) mbar_wait(&bars[B_FULL + s], (uint32_t)(issued[s] - 1) & 1u, DRAIN_NS, nullptr, a.err);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ MMA issuers
     if (lane == 0) {
-      constexpr uint32_t ID_QK = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t ID_KV = idesc_bf16(128, TN, 1, 1);
-      constexpr uint32_t ID_O = idesc_bf16(128, TN, 0, 1);
+      constexpr uint32_t ID_QK = idesc_bf16(128, 128, 0, 0);  // A = Q K^T
+      constexpr uint32_t ID_PV = idesc_bf16(128, TN, 0, 1);   // O_intra = P V
+      constexpr uint32_t ID_W = idesc_bf16(128, 2 * TN, 1, 1);  // U = K^T [Vt_hi | Vt_lo]
+      constexpr uint32_t ID_QS = idesc_bf16(128, 2 * TN, 0, 1); // O_inter = Q [S_hi | S_lo]
       const uint32_t vt = sbase + OFF_VT;
       for (int c = 0; c < nc; ++c) {
         const int s = c & 1;
         const uint32_t ph = (uint32_t)(c >> 1) & 1u, pc = (uint32_t)c & 1u;
         const uint32_t st = sbase + (uint32_t)s * SZ_STAGE;
-        const int b = c & 1;  // S_prev buffer and O buffer of this chunk
-        const uint32_t fb = (uint32_t)(c >> 1) & 1u;
-        const uint32_t ocol = TM_O + (uint32_t)b * 128u;
         if (!mbar_wait(&bars[B_FULL + s], ph, a.wait_ns, abort_flag, a.err)) break;
-        if (!mbar_wait(&bars[B_A_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
-        tc_fence_after();
-        // MMA1  A = Q K^T
-        for (int kk = 0; kk < 6; ++kk)
-          umma(tmem + TM_A, desc_q(st, kk), desc_kmajor_sw128(st + ST_K, kk), ID_QK, kk > 0);
-        umma_commit(&bars[B_A_FULL]);
-        // MMA4  U = K^T Vt_hi + K^T Vt_lo
-        if (!mbar_wait(&bars[B_VT_FULL], pc, a.wait_ns, abort_flag, a.err)) break;
-        if (!mbar_wait(&bars[B_U_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
-        tc_fence_after();
-        for (int part = 0; part < 2; ++part)
-          for (int kk = 0; kk < 8; ++kk)
-            umma(tmem + TM_U, desc_mn_sw128(st + ST_K, kk, 16384), desc_mn_sw128(vt + part * SZ_V, kk, 8192), ID_KV,
-                 part + kk > 0);
-        umma_commit(&bars[B_U_FULL]);
-        umma_commit(&bars[B_VT_EMPTY]);
-        // MMA3  O_inter = Q S_hi + Q S_lo
-        if (!mbar_wait(&bars[B_SP_FULL + b], fb, a.wait_ns, abort_flag, a.err)) break;
-        if (!mbar_wait(&bars[B_O_EMPTY + b], fb ^ 1u, a.wait_ns, abort_flag, a.err)) break;
-        tc_fence_after();
-        const uint32_t spb = sbase + OFF_SP + (uint32_t)b * SZ_SP;
-        for (int part = 0; part < 2; ++part)
+        if (warp == 1) {
+          if (!mbar_wait(&bars[B_A_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+          tc_fence_after();
           for (int kk = 0; kk < 6; ++kk)
-            umma(tmem + ocol + TN, desc_q(st, kk), desc_mn_sw128(spb + part * SZ_SPH, kk, 8192), ID_O, part + kk > 0);
-        umma_commit(&bars[B_SP_EMPTY + b]);
-        // MMA2  O_intra = P V   (P from tensor memory: 8 columns of bf16 pairs per 16-wide K step)
-        if (!mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag, a.err)) break;
-        tc_fence_after();
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + ocol, tmem + TM_P + 8u * kk, desc_mn_sw128(st + ST_V, kk, 8192), ID_O, kk > 0);
-        umma_commit(&bars[B_O_FULL + b]);
-        umma_commit(&bars[B_P_EMPTY]);
-        umma_commit(&bars[B_EMPTY + s]);
+            umma(tmem + TM_A, desc_q(st, kk), desc_kmajor_sw128(st + ST_K, kk), ID_QK, kk > 0);
+          umma_commit(&bars[B_A_FULL]);
+          umma_commit(&bars[B_EMPTY + s]);
+        } else if (warp == 3) {
+          if (!mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag, a.err)) break;
+          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+          tc_fence_after();
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + TM_OI, tmem + TM_P + 8u * kk, desc_mn_sw128(st + ST_V, kk, 8192), ID_PV, kk > 0);
+          umma_commit(&bars[B_P_EMPTY]);
+          umma_commit(&bars[B_O_FULL]);
+          umma_commit(&bars[B_EMPTY + s]);
+        } else {
+          if (!mbar_wait(&bars[B_VT_FULL], pc, a.wait_ns, abort_flag, a.err)) break;
+          if (!mbar_wait(&bars[B_U_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+          tc_fence_after();
+          for (int kk = 0; kk < 8; ++kk)
+            umma(tmem + TM_U, desc_mn_sw128(st + ST_K, kk, 16384), desc_mn_sw128(vt, kk, SZ_V), ID_W, kk > 0);
+          umma_commit(&bars[B_U_FULL]);
+          umma_commit(&bars[B_VT_EMPTY]);
+          const int b = c & 1;
+          const uint32_t fb = (uint32_t)(c >> 1) & 1u;
+          if (!mbar_wait(&bars[B_SP_FULL + b], fb, a.wait_ns, abort_flag, a.err)) break;
+          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+          tc_fence_after();
+          const uint32_t spb = sbase + OFF_SP + (uint32_t)b * SZ_SP;
+          for (int kk = 0; kk < 6; ++kk)
+            umma(tmem + TM_OE, desc_q(st, kk), desc_mn_sw128(spb, kk, SZ_SPH), ID_QS, kk > 0);
+          umma_commit(&bars[B_SP_EMPTY + b]);
+          umma_commit(&bars[B_O_FULL]);
+          umma_commit(&bars[B_EMPTY + s]);
+        }
       }
       // All MMAs (and their barrier arrivals) finish before tensor memory is released.
-      umma_commit(&bars[B_DRAIN]);
-      mbar_wait(&bars[B_DRAIN], 0, DRAIN_NS, nullptr, a.err);
+      uint64_t* drain = &bars[B_DRAIN + (warp - 1)];
+      umma_commit(drain);
+      mbar_wait(drain, 0, DRAIN_NS, nullptr, a.err);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ------------------------------------------------------------------ Vt = lambda^(L-1-j) V
-    const int t = threadIdx.x - 64;  // 0..63
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ Vt, then decay mask A -> P
+    const int i = threadIdx.x - 128;  // query row = tensor-memory lane; also the Vt row
+    const int q = warp & 3;           // this warp's lanes are rows 32q .. 32q + 31
+    const uint32_t lane_addr = tmem + ((uint32_t)(q << 5) << 16);
+    const float lam = pw[1];
+    const float2 lam2 = make_float2(lam * lam, lam * lam);
+    {  // P columns of groups past this warp's rows stay zero for the whole kernel: write them once
+      uint32_t z[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) z[e] = 0u;
+      for (int g = q + 1; g < 4; ++g) tmem_st16(lane_addr + TM_P + 16u * g, z);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    }
     for (int c = 0; c < nc; ++c) {
       const int s = c & 1;
       const uint32_t ph = (uint32_t)(c >> 1) & 1u, pc = (uint32_t)c & 1u;
       const int L = min(CHUNK, len - c * CHUNK);
       if (!warp_wait(&bars[B_FULL + s], ph, a, abort_flag)) break;
       if (!warp_wait(&bars[B_VT_EMPTY], pc ^ 1u, a, abort_flag)) break;
-      const uint8_t* vsrc = sm + s * SZ_STAGE + ST_V;
-      uint8_t* vhi = sm + OFF_VT;
-      uint8_t* vlo = sm + OFF_VT + SZ_V;
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int j = t + 64 * rr;
-        const float f = j < L ? pw[L - 1 - j] : 0.f;
+      {  // Vt row i = lambda^(L-1-i) v_i, split into hi and lo
+        const uint8_t* vsrc = sm + s * SZ_STAGE + ST_V;
+        uint8_t* vhi = sm + OFF_VT;
+        uint8_t* vlo = sm + OFF_VT + SZ_V;
+        const float fi = i < L ? pw[L - 1 - i] : 0.f;
+        const float2 f = make_float2(fi, fi);
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
-          const int off = j * 128 + ((p ^ (j & 7)) << 4);
-          uint4 x = *reinterpret_cast<const uint4*>(vsrc + off);
-          uint32_t w[4] = {x.x, x.y, x.z, x.w}, hi[4], lo[4];
+          const int off = i * 128 + ((p ^ (i & 7)) << 4);  // same permutation on both sides
+          const uint4 x = *reinterpret_cast<const uint4*>(vsrc + off);
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float2 fv = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[e]));
-            split_bf16x2(fv.x * f, fv.y * f, hi[e], lo[e]);
-          }
+          for (int e = 0; e < 4; ++e) split_bf16x2(mul2(bf2_to_f2(w[e]), f), hi[e], lo[e]);
           *reinterpret_cast<uint4*>(vhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(vlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
+        fence_async_smem();
+        mbar_arrive(&bars[B_VT_FULL]);
       }
-      fence_async_smem();
-      mbar_arrive(&bars[B_VT_FULL]);
-    }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------------ decay mask A -> P
-    const int i = ((warp & 3) << 5) + lane;  // query row = tensor-memory lane
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
-    for (int c = 0; c < nc; ++c) {
-      const uint32_t pc = (uint32_t)c & 1u;
-      const int L = min(CHUNK, len - c * CHUNK);
       if (!warp_wait(&bars[B_A_FULL], pc, a, abort_flag)) break;
-      tc_fence_after();
       if (!warp_wait(&bars[B_P_EMPTY], pc ^ 1u, a, abort_flag)) break;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[64];
-        tmem_ld64(lane_addr + TM_A + 64u * half, r);
-        if (half == 1) {
+      tc_fence_after();
+      // P row i = s lambda^(i-j) A_ij for j <= i and i < L, one 32-column group at a time, each
+      // stored straight back to tensor memory.  Below the diagonal group the factors come from one
+      // table read and a multiplicative chain toward larger i - j (the values only shrink, so an
+      // underflow to zero loses nothing); the diagonal group reads the table per element.
+      for (int g = 0; g <= q; ++g) {
+        uint32_t r[32];
+        tmem_ld32(lane_addr + TM_A + 32u * g, r);
+        if (g == q) {
           tc_fence_before();
           mbar_arrive(&bars[B_A_EMPTY]);
         }
-        uint32_t w[32];
+        uint32_t pkg[16];
+        const int d0 = i - 32 * g;  // i - j at the group's first column
+        if (g < q) {
+          // f = (pws[d0 - 2e], pws[d0 - 2e - 1]), from e = 15 down to e = 0
+          float2 f = i < L ? make_float2(pws[d0 - 30], pws[d0 - 31]) : make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float pv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int jj = 2 * e + u;
-            const int d = i - (half * 64 + jj);
-            const float f = (d >= 0 && i < L) ? pws[d >= 0 ? d : 0] : 0.f;
-            pv[u] = f * __uint_as_float(r[jj]);
+          for (int e = 15; e >= 0; --e) {
+            if (e < 15) f = mul2(f, lam2);
+            const float2 pv = mul2(f, ld_f2(r, 2 * e));
+            pkg[e] = pack_bf16(pv.x, pv.y);
           }
-          w[e] = pack_bf16(pv[0], pv[1]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int d = d0 - 2 * e;
+            const float f0 = (d >= 0 && i < L) ? pws[max(d, 0)] : 0.f;
+            const float f1 = (d >= 1 && i < L) ? pws[max(d - 1, 0)] : 0.f;
+            pkg[e] = pack_bf16(f0 * __uint_as_float(r[2 * e]), f1 * __uint_as_float(r[2 * e + 1]));
+          }
         }
-        tmem_st32(lane_addr + TM_P + 32u * half, w);
+        tmem_st16(lane_addr + TM_P + 16u * g, pkg);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
@@ -424,7 +487,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_consta
         for (int cc = 0; cc < 8; ++cc) {
           uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) split_bf16x2(S[8 * cc + 2 * e], S[8 * cc + 2 * e + 1], hi[e], lo[e]);
+          for (int e = 0; e < 4; ++e) split_bf16x2(make_float2(S[8 * cc + 2 * e], S[8 * cc + 2 * e + 1]), hi[e], lo[e]);
           const uint32_t off = (uint32_t)((cc ^ (r_ & 7)) << 4);
           st_shared_v4(row + off, hi[0], hi[1], hi[2], hi[3]);
           st_shared_v4(row + SZ_SPH + off, lo[0], lo[1], lo[2], lo[3]);
@@ -437,54 +500,56 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_fwd_kernel(const __grid_consta
     bool aborted = false;
     for (int c = 0; c < nc; ++c) {
       const uint32_t pc = (uint32_t)c & 1u;
-      const int b = c & 1;
-      const uint32_t fb = (uint32_t)(c >> 1) & 1u;
       const int L = min(CHUNK, len - c * CHUNK);
-      // S <- lambda^L S + U
+      // S <- lambda^L S + U_hi + U_lo
       if (!warp_wait(&bars[B_U_FULL], pc, a, abort_flag)) { aborted = true; break; }
       tc_fence_after();
-      {
-        uint32_t u[64];
-        tmem_ld64(lane_addr + TM_U, u);
-        tc_fence_before();
-        mbar_arrive(&bars[B_U_EMPTY]);
-        const float lamL = pw[L];
+      const float lamL = pw[L];
 #pragma unroll
-        for (int x = 0; x < TN; ++x) S[x] = fmaf(lamL, S[x], __uint_as_float(u[x]));
+      for (int qq = 0; qq < 4; ++qq) {
+        uint32_t u[32];  // [0, 16): hi columns, [16, 32): lo columns of this quarter
+        tmem_ld16x2(lane_addr + TM_U + 16u * qq, lane_addr + TM_U + TN + 16u * qq, u);
+#pragma unroll
+        for (int x = 0; x < 16; x += 2) {
+          const float2 sv = fma2(make_float2(lamL, lamL), make_float2(S[16 * qq + x], S[16 * qq + x + 1]),
+                                 add2(ld_f2(u, x), ld_f2(u, 16 + x)));
+          S[16 * qq + x] = sv.x;
+          S[16 * qq + x + 1] = sv.y;
+        }
       }
+      tc_fence_before();
+      mbar_arrive(&bars[B_U_EMPTY]);
       if (c + 1 < nc) {
         const int b2 = (c + 1) & 1;
         const uint32_t f2 = (uint32_t)((c + 1) >> 1) & 1u;
         if (!warp_wait(&bars[B_SP_EMPTY + b2], f2 ^ 1u, a, abort_flag)) { aborted = true; break; }
         write_sprev(b2);
       }
-      // o = O_intra + s lambda^(i+1) O_inter
-      if (!warp_wait(&bars[B_O_FULL + b], fb, a, abort_flag)) { aborted = true; break; }
+      // o = O_intra + s lambda^(i+1) (O_inter_hi + O_inter_lo)
+      if (!warp_wait(&bars[B_O_FULL], pc, a, abort_flag)) { aborted = true; break; }
       tc_fence_after();
-      const uint32_t ocol = TM_O + (uint32_t)b * 128u;
-      const float f = pws[r_ < CHUNK - 1 ? r_ + 1 : CHUNK];
+      const float f = pws[r_ + 1];
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
                                             ((tb + (long long)c * CHUNK + r_) * a.H + h) * (long long)DV + col0);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t ov[64];  // [0, 32): intra columns, [32, 64): inter columns of this half
-        tmem_ld32x2(lane_addr + ocol + 32u * half, lane_addr + ocol + TN + 32u * half, ov);
-        if (half == 1) {
+      for (int qq = 0; qq < 4; ++qq) {
+        uint32_t ov[48];  // 16 intra, 16 inter-hi, 16 inter-lo columns
+        tmem_ld16x3(lane_addr + TM_OI + 16u * qq, lane_addr + TM_OE + 16u * qq,
+                    lane_addr + TM_OE + TN + 16u * qq, ov);
+        if (qq == 3) {
           tc_fence_before();
-          mbar_arrive(&bars[B_O_EMPTY + b]);
+          mbar_arrive(&bars[B_O_EMPTY]);
+        }
+        uint32_t ob[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int x = 2 * e;
+          const float2 ovx = fma2(make_float2(f, f), add2(ld_f2(ov, 16 + x), ld_f2(ov, 32 + x)), ld_f2(ov, x));
+          ob[e] = pack_bf16(ovx.x, ovx.y);
         }
         if (r_ < L) {
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int x = cc * 8 + e * 2;
-              w[e] = pack_bf16(fmaf(f, __uint_as_float(ov[32 + x]), __uint_as_float(ov[x])),
-                               fmaf(f, __uint_as_float(ov[33 + x]), __uint_as_float(ov[x + 1])));
-            }
-            dst[half * 4 + cc] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          dst[2 * qq] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+          dst[2 * qq + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
         }
       }
     }
