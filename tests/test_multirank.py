@@ -1,0 +1,45 @@
+"""The benchmark's multi-rank host logic on CPU: two gloo ranks, barrier and max-over-ranks.
+
+Every GPU rank runs an independent replica of the workload (no collective on the data path); the
+only collectives are the timing barrier and the max reduction of the per-rank step time, and the
+whole-job value is the sum of the ranks' tokens over that max time."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    d = bench.Dist(torch)
+    d.init("gloo")
+    d.barrier()
+    t = d.max(1.5 + rank)            # rank 1 is the slow one
+    tokens_per_rank = 16384
+    value = tokens_per_rank * d.world / (t / 1e3)
+    out[rank] = (t, value, d.rank, d.world)
+    d.close()
+
+
+def test_two_rank_max_and_aggregate():
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    assert res[0][0] == res[1][0] == 2.5                       # max over ranks
+    assert res[0][1] == pytest.approx(2 * 16384 / 2.5e-3)      # summed tokens / slowest time
+    assert {res[0][2], res[1][2]} == {0, 1} and res[0][3] == 2
