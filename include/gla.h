@@ -121,6 +121,22 @@ int gla_decode_step(const void* q, const void* k, const void* v, const float* lo
                     float scale, float* state, const int32_t* slot, int pool_rows, void* o, int N,
                     int H, int dk, int dv, int dtype, gla_stream_t stream);
 
+/* The forward without any device allocation (no counterpart in the paper).  For callers that
+ * cannot allocate device memory per call, such as a serving engine whose memory is all handed to
+ * its own pool at start-up: same arguments and results as gla_chunk_fwd, minus the workspace.
+ * The longest-first schedule of packed sequences lives instead in a library-owned device array of
+ * GLA_NOALLOC_MAX_SEQS int32 (64 KB), kept by every GPU that loads the library until exit.
+ *   n_seq > GLA_NOALLOC_MAX_SEQS with cu_seqlens returns GLA_ERR_WORKSPACE (nothing launched).
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress); make
+ *   that first call before any stream capture on the device.
+ *   Calls share the array: calls that overlap on the GPU (unordered streams) race on it.  Calls
+ *   ordered on one stream do not; each rewrites the entries it uses before reading them. */
+#define GLA_NOALLOC_MAX_SEQS 16384
+int gla_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* log_lambda,
+                          const float* h0, float scale, void* o, float* hT,
+                          const int32_t* cu_seqlens, int n_seq, int T, int H, int dk, int dv,
+                          int dtype, gla_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the current device's sticky error word:
  * GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_SHAPE; GLA_ERR_LAUNCH if the stream itself failed. */
 int gla_get_device_error(gla_stream_t stream);

@@ -18,14 +18,17 @@ import torch
 
 __all__ = [
     "GlaError", "load_library", "library_path", "gla_workspace_bytes", "gla_chunk_fwd",
-    "gla_chunk_bwd", "gla_decode_step", "gla_get_device_error", "gla_set_wait_limit_ns",
+    "gla_chunk_bwd", "gla_decode_step", "gla_chunk_fwd_noalloc", "gla_get_device_error",
+    "gla_set_wait_limit_ns",
     "gla_status_string", "DK", "DV", "CHUNK", "EXPORTS",
 ]
 
 DK, DV, CHUNK = 96, 192, 128
 GLA_BF16, GLA_F32 = 0, 1
 EXPORTS = ("gla_workspace_bytes", "gla_chunk_fwd", "gla_chunk_bwd", "gla_decode_step",
-           "gla_get_device_error", "gla_set_wait_limit_ns", "gla_status_string")
+           "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
+           "gla_status_string")
+NOALLOC_MAX_SEQS = 16384
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libgla.so")
@@ -64,6 +67,8 @@ def load_library(build: bool = True):
         lib.gla_chunk_fwd.restype = I
         lib.gla_chunk_bwd.argtypes = [P, P, P, P, P, F, P, P, P, P, P, P, P, I, I, I, I, I, I, P, Z, P]
         lib.gla_chunk_bwd.restype = I
+        lib.gla_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, F, P, P, P, I, I, I, I, I, I, P]
+        lib.gla_chunk_fwd_noalloc.restype = I
         lib.gla_decode_step.argtypes = [P, P, P, P, F, P, P, I, P, I, I, I, I, I, P]
         lib.gla_decode_step.restype = I
         lib.gla_get_device_error.argtypes = [P]
@@ -181,6 +186,39 @@ def gla_chunk_fwd(q, k, v, log_lambda, scale=None, h0=None, cu_seqlens=None,
                                _ptr(hT), _ptr(cu_seqlens), n_seq, T, H, DK, DV, dt, _ptr(ws),
                                ws_bytes, _stream(dev))
     _check(rc, "gla_chunk_fwd")
+    return o, hT
+
+
+def gla_chunk_fwd_noalloc(q, k, v, log_lambda, scale=None, h0=None, cu_seqlens=None, o=None, hT=None):
+    """The forward with no device allocation inside the library and no workspace argument.
+
+    For callers that cannot allocate device memory per call (for instance a serving engine that
+    hands all device memory to its own pool at start-up): pass preallocated ``o`` and ``hT`` and
+    nothing is allocated here either.  The packed schedule lives in a 64 KB library-owned device
+    array, so ``cu_seqlens`` may describe at most ``NOALLOC_MAX_SEQS`` sequences, and calls that
+    overlap on the GPU (unordered streams) race on it.  Returns ``(o, hT)``."""
+    lib = load_library()
+    dev = q.device
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, q.dtype, dev)
+    _need(log_lambda, "log_lambda", torch.float32, dev)
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
+    n_seq, T, H = _layout(q, k, v, cu_seqlens)
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, dev)
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    _need(o, "o", v.dtype, dev)
+    if hT is not None:
+        _need(hT, "hT", torch.float32, dev)
+    s = float(DK ** -0.5) if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        rc = lib.gla_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), s,
+                                       _ptr(o), _ptr(hT), _ptr(cu_seqlens), n_seq, T, H, DK, DV, dt,
+                                       _stream(dev))
+    _check(rc, "gla_chunk_fwd_noalloc")
     return o, hT
 
 

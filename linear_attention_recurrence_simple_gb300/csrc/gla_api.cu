@@ -94,6 +94,19 @@ int to_status(cudaError_t e) { return e == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH
 
 }  // namespace
 
+namespace gla {
+// Internal accessors for the allocation-free entry point (gla_noalloc.cu); the entry points
+// above do not go through them.
+int current_device_state(unsigned** err, unsigned long long* wait_ns) {
+  int dev;
+  return device_state(&dev, err, wait_ns);
+}
+cudaError_t launch_lpt_order(const int32_t* cu_seqlens, int n_seq, int32_t* order, cudaStream_t stream) {
+  lpt_order_kernel<<<(n_seq + 255) / 256, 256, 0, stream>>>(cu_seqlens, n_seq, order);
+  return cudaGetLastError();
+}
+}  // namespace gla
+
 extern "C" {
 
 size_t gla_workspace_bytes(int n_seq, int H) {
