@@ -95,6 +95,12 @@ int gla_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
                   int n_seq, int T, int H, int dk, int dv, int dtype, void* workspace,
                   size_t ws_bytes, gla_stream_t stream);
 
+/* Bytes of device workspace that gla_chunk_bwd needs; n_seq, T, H as in that call, packed != 0
+ * when cu_seqlens is given, dtype the gla_dtype.  In bf16 mode the workspace holds fp32 partial
+ * sums of dq and dk (2 x T_total x H x 96 x 4 bytes) plus the packed schedule; in fp32 mode only
+ * the packed schedule (0 extra bytes for fixed-length calls). */
+size_t gla_bwd_workspace_bytes(int n_seq, int T, int H, int packed, int dtype);
+
 /* Chunked backward: gradients of L(o, hT) given dO = dL/do and dhT = dL/dhT.
  *   q, k, v, log_lambda, h0, scale, cu_seqlens, n_seq, T, H, dtype: as in gla_chunk_fwd
  *                (h0 NULL = zeros).
@@ -102,7 +108,10 @@ int gla_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
  *   dhT          [n_seq, H, 96, 192] fp32, or NULL for zero.
  *   dq, dk       outputs, layout of q; dv output, layout of v; all of dtype `dtype`.
  *   dh0          [n_seq, H, 96, 192] fp32 output, or NULL to skip.
- * The forward state is recomputed on chip; nothing from gla_chunk_fwd is needed. */
+ *   workspace    >= gla_bwd_workspace_bytes(n_seq, T, H, cu_seqlens != NULL, dtype) bytes.
+ * The forward state is recomputed on chip; nothing from gla_chunk_fwd is needed.  In bf16 mode dv
+ * and dh0 come from one reverse scan, dq and dk from scans over each 64-column tile of d_v whose
+ * fp32 partial sums meet in the workspace before the final bf16 rounding. */
 int gla_chunk_bwd(const void* q, const void* k, const void* v, const float* log_lambda,
                   const float* h0, float scale, const void* dO, const float* dhT, void* dq,
                   void* dk, void* dv, float* dh0, const int32_t* cu_seqlens, int n_seq, int T,

@@ -17,7 +17,8 @@ import threading
 import torch
 
 __all__ = [
-    "GlaError", "load_library", "library_path", "gla_workspace_bytes", "gla_chunk_fwd",
+    "GlaError", "load_library", "library_path", "gla_workspace_bytes", "gla_bwd_workspace_bytes",
+    "gla_chunk_fwd",
     "gla_chunk_bwd", "gla_decode_step", "gla_chunk_fwd_noalloc", "gla_get_device_error",
     "gla_set_wait_limit_ns",
     "gla_status_string", "DK", "DV", "CHUNK", "EXPORTS",
@@ -25,7 +26,8 @@ __all__ = [
 
 DK, DV, CHUNK = 96, 192, 128
 GLA_BF16, GLA_F32 = 0, 1
-EXPORTS = ("gla_workspace_bytes", "gla_chunk_fwd", "gla_chunk_bwd", "gla_decode_step",
+EXPORTS = ("gla_workspace_bytes", "gla_bwd_workspace_bytes", "gla_chunk_fwd", "gla_chunk_bwd",
+           "gla_decode_step",
            "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
            "gla_status_string")
 NOALLOC_MAX_SEQS = 16384
@@ -63,6 +65,8 @@ def load_library(build: bool = True):
                          ctypes.c_ulonglong)
         lib.gla_workspace_bytes.argtypes = [I, I]
         lib.gla_workspace_bytes.restype = Z
+        lib.gla_bwd_workspace_bytes.argtypes = [I, I, I, I, I]
+        lib.gla_bwd_workspace_bytes.restype = Z
         lib.gla_chunk_fwd.argtypes = [P, P, P, P, P, F, P, P, P, I, I, I, I, I, I, P, Z, P]
         lib.gla_chunk_fwd.restype = I
         lib.gla_chunk_bwd.argtypes = [P, P, P, P, P, F, P, P, P, P, P, P, P, I, I, I, I, I, I, P, Z, P]
@@ -143,6 +147,11 @@ def _layout(q, k, v, cu_seqlens):
 
 def gla_workspace_bytes(n_seq: int, H: int) -> int:
     return int(load_library().gla_workspace_bytes(int(n_seq), int(H)))
+
+
+def gla_bwd_workspace_bytes(n_seq: int, T: int, H: int, packed: bool, dtype_code: int) -> int:
+    return int(load_library().gla_bwd_workspace_bytes(int(n_seq), int(T), int(H), int(bool(packed)),
+                                                      int(dtype_code)))
 
 
 def _workspace(cu_seqlens, n_seq, H, device, workspace):
@@ -245,12 +254,15 @@ def gla_chunk_bwd(q, k, v, log_lambda, dO, scale=None, h0=None, dhT=None, cu_seq
     dk = torch.empty(k.shape, dtype=k.dtype, device=dev)
     dv = torch.empty(v.shape, dtype=v.dtype, device=dev)
     dh0 = torch.empty((n_seq, H, DK, DV), dtype=torch.float32, device=dev) if need_dh0 else None
-    ws, ws_bytes = _workspace(cu_seqlens, n_seq, H, dev, workspace)
+    need = gla_bwd_workspace_bytes(n_seq, T, H, cu_seqlens is not None, dt)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     s = float(DK ** -0.5) if scale is None else float(scale)
     with torch.cuda.device(dev):
         rc = lib.gla_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), s, _ptr(dO),
                                _ptr(dhT), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dh0), _ptr(cu_seqlens),
-                               n_seq, T, H, DK, DV, dt, _ptr(ws), ws_bytes, _stream(dev))
+                               n_seq, T, H, DK, DV, dt, _ptr(workspace), ws_bytes, _stream(dev))
     _check(rc, "gla_chunk_bwd")
     return dq, dk, dv, dh0
 

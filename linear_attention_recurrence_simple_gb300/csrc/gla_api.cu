@@ -13,6 +13,8 @@ cudaError_t launch_decode_step(int dtype_f32, const void* q, const void* k, cons
 cudaError_t launch_simt_fwd(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_simt_bwd(int dtype_f32, const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream);
+cudaError_t launch_tc_bwd(const ChunkArgs& a, float* acc_q, float* acc_k, cudaStream_t stream);
+size_t tc_bwd_acc_bytes(long long T_total, int H);
 }  // namespace gla
 
 namespace {
@@ -115,6 +117,17 @@ size_t gla_workspace_bytes(int n_seq, int H) {
   return 256 + (((size_t)n_seq * sizeof(int32_t) + 255) / 256) * 256;
 }
 
+size_t gla_bwd_workspace_bytes(int n_seq, int T, int H, int packed, int dtype) {
+  if (n_seq < 0 || T < 0 || H < 1) return 0;
+  size_t bytes = packed ? gla_workspace_bytes(n_seq, H) : 0;
+  if (dtype == GLA_BF16) {
+    const long long T_total = packed ? (long long)T : (long long)n_seq * T;
+    const size_t acc = ((gla::tc_bwd_acc_bytes(T_total, H) + 255) / 256) * 256;
+    bytes = (bytes ? bytes : 256) + 2 * acc;
+  }
+  return bytes;
+}
+
 int gla_chunk_fwd(const void* q, const void* k, const void* v, const float* log_lambda,
                   const float* h0, float scale, void* o, float* hT, const int32_t* cu_seqlens,
                   int n_seq, int T, int H, int dk, int dv, int dtype, void* workspace,
@@ -170,6 +183,9 @@ int gla_chunk_bwd(const void* q, const void* k, const void* v, const float* log_
                             &tokens);
   if (rc) return rc;
   if (n_seq == 0) return GLA_OK;
+  const size_t ws_need = gla_bwd_workspace_bytes(n_seq, T, H, cu_seqlens != nullptr, dtype);
+  if (ws_need > 0 && (!workspace || ws_bytes < ws_need)) return GLA_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return GLA_ERR_ALIGN;
   if (!log_lambda) return GLA_ERR_NULL;
   if (tokens > 0 && (!q || !k || !v || !dO || !dq || !dk || !dv)) return GLA_ERR_NULL;
   for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)dO,
@@ -202,13 +218,19 @@ int gla_chunk_bwd(const void* q, const void* k, const void* v, const float* log_
   a.err = err;
   a.wait_ns = wait_ns;
   cudaStream_t s = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
   if (cu_seqlens) {
-    int32_t* order = (int32_t*)((char*)workspace + 256);
+    int32_t* order = (int32_t*)(ws + 256);
     lpt_order_kernel<<<(n_seq + 255) / 256, 256, 0, s>>>(cu_seqlens, n_seq, order);
     if (cudaGetLastError() != cudaSuccess) return GLA_ERR_LAUNCH;
     a.order = order;
   }
-  return to_status(gla::launch_simt_bwd(dtype == GLA_F32, a, s));
+  if (dtype == GLA_F32) return to_status(gla::launch_simt_bwd(1, a, s));
+  const size_t head = cu_seqlens ? gla_workspace_bytes(n_seq, H) : 256;
+  const size_t acc = ((gla::tc_bwd_acc_bytes(tokens, H) + 255) / 256) * 256;
+  float* acc_q = (float*)(ws + head);
+  float* acc_k = (float*)(ws + head + acc);
+  return to_status(gla::launch_tc_bwd(a, acc_q, acc_k, s));
 }
 
 int gla_decode_step(const void* q, const void* k, const void* v, const float* log_lambda,

@@ -100,7 +100,7 @@ def test_fwd_argument_errors(lib):
 def test_bwd_argument_errors(lib):
     P = ctypes.c_void_p
 
-    def bwd(q=A, dO=A, dq=A, dh0=None, dt=0, dk=96, n=2, cu=None, ws=None, wsb=0):
+    def bwd(q=A, dO=A, dq=A, dh0=None, dt=0, dk=96, n=2, cu=None, ws=A, wsb=1 << 40):
         return lib.gla_chunk_bwd(P(q), P(A), P(A), P(A), None, 0.1, P(dO), None, P(dq), P(A), P(A),
                                  P(dh0), P(cu), n, 8, 2, dk, 192, dt, P(ws), wsb, None)
     assert bwd(dt=2) == DTYPE
@@ -109,8 +109,18 @@ def test_bwd_argument_errors(lib):
     assert bwd(dO=None) == NULL
     assert bwd(dq=None) == NULL
     assert bwd(dh0=MIS) == ALIGN
-    assert bwd(cu=A) == WS
+    assert bwd(cu=A, wsb=16) == WS
+    assert bwd(ws=None, wsb=0) == WS          # bf16 mode keeps fp32 partial sums in the workspace
+    assert bwd(ws=MIS) == ALIGN
     assert bwd(n=0) == OK
+
+
+def test_bwd_workspace_bytes(lib):
+    acc = 2 * 8 * 2048 * 16 * 96 * 4
+    assert gla.gla_bwd_workspace_bytes(8, 2048, 16, False, 0) == 256 + acc
+    assert gla.gla_bwd_workspace_bytes(8, 2048, 16, False, 1) == 0
+    assert gla.gla_bwd_workspace_bytes(3, 1000, 2, True, 1) == gla.gla_workspace_bytes(3, 2)
+    assert gla.gla_bwd_workspace_bytes(3, 1000, 2, True, 0) == gla.gla_workspace_bytes(3, 2) + 2 * 768000
 
 
 def test_decode_argument_errors(lib):

@@ -218,3 +218,17 @@ def test_bwd_layer_workload_sampled():
             assert np.all(np.isfinite(xs))
             assert rel_err(xs, r[:, 0], bf16_out=True) <= BF16_TOL, (n, h)
         assert rel_err(dh0[n, h].cpu().numpy(), ref[3][0, 0]) <= BF16_TOL, (n, h)
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_bwd_pages_decay_schedule(bf16):
+    """Backward with the half-life schedule (lambda from 0.5 to 0.9997) on ragged lengths."""
+    H = 16
+    lens = [384, 257]
+    d = host_chunk_inputs(91, lens, H, bf16, with_h0=True, packed=True, grad=True,
+                          log_lambda=gs.halflife_log_lambda(H))
+    d["scale"] = float(gs.SCALE)
+    g = to_device(d, bf16, packed=True)
+    res = gla.gla_chunk_bwd(g["q"], g["k"], g["v"], g["log_lambda"], g["dO"], d["scale"], h0=g["h0"],
+                            dhT=g["dhT"], cu_seqlens=g["cu_seqlens"])
+    _check_bwd(d, res, True, BF16_TOL if bf16 else F32_TOL)
