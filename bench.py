@@ -292,7 +292,7 @@ def bench_bwd(torch, gla, wl, dist, args, peaks):
                               + 128 * DV + 128 * DK + 128 * DK + 128 * DV + 4 * DK * DV)  # dk, dv scan
     res = {"workload": w.name, "tokens": tokens, "ms_per_step": region,
            "value": tokens * dist.world / (region / 1e3), "unit": "tokens/s",
-           "roofline": roofline(byts, flops, per_call / 1e3, peaks), "launches_per_step": 3}
+           "roofline": roofline(byts, flops, per_call / 1e3, peaks), "launches_per_step": 4}
     del g
     return res
 

@@ -51,6 +51,8 @@
 #include <cuda.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "gla_common.cuh"
 
 namespace gla {
@@ -770,8 +772,33 @@ cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream) {
   return launch_scan<MODE_FWD>(a.q, a.k, a.v, p, stream);
 }
 
+namespace {
+// Two side streams per device for the backward's independent scans (created on first use).
+constexpr int kMaxDevices = 64;
+std::mutex g_stream_mu;
+cudaStream_t g_side[kMaxDevices][2];
+
+cudaError_t side_streams(cudaStream_t (&out)[2]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_stream_mu);
+  for (int i = 0; i < 2; ++i) {
+    if (!g_side[dev][i]) {
+      e = cudaStreamCreateWithFlags(&g_side[dev][i], cudaStreamNonBlocking);
+      if (e != cudaSuccess) return e;
+    }
+    out[i] = g_side[dev][i];
+  }
+  return cudaSuccess;
+}
+}  // namespace
+
 // Backward in bf16: dv and dh0 directly; dq and dk through fp32 partial sums in acc_q / acc_k
-// (each tc_bwd_acc_bytes, 16-byte aligned), converted to bf16 at the end.
+// (each tc_bwd_acc_bytes, 16-byte aligned), rounded to bf16 at the end.  The three scans are
+// independent until that rounding: DV runs on the caller's stream, DK and DQ on two side streams
+// forked from it and joined back with events, so their CTAs fill each other's last waves.
 cudaError_t launch_tc_bwd(const ChunkArgs& a, float* acc_q, float* acc_k, cudaStream_t stream) {
   const long long T_total = a.cu_seqlens ? (long long)a.T : (long long)a.n_seq * a.T;
   const size_t acc = tc_bwd_acc_bytes(T_total, a.H);
@@ -780,18 +807,34 @@ cudaError_t launch_tc_bwd(const ChunkArgs& a, float* acc_q, float* acc_k, cudaSt
     if ((e = cudaMemsetAsync(acc_q, 0, acc, stream)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(acc_k, 0, acc, stream)) != cudaSuccess) return e;
   }
+  cudaStream_t side[2];
+  if ((e = side_streams(side)) != cudaSuccess) return e;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  for (int i = 0; i < 3; ++i)
+    if ((e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming)) != cudaSuccess) break;
+  if (e == cudaSuccess) e = cudaEventRecord(ev[0], stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side[0], ev[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side[1], ev[0], 0);
   ScanParams p;
   p.a = a;
   p.s0 = a.dhT;
-  p.s_out = a.hT;  // dh0
-  p.out = a.dv;
-  if ((e = launch_scan<MODE_DV>(a.k, a.q, a.dO, p, stream)) != cudaSuccess) return e;
   p.s_out = nullptr;
   p.out = acc_k;
-  if ((e = launch_scan<MODE_DK>(a.v, a.dO, a.q, p, stream)) != cudaSuccess) return e;
+  if (e == cudaSuccess) e = launch_scan<MODE_DK>(a.v, a.dO, a.q, p, side[0]);
   p.s0 = a.h0;
   p.out = acc_q;
-  if ((e = launch_scan<MODE_DQ>(a.dO, a.v, a.k, p, stream)) != cudaSuccess) return e;
+  if (e == cudaSuccess) e = launch_scan<MODE_DQ>(a.dO, a.v, a.k, p, side[1]);
+  p.s0 = a.dhT;
+  p.s_out = a.hT;  // dh0
+  p.out = a.dv;
+  if (e == cudaSuccess) e = launch_scan<MODE_DV>(a.k, a.q, a.dO, p, stream);
+  if (e == cudaSuccess) e = cudaEventRecord(ev[1], side[0]);
+  if (e == cudaSuccess) e = cudaEventRecord(ev[2], side[1]);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[1], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[2], 0);
+  for (int i = 0; i < 3; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
+  if (e != cudaSuccess) return e;
   const long long n4 = T_total * a.H * DK / 4;
   if (n4 > 0) {
     int dev = 0, sms = 152;
