@@ -32,19 +32,21 @@
 // lo = bf16(x - hi): the state copy in MMA3 and the weighted Z4 in MMA4, about 16 significant
 // bits on the state path; only P is a single bf16 rounding.
 //
-// Work split: one CTA per (sequence, head, 64-column tile of d_v), 384 threads, 1 CTA per SM.
-// Each tcgen05.mma costs about 100 cycles to issue regardless of N <= 128, so the kernel keeps
-// the instruction count low (hi/lo halves ride in one N = 128 MMA where N allows) and issues from
-// three threads in parallel, one per independent accumulator chain.  Warp roles:
+// Work split: one CTA per (sequence, head, 64-column tile of d_v), 512 threads, 1 CTA per SM.
+// One thread issues at most one tcgen05.mma (M = 128, K = 16) per ~135 cycles whatever N <= 128
+// is (measured), so the kernel keeps the instruction count low (hi/lo halves ride in one N = 128
+// MMA where N allows) and issues from three threads in parallel, one per accumulator chain.  Warp roles:
 //   warp 0      TMA producer: X, Y, Z chunk tiles into a 2-stage ring.
 //   warp 1      allocates tensor memory; one lane issues MMA1 (X Y^T).
 //   warp 2      one lane issues MMA4 (K4^T [Z4t_hi | Z4t_lo]) and MMA3 (X times the state copy).
 //   warp 3      one lane issues MMA2 (P Z, P read from tensor memory).
-//   warps 4-7   per chunk: the weighted Z4 (hi and lo, zero past the sequence end), then the decay
-//               mask A (TMEM) -> P (bf16 pairs, back into TMEM).  A is released as soon as it is
-//               in registers, so the next chunk's MMA1 overlaps this one's P.
+//   warps 4-7   decay mask A (TMEM) -> P (bf16 pairs, back into TMEM).  A is released as soon as
+//               it is in registers, so the next chunk's MMA1 overlaps this one's P.
 //   warps 8-11  epilogue: U (TMEM) -> state = lambda^L state + U in fp32 registers -> bf16 hi/lo
 //               copy for the next chunk's MMA3; O (TMEM) -> output row.
+//   warps 12-15 the weighted Z4 for MMA4 (hi and lo, zero past the sequence end).
+// Registers: the block launches with 128 per thread; warpgroups 0 and 3 give theirs back down
+// to 64 and 80 and warpgroups 1 and 2 (mask, epilogue) take 184 (setmaxnreg in each role).
 // Tensor memory (512 columns): A [0,128), P [128,192), then O_intra, O_inter and U [384,512).
 // Every mbarrier wait is bounded (see gla_common.cuh); on a timeout the CTA records
 // GLA_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and returns.
@@ -63,7 +65,11 @@ namespace {
 
 constexpr int TN = 64;             // d_v columns per CTA
 constexpr int NTILE = DV / TN;     // 3
-constexpr int NTHREADS = 384;
+constexpr int NTHREADS = 512;
+// Per-thread registers of the four warpgroups after setmaxnreg (launched with 128 each; the sum
+// times 128 threads must stay 65536): control (TMA + MMA issue), mask and epilogue, weighted Z4.
+constexpr int REG_CTRL = 64, REG_WIDE = 184, REG_Z4 = 80;
+static_assert(128 * (REG_CTRL + 2 * REG_WIDE + REG_Z4) == 65536, "register split");
 
 template <int MODE>
 struct Cfg {
@@ -294,6 +300,16 @@ struct ScanParams {
   void* out;        // FWD / DV: bf16 [T, H, 192];  DQ / DK: fp32 [T, H, 96] accumulator
 };
 
+// Per-warpgroup register budgets (every warp of the warpgroup executes the same instruction).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_constant__ TmaMaps maps, const ScanParams prm) {
   using C = Cfg<MODE>;
@@ -325,7 +341,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       uint32_t cnt = 1;
       if (i == B_EMPTY || i == B_EMPTY + 1) cnt = 3;
       if (i == B_O_FULL) cnt = 2;
-      if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_U_EMPTY || i == B_SP_FULL ||
+            if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_U_EMPTY || i == B_SP_FULL ||
           i == B_SP_FULL + 1 || i == B_O_EMPTY)
         cnt = 128;
       mbar_init(&bars[i], cnt);
@@ -358,6 +374,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
+    setmaxnreg_dec<REG_CTRL>();
     if (lane == 0) {
       int issued[2] = {0, 0};
       for (int it = 0; it < nc; ++it) {
@@ -390,6 +407,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     __syncwarp();
   } else if (warp < 4) {
     // ------------------------------------------------------------------ MMA issuers
+    setmaxnreg_dec<REG_CTRL>();
     if (lane == 0) {
       constexpr uint32_t ID_A = idesc_bf16(128, 128, 0, 0);           // A = X Y^T
       constexpr uint32_t ID_PZ = idesc_bf16(128, C::OW, 0, 1);        // O_intra = P Z
@@ -462,8 +480,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     }
     __syncwarp();
   } else if (warp < 8) {
-    // ------------------------------------------------------------------ weighted Z4, decay mask
-    const int i = threadIdx.x - 128;  // query row = tensor-memory lane; also the Z4 row
+    // ------------------------------------------------------------------ decay mask
+    setmaxnreg_inc<REG_WIDE>();
+    const int i = threadIdx.x - 128;  // query row = tensor-memory lane
     const int q = warp & 3;           // this warp's lanes are rows 32q .. 32q + 31
     const uint32_t lane_addr = tmem + ((uint32_t)(q << 5) << 16);
     const float lam = pw[1];
@@ -478,31 +497,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     }
     for (int it = 0; it < nc; ++it) {
       const int c = chunk_of(it);
-      const int s = it & 1;
-      const uint32_t ph = (uint32_t)(it >> 1) & 1u, pc = (uint32_t)it & 1u;
+      const uint32_t pc = (uint32_t)it & 1u;
       const int L = min(CHUNK, len - c * CHUNK);
-      if (!warp_wait(&bars[B_FULL + s], ph, a, abort_flag)) break;
-      if (!warp_wait(&bars[B_VT_EMPTY], pc ^ 1u, a, abort_flag)) break;
-      {  // Z4t row i = w_i z_i, split into hi and lo; w_i = 0 past the sequence end
-        const uint8_t* zsrc = sm + s * C::SZ_STAGE + C::ST_Z4;
-        uint8_t* zhi = sm + SMM::OFF_VT;
-        uint8_t* zlo = sm + SMM::OFF_VT + SZ_TILE64;
-        const float wi = i < L ? (C::REVERSE ? pws[i + 1] : pw[L - 1 - i]) : 0.f;
-        const float2 f = make_float2(wi, wi);
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const int off = i * 128 + ((p ^ (i & 7)) << 4);  // same permutation on both sides
-          const uint4 x = *reinterpret_cast<const uint4*>(zsrc + off);
-          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) split_bf16x2(mul2(bf2_to_f2(w[e]), f), hi[e], lo[e]);
-          *reinterpret_cast<uint4*>(zhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(zlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-        fence_async_smem();
-        mbar_arrive(&bars[B_VT_FULL]);
-      }
       if (!warp_wait(&bars[B_A_FULL], pc, a, abort_flag)) break;
       if (!warp_wait(&bars[B_P_EMPTY], pc ^ 1u, a, abort_flag)) break;
       tc_fence_after();
@@ -559,8 +555,42 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       tc_fence_before();
       mbar_arrive(&bars[B_P_FULL]);
     }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------------ weighted Z4 (hi and lo)
+    setmaxnreg_dec<REG_Z4>();
+    const int t = threadIdx.x - 384;  // row of the chunk
+    for (int it = 0; it < nc; ++it) {
+      const int c = chunk_of(it);
+      const int s = it & 1;
+      const uint32_t ph = (uint32_t)(it >> 1) & 1u, pc = (uint32_t)it & 1u;
+      const int L = min(CHUNK, len - c * CHUNK);
+      if (!warp_wait(&bars[B_FULL + s], ph, a, abort_flag)) break;
+      if (!warp_wait(&bars[B_VT_EMPTY], pc ^ 1u, a, abort_flag)) break;
+      const uint8_t* zsrc = sm + s * C::SZ_STAGE + C::ST_Z4;
+      uint8_t* zhi = sm + SMM::OFF_VT;
+      uint8_t* zlo = sm + SMM::OFF_VT + SZ_TILE64;
+      {  // Z4t row j = w_j z_j; w_j = 0 past the sequence end
+        const int j = t;
+        const float wj = j < L ? (C::REVERSE ? pws[j + 1] : pw[L - 1 - j]) : 0.f;
+        const float2 f = make_float2(wj, wj);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const int off = j * 128 + ((p ^ (j & 7)) << 4);  // same permutation on both sides
+          const uint4 x = *reinterpret_cast<const uint4*>(zsrc + off);
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split_bf16x2(mul2(bf2_to_f2(w[e]), f), hi[e], lo[e]);
+          *reinterpret_cast<uint4*>(zhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(zlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      fence_async_smem();
+      mbar_arrive(&bars[B_VT_FULL]);
+    }
   } else {
     // ------------------------------------------------------------------ epilogue
+    setmaxnreg_inc<REG_WIDE>();
     const int r_ = ((warp & 3) << 5) + lane;  // d_k row of the state and U; query row of O
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
     const long long sbase_g = (((long long)n * a.H + h) * DK + r_) * DV + col0;

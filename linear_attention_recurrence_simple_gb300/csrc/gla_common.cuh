@@ -82,9 +82,10 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 }
 
 // ------------------------------------------------------------------------------------------
-// mbarrier helpers (shared::cta).  Every wait is bounded: it polls try_wait, reads the global
-// timer every 64 polls, and gives up after `limit_ns` (or as soon as *abort is set), raising
-// ERR_TIMEOUT.  Returns true when the phase completed.
+// mbarrier helpers (shared::cta).  Every wait is bounded: it repeats try_wait (each may suspend
+// the thread for up to SUSPEND_NS), reads the global timer after each, and gives up after
+// `limit_ns` (or as soon as *abort is set), raising ERR_TIMEOUT.  Returns true when the phase
+// completed.
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -106,12 +107,16 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+// One try_wait: the hardware may suspend the thread until the phase completes, for at most
+// SUSPEND_NS, instead of returning at once; waiting threads then leave the issue slots and the
+// shared-memory pipe to the threads that work.
+constexpr uint32_t SUSPEND_NS = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(SUSPEND_NS)
       : "memory");
   return ok != 0;
 }
@@ -120,15 +125,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
                                           volatile int* abort_flag, unsigned* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
-      if (abort_flag && *abort_flag) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
-        if (abort_flag) *abort_flag = 1;
-        raise_error(err, ERR_TIMEOUT);
-        return false;
-      }
+    if (abort_flag && *abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      if (abort_flag) *abort_flag = 1;
+      raise_error(err, ERR_TIMEOUT);
+      return false;
     }
   }
 }
