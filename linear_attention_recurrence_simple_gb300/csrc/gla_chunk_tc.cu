@@ -279,7 +279,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // Warp-uniform bounded wait: every lane waits (and so acquires), then the warp agrees.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const ChunkArgs& a, volatile int* abort_flag) {
-  const bool ok = mbar_wait(bar, parity, a.wait_ns, abort_flag, a.err);
+  const bool ok = mbar_wait(bar, parity, a.wait_ns, abort_flag);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         const int c = chunk_of(it);
         const int s = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-        if (!mbar_wait(&bars[B_EMPTY + s], ph ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+        if (!mbar_wait(&bars[B_EMPTY + s], ph ^ 1u, a.wait_ns, abort_flag)) break;
         const uint32_t st = sbase + (uint32_t)s * C::SZ_STAGE;
         uint64_t* full = &bars[B_FULL + s];
         mbar_expect_tx(full, C::SZ_STAGE);
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       }
       // Never leave a copy in flight into shared memory that is about to be released.
       for (int s = 0; s < 2; ++s)
-        if (issued[s]) mbar_wait(&bars[B_FULL + s], (uint32_t)(issued[s] - 1) & 1u, DRAIN_NS, nullptr, a.err);
+        if (issued[s]) mbar_wait_drain(&bars[B_FULL + s], (uint32_t)(issued[s] - 1) & 1u, DRAIN_NS, a.err);
     }
     __syncwarp();
   } else if (warp < 4) {
@@ -419,9 +419,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         const int s = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u, pc = (uint32_t)it & 1u;
         const uint32_t st = sbase + (uint32_t)s * C::SZ_STAGE;
-        if (!mbar_wait(&bars[B_FULL + s], ph, a.wait_ns, abort_flag, a.err)) break;
+        if (!mbar_wait(&bars[B_FULL + s], ph, a.wait_ns, abort_flag)) break;
         if (warp == 1) {
-          if (!mbar_wait(&bars[B_A_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+          if (!mbar_wait(&bars[B_A_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
           tc_fence_after();
           for (int kk = 0; kk < C::K1; ++kk) {
             const uint64_t da = C::NARROW ? desc_k64(st + C::ST_X, kk) : desc_k96(st + C::ST_X, st + C::ST_X1, kk);
@@ -431,8 +431,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           umma_commit(&bars[B_A_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
         } else if (warp == 3) {
-          if (!mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag, a.err)) break;
-          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+          if (!mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag)) break;
+          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
           tc_fence_after();
           for (int kk = 0; kk < 8; ++kk)
             umma_ts(tmem + C::TM_OI, tmem + C::TM_P + 8u * kk,
@@ -441,8 +441,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           umma_commit(&bars[B_O_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
         } else {
-          if (!mbar_wait(&bars[B_VT_FULL], pc, a.wait_ns, abort_flag, a.err)) break;
-          if (!mbar_wait(&bars[B_U_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+          if (!mbar_wait(&bars[B_VT_FULL], pc, a.wait_ns, abort_flag)) break;
+          if (!mbar_wait(&bars[B_U_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
           tc_fence_after();
           for (int kk = 0; kk < 8; ++kk)
             umma(tmem + C::TM_U, desc_mn_sw128(st + C::ST_K4, kk, 16384), desc_mn_sw128(vt, kk, SZ_TILE64), ID_U,
@@ -451,8 +451,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           umma_commit(&bars[B_VT_EMPTY]);
           const int b = it & 1;
           const uint32_t fb = (uint32_t)(it >> 1) & 1u;
-          if (!mbar_wait(&bars[B_SP_FULL + b], fb, a.wait_ns, abort_flag, a.err)) break;
-          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag, a.err)) break;
+          if (!mbar_wait(&bars[B_SP_FULL + b], fb, a.wait_ns, abort_flag)) break;
+          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
           tc_fence_after();
           const uint32_t spb = sbase + SMM::OFF_SP + (uint32_t)b * SZ_SP;
           if (C::NARROW) {
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       // All MMAs (and their barrier arrivals) finish before tensor memory is released.
       uint64_t* drain = &bars[B_DRAIN + (warp - 1)];
       umma_commit(drain);
-      mbar_wait(drain, 0, DRAIN_NS, nullptr, a.err);
+      mbar_wait_drain(drain, 0, DRAIN_NS, a.err);
     }
     __syncwarp();
   } else if (warp < 8) {
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         const int j = t;
         const float wj = j < L ? (C::REVERSE ? pws[j + 1] : pw[L - 1 - j]) : 0.f;
         const float2 f = make_float2(wj, wj);
-#pragma unroll
+#pragma unroll 1
         for (int p = 0; p < 8; ++p) {
           const int off = j * 128 + ((p ^ (j & 7)) << 4);  // same permutation on both sides
           const uint4 x = *reinterpret_cast<const uint4*>(zsrc + off);
@@ -624,36 +624,41 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       fence_async_smem();
       mbar_arrive(&bars[B_SP_FULL + buf]);
     };
-    write_sprev(0);
+    // Iteration it: the state update of chunk it, the state copy for chunk it + 1, the output rows
+    // of chunk it (it = -1 only writes the copy of the initial state).  One site for each part
+    // keeps the code small.
     bool aborted = false;
-    for (int it = 0; it < nc; ++it) {
-      const int c = chunk_of(it);
+    for (int it = -1; it < nc; ++it) {
       const uint32_t pc = (uint32_t)it & 1u;
+      const int c = it >= 0 ? chunk_of(it) : 0;
       const int L = min(CHUNK, len - c * CHUNK);
-      // state <- lambda^L state + U_hi + U_lo
-      if (!warp_wait(&bars[B_U_FULL], pc, a, abort_flag)) { aborted = true; break; }
-      tc_fence_after();
-      const float lamL = pw[L];
+      if (it >= 0) {
+        // state <- lambda^L state + U_hi + U_lo
+        if (!warp_wait(&bars[B_U_FULL], pc, a, abort_flag)) { aborted = true; break; }
+        tc_fence_after();
+        const float lamL = pw[L];
 #pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
-        uint32_t u[32];  // [0, 16): hi columns, [16, 32): lo columns of this quarter
-        tmem_ld16x2(lane_addr + C::TM_U + 16u * qq, lane_addr + C::TM_U + TN + 16u * qq, u);
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t u[32];  // [0, 16): hi columns, [16, 32): lo columns of this quarter
+          tmem_ld16x2(lane_addr + C::TM_U + 16u * qq, lane_addr + C::TM_U + TN + 16u * qq, u);
 #pragma unroll
-        for (int x = 0; x < 16; x += 2) {
-          const float2 sv = fma2(make_float2(lamL, lamL), make_float2(S[16 * qq + x], S[16 * qq + x + 1]),
-                                 add2(ld_f2(u, x), ld_f2(u, 16 + x)));
-          S[16 * qq + x] = sv.x;
-          S[16 * qq + x + 1] = sv.y;
+          for (int x = 0; x < 16; x += 2) {
+            const float2 sv = fma2(make_float2(lamL, lamL), make_float2(S[16 * qq + x], S[16 * qq + x + 1]),
+                                   add2(ld_f2(u, x), ld_f2(u, 16 + x)));
+            S[16 * qq + x] = sv.x;
+            S[16 * qq + x + 1] = sv.y;
+          }
         }
+        tc_fence_before();
+        mbar_arrive(&bars[B_U_EMPTY]);
       }
-      tc_fence_before();
-      mbar_arrive(&bars[B_U_EMPTY]);
       if (it + 1 < nc) {
         const int b2 = (it + 1) & 1;
         const uint32_t f2 = (uint32_t)((it + 1) >> 1) & 1u;
         if (!warp_wait(&bars[B_SP_EMPTY + b2], f2 ^ 1u, a, abort_flag)) { aborted = true; break; }
         write_sprev(b2);
       }
+      if (it < 0) continue;
       // out row = O_intra + g * O_inter;  g = s lambda^(i+1) (forward scans) or lambda^(L-1-i)
       if (!warp_wait(&bars[B_O_FULL], pc, a, abort_flag)) { aborted = true; break; }
       tc_fence_after();
@@ -716,6 +721,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
   }
+  if (threadIdx.x == 0 && *abort_flag) raise_error(a.err, ERR_TIMEOUT);
 }
 
 // fp32 partial-sum accumulators [T, H, 96] -> bf16 outputs (dq and dk in one pass).

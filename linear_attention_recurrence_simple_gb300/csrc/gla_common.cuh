@@ -84,8 +84,7 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 // ------------------------------------------------------------------------------------------
 // mbarrier helpers (shared::cta).  Every wait is bounded: it repeats try_wait (each may suspend
 // the thread for up to SUSPEND_NS), reads the global timer after each, and gives up after
-// `limit_ns` (or as soon as *abort is set), raising ERR_TIMEOUT.  Returns true when the phase
-// completed.
+// `limit_ns` (or as soon as *abort is set).
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -121,17 +120,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Bounded wait of a CTA role.  It gives up once `limit_ns` has passed since its first failed
+// try_wait, or as soon as another role has given up (*abort set), and then sets *abort and returns
+// false; the kernel reports ERR_TIMEOUT once, at exit, when *abort is set.  Kept small because
+// every wait site is inlined into the warp-specialised kernels, whose speed depends on their code
+// fitting the instruction caches.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns,
-                                          volatile int* abort_flag, unsigned* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (abort_flag && *abort_flag) return false;
-    if (global_timer_ns() - t0 > limit_ns) {
-      if (abort_flag) *abort_flag = 1;
-      raise_error(err, ERR_TIMEOUT);
+                                          volatile int* abort) {
+  unsigned long long t0 = ~0ull;
+  while (!mbar_try_wait(bar, parity)) {
+    const unsigned long long t = global_timer_ns();
+    if (t0 == ~0ull) {
+      t0 = t;
+    } else if (*abort || t - t0 > limit_ns) {
+      *abort = 1;
       return false;
+    }
+  }
+  return true;
+}
+
+// Bounded wait on the exit path (no abort flag): raises ERR_TIMEOUT itself.
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity, unsigned long long limit_ns,
+                                                unsigned* err) {
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) {
+      raise_error(err, ERR_TIMEOUT);
+      return;
     }
   }
 }
