@@ -122,31 +122,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 }
 constexpr uint32_t LAYOUT_SW128 = 2, LAYOUT_SW64 = 4;
 
-// Shared-memory matrix descriptor: start address, leading / stride byte offsets (>> 4), fixed
-// version bits 46-47 = 1, swizzle layout in bits 61-63.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
-         ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
+// Shared-memory matrix descriptor, kept as its two 32-bit words: lo = start address >> 4
+// (bits 0-13) | leading byte offset >> 4 (bits 16-29); hi = stride byte offset >> 4 | the fixed
+// version bit (bit 46 of the descriptor) | swizzle layout (bits 61-63).
+// Stepping along K or to another panel only adds (bytes >> 4) to lo, so each MMA of a K loop costs
+// one integer add in the issuing thread (the issue rate of a thread depends on that work).
+struct SDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  return {((saddr & 0x3FFFFu) >> 4) | (((lbo & 0x3FFFFu) >> 4) << 16),
+          ((sbo & 0x3FFFFu) >> 4) | (1u << 14) | (layout << 29)};
 }
-
-// K-major operand made of 128-row, 128B-swizzled panels of 64 bf16 along K: step kk (16 along K).
-__device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t base, int kk) {
-  return sdesc(base + (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u, 16, 1024, LAYOUT_SW128);
-}
-// A 96-wide K-major tile stored as a 128B-swizzled panel (columns 0..63) at p0 and a 64B-swizzled
-// panel (columns 64..95) at p1: K step kk (16 columns).
-__device__ __forceinline__ uint64_t desc_k96(uint32_t p0, uint32_t p1, int kk) {
-  if (kk < 4) return sdesc(p0 + (uint32_t)kk * 32u, 16, 1024, LAYOUT_SW128);
-  return sdesc(p1 + (uint32_t)(kk - 4) * 32u, 16, 512, LAYOUT_SW64);
-}
-// A 64-wide K-major tile (one 128B-swizzled panel): K step kk.
-__device__ __forceinline__ uint64_t desc_k64(uint32_t p, int kk) {
-  return sdesc(p + (uint32_t)kk * 32u, 16, 1024, LAYOUT_SW128);
-}
-// MN-major operand: rows along K (8-row groups 1024 B apart), 64-element MN blocks `lbo` apart.
-__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t base, int kk, uint32_t lbo) {
-  return sdesc(base + (uint32_t)kk * 2048u, lbo, 1024, LAYOUT_SW128);
-}
+__device__ __forceinline__ SDesc operator+(SDesc d, uint32_t bytes) { return {d.lo + (bytes >> 4), d.hi}; }
 
 // ---- PTX wrappers ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x,
@@ -158,19 +146,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void umma(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
-          d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+      "{\n .reg .pred p;\n .reg .b64 da, db;\n mov.b64 da, {%1, %2};\n mov.b64 db, {%3, %4};\n"
+      " setp.ne.b32 p, %6, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n}" ::"r"(d_tmem),
+      "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(acc));
 }
-
 // Same, with the A operand (M lanes x K/2 columns of bf16 pairs) read from tensor memory.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, SDesc b, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
-          d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+      "{\n .reg .pred p;\n .reg .b64 db;\n mov.b64 db, {%2, %3};\n setp.ne.b32 p, %5, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(acc));
 }
 
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -414,19 +401,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       constexpr uint32_t ID_U = idesc_bf16(128, 2 * TN, 1, 1);        // U = K4^T [Z4t_hi | Z4t_lo]
       constexpr uint32_t ID_E = C::NARROW ? idesc_bf16(128, DK, 0, 0)  // O_inter = X S^T (hi, lo)
                                           : idesc_bf16(128, 2 * TN, 0, 1);  // O_inter = X [S_hi | S_lo]
-      const uint32_t vt = sbase + SMM::OFF_VT;
+      // Operand descriptors (K steps and panels are constant offsets from these):
+      //   X: K-major (wide: 64-column 128B-swizzled panel + 32-column 64B panel; narrow: one panel)
+      //   Y: K-major (wide: two 128B panels);  Z, K4, weighted Z4: MN-major
+      //   state copy: MN-major [hi | lo] (wide) or K-major (narrow)
+      const SDesc dvt = sdesc(sbase + SMM::OFF_VT, SZ_TILE64, 1024, LAYOUT_SW128);
       for (int it = 0; it < nc; ++it) {
         const int s = it & 1;
         const uint32_t ph = (uint32_t)(it >> 1) & 1u, pc = (uint32_t)it & 1u;
         const uint32_t st = sbase + (uint32_t)s * C::SZ_STAGE;
+        const SDesc dx = sdesc(st + C::ST_X, 16, 1024, LAYOUT_SW128);
+        const SDesc dx1 = sdesc(st + C::ST_X1, 16, 512, LAYOUT_SW64);
+        // K step kk of X: 16 columns = 32 bytes along the panel row
+        auto x_step = [&](int kk) {
+          return C::NARROW ? dx + (uint32_t)kk * 32u : (kk < 4 ? dx + (uint32_t)kk * 32u : dx1 + (uint32_t)(kk - 4) * 32u);
+        };
         if (!mbar_wait(&bars[B_FULL + s], ph, a.wait_ns, abort_flag)) break;
         if (warp == 1) {
           if (!mbar_wait(&bars[B_A_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
           tc_fence_after();
+#pragma unroll
           for (int kk = 0; kk < C::K1; ++kk) {
-            const uint64_t da = C::NARROW ? desc_k64(st + C::ST_X, kk) : desc_k96(st + C::ST_X, st + C::ST_X1, kk);
-            const uint64_t db = C::NARROW ? desc_k64(st + C::ST_Y, kk) : desc_kmajor_sw128(st + C::ST_Y, kk);
-            umma(tmem + C::TM_A, da, db, ID_A, kk > 0);
+            const SDesc dy = sdesc(st + C::ST_Y, 16, 1024, LAYOUT_SW128);
+            const SDesc db = C::NARROW ? dy + (uint32_t)kk * 32u
+                                       : dy + (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
+            umma(tmem + C::TM_A, x_step(kk), db, ID_A, kk > 0);
           }
           umma_commit(&bars[B_A_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
@@ -434,9 +433,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           if (!mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag)) break;
           if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
           tc_fence_after();
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma_ts(tmem + C::TM_OI, tmem + C::TM_P + 8u * kk,
-                    desc_mn_sw128(st + C::ST_Z, kk, C::NARROW ? 16384u : 8192u), ID_PZ, kk > 0);
+                    sdesc(st + C::ST_Z, C::NARROW ? 16384u : 8192u, 1024, LAYOUT_SW128) + (uint32_t)kk * 2048u, ID_PZ,
+                    kk > 0);
           umma_commit(&bars[B_P_EMPTY]);
           umma_commit(&bars[B_O_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
@@ -444,29 +445,32 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           if (!mbar_wait(&bars[B_VT_FULL], pc, a.wait_ns, abort_flag)) break;
           if (!mbar_wait(&bars[B_U_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
           tc_fence_after();
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma(tmem + C::TM_U, desc_mn_sw128(st + C::ST_K4, kk, 16384), desc_mn_sw128(vt, kk, SZ_TILE64), ID_U,
-                 kk > 0);
+            umma(tmem + C::TM_U, sdesc(st + C::ST_K4, 16384, 1024, LAYOUT_SW128) + (uint32_t)kk * 2048u,
+                 dvt + (uint32_t)kk * 2048u, ID_U, kk > 0);
           umma_commit(&bars[B_U_FULL]);
           umma_commit(&bars[B_VT_EMPTY]);
           const int b = it & 1;
           const uint32_t fb = (uint32_t)(it >> 1) & 1u;
+          const uint32_t spb = sbase + SMM::OFF_SP + (uint32_t)b * SZ_SP;
+          const SDesc dsp = C::NARROW ? sdesc(spb, 16, 1024, LAYOUT_SW128) : sdesc(spb, SZ_SPH, 1024, LAYOUT_SW128);
           if (!mbar_wait(&bars[B_SP_FULL + b], fb, a.wait_ns, abort_flag)) break;
           if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
           tc_fence_after();
-          const uint32_t spb = sbase + SMM::OFF_SP + (uint32_t)b * SZ_SP;
           if (C::NARROW) {
             // state tile as a K-major B operand: N = 96 rows (d_k), K = this tile's 64 columns
+#pragma unroll
             for (int part = 0; part < 2; ++part)
+#pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma(tmem + C::TM_OE, desc_k64(st + C::ST_X, kk),
-                     sdesc(spb + (uint32_t)part * SZ_SPH + (uint32_t)kk * 32u, 16, 1024, LAYOUT_SW128), ID_E,
+                umma(tmem + C::TM_OE, x_step(kk), dsp + (uint32_t)part * SZ_SPH + (uint32_t)kk * 32u, ID_E,
                      part + kk > 0);
           } else {
             // state tile as an MN-major B operand: K = 96 rows (d_k), N = [hi | lo] x 64 columns
+#pragma unroll
             for (int kk = 0; kk < 6; ++kk)
-              umma(tmem + C::TM_OE, desc_k96(st + C::ST_X, st + C::ST_X1, kk), desc_mn_sw128(spb, kk, SZ_SPH), ID_E,
-                   kk > 0);
+              umma(tmem + C::TM_OE, x_step(kk), dsp + (uint32_t)kk * 2048u, ID_E, kk > 0);
           }
           umma_commit(&bars[B_SP_EMPTY + b]);
           umma_commit(&bars[B_O_FULL]);
