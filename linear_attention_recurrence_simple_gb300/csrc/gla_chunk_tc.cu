@@ -270,6 +270,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
+// 32 bytes to a 32-byte aligned global address.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
@@ -598,6 +605,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     const int r_ = ((warp & 3) << 5) + lane;  // d_k row of the state and U; query row of O
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
     const long long sbase_g = (((long long)n * a.H + h) * DK + r_) * DV + col0;
+    const bool out32 = (reinterpret_cast<uintptr_t>(prm.out) & 31u) == 0;
     float S[TN];
 #pragma unroll
     for (int x = 0; x < TN; ++x) S[x] = 0.f;
@@ -687,8 +695,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
             ob[e] = pack_bf16(ovx.x, ovx.y);
           }
           if (r_ < L) {
-            dst[2 * qq] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-            dst[2 * qq + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
+            if (out32) {  // one full 32-byte sector per store
+              st_global_v8(dst + 2 * qq, ob);
+            } else {
+              dst[2 * qq] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+              dst[2 * qq + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
+            }
           }
         }
       } else {

@@ -98,6 +98,24 @@ def test_fwd_varlen_equals_fixed_bitwise():
     assert torch.equal(o1.view(4, 200, 2, 192), o2) and torch.equal(h1, h2)
 
 
+def test_fwd_output_alignment_16_vs_32_bitwise():
+    """Output rows are written with 32-byte stores when o is 32-byte aligned and with 16-byte stores
+    when it is only 16-byte aligned (the minimum the ABI asks for); both give the same bits."""
+    import torch
+    B, T, H = 2, 200, 2
+    d = host_chunk_inputs(11, [T] * B, H, True, with_h0=True, packed=False)
+    g = to_device(d, True, packed=False)
+    n = B * T * H * 192
+    o32 = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    raw = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")
+    o16 = raw[8:].view(n)  # 16 bytes past a 256-byte aligned allocation
+    assert o32.data_ptr() % 32 == 0 and o16.data_ptr() % 32 == 16
+    o32, o16 = o32.view(B, T, H, 192), o16.view(B, T, H, 192)
+    gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], 0.1, h0=g["h0"], o=o32)
+    gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], 0.1, h0=g["h0"], o=o16)
+    assert torch.equal(o32, o16)
+
+
 def test_fwd_pages_decay_schedule_no_overflow():
     """Half-life schedule 1..2048 tokens: head 0 has lambda = 0.5, so lambda^127 is 2^-127."""
     H = 16
