@@ -93,17 +93,17 @@ struct Cfg {
 
 constexpr uint32_t SZ_TILE64 = 128 * 128;       // one 128-row, 128-byte-row tile
 constexpr uint32_t SZ_SPH = 96 * 128;           // bf16 state tile: 96 rows (d_k) x 64 columns
-constexpr uint32_t SZ_SP = 2 * SZ_SPH;          // one buffer: hi then lo
+constexpr uint32_t SZ_SP = 2 * SZ_SPH;          // hi then lo
 enum {
   B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
-  B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY = B_SP_FULL + 2, B_O_FULL = B_SP_EMPTY + 2, B_O_EMPTY,
+  B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY,
   B_DRAIN, NBAR = B_DRAIN + 3
 };
 template <int MODE>
 struct Smem {
   static constexpr uint32_t OFF_VT = 2 * Cfg<MODE>::SZ_STAGE;
   static constexpr uint32_t OFF_SP = OFF_VT + 2 * SZ_TILE64;
-  static constexpr uint32_t OFF_PW = OFF_SP + 2 * SZ_SP;
+  static constexpr uint32_t OFF_PW = OFF_SP + SZ_SP;
   static constexpr uint32_t OFF_BAR = OFF_PW + 2 * 129 * 4 + 8;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;
@@ -335,8 +335,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       uint32_t cnt = 1;
       if (i == B_EMPTY || i == B_EMPTY + 1) cnt = 3;
       if (i == B_O_FULL) cnt = 2;
-            if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_U_EMPTY || i == B_SP_FULL ||
-          i == B_SP_FULL + 1 || i == B_O_EMPTY)
+      if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_U_EMPTY || i == B_SP_FULL ||
+          i == B_O_EMPTY)
         cnt = 128;
       mbar_init(&bars[i], cnt);
     }
@@ -458,11 +458,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
                  dvt + (uint32_t)kk * 2048u, ID_U, kk > 0);
           umma_commit(&bars[B_U_FULL]);
           umma_commit(&bars[B_VT_EMPTY]);
-          const int b = it & 1;
-          const uint32_t fb = (uint32_t)(it >> 1) & 1u;
-          const uint32_t spb = sbase + SMM::OFF_SP + (uint32_t)b * SZ_SP;
+          // the state before this chunk (one buffer: the epilogue overwrites it after this MMA3)
+          const uint32_t spb = sbase + SMM::OFF_SP;
           const SDesc dsp = C::NARROW ? sdesc(spb, 16, 1024, LAYOUT_SW128) : sdesc(spb, SZ_SPH, 1024, LAYOUT_SW128);
-          if (!mbar_wait(&bars[B_SP_FULL + b], fb, a.wait_ns, abort_flag)) break;
+          if (!mbar_wait(&bars[B_SP_FULL], pc, a.wait_ns, abort_flag)) break;
           if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
           tc_fence_after();
           if (C::NARROW) {
@@ -479,7 +478,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
             for (int kk = 0; kk < 6; ++kk)
               umma(tmem + C::TM_OE, x_step(kk), dsp + (uint32_t)kk * 2048u, ID_E, kk > 0);
           }
-          umma_commit(&bars[B_SP_EMPTY + b]);
+          umma_commit(&bars[B_SP_EMPTY]);
           umma_commit(&bars[B_O_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
         }
@@ -620,9 +619,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         S[4 * x + 3] = v4.w;
       }
     }
-    auto write_sprev = [&](int buf) {
+    auto write_sprev = [&]() {
       if (r_ < DK) {
-        const uint32_t row = sbase + SMM::OFF_SP + (uint32_t)buf * SZ_SP + (uint32_t)r_ * 128u;
+        const uint32_t row = sbase + SMM::OFF_SP + (uint32_t)r_ * 128u;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
           uint32_t hi[4], lo[4];
@@ -634,7 +633,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         }
       }
       fence_async_smem();
-      mbar_arrive(&bars[B_SP_FULL + buf]);
+      mbar_arrive(&bars[B_SP_FULL]);
     };
     // Iteration it: the state update of chunk it, the state copy for chunk it + 1, the output rows
     // of chunk it (it = -1 only writes the copy of the initial state).  One site for each part
@@ -664,11 +663,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         tc_fence_before();
         mbar_arrive(&bars[B_U_EMPTY]);
       }
-      if (it + 1 < nc) {
-        const int b2 = (it + 1) & 1;
-        const uint32_t f2 = (uint32_t)((it + 1) >> 1) & 1u;
-        if (!warp_wait(&bars[B_SP_EMPTY + b2], f2 ^ 1u, a, abort_flag)) { aborted = true; break; }
-        write_sprev(b2);
+      if (it + 1 < nc) {  // after MMA3 of this chunk has read the previous copy
+        if (it >= 0 && !warp_wait(&bars[B_SP_EMPTY], pc, a, abort_flag)) { aborted = true; break; }
+        write_sprev();
       }
       if (it < 0) continue;
       // out row = O_intra + g * O_inter;  g = s lambda^(i+1) (forward scans) or lambda^(L-1-i)
