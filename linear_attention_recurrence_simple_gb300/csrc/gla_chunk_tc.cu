@@ -96,14 +96,15 @@ constexpr uint32_t SZ_SPH = 96 * 128;           // bf16 state tile: 96 rows (d_k
 constexpr uint32_t SZ_SP = 2 * SZ_SPH;          // hi then lo
 enum {
   B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
-  B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY,
+  B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY, B_OST_FULL, B_OST_EMPTY,
   B_DRAIN, NBAR = B_DRAIN + 3
 };
 template <int MODE>
 struct Smem {
   static constexpr uint32_t OFF_VT = 2 * Cfg<MODE>::SZ_STAGE;
   static constexpr uint32_t OFF_SP = OFF_VT + 2 * SZ_TILE64;
-  static constexpr uint32_t OFF_PW = OFF_SP + SZ_SP;
+  static constexpr uint32_t OFF_OST = OFF_SP + SZ_SP;  // wide: bf16 output tile staged for the TMA store
+  static constexpr uint32_t OFF_PW = OFF_OST + (Cfg<MODE>::NARROW ? 0u : SZ_TILE64);
   static constexpr uint32_t OFF_BAR = OFF_PW + 2 * 129 * 4 + 8;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;
@@ -145,6 +146,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Shared -> global tile store (bulk-group completion), and the waits on this thread's bulk groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"((uint64_t)map),
+               "r"(x), "r"(y), "r"(z), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void umma(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc, uint32_t acc) {
   asm volatile(
@@ -282,7 +293,7 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
 }
 
 struct TmaMaps {
-  CUtensorMap x, x1, y, z;
+  CUtensorMap x, x1, y, z, o;  // o: the bf16 output (wide modes)
 };
 
 // What a scan kernel needs besides its tensor maps: sequence layout and decay (in `a`), the
@@ -336,7 +347,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       if (i == B_EMPTY || i == B_EMPTY + 1) cnt = 3;
       if (i == B_O_FULL) cnt = 2;
       if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_U_EMPTY || i == B_SP_FULL ||
-          i == B_O_EMPTY)
+          i == B_O_EMPTY || i == B_OST_FULL)
         cnt = 128;
       mbar_init(&bars[i], cnt);
     }
@@ -639,6 +650,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     // of chunk it (it = -1 only writes the copy of the initial state).  One site for each part
     // keeps the code small.
     bool aborted = false;
+    int nst = 0;  // full chunks stored through the staging tile
     for (int it = -1; it < nc; ++it) {
       const uint32_t pc = (uint32_t)it & 1u;
       const int c = it >= 0 ? chunk_of(it) : 0;
@@ -674,7 +686,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       const float gf = C::REVERSE ? (r_ < L ? pw[L - 1 - r_] : 0.f) : pws[r_ + 1];
       const long long orow = (tb + (long long)c * CHUNK + r_) * a.H + h;
       if (!C::NARROW) {
+        // Full chunks go through the staging tile and one TMA store (a whole 128 x 64 tile, no
+        // per-row stores on the load/store pipe); a partial last chunk is stored row by row so that
+        // nothing past the sequence end is written.
+        const bool staged = L == CHUNK;
+        if (staged && nst > 0) {  // the previous store has finished reading the staging tile
+          if (r_ == 0) {
+            bulk_wait_read_all();
+            mbar_arrive(&bars[B_OST_EMPTY]);
+          }
+          if (!warp_wait(&bars[B_OST_EMPTY], (uint32_t)(nst - 1) & 1u, a, abort_flag)) { aborted = true; break; }
+        }
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(prm.out) + orow * DV + col0);
+        const uint32_t srow = sbase + SMM::OFF_OST + (uint32_t)r_ * 128u;
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
           uint32_t ov[48];  // 16 intra, 16 inter-hi, 16 inter-lo columns
@@ -691,7 +715,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
             const float2 ovx = fma2(make_float2(gf, gf), add2(ld_f2(ov, 16 + x), ld_f2(ov, 32 + x)), ld_f2(ov, x));
             ob[e] = pack_bf16(ovx.x, ovx.y);
           }
-          if (r_ < L) {
+          if (staged) {  // 16-byte pieces 2qq, 2qq + 1 of the row, in the 128B-swizzled layout
+            st_shared_v4(srow + ((uint32_t)((2 * qq) ^ (r_ & 7)) << 4), ob[0], ob[1], ob[2], ob[3]);
+            st_shared_v4(srow + ((uint32_t)((2 * qq + 1) ^ (r_ & 7)) << 4), ob[4], ob[5], ob[6], ob[7]);
+          } else if (r_ < L) {
             if (out32) {  // one full 32-byte sector per store
               st_global_v8(dst + 2 * qq, ob);
             } else {
@@ -699,6 +726,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
               dst[2 * qq + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
             }
           }
+        }
+        if (staged) {
+          fence_async_smem();
+          mbar_arrive(&bars[B_OST_FULL]);
+          if ((warp & 3) == 0) {  // the whole warp waits (so that an abort leaves it in step)
+            if (!warp_wait(&bars[B_OST_FULL], (uint32_t)nst & 1u, a, abort_flag)) { aborted = true; break; }
+            if (lane == 0) tma_store_3d(&maps.o, sbase + SMM::OFF_OST, col0, h, (int)(tb + (long long)c * CHUNK));
+          }
+          ++nst;
         }
       } else {
         float* dst = reinterpret_cast<float*>(prm.out) + orow * DK;
@@ -721,6 +757,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         }
       }
     }
+    if (!C::NARROW && r_ == 0 && nst > 0) bulk_wait_all();  // the last tile store has completed
     if (!aborted && prm.s_out && r_ < DK) {
       float4* dst = reinterpret_cast<float4*>(prm.s_out + sbase_g);
 #pragma unroll
@@ -794,7 +831,8 @@ cudaError_t launch_scan(const void* X, const void* Y, const void* Z, const ScanP
     if (!make_map(&maps.x, X, dx, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         (!C::NARROW && !make_map(&maps.x1, X, DK, a.H, T_total, 32, CU_TENSOR_MAP_SWIZZLE_64B)) ||
         !make_map(&maps.y, Y, dx, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&maps.z, Z, dz, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map(&maps.z, Z, dz, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        (!C::NARROW && !make_map(&maps.o, p.out, DV, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B)))
       return cudaErrorInvalidValue;
   }
   static bool attr_set = false;
