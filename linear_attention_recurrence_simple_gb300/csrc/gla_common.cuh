@@ -82,9 +82,8 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 }
 
 // ------------------------------------------------------------------------------------------
-// mbarrier helpers (shared::cta).  Every wait is bounded: it repeats try_wait (each may suspend
-// the thread for up to SUSPEND_NS), reads the global timer after each, and gives up after
-// `limit_ns` (or as soon as *abort is set).
+// mbarrier helpers (shared::cta).  Every wait is bounded: it repeats try_wait, reads the global
+// timer after each, and gives up after `limit_ns` (or as soon as *abort is set).
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -106,16 +105,15 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
-// One try_wait: the hardware may suspend the thread until the phase completes, for at most
-// SUSPEND_NS, instead of returning at once; waiting threads then leave the issue slots and the
-// shared-memory pipe to the threads that work.
-constexpr uint32_t SUSPEND_NS = 20000;
+// One try_wait (the hardware may suspend the thread for a short, system-dependent time before it
+// returns false).  A suspend-time hint was measured slower once the load/store pipe stopped
+// backing up: a wait whose phase has already completed then cost ~250 cycles.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(SUSPEND_NS)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
