@@ -508,6 +508,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     const uint32_t lane_addr = tmem + ((uint32_t)(q << 5) << 16);
     const float lam = pw[1];
     const float2 lam2 = make_float2(lam * lam, lam * lam);
+    // Decay factors of the diagonal group for this lane: s lambda^(i-j) (forward, j <= i) or
+    // s lambda^(j-i) (reverse, j >= i), zero across the diagonal; element pair e is columns
+    // 32q + 2e and 32q + 2e + 1.
+    float2 dgf[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int d0 = C::REVERSE ? 2 * e - lane : lane - 2 * e;
+      const int d1 = C::REVERSE ? d0 + 1 : d0 - 1;
+      dgf[e] = make_float2(d0 >= 0 ? pws[max(d0, 0)] : 0.f, d1 >= 0 ? pws[max(d1, 0)] : 0.f);
+    }
     {  // P groups on the far side of this warp's diagonal stay zero for the whole kernel
       uint32_t z[16];
 #pragma unroll
@@ -525,9 +535,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       tc_fence_after();
       // P row i, one 32-column group at a time, stored straight back to tensor memory.
       //   forward scans: s lambda^(i-j) A_ij for j <= i;  reverse scans: s lambda^(j-i) A_ij for j >= i
-      // (and only i < L, j < L).  Off the diagonal group the factors come from one table read and a
+      // and j < L.  Forward rows i >= L of a partial chunk are left unmasked: they only reach output
+      // rows that are never stored (j <= i < L bounds the rows that are); reverse rows i >= L have
+      // only columns j >= i >= L.  Off the diagonal group the factors come from one table read and a
       // multiplicative chain toward larger |i - j| (values only shrink, so an underflow to zero loses
-      // nothing); the diagonal group reads the table per element.
+      // nothing); the diagonal group uses the lane's factors from the table, read once.
       const int g_first = C::REVERSE ? q : 0, g_last = C::REVERSE ? 3 : q;
       for (int g = g_first; g <= g_last; ++g) {
         uint32_t r[32];
@@ -540,7 +552,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         if (g != q) {
           if (!C::REVERSE) {
             const int d0 = i - 32 * g;  // i - j at the group's first column (>= 1 here)
-            float2 f = i < L ? make_float2(pws[d0 - 30], pws[d0 - 31]) : make_float2(0.f, 0.f);
+            float2 f = make_float2(pws[d0 - 30], pws[d0 - 31]);
 #pragma unroll
             for (int e = 15; e >= 0; --e) {
               if (e < 15) f = mul2(f, lam2);
@@ -549,7 +561,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
             }
           } else {
             const int d0 = 32 * g - i;  // j - i at the group's first column (>= 1 here)
-            float2 f = i < L ? make_float2(pws[d0], pws[d0 + 1]) : make_float2(0.f, 0.f);
+            float2 f = make_float2(pws[d0], pws[d0 + 1]);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               if (e > 0) f = mul2(f, lam2);
@@ -559,15 +571,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
             }
           }
         } else {
+          // diagonal group: the lane's own factors (fixed for the kernel); reverse columns past the
+          // sequence end are zero
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const int j = 32 * g + 2 * e;
-            const int d = C::REVERSE ? j - i : i - j;
-            const int d1 = C::REVERSE ? d + 1 : d - 1;
-            const bool ok0 = d >= 0 && i < L && j < L, ok1 = d1 >= 0 && i < L && j + 1 < L;
-            const float f0 = ok0 ? pws[max(d, 0)] : 0.f;
-            const float f1 = ok1 ? pws[max(d1, 0)] : 0.f;
-            pkg[e] = pack_bf16(f0 * __uint_as_float(r[2 * e]), f1 * __uint_as_float(r[2 * e + 1]));
+            const float2 pv = mul2(dgf[e], ld_f2(r, 2 * e));
+            if (C::REVERSE) {
+              const int j = 32 * g + 2 * e;
+              pkg[e] = pack_bf16(j < L ? pv.x : 0.f, j + 1 < L ? pv.y : 0.f);
+            } else {
+              pkg[e] = pack_bf16(pv.x, pv.y);
+            }
           }
         }
         tmem_st16(lane_addr + C::TM_P + 16u * g, pkg);
