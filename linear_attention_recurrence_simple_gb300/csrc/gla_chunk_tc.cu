@@ -99,12 +99,17 @@ enum {
   B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY, B_OST_FULL, B_OST_EMPTY,
   B_DRAIN, NBAR = B_DRAIN + 3
 };
+constexpr uint32_t RED_ROW = 208;                 // 192 bytes of fp32 + 16 (bank spread)
+constexpr uint32_t RED_WARP_BYTES = 32 * RED_ROW;
 template <int MODE>
 struct Smem {
   static constexpr uint32_t OFF_VT = 2 * Cfg<MODE>::SZ_STAGE;
   static constexpr uint32_t OFF_SP = OFF_VT + 2 * SZ_TILE64;
-  static constexpr uint32_t OFF_OST = OFF_SP + SZ_SP;  // wide: bf16 output tile staged for the TMA store
-  static constexpr uint32_t OFF_PW = OFF_OST + (Cfg<MODE>::NARROW ? 0u : SZ_TILE64);
+  // output staging: wide, the bf16 output tile for the TMA store; narrow, one region per epilogue
+  // warp (32 rows x 48 fp32, rows padded to 208 bytes) that turns row-wise sums into adds of
+  // contiguous row segments
+  static constexpr uint32_t OFF_OST = OFF_SP + SZ_SP;
+  static constexpr uint32_t OFF_PW = OFF_OST + (Cfg<MODE>::NARROW ? 4u * RED_WARP_BYTES : SZ_TILE64);
   static constexpr uint32_t OFF_BAR = OFF_PW + 2 * 129 * 4 + 8;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;
@@ -271,6 +276,11 @@ __device__ __forceinline__ void split_bf16x2(float2 x, uint32_t& hi, uint32_t& l
   lo = pack_bf16(r.x, r.y);
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -751,23 +761,41 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           ++nst;
         }
       } else {
-        float* dst = reinterpret_cast<float*>(prm.out) + orow * DK;
+        // fp32 partial sums for the accumulator, 48 columns at a time: each thread writes its row
+        // into the warp's region, then the warp adds contiguous 16-byte pieces (12 per row), so one
+        // red.add instruction covers about three rows' segments instead of 32 rows.
+        const uint32_t wreg = sbase + SMM::OFF_OST + (uint32_t)(warp & 3) * RED_WARP_BYTES;
+        const long long row0 = (tb + (long long)c * CHUNK + ((warp & 3) << 5)) * a.H + h;  // lane 0's row
 #pragma unroll
-        for (int qq = 0; qq < 6; ++qq) {
-          uint32_t ov[32];  // 16 intra, 16 inter columns
-          tmem_ld16x2(lane_addr + C::TM_OI + 16u * qq, lane_addr + C::TM_OE + 16u * qq, ov);
-          if (qq == 5) {
-            tc_fence_before();
-            mbar_arrive(&bars[B_O_EMPTY]);
-          }
-          if (r_ < L) {
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int q3 = 0; q3 < 3; ++q3) {
+            const int qq = 3 * half + q3;
+            uint32_t ov[32];  // 16 intra, 16 inter columns
+            tmem_ld16x2(lane_addr + C::TM_OI + 16u * qq, lane_addr + C::TM_OE + 16u * qq, ov);
+            if (qq == 5) {
+              tc_fence_before();
+              mbar_arrive(&bars[B_O_EMPTY]);
+            }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 v0 = fma2(make_float2(gf, gf), ld_f2(ov, 16 + 4 * e), ld_f2(ov, 4 * e));
               const float2 v1 = fma2(make_float2(gf, gf), ld_f2(ov, 18 + 4 * e), ld_f2(ov, 4 * e + 2));
-              red_add_v4(dst + 16 * qq + 4 * e, v0.x, v0.y, v1.x, v1.y);
+              st_shared_v4(wreg + (uint32_t)lane * RED_ROW + (uint32_t)(4 * q3 + e) * 16u, __float_as_uint(v0.x),
+                           __float_as_uint(v0.y), __float_as_uint(v1.x), __float_as_uint(v1.y));
             }
           }
+          __syncwarp();
+#pragma unroll 2
+          for (int k = 0; k < 12; ++k) {
+            const int pidx = k * 32 + lane, row = pidx / 12, pc = pidx - row * 12;
+            if (((warp & 3) << 5) + row < L) {
+              const uint4 v = ld_shared_v4(wreg + (uint32_t)row * RED_ROW + (uint32_t)pc * 16u);
+              red_add_v4(reinterpret_cast<float*>(prm.out) + (row0 + (long long)row * a.H) * DK + 48 * half + 4 * pc,
+                         __uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+            }
+          }
+          __syncwarp();
         }
       }
     }
