@@ -816,13 +816,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
   if (threadIdx.x == 0 && *abort_flag) raise_error(a.err, ERR_TIMEOUT);
 }
 
-// fp32 partial-sum accumulators [T, H, 96] -> bf16 outputs (dq and dk in one pass).
-__global__ void acc_to_bf16_kernel(const float4* __restrict__ acc_q, const float4* __restrict__ acc_k,
-                                   uint2* __restrict__ dq, uint2* __restrict__ dk, long long n4) {
+// fp32 partial-sum accumulator [T, H, 96] -> bf16 output (dq or dk).
+__global__ void acc_to_bf16_kernel(const float4* __restrict__ acc, uint2* __restrict__ out, long long n4) {
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < n4; e += (long long)gridDim.x * blockDim.x) {
-    const float4 a = acc_q[e], b = acc_k[e];
-    dq[e] = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
-    dk[e] = make_uint2(pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
+    const float4 a = acc[e];
+    out[e] = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
   }
 }
 
@@ -925,59 +923,68 @@ cudaError_t side_streams(cudaStream_t (&out)[2]) {
 }  // namespace
 
 // Backward in bf16: dv and dh0 directly; dq and dk through fp32 partial sums in acc_q / acc_k
-// (each tc_bwd_acc_bytes, 16-byte aligned), rounded to bf16 at the end.  The three scans are
-// independent until that rounding: DV runs on the caller's stream, DK and DQ on two side streams
-// forked from it and joined back with events, so their CTAs fill each other's last waves.
+// (each tc_bwd_acc_bytes, 16-byte aligned), each rounded to bf16 once its scan is done.  The three
+// scans are independent: DV runs on the caller's stream, and DK and DQ (each with its zeroing and
+// its rounding pass) on two side streams forked from it and joined back with events, so their
+// kernels fill each other's idle SMs.
 cudaError_t launch_tc_bwd(const ChunkArgs& a, float* acc_q, float* acc_k, cudaStream_t stream) {
   const long long T_total = a.cu_seqlens ? (long long)a.T : (long long)a.n_seq * a.T;
   const size_t acc = tc_bwd_acc_bytes(T_total, a.H);
+  const long long n4 = T_total * a.H * DK / 4;
   cudaError_t e;
-  if (acc) {
-    if ((e = cudaMemsetAsync(acc_q, 0, acc, stream)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(acc_k, 0, acc, stream)) != cudaSuccess) return e;
-  }
   cudaStream_t side[2];
   if ((e = side_streams(side)) != cudaSuccess) return e;
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long conv_blocks = (n4 + 255) / 256;
+  if (conv_blocks > (long long)sms * 8) conv_blocks = (long long)sms * 8;
+  // One side stream per accumulator: zero it, run its scan, round it to bf16.
+  auto partial_scan = [&](cudaStream_t st, float* acc_p, void* out, bool dk_scan) -> cudaError_t {
+    cudaError_t r;
+    if (acc && (r = cudaMemsetAsync(acc_p, 0, acc, st)) != cudaSuccess) return r;
+    ScanParams p;
+    p.a = a;
+    p.s_out = nullptr;
+    p.out = acc_p;
+    if (dk_scan) {
+      p.s0 = a.dhT;
+      r = launch_scan<MODE_DK>(a.v, a.dO, a.q, p, st);
+    } else {
+      p.s0 = a.h0;
+      r = launch_scan<MODE_DQ>(a.dO, a.v, a.k, p, st);
+    }
+    if (r != cudaSuccess) return r;
+    if (n4 > 0) {
+      acc_to_bf16_kernel<<<(unsigned)conv_blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(acc_p),
+                                                                reinterpret_cast<uint2*>(out), n4);
+      r = cudaGetLastError();
+    }
+    return r;
+  };
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   for (int i = 0; i < 3; ++i)
     if ((e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming)) != cudaSuccess) break;
   if (e == cudaSuccess) e = cudaEventRecord(ev[0], stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side[0], ev[0], 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(side[1], ev[0], 0);
-  ScanParams p;
-  p.a = a;
-  p.s0 = a.dhT;
-  p.s_out = nullptr;
-  p.out = acc_k;
-  if (e == cudaSuccess) e = launch_scan<MODE_DK>(a.v, a.dO, a.q, p, side[0]);
-  p.s0 = a.h0;
-  p.out = acc_q;
-  if (e == cudaSuccess) e = launch_scan<MODE_DQ>(a.dO, a.v, a.k, p, side[1]);
-  p.s0 = a.dhT;
-  p.s_out = a.hT;  // dh0
-  p.out = a.dv;
-  if (e == cudaSuccess) e = launch_scan<MODE_DV>(a.k, a.q, a.dO, p, stream);
+  if (e == cudaSuccess) e = partial_scan(side[0], acc_k, a.dk, true);
+  if (e == cudaSuccess) e = partial_scan(side[1], acc_q, a.o, false);  // a.o carries dq here
+  if (e == cudaSuccess) {
+    ScanParams p;
+    p.a = a;
+    p.s0 = a.dhT;
+    p.s_out = a.hT;  // dh0
+    p.out = a.dv;
+    e = launch_scan<MODE_DV>(a.k, a.q, a.dO, p, stream);
+  }
   if (e == cudaSuccess) e = cudaEventRecord(ev[1], side[0]);
   if (e == cudaSuccess) e = cudaEventRecord(ev[2], side[1]);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[1], 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[2], 0);
   for (int i = 0; i < 3; ++i)
     if (ev[i]) cudaEventDestroy(ev[i]);
-  if (e != cudaSuccess) return e;
-  const long long n4 = T_total * a.H * DK / 4;
-  if (n4 > 0) {
-    int dev = 0, sms = 152;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    long long blocks = (n4 + 255) / 256;
-    if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
-    acc_to_bf16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc_q),
-                                                              reinterpret_cast<const float4*>(acc_k),
-                                                              reinterpret_cast<uint2*>(a.o),
-                                                              reinterpret_cast<uint2*>(a.dk), n4);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  return e;
 }
 
 }  // namespace gla
