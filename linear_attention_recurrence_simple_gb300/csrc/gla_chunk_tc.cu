@@ -97,7 +97,7 @@ constexpr uint32_t SZ_SP = 2 * SZ_SPH;          // hi then lo
 enum {
   B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
   B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY, B_OST_FULL, B_OST_EMPTY,
-  B_DRAIN, NBAR = B_DRAIN + 3
+  B_ZR, B_DRAIN = B_ZR + 2, NBAR = B_DRAIN + 3
 };
 constexpr uint32_t RED_ROW = 208;                 // 192 bytes of fp32 + 16 (bank spread)
 constexpr uint32_t RED_WARP_BYTES = 32 * RED_ROW;
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       if (i == B_EMPTY || i == B_EMPTY + 1) cnt = 3;
       if (i == B_O_FULL) cnt = 2;
       if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_U_EMPTY || i == B_SP_FULL ||
-          i == B_O_EMPTY || i == B_OST_FULL)
+          i == B_O_EMPTY || i == B_OST_FULL || i == B_ZR || i == B_ZR + 1)
         cnt = 128;
       mbar_init(&bars[i], cnt);
     }
@@ -458,6 +458,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           umma_commit(&bars[B_A_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
         } else if (warp == 3) {
+          if (C::REVERSE && !mbar_wait(&bars[B_ZR + s], ph, a.wait_ns, abort_flag)) break;
           if (!mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag)) break;
           if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
           tc_fence_after();
@@ -544,10 +545,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       if (!warp_wait(&bars[B_P_EMPTY], pc ^ 1u, a, abort_flag)) break;
       tc_fence_after();
       // P row i, one 32-column group at a time, stored straight back to tensor memory.
-      //   forward scans: s lambda^(i-j) A_ij for j <= i;  reverse scans: s lambda^(j-i) A_ij for j >= i
-      // and j < L.  Forward rows i >= L of a partial chunk are left unmasked: they only reach output
-      // rows that are never stored (j <= i < L bounds the rows that are); reverse rows i >= L have
-      // only columns j >= i >= L.  Off the diagonal group the factors come from one table read and a
+      //   forward scans: s lambda^(i-j) A_ij for j <= i;  reverse scans: s lambda^(j-i) A_ij for j >= i.
+      // Nothing is masked at the sequence end of a partial chunk: forward rows i >= L only reach
+      // output rows that are never stored (j <= i < L bounds the rows that are), and in the reverse
+      // scans the Z4 warps zero the rows j >= L of Z, which columns j >= L of P multiply.  Off the diagonal group the factors come from one table read and a
       // multiplicative chain toward larger |i - j| (values only shrink, so an underflow to zero loses
       // nothing); the diagonal group uses the lane's factors from the table, read once.
       const int g_first = C::REVERSE ? q : 0, g_last = C::REVERSE ? 3 : q;
@@ -575,23 +576,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               if (e > 0) f = mul2(f, lam2);
-              const int j = 32 * g + 2 * e;
               const float2 pv = mul2(f, ld_f2(r, 2 * e));
-              pkg[e] = pack_bf16(j < L ? pv.x : 0.f, j + 1 < L ? pv.y : 0.f);
+              pkg[e] = pack_bf16(pv.x, pv.y);
             }
           }
         } else {
-          // diagonal group: the lane's own factors (fixed for the kernel); reverse columns past the
-          // sequence end are zero
+          // diagonal group: the lane's own factors (fixed for the kernel)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const float2 pv = mul2(dgf[e], ld_f2(r, 2 * e));
-            if (C::REVERSE) {
-              const int j = 32 * g + 2 * e;
-              pkg[e] = pack_bf16(j < L ? pv.x : 0.f, j + 1 < L ? pv.y : 0.f);
-            } else {
-              pkg[e] = pack_bf16(pv.x, pv.y);
-            }
+            pkg[e] = pack_bf16(pv.x, pv.y);
           }
         }
         tmem_st16(lane_addr + C::TM_P + 16u * g, pkg);
@@ -629,9 +623,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           *reinterpret_cast<uint4*>(zhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(zlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
+        if (C::REVERSE && j >= L) {
+          // Reverse scans: rows of Z past the sequence end are zeroed, so MMA2 needs no column mask
+          // on P (the mask warps leave P's columns j >= L unmasked).
+          uint8_t* zrow = sm + s * C::SZ_STAGE + C::ST_Z + j * 128;
+#pragma unroll 1
+          for (int p = 0; p < (C::NARROW ? 16 : 8); ++p)
+            *reinterpret_cast<uint4*>(zrow + (p >> 3) * 16384 + (((p & 7) ^ (j & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+        }
       }
       fence_async_smem();
       mbar_arrive(&bars[B_VT_FULL]);
+      if (C::REVERSE) mbar_arrive(&bars[B_ZR + s]);
     }
   } else {
     // ------------------------------------------------------------------ epilogue
