@@ -37,8 +37,9 @@
 // is (measured), so the kernel keeps the instruction count low (hi/lo halves ride in one N = 128
 // MMA where N allows) and issues from three threads in parallel, one per accumulator chain.  Warp roles:
 //   warp 0      TMA producer: X, Y, Z chunk tiles into a 2-stage ring.
-//   warp 1      allocates tensor memory; one lane issues MMA1 (X Y^T).
-//   warp 2      one lane issues MMA4 (K4^T [Z4t_hi | Z4t_lo]) and MMA3 (X times the state copy).
+//   warp 1      allocates tensor memory; one lane issues MMA1 (X Y^T), then MMA3 (X times the
+//               state copy), whose inputs are ready long before the weighted Z4 that MMA4 waits for.
+//   warp 2      one lane issues MMA4 (K4^T [Z4t_hi | Z4t_lo]).
 //   warp 3      one lane issues MMA2 (P Z, P read from tensor memory).
 //   warps 4-7   decay mask A (TMEM) -> P (bf16 pairs, back into TMEM).  A is released as soon as
 //               it is in registers, so the next chunk's MMA1 overlaps this one's P.
@@ -456,6 +457,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
             umma(tmem + C::TM_A, x_step(kk), db, ID_A, kk > 0);
           }
           umma_commit(&bars[B_A_FULL]);
+          // the state before this chunk (one buffer: the epilogue overwrites it after this MMA3)
+          const uint32_t spb = sbase + SMM::OFF_SP;
+          const SDesc dsp = C::NARROW ? sdesc(spb, 16, 1024, LAYOUT_SW128) : sdesc(spb, SZ_SPH, 1024, LAYOUT_SW128);
+          if (!mbar_wait(&bars[B_SP_FULL], pc, a.wait_ns, abort_flag)) break;
+          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
+          tc_fence_after();
+          if (C::NARROW) {
+            // state tile as a K-major B operand: N = 96 rows (d_k), K = this tile's 64 columns
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma(tmem + C::TM_OE, x_step(kk), dsp + (uint32_t)part * SZ_SPH + (uint32_t)kk * 32u, ID_E,
+                     part + kk > 0);
+          } else {
+            // state tile as an MN-major B operand: K = 96 rows (d_k), N = [hi | lo] x 64 columns
+#pragma unroll
+            for (int kk = 0; kk < 6; ++kk)
+              umma(tmem + C::TM_OE, x_step(kk), dsp + (uint32_t)kk * 2048u, ID_E, kk > 0);
+          }
+          umma_commit(&bars[B_SP_EMPTY]);
+          umma_commit(&bars[B_O_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
         } else if (warp == 3) {
           if (C::REVERSE && !mbar_wait(&bars[B_ZR + s], ph, a.wait_ns, abort_flag)) break;
@@ -480,28 +503,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
                  dvt + (uint32_t)kk * 2048u, ID_U, kk > 0);
           umma_commit(&bars[B_U_FULL]);
           umma_commit(&bars[B_VT_EMPTY]);
-          // the state before this chunk (one buffer: the epilogue overwrites it after this MMA3)
-          const uint32_t spb = sbase + SMM::OFF_SP;
-          const SDesc dsp = C::NARROW ? sdesc(spb, 16, 1024, LAYOUT_SW128) : sdesc(spb, SZ_SPH, 1024, LAYOUT_SW128);
-          if (!mbar_wait(&bars[B_SP_FULL], pc, a.wait_ns, abort_flag)) break;
-          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
-          tc_fence_after();
-          if (C::NARROW) {
-            // state tile as a K-major B operand: N = 96 rows (d_k), K = this tile's 64 columns
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma(tmem + C::TM_OE, x_step(kk), dsp + (uint32_t)part * SZ_SPH + (uint32_t)kk * 32u, ID_E,
-                     part + kk > 0);
-          } else {
-            // state tile as an MN-major B operand: K = 96 rows (d_k), N = [hi | lo] x 64 columns
-#pragma unroll
-            for (int kk = 0; kk < 6; ++kk)
-              umma(tmem + C::TM_OE, x_step(kk), dsp + (uint32_t)kk * 2048u, ID_E, kk > 0);
-          }
-          umma_commit(&bars[B_SP_EMPTY]);
-          umma_commit(&bars[B_O_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
         }
       }
