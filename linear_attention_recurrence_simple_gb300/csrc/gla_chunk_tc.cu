@@ -98,7 +98,7 @@ constexpr uint32_t SZ_SP = 2 * SZ_SPH;          // hi then lo
 enum {
   B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
   B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY, B_OST_FULL, B_OST_EMPTY,
-  B_ZR, B_DRAIN = B_ZR + 2, NBAR = B_DRAIN + 3
+  B_ZR, B_P_HALF = B_ZR + 2, B_DRAIN, NBAR = B_DRAIN + 3
 };
 constexpr uint32_t RED_ROW = 208;                 // 192 bytes of fp32 + 16 (bank spread)
 constexpr uint32_t RED_WARP_BYTES = 32 * RED_ROW;
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       uint32_t cnt = 1;
       if (i == B_EMPTY || i == B_EMPTY + 1) cnt = 3;
       if (i == B_O_FULL) cnt = 2;
-      if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_U_EMPTY || i == B_SP_FULL ||
+      if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_P_HALF || i == B_U_EMPTY || i == B_SP_FULL ||
           i == B_O_EMPTY || i == B_OST_FULL || i == B_ZR || i == B_ZR + 1)
         cnt = 128;
       mbar_init(&bars[i], cnt);
@@ -482,14 +482,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           umma_commit(&bars[B_EMPTY + s]);
         } else if (warp == 3) {
           if (C::REVERSE && !mbar_wait(&bars[B_ZR + s], ph, a.wait_ns, abort_flag)) break;
-          if (!mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag)) break;
+          if (!mbar_wait(&bars[C::REVERSE ? B_P_HALF : B_P_FULL], pc, a.wait_ns, abort_flag)) break;
           if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
           tc_fence_after();
+          const SDesc dz = sdesc(st + C::ST_Z, C::NARROW ? 16384u : 8192u, 1024, LAYOUT_SW128);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ts(tmem + C::TM_OI, tmem + C::TM_P + 8u * kk,
-                    sdesc(st + C::ST_Z, C::NARROW ? 16384u : 8192u, 1024, LAYOUT_SW128) + (uint32_t)kk * 2048u, ID_PZ,
-                    kk > 0);
+          for (int kk = 0; kk < 4; ++kk)
+            umma_ts(tmem + C::TM_OI, tmem + C::TM_P + 8u * kk, dz + (uint32_t)kk * 2048u, ID_PZ, kk > 0);
+          if (C::REVERSE && !mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 4; kk < 8; ++kk)
+            umma_ts(tmem + C::TM_OI, tmem + C::TM_P + 8u * kk, dz + (uint32_t)kk * 2048u, ID_PZ, 1);
           umma_commit(&bars[B_P_EMPTY]);
           umma_commit(&bars[B_O_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
@@ -552,7 +556,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       // scans the Z4 warps zero the rows j >= L of Z, which columns j >= L of P multiply.  Off the diagonal group the factors come from one table read and a
       // multiplicative chain toward larger |i - j| (values only shrink, so an underflow to zero loses
       // nothing); the diagonal group uses the lane's factors from the table, read once.
+      // Reverse scans: P columns 0..63 (groups 0, 1, scaled first by the row blocks with the most
+      // groups) are announced on their own, so that MMA2 can take its first four K steps while the
+      // later groups are scaled.  (In the forward scans this measured slower.)
       const int g_first = C::REVERSE ? q : 0, g_last = C::REVERSE ? 3 : q;
+      if (C::REVERSE && g_first > 1) mbar_arrive(&bars[B_P_HALF]);
       for (int g = g_first; g <= g_last; ++g) {
         uint32_t r[32];
         tmem_ld32(lane_addr + C::TM_A + 32u * g, r);
@@ -590,6 +598,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           }
         }
         tmem_st16(lane_addr + C::TM_P + 16u * g, pkg);
+        if (C::REVERSE && g == 1) {
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          mbar_arrive(&bars[B_P_HALF]);
+        }
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
