@@ -98,8 +98,10 @@ constexpr uint32_t SZ_SP = 2 * SZ_SPH;          // hi then lo
 enum {
   B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
   B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY, B_OST_FULL, B_OST_EMPTY,
-  B_ZR, B_P_HALF = B_ZR + 2, B_DRAIN, NBAR = B_DRAIN + 3
+  B_ZR, B_P_HALF = B_ZR + 2, B_TBL_FULL, B_TBL_EMPTY = B_TBL_FULL + 2, B_DRAIN = B_TBL_EMPTY + 2,
+  NBAR = B_DRAIN + 3
 };
+constexpr int PW_FLOATS = 2 * 129;  // lambda^d and scale * lambda^d, d = 0..128
 constexpr uint32_t RED_ROW = 208;                 // 192 bytes of fp32 + 16 (bank spread)
 constexpr uint32_t RED_WARP_BYTES = 32 * RED_ROW;
 template <int MODE>
@@ -111,7 +113,7 @@ struct Smem {
   // contiguous row segments
   static constexpr uint32_t OFF_OST = OFF_SP + SZ_SP;
   static constexpr uint32_t OFF_PW = OFF_OST + (Cfg<MODE>::NARROW ? 4u * RED_WARP_BYTES : SZ_TILE64);
-  static constexpr uint32_t OFF_BAR = OFF_PW + 2 * 129 * 4 + 8;
+  static constexpr uint32_t OFF_BAR = OFF_PW + 2 * PW_FLOATS * 4 + 8;  // two tables (per unit parity)
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;
   static_assert(BYTES <= 232448, "shared memory budget");
@@ -338,24 +340,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SMM::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SMM::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SMM::OFF_MISC + 4);
-  float* pw = reinterpret_cast<float*>(sm + SMM::OFF_PW);  // lambda^d, d = 0..128
-  float* pws = pw + 129;                                    // scale * lambda^d
+  // Decay tables of a work unit (lambda^d and scale * lambda^d, d = 0..128), two buffers used by
+  // alternate units of this CTA.
+  float* const pw_base = reinterpret_cast<float*>(sm + SMM::OFF_PW);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int n, h, tile;
-  unit_of_block(a, NTILE, n, h, tile);
-  long long tb, te;
-  seq_range(a, n, tb, te);
-  const int len = (int)(te - tb);
-  const int nc = (len + CHUNK - 1) / CHUNK;
-  const int col0 = tile * TN;
-  // iteration `it` visits chunk chunk_of(it): ascending, or descending for the reverse scans
-  auto chunk_of = [&](int it) { return C::REVERSE ? nc - 1 - it : it; };
+  // Persistent CTAs: this CTA runs work units blockIdx.x, blockIdx.x + gridDim.x, ... (a unit is a
+  // (sequence, head, 64-column tile of d_v)); the chunk pipeline runs on across unit boundaries,
+  // so a unit's first loads overlap the previous unit's last chunks.  Barrier phases count the
+  // CTA's chunks over all its units (gk).
+  const int n_units = a.n_seq * a.H * NTILE;  // below 2^31 (checked on the host)
+  struct Unit {
+    int n, h, tile, len, nc;
+    long long tb;
+  };
+  auto unit_at = [&](int u) {
+    Unit w;
+    unit_of(a, NTILE, u, w.n, w.h, w.tile);
+    long long te;
+    seq_range(a, w.n, w.tb, te);
+    w.len = (int)(te - w.tb);
+    w.nc = (w.len + CHUNK - 1) / CHUNK;
+    return w;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
       uint32_t cnt = 1;
       if (i == B_EMPTY || i == B_EMPTY + 1) cnt = 3;
+      if (i == B_TBL_FULL || i == B_TBL_FULL + 1) cnt = 128;   // the Z4 warps write a unit's table
+      if (i == B_TBL_EMPTY || i == B_TBL_EMPTY + 1) cnt = 384; // mask, Z4 and epilogue warps read it
       if (i == B_O_FULL) cnt = 2;
       if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_P_HALF || i == B_U_EMPTY || i == B_SP_FULL ||
           i == B_O_EMPTY || i == B_OST_FULL || i == B_ZR || i == B_ZR + 1)
@@ -365,12 +379,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
-  }
-  if (threadIdx.x < 129) {
-    const float ll = a.log_lambda[h];
-    const float p = threadIdx.x == 0 ? 1.f : expf((float)threadIdx.x * ll);
-    pw[threadIdx.x] = p;
-    pws[threadIdx.x] = a.scale * p;
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -393,15 +401,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     setmaxnreg_dec<REG_CTRL>();
     if (lane == 0) {
       int issued[2] = {0, 0};
-      for (int it = 0; it < nc; ++it) {
-        const int c = chunk_of(it);
-        const int s = it & 1;
-        const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-        if (!mbar_wait(&bars[B_EMPTY + s], ph ^ 1u, a.wait_ns, abort_flag)) break;
+      int gk = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+       const Unit w = unit_at(u);
+       const int h = w.h, col0 = w.tile * TN;
+       for (int it = 0; it < w.nc; ++it, ++gk) {
+        const int c = C::REVERSE ? w.nc - 1 - it : it;
+        const int s = gk & 1;
+        const uint32_t ph = (uint32_t)(gk >> 1) & 1u;
+        if (!mbar_wait(&bars[B_EMPTY + s], ph ^ 1u, a.wait_ns, abort_flag)) { stop = true; break; }
         const uint32_t st = sbase + (uint32_t)s * C::SZ_STAGE;
         uint64_t* full = &bars[B_FULL + s];
         mbar_expect_tx(full, C::SZ_STAGE);
-        const int tok = (int)(tb + (long long)c * CHUNK);
+        const int tok = (int)(w.tb + (long long)c * CHUNK);
         if (C::NARROW) {
           tma_load_3d(st + C::ST_X, &maps.x, full, col0, h, tok);
           tma_load_3d(st + C::ST_Y, &maps.y, full, col0, h, tok);
@@ -415,6 +428,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           tma_load_3d(st + C::ST_Z, &maps.z, full, col0, h, tok);
         }
         ++issued[s];
+       }
       }
       // Never leave a copy in flight into shared memory that is about to be released.
       for (int s = 0; s < 2; ++s)
@@ -435,9 +449,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       //   Y: K-major (wide: two 128B panels);  Z, K4, weighted Z4: MN-major
       //   state copy: MN-major [hi | lo] (wide) or K-major (narrow)
       const SDesc dvt = sdesc(sbase + SMM::OFF_VT, SZ_TILE64, 1024, LAYOUT_SW128);
-      for (int it = 0; it < nc; ++it) {
-        const int s = it & 1;
-        const uint32_t ph = (uint32_t)(it >> 1) & 1u, pc = (uint32_t)it & 1u;
+      int gk = 0;
+      bool stop = false;
+      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+       const int nc = unit_at(u).nc;
+       for (int it = 0; it < nc; ++it, ++gk) {
+        const int s = gk & 1;
+        const uint32_t ph = (uint32_t)(gk >> 1) & 1u, pc = (uint32_t)gk & 1u;
         const uint32_t st = sbase + (uint32_t)s * C::SZ_STAGE;
         const SDesc dx = sdesc(st + C::ST_X, 16, 1024, LAYOUT_SW128);
         const SDesc dx1 = sdesc(st + C::ST_X1, 16, 512, LAYOUT_SW64);
@@ -445,9 +463,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         auto x_step = [&](int kk) {
           return C::NARROW ? dx + (uint32_t)kk * 32u : (kk < 4 ? dx + (uint32_t)kk * 32u : dx1 + (uint32_t)(kk - 4) * 32u);
         };
-        if (!mbar_wait(&bars[B_FULL + s], ph, a.wait_ns, abort_flag)) break;
+        if (!mbar_wait(&bars[B_FULL + s], ph, a.wait_ns, abort_flag)) { stop = true; break; }
         if (warp == 1) {
-          if (!mbar_wait(&bars[B_A_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
+          if (!mbar_wait(&bars[B_A_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) { stop = true; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < C::K1; ++kk) {
@@ -460,8 +478,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           // the state before this chunk (one buffer: the epilogue overwrites it after this MMA3)
           const uint32_t spb = sbase + SMM::OFF_SP;
           const SDesc dsp = C::NARROW ? sdesc(spb, 16, 1024, LAYOUT_SW128) : sdesc(spb, SZ_SPH, 1024, LAYOUT_SW128);
-          if (!mbar_wait(&bars[B_SP_FULL], pc, a.wait_ns, abort_flag)) break;
-          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
+          if (!mbar_wait(&bars[B_SP_FULL], pc, a.wait_ns, abort_flag)) { stop = true; break; }
+          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) { stop = true; break; }
           tc_fence_after();
           if (C::NARROW) {
             // state tile as a K-major B operand: N = 96 rows (d_k), K = this tile's 64 columns
@@ -481,15 +499,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           umma_commit(&bars[B_O_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
         } else if (warp == 3) {
-          if (C::REVERSE && !mbar_wait(&bars[B_ZR + s], ph, a.wait_ns, abort_flag)) break;
-          if (!mbar_wait(&bars[C::REVERSE ? B_P_HALF : B_P_FULL], pc, a.wait_ns, abort_flag)) break;
-          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
+          if (C::REVERSE && !mbar_wait(&bars[B_ZR + s], ph, a.wait_ns, abort_flag)) { stop = true; break; }
+          if (!mbar_wait(&bars[C::REVERSE ? B_P_HALF : B_P_FULL], pc, a.wait_ns, abort_flag)) { stop = true; break; }
+          if (!mbar_wait(&bars[B_O_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) { stop = true; break; }
           tc_fence_after();
           const SDesc dz = sdesc(st + C::ST_Z, C::NARROW ? 16384u : 8192u, 1024, LAYOUT_SW128);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma_ts(tmem + C::TM_OI, tmem + C::TM_P + 8u * kk, dz + (uint32_t)kk * 2048u, ID_PZ, kk > 0);
-          if (C::REVERSE && !mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag)) break;
+          if (C::REVERSE && !mbar_wait(&bars[B_P_FULL], pc, a.wait_ns, abort_flag)) { stop = true; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 4; kk < 8; ++kk)
@@ -498,8 +516,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           umma_commit(&bars[B_O_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
         } else {
-          if (!mbar_wait(&bars[B_VT_FULL], pc, a.wait_ns, abort_flag)) break;
-          if (!mbar_wait(&bars[B_U_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) break;
+          if (!mbar_wait(&bars[B_VT_FULL], pc, a.wait_ns, abort_flag)) { stop = true; break; }
+          if (!mbar_wait(&bars[B_U_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) { stop = true; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -509,6 +527,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           umma_commit(&bars[B_VT_EMPTY]);
           umma_commit(&bars[B_EMPTY + s]);
         }
+       }
       }
       // All MMAs (and their barrier arrivals) finish before tensor memory is released.
       uint64_t* drain = &bars[B_DRAIN + (warp - 1)];
@@ -522,18 +541,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     const int i = threadIdx.x - 128;  // query row = tensor-memory lane
     const int q = warp & 3;           // this warp's lanes are rows 32q .. 32q + 31
     const uint32_t lane_addr = tmem + ((uint32_t)(q << 5) << 16);
-    const float lam = pw[1];
-    const float2 lam2 = make_float2(lam * lam, lam * lam);
-    // Decay factors of the diagonal group for this lane: s lambda^(i-j) (forward, j <= i) or
-    // s lambda^(j-i) (reverse, j >= i), zero across the diagonal; element pair e is columns
-    // 32q + 2e and 32q + 2e + 1.
-    float2 dgf[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int d0 = C::REVERSE ? 2 * e - lane : lane - 2 * e;
-      const int d1 = C::REVERSE ? d0 + 1 : d0 - 1;
-      dgf[e] = make_float2(d0 >= 0 ? pws[max(d0, 0)] : 0.f, d1 >= 0 ? pws[max(d1, 0)] : 0.f);
-    }
     {  // P groups on the far side of this warp's diagonal stay zero for the whole kernel
       uint32_t z[16];
 #pragma unroll
@@ -542,20 +549,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         if (C::REVERSE ? g < q : g > q) tmem_st16(lane_addr + C::TM_P + 16u * g, z);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     }
-    for (int it = 0; it < nc; ++it) {
-      const int c = chunk_of(it);
-      const uint32_t pc = (uint32_t)it & 1u;
-      const int L = min(CHUNK, len - c * CHUNK);
-      if (!warp_wait(&bars[B_A_FULL], pc, a, abort_flag)) break;
-      if (!warp_wait(&bars[B_P_EMPTY], pc ^ 1u, a, abort_flag)) break;
+    int gk = 0, ku = 0;
+    bool stop = false;
+    for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x, ++ku) {
+     const int nc = unit_at(u).nc;
+     const int tbuf = ku & 1;
+     if (!warp_wait(&bars[B_TBL_FULL + tbuf], (uint32_t)(ku >> 1) & 1u, a, abort_flag)) break;
+     const float* pws = pw_base + tbuf * PW_FLOATS + 129;  // scale * lambda^d of this unit's head
+     const float lam = pw_base[tbuf * PW_FLOATS + 1];
+     const float2 lam2 = make_float2(lam * lam, lam * lam);
+     // Decay factors of the diagonal group for this lane: s lambda^(i-j) (forward, j <= i) or
+     // s lambda^(j-i) (reverse, j >= i), zero across the diagonal; element pair e is columns
+     // 32q + 2e and 32q + 2e + 1.
+     float2 dgf[16];
+#pragma unroll
+     for (int e = 0; e < 16; ++e) {
+       const int d0 = C::REVERSE ? 2 * e - lane : lane - 2 * e;
+       const int d1 = C::REVERSE ? d0 + 1 : d0 - 1;
+       dgf[e] = make_float2(d0 >= 0 ? pws[max(d0, 0)] : 0.f, d1 >= 0 ? pws[max(d1, 0)] : 0.f);
+     }
+     for (int it = 0; it < nc; ++it, ++gk) {
+      const uint32_t pc = (uint32_t)gk & 1u;
+      if (!warp_wait(&bars[B_A_FULL], pc, a, abort_flag)) { stop = true; break; }
+      if (!warp_wait(&bars[B_P_EMPTY], pc ^ 1u, a, abort_flag)) { stop = true; break; }
       tc_fence_after();
       // P row i, one 32-column group at a time, stored straight back to tensor memory.
       //   forward scans: s lambda^(i-j) A_ij for j <= i;  reverse scans: s lambda^(j-i) A_ij for j >= i.
       // Nothing is masked at the sequence end of a partial chunk: forward rows i >= L only reach
       // output rows that are never stored (j <= i < L bounds the rows that are), and in the reverse
-      // scans the Z4 warps zero the rows j >= L of Z, which columns j >= L of P multiply.  Off the diagonal group the factors come from one table read and a
-      // multiplicative chain toward larger |i - j| (values only shrink, so an underflow to zero loses
-      // nothing); the diagonal group uses the lane's factors from the table, read once.
+      // scans the Z4 warps zero the rows j >= L of Z, which columns j >= L of P multiply.  Off the
+      // diagonal group the factors come from one table read and a multiplicative chain toward
+      // larger |i - j| (values only shrink, so an underflow to zero loses nothing); the diagonal
+      // group uses the lane's factors, read from the table once per unit.
       // Reverse scans: P columns 0..63 (groups 0, 1, scaled first by the row blocks with the most
       // groups) are announced on their own, so that MMA2 can take its first four K steps while the
       // later groups are scaled.  (In the forward scans this measured slower.)
@@ -607,18 +632,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       mbar_arrive(&bars[B_P_FULL]);
+     }
+     mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------------ weighted Z4 (hi and lo)
     setmaxnreg_dec<REG_Z4>();
     const int t = threadIdx.x - 384;  // row of the chunk
-    for (int it = 0; it < nc; ++it) {
-      const int c = chunk_of(it);
-      const int s = it & 1;
-      const uint32_t ph = (uint32_t)(it >> 1) & 1u, pc = (uint32_t)it & 1u;
-      const int L = min(CHUNK, len - c * CHUNK);
-      if (!warp_wait(&bars[B_FULL + s], ph, a, abort_flag)) break;
-      if (!warp_wait(&bars[B_VT_EMPTY], pc ^ 1u, a, abort_flag)) break;
+    int gk = 0, ku = 0;
+    bool stop = false;
+    for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x, ++ku) {
+     const Unit w = unit_at(u);
+     // This unit's decay table, into the buffer that unit ku - 2 used (once all its readers are done).
+     const int tbuf = ku & 1;
+     float* pw = pw_base + tbuf * PW_FLOATS;
+     float* pws = pw + 129;
+     if (ku >= 2 && !warp_wait(&bars[B_TBL_EMPTY + tbuf], (uint32_t)((ku - 2) >> 1) & 1u, a, abort_flag)) break;
+     {
+       const float ll = a.log_lambda[w.h];
+       for (int d = t; d <= 128; d += 128) {
+         const float pv = d == 0 ? 1.f : expf((float)d * ll);
+         pw[d] = pv;
+         pws[d] = a.scale * pv;
+       }
+     }
+     mbar_arrive(&bars[B_TBL_FULL + tbuf]);
+     if (!warp_wait(&bars[B_TBL_FULL + tbuf], (uint32_t)(ku >> 1) & 1u, a, abort_flag)) break;
+     for (int it = 0; it < w.nc; ++it, ++gk) {
+      const int c = C::REVERSE ? w.nc - 1 - it : it;
+      const int s = gk & 1;
+      const uint32_t ph = (uint32_t)(gk >> 1) & 1u, pc = (uint32_t)gk & 1u;
+      const int L = min(CHUNK, w.len - c * CHUNK);
+      if (!warp_wait(&bars[B_FULL + s], ph, a, abort_flag)) { stop = true; break; }
+      if (!warp_wait(&bars[B_VT_EMPTY], pc ^ 1u, a, abort_flag)) { stop = true; break; }
       const uint8_t* zsrc = sm + s * C::SZ_STAGE + C::ST_Z4;
       uint8_t* zhi = sm + SMM::OFF_VT;
       uint8_t* zlo = sm + SMM::OFF_VT + SZ_TILE64;
@@ -649,28 +695,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       fence_async_smem();
       mbar_arrive(&bars[B_VT_FULL]);
       if (C::REVERSE) mbar_arrive(&bars[B_ZR + s]);
+     }
+     mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
     }
   } else {
     // ------------------------------------------------------------------ epilogue
     setmaxnreg_inc<REG_WIDE>();
     const int r_ = ((warp & 3) << 5) + lane;  // d_k row of the state and U; query row of O
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
-    const long long sbase_g = (((long long)n * a.H + h) * DK + r_) * DV + col0;
     const bool out32 = (reinterpret_cast<uintptr_t>(prm.out) & 31u) == 0;
     float S[TN];
-#pragma unroll
-    for (int x = 0; x < TN; ++x) S[x] = 0.f;
-    if (prm.s0 && r_ < DK) {
-      const float4* src = reinterpret_cast<const float4*>(prm.s0 + sbase_g);
-#pragma unroll
-      for (int x = 0; x < TN / 4; ++x) {
-        const float4 v4 = src[x];
-        S[4 * x] = v4.x;
-        S[4 * x + 1] = v4.y;
-        S[4 * x + 2] = v4.z;
-        S[4 * x + 3] = v4.w;
-      }
-    }
     auto write_sprev = [&]() {
       if (r_ < DK) {
         const uint32_t row = sbase + SMM::OFF_SP + (uint32_t)r_ * 128u;
@@ -687,15 +721,37 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       fence_async_smem();
       mbar_arrive(&bars[B_SP_FULL]);
     };
-    // Iteration it: the state update of chunk it, the state copy for chunk it + 1, the output rows
-    // of chunk it (it = -1 only writes the copy of the initial state).  One site for each part
-    // keeps the code small.
+    // Iteration it of a unit: the state update of chunk it, the state copy for chunk it + 1, the
+    // output rows of chunk it (it = -1 only loads the initial state and writes its copy).  One site
+    // for each part keeps the code small.
     bool aborted = false;
     int nst = 0;  // full chunks stored through the staging tile
-    for (int it = -1; it < nc; ++it) {
-      const uint32_t pc = (uint32_t)it & 1u;
-      const int c = it >= 0 ? chunk_of(it) : 0;
-      const int L = min(CHUNK, len - c * CHUNK);
+    int gk = 0, ku = 0;
+    for (int u = blockIdx.x; u < n_units && !aborted; u += gridDim.x, ++ku) {
+     const Unit w = unit_at(u);
+     const int h = w.h, col0 = w.tile * TN, nc = w.nc, tbuf = ku & 1;
+     const long long sbase_g = (((long long)w.n * a.H + h) * DK + r_) * DV + col0;
+     if (!warp_wait(&bars[B_TBL_FULL + tbuf], (uint32_t)(ku >> 1) & 1u, a, abort_flag)) { aborted = true; break; }
+     const float* pw = pw_base + tbuf * PW_FLOATS;
+     const float* pws = pw + 129;
+#pragma unroll
+     for (int x = 0; x < TN; ++x) S[x] = 0.f;
+     if (prm.s0 && r_ < DK) {
+       const float4* src = reinterpret_cast<const float4*>(prm.s0 + sbase_g);
+#pragma unroll
+       for (int x = 0; x < TN / 4; ++x) {
+         const float4 v4 = src[x];
+         S[4 * x] = v4.x;
+         S[4 * x + 1] = v4.y;
+         S[4 * x + 2] = v4.z;
+         S[4 * x + 3] = v4.w;
+       }
+     }
+     for (int it = -1; it < nc; ++it) {
+      const int g = gk + it;  // the CTA's chunk count
+      const uint32_t pc = (uint32_t)g & 1u;
+      const int c = it < 0 ? 0 : (C::REVERSE ? nc - 1 - it : it);
+      const int L = min(CHUNK, w.len - c * CHUNK);
       if (it >= 0) {
         // state <- lambda^L state + U_hi + U_lo
         if (!warp_wait(&bars[B_U_FULL], pc, a, abort_flag)) { aborted = true; break; }
@@ -717,7 +773,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         mbar_arrive(&bars[B_U_EMPTY]);
       }
       if (it + 1 < nc) {  // after MMA3 of this chunk has read the previous copy
-        if (it >= 0 && !warp_wait(&bars[B_SP_EMPTY], pc, a, abort_flag)) { aborted = true; break; }
+        if (g >= 0 && !warp_wait(&bars[B_SP_EMPTY], pc, a, abort_flag)) { aborted = true; break; }
         write_sprev();
       }
       if (it < 0) continue;
@@ -725,7 +781,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       if (!warp_wait(&bars[B_O_FULL], pc, a, abort_flag)) { aborted = true; break; }
       tc_fence_after();
       const float gf = C::REVERSE ? (r_ < L ? pw[L - 1 - r_] : 0.f) : pws[r_ + 1];
-      const long long orow = (tb + (long long)c * CHUNK + r_) * a.H + h;
+      const long long orow = (w.tb + (long long)c * CHUNK + r_) * a.H + h;
       if (!C::NARROW) {
         // Full chunks go through the staging tile and one TMA store (a whole 128 x 64 tile, no
         // per-row stores on the load/store pipe); a partial last chunk is stored row by row so that
@@ -773,7 +829,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
           mbar_arrive(&bars[B_OST_FULL]);
           if ((warp & 3) == 0) {  // the whole warp waits (so that an abort leaves it in step)
             if (!warp_wait(&bars[B_OST_FULL], (uint32_t)nst & 1u, a, abort_flag)) { aborted = true; break; }
-            if (lane == 0) tma_store_3d(&maps.o, sbase + SMM::OFF_OST, col0, h, (int)(tb + (long long)c * CHUNK));
+            if (lane == 0) tma_store_3d(&maps.o, sbase + SMM::OFF_OST, col0, h, (int)(w.tb + (long long)c * CHUNK));
           }
           ++nst;
         }
@@ -782,7 +838,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         // into the warp's region, then the warp adds contiguous 16-byte pieces (12 per row), so one
         // red.add instruction covers about three rows' segments instead of 32 rows.
         const uint32_t wreg = sbase + SMM::OFF_OST + (uint32_t)(warp & 3) * RED_WARP_BYTES;
-        const long long row0 = (tb + (long long)c * CHUNK + ((warp & 3) << 5)) * a.H + h;  // lane 0's row
+        const long long row0 = (w.tb + (long long)c * CHUNK + ((warp & 3) << 5)) * a.H + h;  // lane 0's row
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -816,12 +872,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
         }
       }
     }
-    if (!C::NARROW && r_ == 0 && nst > 0) bulk_wait_all();  // the last tile store has completed
-    if (!aborted && prm.s_out && r_ < DK) {
-      float4* dst = reinterpret_cast<float4*>(prm.s_out + sbase_g);
+     if (aborted) break;
+     if (prm.s_out && r_ < DK) {
+       float4* dst = reinterpret_cast<float4*>(prm.s_out + sbase_g);
 #pragma unroll
-      for (int x = 0; x < TN / 4; ++x) dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+       for (int x = 0; x < TN / 4; ++x) dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+     }
+     mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
+     gk += nc;
     }
+    if (!C::NARROW && r_ == 0 && nst > 0) bulk_wait_all();  // the last tile store has completed
   }
 
   tc_fence_before();
@@ -874,12 +934,16 @@ bool make_map(CUtensorMap* m, const void* base, int d, int H, long long T, int b
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// max_ctas > 0 makes the CTAs persistent: at most max_ctas of them, each running every
+// gridDim.x-th work unit; 0 launches one CTA per unit and leaves the order to the block scheduler.
 template <int MODE>
-cudaError_t launch_scan(const void* X, const void* Y, const void* Z, const ScanParams& p, cudaStream_t stream) {
+cudaError_t launch_scan(const void* X, const void* Y, const void* Z, const ScanParams& p, cudaStream_t stream,
+                        int max_ctas) {
   using C = Cfg<MODE>;
   const ChunkArgs& a = p.a;
-  const long long blocks = (long long)a.n_seq * a.H * NTILE;
+  long long blocks = (long long)a.n_seq * a.H * NTILE;  // work units
   if (blocks == 0) return cudaSuccess;
+  if (max_ctas > 0 && blocks > max_ctas) blocks = max_ctas;
   const long long T_total = a.cu_seqlens ? (long long)a.T : (long long)a.n_seq * a.T;
   TmaMaps maps;
   memset(&maps, 0, sizeof(maps));
@@ -913,7 +977,17 @@ cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream) {
   p.s0 = a.h0;
   p.s_out = a.hT;
   p.out = a.o;
-  return launch_scan<MODE_FWD>(a.q, a.k, a.v, p, stream);
+  // Equal-length batches: one persistent CTA per SM (a unit's first loads overlap the previous
+  // unit's last chunks).  Packed varlen batches: one CTA per unit, so that the block scheduler
+  // hands the next (longest-first) unit to whichever SM frees up.
+  int max_ctas = 0;
+  if (!a.cu_seqlens) {
+    int dev = 0;
+    max_ctas = 152;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&max_ctas, cudaDevAttrMultiProcessorCount, dev);
+  }
+  return launch_scan<MODE_FWD>(a.q, a.k, a.v, p, stream, max_ctas);
 }
 
 namespace {
@@ -966,10 +1040,10 @@ cudaError_t launch_tc_bwd(const ChunkArgs& a, float* acc_q, float* acc_k, cudaSt
     p.out = acc_p;
     if (dk_scan) {
       p.s0 = a.dhT;
-      r = launch_scan<MODE_DK>(a.v, a.dO, a.q, p, st);
+      r = launch_scan<MODE_DK>(a.v, a.dO, a.q, p, st, 0);
     } else {
       p.s0 = a.h0;
-      r = launch_scan<MODE_DQ>(a.dO, a.v, a.k, p, st);
+      r = launch_scan<MODE_DQ>(a.dO, a.v, a.k, p, st, 0);
     }
     if (r != cudaSuccess) return r;
     if (n4 > 0) {
@@ -993,7 +1067,7 @@ cudaError_t launch_tc_bwd(const ChunkArgs& a, float* acc_q, float* acc_k, cudaSt
     p.s0 = a.dhT;
     p.s_out = a.hT;  // dh0
     p.out = a.dv;
-    e = launch_scan<MODE_DV>(a.k, a.q, a.dO, p, stream);
+    e = launch_scan<MODE_DV>(a.k, a.q, a.dO, p, stream, 0);
   }
   if (e == cudaSuccess) e = cudaEventRecord(ev[1], side[0]);
   if (e == cudaSuccess) e = cudaEventRecord(ev[2], side[1]);

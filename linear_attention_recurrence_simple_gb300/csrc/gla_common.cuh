@@ -63,16 +63,18 @@ __device__ __forceinline__ void seq_range(const ChunkArgs& a, int n, long long& 
   }
 }
 
-// Splits a 1-D block index into (sequence, head, tile) with the sequence slowest, so that with
-// a longest-first order the longest sequences start first.
-__device__ __forceinline__ void unit_of_block(const ChunkArgs& a, int tiles, int& n, int& h, int& tile) {
-  const long long b = blockIdx.x;
-  const long long per_seq = (long long)a.H * tiles;
-  const int rank = (int)(b / per_seq);
-  const int rem = (int)(b % per_seq);
+// Splits a 1-D work-unit index into (sequence, head, tile) with the sequence slowest, so that
+// with a longest-first order the longest sequences start first.
+__device__ __forceinline__ void unit_of(const ChunkArgs& a, int tiles, int b, int& n, int& h, int& tile) {
+  const unsigned per_seq = (unsigned)a.H * (unsigned)tiles;  // the host keeps unit counts below 2^31
+  const int rank = (int)((unsigned)b / per_seq);
+  const int rem = (int)((unsigned)b - (unsigned)rank * per_seq);
   h = rem / tiles;
   tile = rem % tiles;
   n = a.order ? a.order[rank] : rank;
+}
+__device__ __forceinline__ void unit_of_block(const ChunkArgs& a, int tiles, int& n, int& h, int& tile) {
+  unit_of(a, tiles, (int)blockIdx.x, n, h, tile);
 }
 
 __device__ __forceinline__ unsigned long long global_timer_ns() {
