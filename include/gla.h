@@ -58,7 +58,7 @@ typedef enum {
   GLA_OK = 0,
   GLA_ERR_NULL = -1,        /* a required pointer is NULL */
   GLA_ERR_SHAPE = -2,       /* negative size, bad cu_seqlens, pool slot out of range, or
-                               n_seq * H * 8 or the token count reaches 2^31 */
+                               n_seq * H * 96 or the token count reaches 2^31 */
   GLA_ERR_DTYPE = -3,       /* dtype is not a gla_dtype */
   GLA_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned */
   GLA_ERR_UNSUPPORTED = -5, /* d_k != 96, d_v != 192, or no sm_103 device current */

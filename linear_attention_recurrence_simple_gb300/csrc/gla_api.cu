@@ -81,8 +81,8 @@ int check_chunk_call(int n_seq, int T, int H, int dk, int dv, int dtype, const i
   if (dk != GLA_DK || dv != GLA_DV) return GLA_ERR_UNSUPPORTED;
   if (n_seq < 0 || T < 0 || H < 1) return GLA_ERR_SHAPE;
   *tokens = cu_seqlens ? (long long)T : (long long)n_seq * T;
-  // work units (sequence, head, column tile) and token coordinates are 32-bit on the device
-  if ((long long)n_seq * H * 8 >= (1ll << 31) || *tokens >= (1ll << 31)) return GLA_ERR_SHAPE;
+  // state rows (sequence, head, d_k row), work units and token coordinates are 32-bit on the device
+  if ((long long)n_seq * H * GLA_DK >= (1ll << 31) || *tokens >= (1ll << 31)) return GLA_ERR_SHAPE;
   if (cu_seqlens) {
     if ((uintptr_t)cu_seqlens & 3u) return GLA_ERR_ALIGN;
     if (n_seq > 0) {

@@ -98,8 +98,8 @@ constexpr uint32_t SZ_SP = 2 * SZ_SPH;          // hi then lo
 enum {
   B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
   B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY, B_OST_FULL, B_OST_EMPTY,
-  B_ZR, B_P_HALF = B_ZR + 2, B_TBL_FULL, B_TBL_EMPTY = B_TBL_FULL + 2, B_DRAIN = B_TBL_EMPTY + 2,
-  NBAR = B_DRAIN + 3
+  B_ZR, B_P_HALF = B_ZR + 2, B_TBL_FULL, B_TBL_EMPTY = B_TBL_FULL + 2, B_ST_FULL = B_TBL_EMPTY + 2, B_ST_EMPTY,
+  B_DRAIN, NBAR = B_DRAIN + 3
 };
 constexpr int PW_FLOATS = 2 * 129;  // lambda^d and scale * lambda^d, d = 0..128
 constexpr uint32_t RED_ROW = 208;                 // 192 bytes of fp32 + 16 (bank spread)
@@ -155,7 +155,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Shared -> global tile store (bulk-group completion), and the waits on this thread's bulk groups.
+// Shared -> global tile store (bulk-group completion), and the wait for this thread's bulk groups
+// to have read shared memory (the global writes are complete by the end of the grid).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"((uint64_t)map),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"((uint64_t)map),
                "r"(x), "r"(y), "r"(z), "r"(src)
@@ -163,7 +170,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void umma(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc, uint32_t acc) {
   asm volatile(
@@ -307,6 +313,7 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
 
 struct TmaMaps {
   CUtensorMap x, x1, y, z, o;  // o: the bf16 output (wide modes)
+  CUtensorMap s;                // fp32 final state (forward), 32-column x 96-row boxes
 };
 
 // What a scan kernel needs besides its tensor maps: sequence layout and decay (in `a`), the
@@ -371,6 +378,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       if (i == B_TBL_FULL || i == B_TBL_FULL + 1) cnt = 128;   // the Z4 warps write a unit's table
       if (i == B_TBL_EMPTY || i == B_TBL_EMPTY + 1) cnt = 384; // mask, Z4 and epilogue warps read it
       if (i == B_O_FULL) cnt = 2;
+      if (i == B_ST_FULL) cnt = 128;  // the epilogue threads have staged the final state
       if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_P_HALF || i == B_U_EMPTY || i == B_SP_FULL ||
           i == B_O_EMPTY || i == B_OST_FULL || i == B_ZR || i == B_ZR + 1)
         cnt = 128;
@@ -730,14 +738,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     for (int u = blockIdx.x; u < n_units && !aborted; u += gridDim.x, ++ku) {
      const Unit w = unit_at(u);
      const int h = w.h, col0 = w.tile * TN, nc = w.nc, tbuf = ku & 1;
-     const long long sbase_g = (((long long)w.n * a.H + h) * DK + r_) * DV + col0;
      if (!warp_wait(&bars[B_TBL_FULL + tbuf], (uint32_t)(ku >> 1) & 1u, a, abort_flag)) { aborted = true; break; }
      const float* pw = pw_base + tbuf * PW_FLOATS;
      const float* pws = pw + 129;
+     const uint32_t spb = sbase + SMM::OFF_SP;
+     const int srow0 = (w.n * a.H + h) * DK;  // the unit's first state row
 #pragma unroll
      for (int x = 0; x < TN; ++x) S[x] = 0.f;
+     if (MODE == MODE_FWD && prm.s_out && ku > 0) {  // the previous unit's final-state store has read the buffer
+       if (r_ == 0) {
+         bulk_wait_read_all();
+         mbar_arrive(&bars[B_ST_EMPTY]);
+       }
+       if (!warp_wait(&bars[B_ST_EMPTY], (uint32_t)(ku - 1) & 1u, a, abort_flag)) { aborted = true; break; }
+     }
      if (prm.s0 && r_ < DK) {
-       const float4* src = reinterpret_cast<const float4*>(prm.s0 + sbase_g);
+       const float4* src = reinterpret_cast<const float4*>(prm.s0 + ((long long)srow0 + r_) * DV + col0);
 #pragma unroll
        for (int x = 0; x < TN / 4; ++x) {
          const float4 v4 = src[x];
@@ -873,15 +889,39 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       }
     }
      if (aborted) break;
-     if (prm.s_out && r_ < DK) {
-       float4* dst = reinterpret_cast<float4*>(prm.s_out + sbase_g);
+     if (MODE == MODE_FWD && prm.s_out) {
+       // Forward (persistent CTAs): the final state leaves through the state-copy buffer and two
+       // TMA stores of 32-column halves (128B-swizzled fp32 rows; thread r_'s row covers exactly
+       // the bytes of its own hi and lo copy rows), so that 96 rows of per-thread global stores do
+       // not hold up the load/store pipe at the unit boundary.  The buffer is free: every thread
+       // has waited for the unit's last O_FULL, which follows its last MMA3.  The next unit's
+       // first state copy waits (B_ST_EMPTY) until the stores have read it.
+       if (r_ < DK) {
+#pragma unroll
+         for (int x = 0; x < TN / 4; ++x)
+           st_shared_v4(spb + (uint32_t)(x >> 3) * SZ_SPH + (uint32_t)r_ * 128u + ((uint32_t)((x & 7) ^ (r_ & 7)) << 4),
+                        __float_as_uint(S[4 * x]), __float_as_uint(S[4 * x + 1]), __float_as_uint(S[4 * x + 2]),
+                        __float_as_uint(S[4 * x + 3]));
+       }
+       fence_async_smem();
+       mbar_arrive(&bars[B_ST_FULL]);
+       if ((warp & 3) == 0) {  // the whole warp waits, lane 0 issues
+         if (!warp_wait(&bars[B_ST_FULL], (uint32_t)ku & 1u, a, abort_flag)) { aborted = true; break; }
+         if (lane == 0) {
+           tma_store_2d(&maps.s, spb, col0, srow0);
+           tma_store_2d(&maps.s, spb + SZ_SPH, col0 + 32, srow0);
+         }
+       }
+     }
+     if (MODE != MODE_FWD && prm.s_out && r_ < DK) {
+       float4* dst = reinterpret_cast<float4*>(prm.s_out + ((long long)srow0 + r_) * DV + col0);
 #pragma unroll
        for (int x = 0; x < TN / 4; ++x) dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
      }
      mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
      gk += nc;
     }
-    if (!C::NARROW && r_ == 0 && nst > 0) bulk_wait_all();  // the last tile store has completed
+    if (r_ == 0) bulk_wait_read_all();  // the last tile and state stores have read shared memory
   }
 
   tc_fence_before();
@@ -934,6 +974,20 @@ bool make_map(CUtensorMap* m, const void* base, int d, int H, long long T, int b
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D view [n_seq * H * 96, 192] of an fp32 state tensor [n_seq, H, 96, 192]; box = 32 columns x
+// 96 rows (half of a unit's tile), 128B swizzle.
+bool make_state_map(CUtensorMap* m, const void* base, long long rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)DV, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)DV * 4};
+  const cuuint32_t box[2] = {32, (cuuint32_t)DK};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // max_ctas > 0 makes the CTAs persistent: at most max_ctas of them, each running every
 // gridDim.x-th work unit; 0 launches one CTA per unit and leaves the order to the block scheduler.
 template <int MODE>
@@ -956,6 +1010,9 @@ cudaError_t launch_scan(const void* X, const void* Y, const void* Z, const ScanP
         (!C::NARROW && !make_map(&maps.o, p.out, DV, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B)))
       return cudaErrorInvalidValue;
   }
+  const long long state_rows = (long long)a.n_seq * a.H * DK;
+  if (MODE == MODE_FWD && p.s_out && !make_state_map(&maps.s, p.s_out, state_rows))
+    return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(tc_scan_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
