@@ -55,6 +55,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "gla_common.cuh"
 
@@ -66,16 +67,22 @@ namespace {
 
 constexpr int TN = 64;             // d_v columns per CTA
 constexpr int NTILE = DV / TN;     // 3
-constexpr int NTHREADS = 512;
-// Per-thread registers of the four warpgroups after setmaxnreg (launched with 128 each; the sum
-// times 128 threads must stay 65536): control (TMA + MMA issue), mask and epilogue, weighted Z4.
-constexpr int REG_CTRL = 64, REG_WIDE = 184, REG_Z4 = 80;
-static_assert(128 * (REG_CTRL + 2 * REG_WIDE + REG_Z4) == 65536, "register split");
 
 template <int MODE>
 struct Cfg {
   static constexpr bool REVERSE = MODE == MODE_DV || MODE == MODE_DK;  // reverse scan, j >= i mask
   static constexpr bool NARROW = MODE == MODE_DQ || MODE == MODE_DK;   // X, Y are 64-wide d_v tiles
+  // Warp roles: 16 warps with one epilogue warpgroup (forward), or 20 with the epilogue's state
+  // and output parts in two warpgroups (backward scans).  Per-thread registers of each warpgroup
+  // after setmaxnreg add up to the launch count times the number of warpgroups (the host checks
+  // the compiled count before the first launch: any other split could wait forever).
+  static constexpr bool SPLIT = MODE != MODE_FWD;
+  static constexpr int THREADS = SPLIT ? 640 : 512;
+  static constexpr int REG_LAUNCH = SPLIT ? 96 : 128;
+  static constexpr int REG_CTRL = 64, REG_MASK = SPLIT ? 112 : 184, REG_STATE = SPLIT ? 136 : 184;
+  static constexpr int REG_Z4 = SPLIT ? 72 : 80, REG_OUT = SPLIT ? 96 : 0;
+  static_assert(REG_CTRL + REG_MASK + REG_STATE + REG_Z4 + REG_OUT == THREADS / 128 * REG_LAUNCH, "register split");
+  static_assert(THREADS * REG_LAUNCH <= 65536, "launch registers");
   // shared memory of one stage (byte offsets; each tile 1024-aligned)
   //   wide:   X panel 0 (16 KB) | Y 2 panels (32 KB) | Z tile (16 KB) | X panel 1 (8 KB, 64B swizzle)
   //   narrow: X tile (16 KB) | Y tile (16 KB) | Z 2 panels (32 KB)
@@ -336,7 +343,7 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_constant__ TmaMaps maps, const ScanParams prm) {
+__global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __grid_constant__ TmaMaps maps, const ScanParams prm) {
   using C = Cfg<MODE>;
   using SMM = Smem<MODE>;
   const ChunkArgs& a = prm.a;
@@ -376,7 +383,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
       uint32_t cnt = 1;
       if (i == B_EMPTY || i == B_EMPTY + 1) cnt = 3;
       if (i == B_TBL_FULL || i == B_TBL_FULL + 1) cnt = 128;   // the Z4 warps write a unit's table
-      if (i == B_TBL_EMPTY || i == B_TBL_EMPTY + 1) cnt = 384; // mask, Z4 and epilogue warps read it
+      if (i == B_TBL_EMPTY || i == B_TBL_EMPTY + 1) cnt = C::SPLIT ? 512 : 384;  // its reader warps
       if (i == B_O_FULL) cnt = 2;
       if (i == B_ST_FULL) cnt = 128;  // the epilogue threads have staged the final state
       if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_P_HALF || i == B_U_EMPTY || i == B_SP_FULL ||
@@ -406,7 +413,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    setmaxnreg_dec<REG_CTRL>();
+    setmaxnreg_dec<C::REG_CTRL>();
     if (lane == 0) {
       int issued[2] = {0, 0};
       int gk = 0;
@@ -445,7 +452,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     __syncwarp();
   } else if (warp < 4) {
     // ------------------------------------------------------------------ MMA issuers
-    setmaxnreg_dec<REG_CTRL>();
+    setmaxnreg_dec<C::REG_CTRL>();
     if (lane == 0) {
       constexpr uint32_t ID_A = idesc_bf16(128, 128, 0, 0);           // A = X Y^T
       constexpr uint32_t ID_PZ = idesc_bf16(128, C::OW, 0, 1);        // O_intra = P Z
@@ -545,7 +552,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     __syncwarp();
   } else if (warp < 8) {
     // ------------------------------------------------------------------ decay mask
-    setmaxnreg_inc<REG_WIDE>();
+    setmaxnreg_inc<C::REG_MASK>();
     const int i = threadIdx.x - 128;  // query row = tensor-memory lane
     const int q = warp & 3;           // this warp's lanes are rows 32q .. 32q + 31
     const uint32_t lane_addr = tmem + ((uint32_t)(q << 5) << 16);
@@ -643,9 +650,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
      }
      mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
     }
-  } else if (warp >= 12) {
+  } else if (warp >= 12 && warp < 16) {
     // ------------------------------------------------------------------ weighted Z4 (hi and lo)
-    setmaxnreg_dec<REG_Z4>();
+    setmaxnreg_dec<C::REG_Z4>();
     const int t = threadIdx.x - 384;  // row of the chunk
     int gk = 0, ku = 0;
     bool stop = false;
@@ -708,222 +715,248 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_scan_kernel(const __grid_const
     }
   } else {
     // ------------------------------------------------------------------ epilogue
-    setmaxnreg_inc<REG_WIDE>();
-    const int r_ = ((warp & 3) << 5) + lane;  // d_k row of the state and U; query row of O
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
-    const bool out32 = (reinterpret_cast<uintptr_t>(prm.out) & 31u) == 0;
-    float S[TN];
-    auto write_sprev = [&]() {
-      if (r_ < DK) {
-        const uint32_t row = sbase + SMM::OFF_SP + (uint32_t)r_ * 128u;
+    // The running state of the unit's 96 x 64 tile (fp32 registers, thread r_ = d_k row):
+    // S <- lambda^L S + U_hi + U_lo per chunk, its bf16 hi/lo copy for MMA3 and the final state;
+    // and the output rows of each chunk from O_intra and O_inter (thread r_ = query row).  One
+    // body, instantiated as a single role (forward: warps 8-11 do both, in the order update of
+    // chunk it, copy for chunk it + 1, output of chunk it) or as two (backward: warps 8-11 the
+    // state, warps 16-19 the output).
+    auto epilogue = [&](auto do_state_t, auto do_out_t) {
+      constexpr bool DO_STATE = decltype(do_state_t)::value, DO_OUT = decltype(do_out_t)::value;
+      const int r_ = ((warp & 3) << 5) + lane;  // d_k row of the state and U; query row of O
+      const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) << 5) << 16);
+      const uint32_t spb = sbase + SMM::OFF_SP;
+      const bool out32 = (reinterpret_cast<uintptr_t>(prm.out) & 31u) == 0;
+      float S[TN];
+      auto write_sprev = [&]() {
+        if (r_ < DK) {
+          const uint32_t row = sbase + SMM::OFF_SP + (uint32_t)r_ * 128u;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint32_t hi[4], lo[4];
+          for (int cc = 0; cc < 8; ++cc) {
+            uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) split_bf16x2(make_float2(S[8 * cc + 2 * e], S[8 * cc + 2 * e + 1]), hi[e], lo[e]);
-          const uint32_t off = (uint32_t)((cc ^ (r_ & 7)) << 4);
-          st_shared_v4(row + off, hi[0], hi[1], hi[2], hi[3]);
-          st_shared_v4(row + SZ_SPH + off, lo[0], lo[1], lo[2], lo[3]);
-        }
-      }
-      fence_async_smem();
-      mbar_arrive(&bars[B_SP_FULL]);
-    };
-    // Iteration it of a unit: the state update of chunk it, the state copy for chunk it + 1, the
-    // output rows of chunk it (it = -1 only loads the initial state and writes its copy).  One site
-    // for each part keeps the code small.
-    bool aborted = false;
-    int nst = 0;  // full chunks stored through the staging tile
-    int gk = 0, ku = 0;
-    for (int u = blockIdx.x; u < n_units && !aborted; u += gridDim.x, ++ku) {
-     const Unit w = unit_at(u);
-     const int h = w.h, col0 = w.tile * TN, nc = w.nc, tbuf = ku & 1;
-     if (!warp_wait(&bars[B_TBL_FULL + tbuf], (uint32_t)(ku >> 1) & 1u, a, abort_flag)) { aborted = true; break; }
-     const float* pw = pw_base + tbuf * PW_FLOATS;
-     const float* pws = pw + 129;
-     const uint32_t spb = sbase + SMM::OFF_SP;
-     const int srow0 = (w.n * a.H + h) * DK;  // the unit's first state row
-#pragma unroll
-     for (int x = 0; x < TN; ++x) S[x] = 0.f;
-     if (MODE == MODE_FWD && prm.s_out && ku > 0) {  // the previous unit's final-state store has read the buffer
-       if (r_ == 0) {
-         bulk_wait_read_all();
-         mbar_arrive(&bars[B_ST_EMPTY]);
-       }
-       if (!warp_wait(&bars[B_ST_EMPTY], (uint32_t)(ku - 1) & 1u, a, abort_flag)) { aborted = true; break; }
-     }
-     if (prm.s0 && r_ < DK) {
-       const float4* src = reinterpret_cast<const float4*>(prm.s0 + ((long long)srow0 + r_) * DV + col0);
-#pragma unroll
-       for (int x = 0; x < TN / 4; ++x) {
-         const float4 v4 = src[x];
-         S[4 * x] = v4.x;
-         S[4 * x + 1] = v4.y;
-         S[4 * x + 2] = v4.z;
-         S[4 * x + 3] = v4.w;
-       }
-     }
-     for (int it = -1; it < nc; ++it) {
-      const int g = gk + it;  // the CTA's chunk count
-      const uint32_t pc = (uint32_t)g & 1u;
-      const int c = it < 0 ? 0 : (C::REVERSE ? nc - 1 - it : it);
-      const int L = min(CHUNK, w.len - c * CHUNK);
-      if (it >= 0) {
-        // state <- lambda^L state + U_hi + U_lo
-        if (!warp_wait(&bars[B_U_FULL], pc, a, abort_flag)) { aborted = true; break; }
-        tc_fence_after();
-        const float lamL = pw[L];
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          uint32_t u[32];  // [0, 16): hi columns, [16, 32): lo columns of this quarter
-          tmem_ld16x2(lane_addr + C::TM_U + 16u * qq, lane_addr + C::TM_U + TN + 16u * qq, u);
-#pragma unroll
-          for (int x = 0; x < 16; x += 2) {
-            const float2 sv = fma2(make_float2(lamL, lamL), make_float2(S[16 * qq + x], S[16 * qq + x + 1]),
-                                   add2(ld_f2(u, x), ld_f2(u, 16 + x)));
-            S[16 * qq + x] = sv.x;
-            S[16 * qq + x + 1] = sv.y;
+            for (int e = 0; e < 4; ++e) split_bf16x2(make_float2(S[8 * cc + 2 * e], S[8 * cc + 2 * e + 1]), hi[e], lo[e]);
+            const uint32_t off = (uint32_t)((cc ^ (r_ & 7)) << 4);
+            st_shared_v4(row + off, hi[0], hi[1], hi[2], hi[3]);
+            st_shared_v4(row + SZ_SPH + off, lo[0], lo[1], lo[2], lo[3]);
           }
         }
-        tc_fence_before();
-        mbar_arrive(&bars[B_U_EMPTY]);
-      }
-      if (it + 1 < nc) {  // after MMA3 of this chunk has read the previous copy
-        if (g >= 0 && !warp_wait(&bars[B_SP_EMPTY], pc, a, abort_flag)) { aborted = true; break; }
-        write_sprev();
-      }
-      if (it < 0) continue;
-      // out row = O_intra + g * O_inter;  g = s lambda^(i+1) (forward scans) or lambda^(L-1-i)
-      if (!warp_wait(&bars[B_O_FULL], pc, a, abort_flag)) { aborted = true; break; }
-      tc_fence_after();
-      const float gf = C::REVERSE ? (r_ < L ? pw[L - 1 - r_] : 0.f) : pws[r_ + 1];
-      const long long orow = (w.tb + (long long)c * CHUNK + r_) * a.H + h;
-      if (!C::NARROW) {
-        // Full chunks go through the staging tile and one TMA store (a whole 128 x 64 tile, no
-        // per-row stores on the load/store pipe); a partial last chunk is stored row by row so that
-        // nothing past the sequence end is written.
-        const bool staged = L == CHUNK;
-        if (staged && nst > 0) {  // the previous store has finished reading the staging tile
-          if (r_ == 0) {
-            bulk_wait_read_all();
-            mbar_arrive(&bars[B_OST_EMPTY]);
-          }
-          if (!warp_wait(&bars[B_OST_EMPTY], (uint32_t)(nst - 1) & 1u, a, abort_flag)) { aborted = true; break; }
-        }
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(prm.out) + orow * DV + col0);
-        const uint32_t srow = sbase + SMM::OFF_OST + (uint32_t)r_ * 128u;
+        fence_async_smem();
+        mbar_arrive(&bars[B_SP_FULL]);
+      };
+      bool aborted = false;
+      int nst = 0;  // full chunks stored through the staging tile
+      int gk = 0, ku = 0;
+      for (int u = blockIdx.x; u < n_units && !aborted; u += gridDim.x, ++ku) {
+       const Unit w = unit_at(u);
+       const int h = w.h, col0 = w.tile * TN, nc = w.nc, tbuf = ku & 1;
+       if (!warp_wait(&bars[B_TBL_FULL + tbuf], (uint32_t)(ku >> 1) & 1u, a, abort_flag)) { aborted = true; break; }
+       const float* pw = pw_base + tbuf * PW_FLOATS;
+       const float* pws = pw + 129;
+       const int srow0 = (w.n * a.H + h) * DK;  // the unit's first state row
+       if constexpr (DO_STATE) {
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          uint32_t ov[48];  // 16 intra, 16 inter-hi, 16 inter-lo columns
-          tmem_ld16x3(lane_addr + C::TM_OI + 16u * qq, lane_addr + C::TM_OE + 16u * qq,
-                      lane_addr + C::TM_OE + TN + 16u * qq, ov);
-          if (qq == 3) {
-            tc_fence_before();
-            mbar_arrive(&bars[B_O_EMPTY]);
-          }
-          uint32_t ob[8];
+         for (int x = 0; x < TN; ++x) S[x] = 0.f;
+         if (MODE == MODE_FWD && prm.s_out && ku > 0) {  // the previous unit's final-state store has read the buffer
+           if (r_ == 0) {
+             bulk_wait_read_all();
+             mbar_arrive(&bars[B_ST_EMPTY]);
+           }
+           if (!warp_wait(&bars[B_ST_EMPTY], (uint32_t)(ku - 1) & 1u, a, abort_flag)) { aborted = true; break; }
+         }
+         if (prm.s0 && r_ < DK) {
+           const float4* src = reinterpret_cast<const float4*>(prm.s0 + ((long long)srow0 + r_) * DV + col0);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int x = 2 * e;
-            const float2 ovx = fma2(make_float2(gf, gf), add2(ld_f2(ov, 16 + x), ld_f2(ov, 32 + x)), ld_f2(ov, x));
-            ob[e] = pack_bf16(ovx.x, ovx.y);
-          }
-          if (staged) {  // 16-byte pieces 2qq, 2qq + 1 of the row, in the 128B-swizzled layout
-            st_shared_v4(srow + ((uint32_t)((2 * qq) ^ (r_ & 7)) << 4), ob[0], ob[1], ob[2], ob[3]);
-            st_shared_v4(srow + ((uint32_t)((2 * qq + 1) ^ (r_ & 7)) << 4), ob[4], ob[5], ob[6], ob[7]);
-          } else if (r_ < L) {
-            if (out32) {  // one full 32-byte sector per store
-              st_global_v8(dst + 2 * qq, ob);
-            } else {
-              dst[2 * qq] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-              dst[2 * qq + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
-            }
-          }
-        }
-        if (staged) {
-          fence_async_smem();
-          mbar_arrive(&bars[B_OST_FULL]);
-          if ((warp & 3) == 0) {  // the whole warp waits (so that an abort leaves it in step)
-            if (!warp_wait(&bars[B_OST_FULL], (uint32_t)nst & 1u, a, abort_flag)) { aborted = true; break; }
-            if (lane == 0) tma_store_3d(&maps.o, sbase + SMM::OFF_OST, col0, h, (int)(w.tb + (long long)c * CHUNK));
-          }
-          ++nst;
-        }
-      } else {
-        // fp32 partial sums for the accumulator, 48 columns at a time: each thread writes its row
-        // into the warp's region, then the warp adds contiguous 16-byte pieces (12 per row), so one
-        // red.add instruction covers about three rows' segments instead of 32 rows.
-        const uint32_t wreg = sbase + SMM::OFF_OST + (uint32_t)(warp & 3) * RED_WARP_BYTES;
-        const long long row0 = (w.tb + (long long)c * CHUNK + ((warp & 3) << 5)) * a.H + h;  // lane 0's row
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int q3 = 0; q3 < 3; ++q3) {
-            const int qq = 3 * half + q3;
-            uint32_t ov[32];  // 16 intra, 16 inter columns
-            tmem_ld16x2(lane_addr + C::TM_OI + 16u * qq, lane_addr + C::TM_OE + 16u * qq, ov);
-            if (qq == 5) {
-              tc_fence_before();
-              mbar_arrive(&bars[B_O_EMPTY]);
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 v0 = fma2(make_float2(gf, gf), ld_f2(ov, 16 + 4 * e), ld_f2(ov, 4 * e));
-              const float2 v1 = fma2(make_float2(gf, gf), ld_f2(ov, 18 + 4 * e), ld_f2(ov, 4 * e + 2));
-              st_shared_v4(wreg + (uint32_t)lane * RED_ROW + (uint32_t)(4 * q3 + e) * 16u, __float_as_uint(v0.x),
-                           __float_as_uint(v0.y), __float_as_uint(v1.x), __float_as_uint(v1.y));
-            }
-          }
-          __syncwarp();
-#pragma unroll 2
-          for (int k = 0; k < 12; ++k) {
-            const int pidx = k * 32 + lane, row = pidx / 12, pc = pidx - row * 12;
-            if (((warp & 3) << 5) + row < L) {
-              const uint4 v = ld_shared_v4(wreg + (uint32_t)row * RED_ROW + (uint32_t)pc * 16u);
-              red_add_v4(reinterpret_cast<float*>(prm.out) + (row0 + (long long)row * a.H) * DK + 48 * half + 4 * pc,
-                         __uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
-            }
-          }
-          __syncwarp();
-        }
-      }
-    }
-     if (aborted) break;
-     if (MODE == MODE_FWD && prm.s_out) {
-       // Forward (persistent CTAs): the final state leaves through the state-copy buffer and two
-       // TMA stores of 32-column halves (128B-swizzled fp32 rows; thread r_'s row covers exactly
-       // the bytes of its own hi and lo copy rows), so that 96 rows of per-thread global stores do
-       // not hold up the load/store pipe at the unit boundary.  The buffer is free: every thread
-       // has waited for the unit's last O_FULL, which follows its last MMA3.  The next unit's
-       // first state copy waits (B_ST_EMPTY) until the stores have read it.
-       if (r_ < DK) {
-#pragma unroll
-         for (int x = 0; x < TN / 4; ++x)
-           st_shared_v4(spb + (uint32_t)(x >> 3) * SZ_SPH + (uint32_t)r_ * 128u + ((uint32_t)((x & 7) ^ (r_ & 7)) << 4),
-                        __float_as_uint(S[4 * x]), __float_as_uint(S[4 * x + 1]), __float_as_uint(S[4 * x + 2]),
-                        __float_as_uint(S[4 * x + 3]));
-       }
-       fence_async_smem();
-       mbar_arrive(&bars[B_ST_FULL]);
-       if ((warp & 3) == 0) {  // the whole warp waits, lane 0 issues
-         if (!warp_wait(&bars[B_ST_FULL], (uint32_t)ku & 1u, a, abort_flag)) { aborted = true; break; }
-         if (lane == 0) {
-           tma_store_2d(&maps.s, spb, col0, srow0);
-           tma_store_2d(&maps.s, spb + SZ_SPH, col0 + 32, srow0);
+           for (int x = 0; x < TN / 4; ++x) {
+             const float4 v4 = src[x];
+             S[4 * x] = v4.x;
+             S[4 * x + 1] = v4.y;
+             S[4 * x + 2] = v4.z;
+             S[4 * x + 3] = v4.w;
+           }
          }
        }
-     }
-     if (MODE != MODE_FWD && prm.s_out && r_ < DK) {
-       float4* dst = reinterpret_cast<float4*>(prm.s_out + ((long long)srow0 + r_) * DV + col0);
+       for (int it = -1; it < nc; ++it) {
+        const int g = gk + it;  // the CTA's chunk count
+        const uint32_t pc = (uint32_t)g & 1u;
+        const int c = it < 0 ? 0 : (C::REVERSE ? nc - 1 - it : it);
+        const int L = min(CHUNK, w.len - c * CHUNK);
+        if constexpr (DO_STATE) {
+          if (it >= 0) {
+            // state <- lambda^L state + U_hi + U_lo
+            if (!warp_wait(&bars[B_U_FULL], pc, a, abort_flag)) { aborted = true; break; }
+            tc_fence_after();
+            const float lamL = pw[L];
 #pragma unroll
-       for (int x = 0; x < TN / 4; ++x) dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
-     }
-     mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
-     gk += nc;
+            for (int qq = 0; qq < 4; ++qq) {
+              uint32_t u[32];  // [0, 16): hi columns, [16, 32): lo columns of this quarter
+              tmem_ld16x2(lane_addr + C::TM_U + 16u * qq, lane_addr + C::TM_U + TN + 16u * qq, u);
+#pragma unroll
+              for (int x = 0; x < 16; x += 2) {
+                const float2 sv = fma2(make_float2(lamL, lamL), make_float2(S[16 * qq + x], S[16 * qq + x + 1]),
+                                       add2(ld_f2(u, x), ld_f2(u, 16 + x)));
+                S[16 * qq + x] = sv.x;
+                S[16 * qq + x + 1] = sv.y;
+              }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars[B_U_EMPTY]);
+          }
+          if (it + 1 < nc) {  // after MMA3 of this chunk has read the previous copy
+            if (g >= 0 && !warp_wait(&bars[B_SP_EMPTY], pc, a, abort_flag)) { aborted = true; break; }
+            write_sprev();
+          }
+        }
+        if (it < 0) continue;
+        if constexpr (DO_OUT) {
+          // out row = O_intra + g * O_inter;  g = s lambda^(i+1) (forward scans) or lambda^(L-1-i)
+          if (!warp_wait(&bars[B_O_FULL], pc, a, abort_flag)) { aborted = true; break; }
+          tc_fence_after();
+          const float gf = C::REVERSE ? (r_ < L ? pw[L - 1 - r_] : 0.f) : pws[r_ + 1];
+          const long long orow = (w.tb + (long long)c * CHUNK + r_) * a.H + h;
+          if (!C::NARROW) {
+            // Full chunks go through the staging tile and one TMA store (a whole 128 x 64 tile, no
+            // per-row stores on the load/store pipe); a partial last chunk is stored row by row so that
+            // nothing past the sequence end is written.
+            const bool staged = L == CHUNK;
+            if (staged && nst > 0) {  // the previous store has finished reading the staging tile
+              if (r_ == 0) {
+                bulk_wait_read_all();
+                mbar_arrive(&bars[B_OST_EMPTY]);
+              }
+              if (!warp_wait(&bars[B_OST_EMPTY], (uint32_t)(nst - 1) & 1u, a, abort_flag)) { aborted = true; break; }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(prm.out) + orow * DV + col0);
+            const uint32_t srow = sbase + SMM::OFF_OST + (uint32_t)r_ * 128u;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              uint32_t ov[48];  // 16 intra, 16 inter-hi, 16 inter-lo columns
+              tmem_ld16x3(lane_addr + C::TM_OI + 16u * qq, lane_addr + C::TM_OE + 16u * qq,
+                          lane_addr + C::TM_OE + TN + 16u * qq, ov);
+              if (qq == 3) {
+                tc_fence_before();
+                mbar_arrive(&bars[B_O_EMPTY]);
+              }
+              uint32_t ob[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int x = 2 * e;
+                const float2 ovx = fma2(make_float2(gf, gf), add2(ld_f2(ov, 16 + x), ld_f2(ov, 32 + x)), ld_f2(ov, x));
+                ob[e] = pack_bf16(ovx.x, ovx.y);
+              }
+              if (staged) {  // 16-byte pieces 2qq, 2qq + 1 of the row, in the 128B-swizzled layout
+                st_shared_v4(srow + ((uint32_t)((2 * qq) ^ (r_ & 7)) << 4), ob[0], ob[1], ob[2], ob[3]);
+                st_shared_v4(srow + ((uint32_t)((2 * qq + 1) ^ (r_ & 7)) << 4), ob[4], ob[5], ob[6], ob[7]);
+              } else if (r_ < L) {
+                if (out32) {  // one full 32-byte sector per store
+                  st_global_v8(dst + 2 * qq, ob);
+                } else {
+                  dst[2 * qq] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+                  dst[2 * qq + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
+                }
+              }
+            }
+            if (staged) {
+              fence_async_smem();
+              mbar_arrive(&bars[B_OST_FULL]);
+              if ((warp & 3) == 0) {  // the whole warp waits (so that an abort leaves it in step)
+                if (!warp_wait(&bars[B_OST_FULL], (uint32_t)nst & 1u, a, abort_flag)) { aborted = true; break; }
+                if (lane == 0) tma_store_3d(&maps.o, sbase + SMM::OFF_OST, col0, h, (int)(w.tb + (long long)c * CHUNK));
+              }
+              ++nst;
+            }
+          } else {
+            // fp32 partial sums for the accumulator, 48 columns at a time: each thread writes its row
+            // into the warp's region, then the warp adds contiguous 16-byte pieces (12 per row), so one
+            // red.add instruction covers about three rows' segments instead of 32 rows.
+            const uint32_t wreg = sbase + SMM::OFF_OST + (uint32_t)(warp & 3) * RED_WARP_BYTES;
+            const long long row0 = (w.tb + (long long)c * CHUNK + ((warp & 3) << 5)) * a.H + h;  // lane 0's row
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+#pragma unroll
+              for (int q3 = 0; q3 < 3; ++q3) {
+                const int qq = 3 * half + q3;
+                uint32_t ov[32];  // 16 intra, 16 inter columns
+                tmem_ld16x2(lane_addr + C::TM_OI + 16u * qq, lane_addr + C::TM_OE + 16u * qq, ov);
+                if (qq == 5) {
+                  tc_fence_before();
+                  mbar_arrive(&bars[B_O_EMPTY]);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 v0 = fma2(make_float2(gf, gf), ld_f2(ov, 16 + 4 * e), ld_f2(ov, 4 * e));
+                  const float2 v1 = fma2(make_float2(gf, gf), ld_f2(ov, 18 + 4 * e), ld_f2(ov, 4 * e + 2));
+                  st_shared_v4(wreg + (uint32_t)lane * RED_ROW + (uint32_t)(4 * q3 + e) * 16u, __float_as_uint(v0.x),
+                               __float_as_uint(v0.y), __float_as_uint(v1.x), __float_as_uint(v1.y));
+                }
+              }
+              __syncwarp();
+#pragma unroll 2
+              for (int k = 0; k < 12; ++k) {
+                const int pidx = k * 32 + lane, row = pidx / 12, pc = pidx - row * 12;
+                if (((warp & 3) << 5) + row < L) {
+                  const uint4 v = ld_shared_v4(wreg + (uint32_t)row * RED_ROW + (uint32_t)pc * 16u);
+                  red_add_v4(reinterpret_cast<float*>(prm.out) + (row0 + (long long)row * a.H) * DK + 48 * half + 4 * pc,
+                             __uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+                }
+              }
+              __syncwarp();
+            }
+          }
+        }
+       }
+       if (aborted) break;
+       if constexpr (DO_STATE) {
+         if (MODE == MODE_FWD && prm.s_out) {
+           // Forward (persistent CTAs): the final state leaves through the state-copy buffer and two
+           // TMA stores of 32-column halves (128B-swizzled fp32 rows; thread r_'s row covers exactly
+           // the bytes of its own hi and lo copy rows), so that 96 rows of per-thread global stores do
+           // not hold up the load/store pipe at the unit boundary.  The buffer is free once the unit's
+           // last MMA3 has read it; the next unit's first state copy waits (B_ST_EMPTY) until the
+           // stores have read it in turn.
+           if constexpr (!DO_OUT) {  // (a single epilogue role has waited for the last O_FULL already)
+             const int gl = gk + nc - 1;  // the unit's last chunk (for an empty unit, the one before)
+             if (gl >= 0 && !warp_wait(&bars[B_SP_EMPTY], (uint32_t)gl & 1u, a, abort_flag)) { aborted = true; break; }
+           }
+           if (r_ < DK) {
+#pragma unroll
+             for (int x = 0; x < TN / 4; ++x)
+               st_shared_v4(spb + (uint32_t)(x >> 3) * SZ_SPH + (uint32_t)r_ * 128u + ((uint32_t)((x & 7) ^ (r_ & 7)) << 4),
+                            __float_as_uint(S[4 * x]), __float_as_uint(S[4 * x + 1]), __float_as_uint(S[4 * x + 2]),
+                            __float_as_uint(S[4 * x + 3]));
+           }
+           fence_async_smem();
+           mbar_arrive(&bars[B_ST_FULL]);
+           if ((warp & 3) == 0) {  // the whole warp waits, lane 0 issues
+             if (!warp_wait(&bars[B_ST_FULL], (uint32_t)ku & 1u, a, abort_flag)) { aborted = true; break; }
+             if (lane == 0) {
+               tma_store_2d(&maps.s, spb, col0, srow0);
+               tma_store_2d(&maps.s, spb + SZ_SPH, col0 + 32, srow0);
+             }
+           }
+         }
+         if (MODE != MODE_FWD && prm.s_out && r_ < DK) {
+           float4* dst = reinterpret_cast<float4*>(prm.s_out + ((long long)srow0 + r_) * DV + col0);
+#pragma unroll
+           for (int x = 0; x < TN / 4; ++x) dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+         }
+       }
+       mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
+       gk += nc;
+      }
+      if (r_ == 0) bulk_wait_read_all();  // the last tile and state stores have read shared memory
+    };
+    if constexpr (!C::SPLIT) {
+      setmaxnreg_inc<C::REG_STATE>();
+      epilogue(std::true_type(), std::true_type());
+    } else if (warp < 12) {
+      setmaxnreg_inc<C::REG_STATE>();
+      epilogue(std::true_type(), std::false_type());
+    } else {
+      setmaxnreg_dec<C::REG_OUT>();
+      epilogue(std::false_type(), std::true_type());
     }
-    if (r_ == 0) bulk_wait_read_all();  // the last tile and state stores have read shared memory
   }
-
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1015,12 +1048,17 @@ cudaError_t launch_scan(const void* X, const void* Y, const void* Z, const ScanP
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_scan_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Smem<MODE>::BYTES);
+    // The warpgroups' setmaxnreg split redistributes exactly the registers the CTA is launched
+    // with; with any other compiled count an increase could wait forever, so refuse to launch.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, tc_scan_kernel<MODE>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(tc_scan_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem<MODE>::BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  tc_scan_kernel<MODE><<<(unsigned)blocks, NTHREADS, Smem<MODE>::BYTES, stream>>>(maps, p);
+  tc_scan_kernel<MODE><<<(unsigned)blocks, C::THREADS, Smem<MODE>::BYTES, stream>>>(maps, p);
   return cudaGetLastError();
 }
 
