@@ -143,6 +143,32 @@ def test_fwd_empty_and_degenerate():
     assert hT.shape == (0, 2, 96, 192)
 
 
+def test_fwd_persistent_units_with_h0():
+    """Equal-length batches run persistent CTAs (one per SM) that take several (sequence, head,
+    d_v tile) units each: 7 x 16 x 3 = 336 units put two or three units on every CTA, so the
+    per-unit decay tables, initial-state loads and final-state stores rotate through their
+    buffers.  T = 300 also ends every unit on a partial chunk.  Compared in full."""
+    B, H, T = 7, 16, 300
+    d = host_chunk_inputs(31, [T] * B, H, True, with_h0=True, packed=False)
+    d["scale"] = float(gs.SCALE)
+    g = to_device(d, True, packed=False)
+    o, hT = gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], d["scale"], h0=g["h0"])
+    _check_fwd(d, o, hT, False, BF16_TOL)
+
+
+def test_fwd_persistent_empty_sequences():
+    """T = 0 with many units per persistent CTA: every unit passes its initial state through as
+    the final state, bit for bit."""
+    import torch
+    B, H = 7, 16
+    ll = torch.from_numpy(gs.laplace_log_lambda(H)).cuda()
+    q = torch.zeros(B, 0, H, 96, device="cuda", dtype=torch.bfloat16)
+    v = torch.zeros(B, 0, H, 192, device="cuda", dtype=torch.bfloat16)
+    h0 = torch.randn(B, H, 96, 192, device="cuda")
+    o, hT = gla.gla_chunk_fwd(q, q, v, ll, 0.1, h0=h0)
+    assert o.numel() == 0 and torch.equal(hT, h0)
+
+
 def _sampled_units(w, units, o, hT, tol):
     import torch
     torch.cuda.synchronize()
