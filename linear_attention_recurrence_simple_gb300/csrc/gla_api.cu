@@ -15,6 +15,7 @@ cudaError_t launch_simt_bwd(int dtype_f32, const ChunkArgs& a, cudaStream_t stre
 cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_tc_bwd(const ChunkArgs& a, float* acc_q, float* acc_k, cudaStream_t stream);
 size_t tc_bwd_acc_bytes(long long T_total, int H);
+cudaError_t tc_clear_handover(cudaStream_t stream);
 }  // namespace gla
 
 namespace {
@@ -269,6 +270,9 @@ int gla_get_device_error(gla_stream_t stream) {
   if (word) {
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return GLA_ERR_LAUNCH;
+    if (gla::tc_clear_handover((cudaStream_t)stream) != cudaSuccess ||
+        cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+      return GLA_ERR_LAUNCH;
   }
   return -(int)word;
 }

@@ -32,10 +32,15 @@
 // lo = bf16(x - hi): the state copy in MMA3 and the weighted Z4 in MMA4, about 16 significant
 // bits on the state path; only P is a single bf16 rounding.
 //
-// Work split: one CTA per (sequence, head, 64-column tile of d_v), 512 threads, 1 CTA per SM.
-// One thread issues at most one tcgen05.mma (M = 128, K = 16) per ~135 cycles whatever N <= 128
-// is (measured), so the kernel keeps the instruction count low (hi/lo halves ride in one N = 128
-// MMA where N allows) and issues from three threads in parallel, one per accumulator chain.  Warp roles:
+// Work split: a work unit is a (sequence, head, 64-column tile of d_v); 1 CTA per SM (all of
+// tensor memory, ~224 KB of shared memory).  Equal-length forward batches run one persistent CTA
+// per SM over a work list built in the prologue; with a final-state output the list is balanced
+// (the chunks of all (sequence, head) pairs cut into equal ranges, one per group of three CTAs,
+// a pair straddling two ranges handed over through its final-state tile; see the kernel).
+// Varlen batches and the backward scans run one CTA per unit.  One thread issues at most one
+// tcgen05.mma (M = 128, K = 16) per ~70 cycles whatever N <= 128 is (measured), so the kernel
+// keeps the instruction count low (hi/lo halves ride in one N = 128 MMA where N allows) and issues
+// from three threads in parallel, one per accumulator chain.  Warp roles:
 //   warp 0      TMA producer: X, Y, Z chunk tiles into a 2-stage ring.
 //   warp 1      allocates tensor memory; one lane issues MMA1 (X Y^T), then MMA3 (X times the
 //               state copy), whose inputs are ready long before the weighted Z4 that MMA4 waits for.
@@ -44,16 +49,20 @@
 //   warps 4-7   decay mask A (TMEM) -> P (bf16 pairs, back into TMEM).  A is released as soon as
 //               it is in registers, so the next chunk's MMA1 overlaps this one's P.
 //   warps 8-11  epilogue: U (TMEM) -> state = lambda^L state + U in fp32 registers -> bf16 hi/lo
-//               copy for the next chunk's MMA3; O (TMEM) -> output row.
+//               copy for the next chunk's MMA3; O (TMEM) -> output row.  In the backward scans
+//               (640 threads) warps 8-11 keep the state part and warps 16-19 take the output part.
 //   warps 12-15 the weighted Z4 for MMA4 (hi and lo, zero past the sequence end).
-// Registers: the block launches with 128 per thread; warpgroups 0 and 3 give theirs back down
-// to 64 and 80 and warpgroups 1 and 2 (mask, epilogue) take 184 (setmaxnreg in each role).
+// Registers: setmaxnreg in each role redistributes exactly the registers the CTA launches with
+// (forward: 128 each, then 64 control, 184 mask, 184 epilogue, 80 Z4; backward: 96 each, then
+// 64, 120, 136, 64, 96 output).
 // Tensor memory (512 columns): A [0,128), P [128,192), then O_intra, O_inter and U [384,512).
 // Every mbarrier wait is bounded (see gla_common.cuh); on a timeout the CTA records
 // GLA_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and returns.
 #include <cuda.h>
 #include <string.h>
 
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -79,8 +88,8 @@ struct Cfg {
   static constexpr bool SPLIT = MODE != MODE_FWD;
   static constexpr int THREADS = SPLIT ? 640 : 512;
   static constexpr int REG_LAUNCH = SPLIT ? 96 : 128;
-  static constexpr int REG_CTRL = 64, REG_MASK = SPLIT ? 112 : 184, REG_STATE = SPLIT ? 136 : 184;
-  static constexpr int REG_Z4 = SPLIT ? 72 : 80, REG_OUT = SPLIT ? 96 : 0;
+  static constexpr int REG_CTRL = 64, REG_MASK = SPLIT ? 120 : 184, REG_STATE = SPLIT ? 136 : 184;
+  static constexpr int REG_Z4 = SPLIT ? 64 : 80, REG_OUT = SPLIT ? 96 : 0;
   static_assert(REG_CTRL + REG_MASK + REG_STATE + REG_Z4 + REG_OUT == THREADS / 128 * REG_LAUNCH, "register split");
   static_assert(THREADS * REG_LAUNCH <= 65536, "launch registers");
   // shared memory of one stage (byte offsets; each tile 1024-aligned)
@@ -106,9 +115,10 @@ enum {
   B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
   B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY, B_OST_FULL, B_OST_EMPTY,
   B_ZR, B_P_HALF = B_ZR + 2, B_TBL_FULL, B_TBL_EMPTY = B_TBL_FULL + 2, B_ST_FULL = B_TBL_EMPTY + 2, B_ST_EMPTY,
-  B_DRAIN, NBAR = B_DRAIN + 3
+  B_HANDOVER, B_DRAIN, NBAR = B_DRAIN + 3
 };
 constexpr int PW_FLOATS = 2 * 129;  // lambda^d and scale * lambda^d, d = 0..128
+constexpr int MAX_ITEMS = 32;       // work units per CTA (the host sizes the grid to keep within it)
 constexpr uint32_t RED_ROW = 208;                 // 192 bytes of fp32 + 16 (bank spread)
 constexpr uint32_t RED_WARP_BYTES = 32 * RED_ROW;
 template <int MODE>
@@ -122,7 +132,8 @@ struct Smem {
   static constexpr uint32_t OFF_PW = OFF_OST + (Cfg<MODE>::NARROW ? 4u * RED_WARP_BYTES : SZ_TILE64);
   static constexpr uint32_t OFF_BAR = OFF_PW + 2 * PW_FLOATS * 4 + 8;  // two tables (per unit parity)
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t OFF_ITEMS = OFF_MISC + 16;  // the CTA's work list (see the kernel)
+  static constexpr uint32_t BYTES = OFF_ITEMS + MAX_ITEMS * 32 + 1024;
   static_assert(BYTES <= 232448, "shared memory budget");
 };
 constexpr uint32_t TMEM_COLS = 512;
@@ -177,6 +188,20 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
 
 __device__ __forceinline__ void umma(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc, uint32_t acc) {
   asm volatile(
@@ -330,7 +355,19 @@ struct ScanParams {
   const float* s0;  // [n_seq, H, 96, 192] initial state (h0 or dhT), or null = zeros
   float* s_out;     // final state (hT or dh0), or null
   void* out;        // FWD / DV: bf16 [T, H, 192];  DQ / DK: fp32 [T, H, 96] accumulator
+  int balanced = 0;  // chunk ranges split evenly over the CTAs (forward, equal lengths, s_out given)
+  int flag_set = 0;  // which set of hand-over flags a balanced launch uses
+  unsigned epoch = 0;  // the value a raised flag holds in this launch (never 0)
 };
+
+// Hand-over flags of balanced launches: flag b of a set is raised (to the launch's epoch) by CTA b
+// once the piece of a unit it ran first (the unit's first chunks) has left its state in the unit's
+// final-state tile, and lowered again (to 0) by CTA b + NTILE, which runs the unit's remaining
+// chunks from that state.  Launches use the sets in turn, so up to FLAG_SETS balanced launches may
+// run at the same time; a flag left raised by a launch that gave up holds another epoch (and the
+// host lowers them all when it reads the error).
+constexpr int FLAG_SETS = 16, FLAG_MAX_CTAS = 1024;
+__device__ unsigned g_handover[FLAG_SETS * FLAG_MAX_CTAS];
 
 // Per-warpgroup register budgets (every warp of the warpgroup executes the same instruction).
 template <int N>
@@ -363,18 +400,46 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
   // (sequence, head, 64-column tile of d_v)); the chunk pipeline runs on across unit boundaries,
   // so a unit's first loads overlap the previous unit's last chunks.  Barrier phases count the
   // CTA's chunks over all its units (gk).
+  // The CTA's work list is built once, in shared memory, by the lanes of warp 0 in the prologue;
+  // every role then reads its next item from it.  An item is a unit (sequence, head, 64-column
+  // tile of d_v) or a piece of one (processing steps [it0, it1) of its chunks).
+  //   plain:    units blockIdx.x, blockIdx.x + gridDim.x, ..., each whole;
+  //   balanced: CTAs work in groups of NTILE, one per d_v tile, so that the tiles of a
+  //             (sequence, head) run at the same time and share its Q and K through L2.  The
+  //             pairs' chunks, concatenated in order, are cut into one equal contiguous range
+  //             per group, and each CTA of group t runs range t for its tile.  A pair that
+  //             straddles ranges t and t + 1 is run in two pieces: its first chunks by group t
+  //             as its first item (a "tail" piece: the final state goes to the unit's final-state
+  //             tile and raises the CTA's hand-over flag), the rest by group t + 1 as its last
+  //             item (a "head" piece: it starts from that state once the flag of the same tile's
+  //             CTA in group t is up).  All CTAs are resident (cooperative launch), so the wait
+  //             ends.
   const int n_units = a.n_seq * a.H * NTILE;  // below 2^31 (checked on the host)
   struct Unit {
     int n, h, tile, len, nc;
     long long tb;
+    int it0, it1;     // processing steps [it0, it1) of the unit's chunks
+    bool head, tail;  // balanced pieces (see below)
   };
-  auto unit_at = [&](int u) {
+  struct ItemInfo {  // 32 bytes
+    long long tb;
+    int n, h, tile, len, it0, it1;  // tile | 256 (head piece) | 512 (tail piece)
+  };
+  ItemInfo* const items = reinterpret_cast<ItemInfo*>(sm + SMM::OFF_ITEMS);
+  int* const n_items_smem = reinterpret_cast<int*>(sm + SMM::OFF_MISC + 8);
+  auto unit_at = [&](int k) {
+    const ItemInfo& t = items[k];
     Unit w;
-    unit_of(a, NTILE, u, w.n, w.h, w.tile);
-    long long te;
-    seq_range(a, w.n, w.tb, te);
-    w.len = (int)(te - w.tb);
+    w.tb = t.tb;
+    w.n = t.n;
+    w.h = t.h;
+    w.tile = t.tile & 255;
+    w.head = (t.tile & 256) != 0;
+    w.tail = (t.tile & 512) != 0;
+    w.len = t.len;
     w.nc = (w.len + CHUNK - 1) / CHUNK;
+    w.it0 = t.it0;
+    w.it1 = t.it1;
     return w;
   };
 
@@ -386,6 +451,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       if (i == B_TBL_EMPTY || i == B_TBL_EMPTY + 1) cnt = C::SPLIT ? 512 : 384;  // its reader warps
       if (i == B_O_FULL) cnt = 2;
       if (i == B_ST_FULL) cnt = 128;  // the epilogue threads have staged the final state
+      if (i == B_HANDOVER) cnt = 128;  // the epilogue threads have seen the hand-over flag
       if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_P_HALF || i == B_U_EMPTY || i == B_SP_FULL ||
           i == B_O_EMPTY || i == B_OST_FULL || i == B_ZR || i == B_ZR + 1)
         cnt = 128;
@@ -394,6 +460,51 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_async_smem();
+  }
+  if (warp == 0) {
+    int n_it, pu0 = 0, pk0 = 0, pu1 = 0, pk1 = 0, ncu = 1;
+    const int my_tile = (int)blockIdx.x % NTILE;
+    if (prm.balanced) {  // equal lengths; each range spans at least one pair's chunks (host-checked)
+      // 32-bit arithmetic: the host keeps the chunk total below 2^31
+      const unsigned groups = gridDim.x / NTILE, grp = blockIdx.x / NTILE;
+      ncu = (a.T + CHUNK - 1) / CHUNK;
+      const unsigned ctot = (unsigned)(n_units / NTILE) * (unsigned)ncu, cq = ctot / groups, cr = ctot % groups;
+      const unsigned g0 = cq * grp + cr * grp / groups, g1 = cq * (grp + 1) + cr * (grp + 1) / groups;
+      pu0 = (int)(g0 / (unsigned)ncu);
+      pk0 = (int)(g0 - (unsigned)pu0 * (unsigned)ncu);
+      pu1 = (int)(g1 / (unsigned)ncu);
+      pk1 = (int)(g1 - (unsigned)pu1 * (unsigned)ncu);
+      n_it = grp < groups ? (pk1 > 0) + (pu1 - pu0) : 0;  // tail piece, whole pairs, head piece
+    } else {
+      n_it = (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    }
+    n_it = min(n_it, MAX_ITEMS);
+    for (int k = lane; k < n_it; k += 32) {
+      int u, it0 = 0, it1 = -1, flags = 0;
+      if (!prm.balanced) {
+        u = (int)blockIdx.x + k * (int)gridDim.x;
+      } else if (pk1 > 0 && k == 0) {
+        u = pu1 * NTILE + my_tile;
+        it1 = pk1;
+        flags = 512;
+      } else if (k - (pk1 > 0) < pu1 - pu0 - (pk0 > 0)) {
+        u = (pu0 + (pk0 > 0) + k - (pk1 > 0)) * NTILE + my_tile;
+      } else {
+        u = pu0 * NTILE + my_tile;
+        it0 = pk0;
+        flags = 256;
+      }
+      ItemInfo t;
+      unit_of(a, NTILE, u, t.n, t.h, t.tile);
+      t.tile |= flags;
+      long long te;
+      seq_range(a, t.n, t.tb, te);
+      t.len = (int)(te - t.tb);
+      t.it0 = it0;
+      t.it1 = it1 >= 0 ? it1 : (t.len + CHUNK - 1) / CHUNK;
+      items[k] = t;
+    }
+    if (lane == 0) *n_items_smem = n_it;
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -410,6 +521,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int n_items = *n_items_smem;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -418,10 +530,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       int issued[2] = {0, 0};
       int gk = 0;
       bool stop = false;
-      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
+      for (int u = 0; u < n_items && !stop; ++u) {
        const Unit w = unit_at(u);
        const int h = w.h, col0 = w.tile * TN;
-       for (int it = 0; it < w.nc; ++it, ++gk) {
+       for (int it = w.it0; it < w.it1; ++it, ++gk) {
         const int c = C::REVERSE ? w.nc - 1 - it : it;
         const int s = gk & 1;
         const uint32_t ph = (uint32_t)(gk >> 1) & 1u;
@@ -466,9 +578,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       const SDesc dvt = sdesc(sbase + SMM::OFF_VT, SZ_TILE64, 1024, LAYOUT_SW128);
       int gk = 0;
       bool stop = false;
-      for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
-       const int nc = unit_at(u).nc;
-       for (int it = 0; it < nc; ++it, ++gk) {
+      for (int u = 0; u < n_items && !stop; ++u) {
+       const Unit wi = unit_at(u);
+       for (int it = wi.it0; it < wi.it1; ++it, ++gk) {
         const int s = gk & 1;
         const uint32_t ph = (uint32_t)(gk >> 1) & 1u, pc = (uint32_t)gk & 1u;
         const uint32_t st = sbase + (uint32_t)s * C::SZ_STAGE;
@@ -566,8 +678,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
     }
     int gk = 0, ku = 0;
     bool stop = false;
-    for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x, ++ku) {
-     const int nc = unit_at(u).nc;
+    for (int u = 0; u < n_items && !stop; ++u, ++ku) {
+     const Unit wi = unit_at(u);
      const int tbuf = ku & 1;
      if (!warp_wait(&bars[B_TBL_FULL + tbuf], (uint32_t)(ku >> 1) & 1u, a, abort_flag)) break;
      const float* pws = pw_base + tbuf * PW_FLOATS + 129;  // scale * lambda^d of this unit's head
@@ -583,7 +695,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
        const int d1 = C::REVERSE ? d0 + 1 : d0 - 1;
        dgf[e] = make_float2(d0 >= 0 ? pws[max(d0, 0)] : 0.f, d1 >= 0 ? pws[max(d1, 0)] : 0.f);
      }
-     for (int it = 0; it < nc; ++it, ++gk) {
+     for (int it = wi.it0; it < wi.it1; ++it, ++gk) {
       const uint32_t pc = (uint32_t)gk & 1u;
       if (!warp_wait(&bars[B_A_FULL], pc, a, abort_flag)) { stop = true; break; }
       if (!warp_wait(&bars[B_P_EMPTY], pc ^ 1u, a, abort_flag)) { stop = true; break; }
@@ -656,7 +768,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
     const int t = threadIdx.x - 384;  // row of the chunk
     int gk = 0, ku = 0;
     bool stop = false;
-    for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x, ++ku) {
+    for (int u = 0; u < n_items && !stop; ++u, ++ku) {
      const Unit w = unit_at(u);
      // This unit's decay table, into the buffer that unit ku - 2 used (once all its readers are done).
      const int tbuf = ku & 1;
@@ -673,7 +785,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
      }
      mbar_arrive(&bars[B_TBL_FULL + tbuf]);
      if (!warp_wait(&bars[B_TBL_FULL + tbuf], (uint32_t)(ku >> 1) & 1u, a, abort_flag)) break;
-     for (int it = 0; it < w.nc; ++it, ++gk) {
+     for (int it = w.it0; it < w.it1; ++it, ++gk) {
       const int c = C::REVERSE ? w.nc - 1 - it : it;
       const int s = gk & 1;
       const uint32_t ph = (uint32_t)(gk >> 1) & 1u, pc = (uint32_t)gk & 1u;
@@ -747,7 +859,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       bool aborted = false;
       int nst = 0;  // full chunks stored through the staging tile
       int gk = 0, ku = 0;
-      for (int u = blockIdx.x; u < n_units && !aborted; u += gridDim.x, ++ku) {
+      for (int u = 0; u < n_items && !aborted; ++u, ++ku) {
        const Unit w = unit_at(u);
        const int h = w.h, col0 = w.tile * TN, nc = w.nc, tbuf = ku & 1;
        if (!warp_wait(&bars[B_TBL_FULL + tbuf], (uint32_t)(ku >> 1) & 1u, a, abort_flag)) { aborted = true; break; }
@@ -764,7 +876,43 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
            }
            if (!warp_wait(&bars[B_ST_EMPTY], (uint32_t)(ku - 1) & 1u, a, abort_flag)) { aborted = true; break; }
          }
-         if (prm.s0 && r_ < DK) {
+         if (MODE == MODE_FWD && w.head) {
+           // The same tile's CTA of the previous group ran this unit's first chunks and left the
+           // state in its final-state tile; once every epilogue thread has seen the flag, lower it
+           // for the next launch.
+           unsigned* flag = &g_handover[prm.flag_set * FLAG_MAX_CTAS + blockIdx.x - NTILE];
+           bool seen = true;
+           {
+             unsigned long long t0 = ~0ull;
+             while (ld_acquire_gpu(flag) != prm.epoch) {
+               const unsigned long long tn = global_timer_ns();
+               if (t0 == ~0ull) {
+                 t0 = tn;
+               } else if (*abort_flag || tn - t0 > a.wait_ns) {
+                 *abort_flag = 1;
+                 seen = false;
+                 break;
+               }
+             }
+           }
+           if (!__all_sync(0xffffffffu, seen)) { aborted = true; break; }
+           mbar_arrive(&bars[B_HANDOVER]);
+           if (r_ < DK) {
+             const float* src = prm.s_out + ((long long)srow0 + r_) * DV + col0;
+#pragma unroll
+             for (int x = 0; x < TN / 4; ++x) {
+               const float4 v4 = ld_cg_f4(src + 4 * x);
+               S[4 * x] = v4.x;
+               S[4 * x + 1] = v4.y;
+               S[4 * x + 2] = v4.z;
+               S[4 * x + 3] = v4.w;
+             }
+           }
+           if ((warp & 3) == 0) {
+             if (!warp_wait(&bars[B_HANDOVER], 0u, a, abort_flag)) { aborted = true; break; }
+             if (lane == 0) *reinterpret_cast<volatile unsigned*>(flag) = 0u;
+           }
+         } else if (prm.s0 && r_ < DK) {
            const float4* src = reinterpret_cast<const float4*>(prm.s0 + ((long long)srow0 + r_) * DV + col0);
 #pragma unroll
            for (int x = 0; x < TN / 4; ++x) {
@@ -776,13 +924,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
            }
          }
        }
-       for (int it = -1; it < nc; ++it) {
-        const int g = gk + it;  // the CTA's chunk count
+       for (int it = w.it0 - 1; it < w.it1; ++it) {
+        const int g = gk + (it - w.it0);  // the CTA's chunk count
         const uint32_t pc = (uint32_t)g & 1u;
-        const int c = it < 0 ? 0 : (C::REVERSE ? nc - 1 - it : it);
+        const int c = it < w.it0 ? 0 : (C::REVERSE ? nc - 1 - it : it);
         const int L = min(CHUNK, w.len - c * CHUNK);
         if constexpr (DO_STATE) {
-          if (it >= 0) {
+          if (it >= w.it0) {
             // state <- lambda^L state + U_hi + U_lo
             if (!warp_wait(&bars[B_U_FULL], pc, a, abort_flag)) { aborted = true; break; }
             tc_fence_after();
@@ -802,12 +950,12 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
             tc_fence_before();
             mbar_arrive(&bars[B_U_EMPTY]);
           }
-          if (it + 1 < nc) {  // after MMA3 of this chunk has read the previous copy
+          if (it + 1 < w.it1) {  // after MMA3 of this chunk has read the previous copy
             if (g >= 0 && !warp_wait(&bars[B_SP_EMPTY], pc, a, abort_flag)) { aborted = true; break; }
             write_sprev();
           }
         }
-        if (it < 0) continue;
+        if (it < w.it0) continue;
         if constexpr (DO_OUT) {
           // out row = O_intra + g * O_inter;  g = s lambda^(i+1) (forward scans) or lambda^(L-1-i)
           if (!warp_wait(&bars[B_O_FULL], pc, a, abort_flag)) { aborted = true; break; }
@@ -915,7 +1063,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
            // last MMA3 has read it; the next unit's first state copy waits (B_ST_EMPTY) until the
            // stores have read it in turn.
            if constexpr (!DO_OUT) {  // (a single epilogue role has waited for the last O_FULL already)
-             const int gl = gk + nc - 1;  // the unit's last chunk (for an empty unit, the one before)
+             const int gl = gk + (w.it1 - w.it0) - 1;  // the item's last chunk (for an empty one, the one before)
              if (gl >= 0 && !warp_wait(&bars[B_SP_EMPTY], (uint32_t)gl & 1u, a, abort_flag)) { aborted = true; break; }
            }
            if (r_ < DK) {
@@ -932,6 +1080,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
              if (lane == 0) {
                tma_store_2d(&maps.s, spb, col0, srow0);
                tma_store_2d(&maps.s, spb + SZ_SPH, col0 + 32, srow0);
+               if (MODE == MODE_FWD && w.tail) {  // the next group's CTA continues this unit from the stored state
+                 bulk_wait_all();
+                 asm volatile("fence.proxy.async.global;" ::: "memory");
+                 st_release_gpu(&g_handover[prm.flag_set * FLAG_MAX_CTAS + blockIdx.x], prm.epoch);
+               }
              }
            }
          }
@@ -942,7 +1095,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
          }
        }
        mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
-       gk += nc;
+       gk += w.it1 - w.it0;
       }
       if (r_ == 0) bulk_wait_read_all();  // the last tile and state stores have read shared memory
     };
@@ -1021,8 +1174,9 @@ bool make_state_map(CUtensorMap* m, const void* base, long long rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// max_ctas > 0 makes the CTAs persistent: at most max_ctas of them, each running every
-// gridDim.x-th work unit; 0 launches one CTA per unit and leaves the order to the block scheduler.
+// max_ctas > 0 makes the CTAs persistent: max_ctas of them (more if a CTA would get more than
+// MAX_ITEMS units), each running every gridDim.x-th work unit; 0 launches one CTA per unit and
+// leaves the order to the block scheduler.
 template <int MODE>
 cudaError_t launch_scan(const void* X, const void* Y, const void* Z, const ScanParams& p, cudaStream_t stream,
                         int max_ctas) {
@@ -1030,7 +1184,7 @@ cudaError_t launch_scan(const void* X, const void* Y, const void* Z, const ScanP
   const ChunkArgs& a = p.a;
   long long blocks = (long long)a.n_seq * a.H * NTILE;  // work units
   if (blocks == 0) return cudaSuccess;
-  if (max_ctas > 0 && blocks > max_ctas) blocks = max_ctas;
+  if (max_ctas > 0 && blocks > max_ctas) blocks = std::max((long long)max_ctas, (blocks + MAX_ITEMS - 1) / MAX_ITEMS);
   const long long T_total = a.cu_seqlens ? (long long)a.T : (long long)a.n_seq * a.T;
   TmaMaps maps;
   memset(&maps, 0, sizeof(maps));
@@ -1058,8 +1212,29 @@ cudaError_t launch_scan(const void* X, const void* Y, const void* Z, const ScanP
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  tc_scan_kernel<MODE><<<(unsigned)blocks, C::THREADS, Smem<MODE>::BYTES, stream>>>(maps, p);
-  return cudaGetLastError();
+  // A balanced launch needs all its CTAs resident at once (a CTA may wait for its predecessor's
+  // flag), which a cooperative launch guarantees or refuses; refused, it runs plain instead.
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = Smem<MODE>::BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  if (p.balanced) {
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, tc_scan_kernel<MODE>, maps, p) == cudaSuccess) return cudaSuccess;
+    (void)cudaGetLastError();
+    ScanParams plain = p;
+    plain.balanced = 0;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, tc_scan_kernel<MODE>, maps, plain);
+  }
+  return cudaLaunchKernelEx(&cfg, tc_scan_kernel<MODE>, maps, p);
 }
 
 }  // namespace
@@ -1075,14 +1250,34 @@ cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream) {
   // Equal-length batches: one persistent CTA per SM (a unit's first loads overlap the previous
   // unit's last chunks).  Packed varlen batches: one CTA per unit, so that the block scheduler
   // hands the next (longest-first) unit to whichever SM frees up.
+  // With at least as many units as SMs and a final-state output to hand states over through, the
+  // chunks are split evenly over the persistent CTAs (balanced), so no SM idles while others run
+  // a last round of whole units.
   int max_ctas = 0;
   if (!a.cu_seqlens) {
     int dev = 0;
     max_ctas = 152;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&max_ctas, cudaDevAttrMultiProcessorCount, dev);
+    const long long units = (long long)a.n_seq * a.H * NTILE;
+    if (a.hT && a.T > 0 && units / NTILE >= max_ctas / NTILE && max_ctas <= FLAG_MAX_CTAS &&
+        units / NTILE * ((a.T + CHUNK - 1) / CHUNK) < (1ll << 31)) {
+      static std::atomic<unsigned> launches{0};
+      const unsigned n = launches.fetch_add(1u);
+      p.balanced = 1;
+      p.flag_set = (int)(n % FLAG_SETS);
+      p.epoch = n / FLAG_SETS % 0xFFFFFFFu + 1u;
+    }
   }
   return launch_scan<MODE_FWD>(a.q, a.k, a.v, p, stream, max_ctas);
+}
+
+// After a wait gave up, a hand-over flag may have been left raised; lower them all.
+cudaError_t tc_clear_handover(cudaStream_t stream) {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_handover);
+  if (e != cudaSuccess) return e;
+  return cudaMemsetAsync(p, 0, sizeof(g_handover), stream);
 }
 
 namespace {
