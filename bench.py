@@ -172,25 +172,30 @@ class Dist:
 
 
 def timed(torch, dist, fn, steps, warmup):
-    """W untimed calls, then exactly K calls between a barrier + synchronize on both sides.
+    """W untimed calls, then exactly K calls between a barrier + synchronize on both sides, timed
+    by one pair of CUDA events around the K calls (nothing else in the stream between them).
+    Then K more calls, each bracketed by its own events, for the per-call (kernel) time.
     Returns (ms per step over the region, mean ms per call from per-call events)."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     dist.barrier()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for i in range(steps):
-        ev[i][0].record(stream)
+    for _ in range(steps):
         fn()
-        ev[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
     region = start.elapsed_time(end) / steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
     per_call = statistics.mean(a.elapsed_time(b) for a, b in ev)
     return region, per_call
 
@@ -233,7 +238,7 @@ def bench_fwd(torch, gla, wl, dist, args, peaks):
     res = {
         "workload": w.name, "tokens": tokens, "ms_per_step": region,
         "value": tokens * dist.world / (region / 1e3),
-        "roofline": roofline(fwd_bytes(tokens, w.n_seq, False), fwd_flops(tokens), per_call / 1e3,
+        "roofline": roofline(fwd_bytes(tokens, w.n_seq, False), fwd_flops(tokens), region / 1e3,
                              peaks),
         "kernel_ms": per_call, "launches_per_step": 1,
     }
@@ -273,7 +278,7 @@ def bench_varlen(torch, gla, wl, dist, args, peaks):
     res = {"workload": w.name, "tokens": w.tokens, "ms_per_step": region,
            "value": w.tokens * dist.world / (region / 1e3), "unit": "tokens/s",
            "roofline": roofline(fwd_bytes(w.tokens, w.n_seq, True), fwd_flops(w.tokens),
-                                per_call / 1e3, peaks),
+                                region / 1e3, peaks),
            "launches_per_step": 2}
     del g, o, hT
     return res
@@ -292,7 +297,7 @@ def bench_bwd(torch, gla, wl, dist, args, peaks):
                               + 128 * DV + 128 * DK + 128 * DK + 128 * DV + 4 * DK * DV)  # dk, dv scan
     res = {"workload": w.name, "tokens": tokens, "ms_per_step": region,
            "value": tokens * dist.world / (region / 1e3), "unit": "tokens/s",
-           "roofline": roofline(byts, flops, per_call / 1e3, peaks), "launches_per_step": 4}
+           "roofline": roofline(byts, flops, region / 1e3, peaks), "launches_per_step": 4}
     del g
     return res
 
@@ -318,7 +323,7 @@ def bench_decode(torch, gla, wl, dist, args, peaks):
            "ms_per_step": region,
            "value": w.seqs * dist.world / (region / 1e3), "unit": "tokens/s",
            "token": "one new token per sequence through all 24 layers",
-           "roofline": roofline(state_bytes, 2 * 2 * w.N * H * DK * DV, per_call / 1e3, peaks),
+           "roofline": roofline(state_bytes, 2 * 2 * w.N * H * DK * DV, region / 1e3, peaks),
            "io_bytes_outside_roofline": io_bytes, "launches_per_step": 1}
     res["roofline"]["algorithmic_bytes_note"] = "fp32 state read + write per step"
     res["roofline"]["traffic"] = profiled_traffic("decode", w.N * H)
