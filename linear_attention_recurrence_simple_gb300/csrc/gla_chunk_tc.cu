@@ -173,6 +173,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Shared -> global tile store (bulk-group completion), and the wait for this thread's bulk groups
 // to have read shared memory (the global writes are complete by the end of the grid).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
@@ -196,11 +204,6 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 }
 __device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
-  float4 v;
-  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
-  return v;
 }
 
 __device__ __forceinline__ void umma(uint32_t d_tmem, SDesc a, SDesc b, uint32_t idesc, uint32_t acc) {
@@ -451,7 +454,6 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       if (i == B_TBL_EMPTY || i == B_TBL_EMPTY + 1) cnt = C::SPLIT ? 512 : 384;  // its reader warps
       if (i == B_O_FULL) cnt = 2;
       if (i == B_ST_FULL) cnt = 128;  // the epilogue threads have staged the final state
-      if (i == B_HANDOVER) cnt = 128;  // the epilogue threads have seen the hand-over flag
       if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_P_HALF || i == B_U_EMPTY || i == B_SP_FULL ||
           i == B_O_EMPTY || i == B_OST_FULL || i == B_ZR || i == B_ZR + 1)
         cnt = 128;
@@ -857,6 +859,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
         mbar_arrive(&bars[B_SP_FULL]);
       };
       bool aborted = false;
+      bool head_pending = false;  // a head piece's state load is in flight (thread r_ = 0)
       int nst = 0;  // full chunks stored through the staging tile
       int gk = 0, ku = 0;
       for (int u = 0; u < n_items && !aborted; ++u, ++ku) {
@@ -878,12 +881,14 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
          }
          if (MODE == MODE_FWD && w.head) {
            // The same tile's CTA of the previous group ran this unit's first chunks and left the
-           // state in its final-state tile; once every epilogue thread has seen the flag, lower it
-           // for the next launch.
-           unsigned* flag = &g_handover[prm.flag_set * FLAG_MAX_CTAS + blockIdx.x - NTILE];
-           bool seen = true;
-           {
+           // state in its final-state tile.  Thread r_ = 0 waits for that CTA's flag, lowers it
+           // for the next launch and loads the tile into the (free) state-copy buffer by TMA; each
+           // thread then takes its fp32 row from there (the row covers exactly the bytes of its
+           // own hi and lo copy rows, so the copy written next overwrites nothing of another's).
+           if (r_ == 0) {
+             unsigned* flag = &g_handover[prm.flag_set * FLAG_MAX_CTAS + blockIdx.x - NTILE];
              unsigned long long t0 = ~0ull;
+             bool seen = true;
              while (ld_acquire_gpu(flag) != prm.epoch) {
                const unsigned long long tn = global_timer_ns();
                if (t0 == ~0ull) {
@@ -894,23 +899,27 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
                  break;
                }
              }
-           }
-           if (!__all_sync(0xffffffffu, seen)) { aborted = true; break; }
-           mbar_arrive(&bars[B_HANDOVER]);
-           if (r_ < DK) {
-             const float* src = prm.s_out + ((long long)srow0 + r_) * DV + col0;
-#pragma unroll
-             for (int x = 0; x < TN / 4; ++x) {
-               const float4 v4 = ld_cg_f4(src + 4 * x);
-               S[4 * x] = v4.x;
-               S[4 * x + 1] = v4.y;
-               S[4 * x + 2] = v4.z;
-               S[4 * x + 3] = v4.w;
+             if (seen) {
+               *reinterpret_cast<volatile unsigned*>(flag) = 0u;
+               asm volatile("fence.proxy.async.global;" ::: "memory");
+               head_pending = true;
+               mbar_expect_tx(&bars[B_HANDOVER], 2 * SZ_SPH);
+               tma_load_2d(spb, &maps.s, &bars[B_HANDOVER], col0, srow0);
+               tma_load_2d(spb + SZ_SPH, &maps.s, &bars[B_HANDOVER], col0 + 32, srow0);
              }
            }
-           if ((warp & 3) == 0) {
-             if (!warp_wait(&bars[B_HANDOVER], 0u, a, abort_flag)) { aborted = true; break; }
-             if (lane == 0) *reinterpret_cast<volatile unsigned*>(flag) = 0u;
+           if (!warp_wait(&bars[B_HANDOVER], 0u, a, abort_flag)) { aborted = true; break; }
+           head_pending = false;
+           if (r_ < DK) {
+#pragma unroll
+             for (int x = 0; x < TN / 4; ++x) {
+               const uint4 v = ld_shared_v4(spb + (uint32_t)(x >> 3) * SZ_SPH + (uint32_t)r_ * 128u +
+                                            ((uint32_t)((x & 7) ^ (r_ & 7)) << 4));
+               S[4 * x] = __uint_as_float(v.x);
+               S[4 * x + 1] = __uint_as_float(v.y);
+               S[4 * x + 2] = __uint_as_float(v.z);
+               S[4 * x + 3] = __uint_as_float(v.w);
+             }
            }
          } else if (prm.s0 && r_ < DK) {
            const float4* src = reinterpret_cast<const float4*>(prm.s0 + ((long long)srow0 + r_) * DV + col0);
@@ -1097,7 +1106,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
        mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
        gk += w.it1 - w.it0;
       }
-      if (r_ == 0) bulk_wait_read_all();  // the last tile and state stores have read shared memory
+      if (r_ == 0) {
+        bulk_wait_read_all();  // the last tile and state stores have read shared memory
+        if (head_pending) mbar_wait_drain(&bars[B_HANDOVER], 0u, DRAIN_NS, a.err);  // after an abort
+      }
     };
     if constexpr (!C::SPLIT) {
       setmaxnreg_inc<C::REG_STATE>();
