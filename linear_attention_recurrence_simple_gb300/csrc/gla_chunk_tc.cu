@@ -53,7 +53,7 @@
 //               (640 threads) warps 8-11 keep the state part and warps 16-19 take the output part.
 //   warps 12-15 the weighted Z4 for MMA4 (hi and lo, zero past the sequence end).
 // Registers: setmaxnreg in each role redistributes exactly the registers the CTA launches with
-// (forward: 128 each, then 64 control, 184 mask, 184 epilogue, 80 Z4; backward: 96 each, then
+// (forward: 128 each, then 72 control, 184 mask, 184 epilogue, 72 Z4; backward: 96 each, then
 // 64, 120, 136, 64, 96 output).
 // Tensor memory (512 columns): A [0,128), P [128,192), then O_intra, O_inter and U [384,512).
 // Every mbarrier wait is bounded (see gla_common.cuh); on a timeout the CTA records
@@ -88,8 +88,8 @@ struct Cfg {
   static constexpr bool SPLIT = MODE != MODE_FWD;
   static constexpr int THREADS = SPLIT ? 640 : 512;
   static constexpr int REG_LAUNCH = SPLIT ? 96 : 128;
-  static constexpr int REG_CTRL = 64, REG_MASK = SPLIT ? 120 : 184, REG_STATE = SPLIT ? 136 : 184;
-  static constexpr int REG_Z4 = SPLIT ? 64 : 80, REG_OUT = SPLIT ? 96 : 0;
+  static constexpr int REG_CTRL = SPLIT ? 64 : 72, REG_MASK = SPLIT ? 120 : 184, REG_STATE = SPLIT ? 136 : 184;
+  static constexpr int REG_Z4 = SPLIT ? 64 : 72, REG_OUT = SPLIT ? 96 : 0;
   static_assert(REG_CTRL + REG_MASK + REG_STATE + REG_Z4 + REG_OUT == THREADS / 128 * REG_LAUNCH, "register split");
   static_assert(THREADS * REG_LAUNCH <= 65536, "launch registers");
   // shared memory of one stage (byte offsets; each tile 1024-aligned)
