@@ -156,6 +156,20 @@ def test_fwd_persistent_units_with_h0():
     _check_fwd(d, o, hT, False, BF16_TOL)
 
 
+@pytest.mark.parametrize("B,H,T", [(5, 10, 1000), (1, 51, 200), (3, 17, 129), (2, 40, 640)])
+def test_fwd_balanced_ranges(B, H, T):
+    """Equal-length batches with an hT output and at least as many (sequence, head) pairs as
+    groups of three SMs run balanced chunk ranges: pairs straddling two ranges are split into a
+    tail piece and a head piece handed over through the pair's hT tile.  These shapes put the
+    range boundaries at varied chunk offsets, including ranges about one pair long, a single
+    sequence with many heads, and partial last chunks.  Compared in full."""
+    d = host_chunk_inputs(40 + B * H + T, [T] * B, H, True, with_h0=(T % 2 == 1), packed=False)
+    d["scale"] = float(gs.SCALE)
+    g = to_device(d, True, packed=False)
+    o, hT = gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], d["scale"], h0=g["h0"])
+    _check_fwd(d, o, hT, False, BF16_TOL)
+
+
 def test_fwd_persistent_empty_sequences():
     """T = 0 with many units per persistent CTA: every unit passes its initial state through as
     the final state, bit for bit."""
