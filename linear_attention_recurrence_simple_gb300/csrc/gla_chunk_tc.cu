@@ -164,6 +164,12 @@ __device__ __forceinline__ SDesc sdesc(uint32_t saddr, uint32_t lbo, uint32_t sb
 __device__ __forceinline__ SDesc operator+(SDesc d, uint32_t bytes) { return {d.lo + (bytes >> 4), d.hi}; }
 
 // ---- PTX wrappers ---------------------------------------------------------------------------
+// Brings a box of a tensor into L2 (no shared memory written, nothing to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"((uint64_t)map), "r"(x), "r"(y),
+               "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int x,
                                             int y, int z) {
   asm volatile(
@@ -555,6 +561,23 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
           tma_load_3d(st + C::ST_Y, &maps.y, full, 0, h, tok);
           tma_load_3d(st + C::ST_Y + 16384u, &maps.y, full, 64, h, tok);
           tma_load_3d(st + C::ST_Z, &maps.z, full, col0, h, tok);
+        }
+        // The same boxes of the unit's chunk two steps on go into L2 now, so that their load,
+        // issued once a stage frees up, does not wait for DRAM.
+        if (it + 2 < w.it1) {
+          const int tp = (int)(w.tb + (long long)(C::REVERSE ? w.nc - 3 - it : it + 2) * CHUNK);
+          if (C::NARROW) {
+            tma_prefetch_3d(&maps.x, col0, h, tp);
+            tma_prefetch_3d(&maps.y, col0, h, tp);
+            tma_prefetch_3d(&maps.z, 0, h, tp);
+            tma_prefetch_3d(&maps.z, 64, h, tp);
+          } else {
+            tma_prefetch_3d(&maps.x, 0, h, tp);
+            tma_prefetch_3d(&maps.x1, 64, h, tp);
+            tma_prefetch_3d(&maps.y, 0, h, tp);
+            tma_prefetch_3d(&maps.y, 64, h, tp);
+            tma_prefetch_3d(&maps.z, col0, h, tp);
+          }
         }
         ++issued[s];
        }
