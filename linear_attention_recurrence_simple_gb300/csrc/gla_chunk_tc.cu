@@ -114,7 +114,7 @@ constexpr uint32_t SZ_SP = 2 * SZ_SPH;          // hi then lo
 enum {
   B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
   B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY, B_OST_FULL, B_OST_EMPTY,
-  B_ZR, B_P_HALF = B_ZR + 2, B_TBL_FULL, B_TBL_EMPTY = B_TBL_FULL + 2, B_ST_FULL = B_TBL_EMPTY + 2, B_ST_EMPTY,
+  B_ZR, B_P_HALF = B_ZR + 2, B_TBL_FULL, B_TBL_EMPTY = B_TBL_FULL + 2, B_ST_FULL = B_TBL_EMPTY + 2,
   B_HANDOVER, B_DRAIN, NBAR = B_DRAIN + 3
 };
 constexpr int PW_FLOATS = 2 * 129;  // lambda^d and scale * lambda^d, d = 0..128
@@ -189,12 +189,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 
 // Shared -> global tile store (bulk-group completion), and the wait for this thread's bulk groups
 // to have read shared memory (the global writes are complete by the end of the grid).
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"((uint64_t)map),
-               "r"(x), "r"(y), "r"(src)
-               : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"((uint64_t)map),
                "r"(x), "r"(y), "r"(z), "r"(src)
@@ -202,7 +196,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -354,7 +347,7 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
 
 struct TmaMaps {
   CUtensorMap x, x1, y, z, o;  // o: the bf16 output (wide modes)
-  CUtensorMap s;                // fp32 final state (forward), 32-column x 96-row boxes
+  CUtensorMap s;                // fp32 final state (forward hand-over loads), 32-column x 96-row boxes
 };
 
 // What a scan kernel needs besides its tensor maps: sequence layout and decay (in `a`), the
@@ -459,7 +452,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       if (i == B_TBL_FULL || i == B_TBL_FULL + 1) cnt = 128;   // the Z4 warps write a unit's table
       if (i == B_TBL_EMPTY || i == B_TBL_EMPTY + 1) cnt = C::SPLIT ? 512 : 384;  // its reader warps
       if (i == B_O_FULL) cnt = 2;
-      if (i == B_ST_FULL) cnt = 128;  // the epilogue threads have staged the final state
+      if (i == B_ST_FULL) cnt = 128;  // the epilogue threads' final-state rows are visible (tail piece)
       if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_P_HALF || i == B_U_EMPTY || i == B_SP_FULL ||
           i == B_O_EMPTY || i == B_OST_FULL || i == B_ZR || i == B_ZR + 1)
         cnt = 128;
@@ -895,14 +888,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
        if constexpr (DO_STATE) {
 #pragma unroll
          for (int x = 0; x < TN; ++x) S[x] = 0.f;
-         if (MODE == MODE_FWD && prm.s_out && ku > 0) {  // the previous unit's final-state store has read the buffer
-           if (r_ == 0) {
-             bulk_wait_read_all();
-             mbar_arrive(&bars[B_ST_EMPTY]);
-           }
-           if (!warp_wait(&bars[B_ST_EMPTY], (uint32_t)(ku - 1) & 1u, a, abort_flag)) { aborted = true; break; }
-         }
          if (MODE == MODE_FWD && w.head) {
+           // (the hand-over tile lands in the state-copy buffer: the last MMA3 must have read it)
+           if (gk > 0 && !warp_wait(&bars[B_SP_EMPTY], (uint32_t)(gk - 1) & 1u, a, abort_flag)) { aborted = true; break; }
            // The same tile's CTA of the previous group ran this unit's first chunks and left the
            // state in its final-state tile.  Thread r_ = 0 waits for that CTA's flag, lowers it
            // for the next launch and loads the tile into the (free) state-copy buffer by TMA; each
@@ -1088,35 +1076,31 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
        if (aborted) break;
        if constexpr (DO_STATE) {
          if (MODE == MODE_FWD && prm.s_out) {
-           // Forward (persistent CTAs): the final state leaves through the state-copy buffer and two
-           // TMA stores of 32-column halves (128B-swizzled fp32 rows; thread r_'s row covers exactly
-           // the bytes of its own hi and lo copy rows), so that 96 rows of per-thread global stores do
-           // not hold up the load/store pipe at the unit boundary.  The buffer is free once the unit's
-           // last MMA3 has read it; the next unit's first state copy waits (B_ST_EMPTY) until the
-           // stores have read it in turn.
-           if constexpr (!DO_OUT) {  // (a single epilogue role has waited for the last O_FULL already)
-             const int gl = gk + (w.it1 - w.it0) - 1;  // the item's last chunk (for an empty one, the one before)
-             if (gl >= 0 && !warp_wait(&bars[B_SP_EMPTY], (uint32_t)gl & 1u, a, abort_flag)) { aborted = true; break; }
-           }
+           // Forward: each thread stores its final-state row straight from registers (no staging,
+           // nothing to wait for); a tail piece raises its hand-over flag once every row is visible.
            if (r_ < DK) {
+             float* dst = prm.s_out + ((long long)srow0 + r_) * DV + col0;
+             if ((reinterpret_cast<uintptr_t>(prm.s_out) & 31u) == 0) {
 #pragma unroll
-             for (int x = 0; x < TN / 4; ++x)
-               st_shared_v4(spb + (uint32_t)(x >> 3) * SZ_SPH + (uint32_t)r_ * 128u + ((uint32_t)((x & 7) ^ (r_ & 7)) << 4),
-                            __float_as_uint(S[4 * x]), __float_as_uint(S[4 * x + 1]), __float_as_uint(S[4 * x + 2]),
-                            __float_as_uint(S[4 * x + 3]));
-           }
-           fence_async_smem();
-           mbar_arrive(&bars[B_ST_FULL]);
-           if ((warp & 3) == 0) {  // the whole warp waits, lane 0 issues
-             if (!warp_wait(&bars[B_ST_FULL], (uint32_t)ku & 1u, a, abort_flag)) { aborted = true; break; }
-             if (lane == 0) {
-               tma_store_2d(&maps.s, spb, col0, srow0);
-               tma_store_2d(&maps.s, spb + SZ_SPH, col0 + 32, srow0);
-               if (MODE == MODE_FWD && w.tail) {  // the next group's CTA continues this unit from the stored state
-                 bulk_wait_all();
-                 asm volatile("fence.proxy.async.global;" ::: "memory");
-                 st_release_gpu(&g_handover[prm.flag_set * FLAG_MAX_CTAS + blockIdx.x], prm.epoch);
+               for (int x = 0; x < TN / 8; ++x) {
+                 const uint32_t v[8] = {__float_as_uint(S[8 * x]),     __float_as_uint(S[8 * x + 1]),
+                                        __float_as_uint(S[8 * x + 2]), __float_as_uint(S[8 * x + 3]),
+                                        __float_as_uint(S[8 * x + 4]), __float_as_uint(S[8 * x + 5]),
+                                        __float_as_uint(S[8 * x + 6]), __float_as_uint(S[8 * x + 7])};
+                 st_global_v8(dst + 8 * x, v);
                }
+             } else {
+#pragma unroll
+               for (int x = 0; x < TN / 4; ++x)
+                 reinterpret_cast<float4*>(dst)[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
+             }
+           }
+           if (w.tail) {  // the next group's CTA continues this unit from the stored state
+             __threadfence();
+             mbar_arrive(&bars[B_ST_FULL]);
+             if (r_ == 0) {
+               if (mbar_wait(&bars[B_ST_FULL], 0u, a.wait_ns, abort_flag))
+                 st_release_gpu(&g_handover[prm.flag_set * FLAG_MAX_CTAS + blockIdx.x], prm.epoch);
              }
            }
          }
