@@ -113,7 +113,7 @@ constexpr uint32_t SZ_SPH = 96 * 128;           // bf16 state tile: 96 rows (d_k
 constexpr uint32_t SZ_SP = 2 * SZ_SPH;          // hi then lo
 enum {
   B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
-  B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY, B_OST_FULL, B_OST_EMPTY,
+  B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY,
   B_ZR, B_P_HALF = B_ZR + 2, B_TBL_FULL, B_TBL_EMPTY = B_TBL_FULL + 2, B_ST_FULL = B_TBL_EMPTY + 2,
   B_HANDOVER, B_DRAIN, NBAR = B_DRAIN + 3
 };
@@ -346,7 +346,7 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
 }
 
 struct TmaMaps {
-  CUtensorMap x, x1, y, z, o;  // o: the bf16 output (wide modes)
+  CUtensorMap x, x1, y, z, o;  // o: the bf16 output (wide modes), 32-row boxes (one per epilogue warp)
   CUtensorMap s;                // fp32 final state (forward hand-over loads), 32-column x 96-row boxes
 };
 
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       if (i == B_O_FULL) cnt = 2;
       if (i == B_ST_FULL) cnt = 128;  // the epilogue threads' final-state rows are visible (tail piece)
       if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_P_HALF || i == B_U_EMPTY || i == B_SP_FULL ||
-          i == B_O_EMPTY || i == B_OST_FULL || i == B_ZR || i == B_ZR + 1)
+          i == B_O_EMPTY || i == B_ZR || i == B_ZR + 1)
         cnt = 128;
       mbar_init(&bars[i], cnt);
     }
@@ -983,16 +983,14 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
           const float gf = C::REVERSE ? (r_ < L ? pw[L - 1 - r_] : 0.f) : pws[r_ + 1];
           const long long orow = (w.tb + (long long)c * CHUNK + r_) * a.H + h;
           if (!C::NARROW) {
-            // Full chunks go through the staging tile and one TMA store (a whole 128 x 64 tile, no
-            // per-row stores on the load/store pipe); a partial last chunk is stored row by row so that
-            // nothing past the sequence end is written.
+            // Full chunks go through the staging tile, each warp's 32 rows with that warp's own TMA
+            // store (no per-row stores on the load/store pipe, and no barrier across the warps: lane 0
+            // waits for its previous store to have read the rows before they are rewritten); a partial
+            // last chunk is stored row by row so that nothing past the sequence end is written.
             const bool staged = L == CHUNK;
-            if (staged && nst > 0) {  // the previous store has finished reading the staging tile
-              if (r_ == 0) {
-                bulk_wait_read_all();
-                mbar_arrive(&bars[B_OST_EMPTY]);
-              }
-              if (!warp_wait(&bars[B_OST_EMPTY], (uint32_t)(nst - 1) & 1u, a, abort_flag)) { aborted = true; break; }
+            if (staged && nst > 0) {
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
             }
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(prm.out) + orow * DV + col0);
             const uint32_t srow = sbase + SMM::OFF_OST + (uint32_t)r_ * 128u;
@@ -1026,11 +1024,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
             }
             if (staged) {
               fence_async_smem();
-              mbar_arrive(&bars[B_OST_FULL]);
-              if ((warp & 3) == 0) {  // the whole warp waits (so that an abort leaves it in step)
-                if (!warp_wait(&bars[B_OST_FULL], (uint32_t)nst & 1u, a, abort_flag)) { aborted = true; break; }
-                if (lane == 0) tma_store_3d(&maps.o, sbase + SMM::OFF_OST, col0, h, (int)(w.tb + (long long)c * CHUNK));
-              }
+              __syncwarp();
+              if (lane == 0)
+                tma_store_3d(&maps.o, sbase + SMM::OFF_OST + (uint32_t)(warp & 3) * 4096u, col0, h,
+                             (int)(w.tb + (long long)c * CHUNK) + 32 * (warp & 3));
               ++nst;
             }
           } else {
@@ -1113,10 +1110,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
        mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
        gk += w.it1 - w.it0;
       }
-      if (r_ == 0) {
-        bulk_wait_read_all();  // the last tile and state stores have read shared memory
-        if (head_pending) mbar_wait_drain(&bars[B_HANDOVER], 0u, DRAIN_NS, a.err);  // after an abort
-      }
+      if (lane == 0) bulk_wait_read_all();  // this warp's last tile store has read shared memory
+      if (r_ == 0 && head_pending) mbar_wait_drain(&bars[B_HANDOVER], 0u, DRAIN_NS, a.err);  // after an abort
     };
     if constexpr (!C::SPLIT) {
       setmaxnreg_inc<C::REG_STATE>();
@@ -1167,12 +1162,13 @@ EncodeTiledFn encode_fn() {
 }
 
 // 3-D view [T_total, H, d] of a token-major bf16 tensor; box = (box_x columns, 1 head, 128 tokens).
-bool make_map(CUtensorMap* m, const void* base, int d, int H, long long T, int box_x, CUtensorMapSwizzle sw) {
+bool make_map(CUtensorMap* m, const void* base, int d, int H, long long T, int box_x, CUtensorMapSwizzle sw,
+              int box_t = CHUNK) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T};
   const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)CHUNK};
+  const cuuint32_t box[3] = {(cuuint32_t)box_x, 1, (cuuint32_t)box_t};
   const cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1213,7 +1209,7 @@ cudaError_t launch_scan(const void* X, const void* Y, const void* Z, const ScanP
         (!C::NARROW && !make_map(&maps.x1, X, DK, a.H, T_total, 32, CU_TENSOR_MAP_SWIZZLE_64B)) ||
         !make_map(&maps.y, Y, dx, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.z, Z, dz, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        (!C::NARROW && !make_map(&maps.o, p.out, DV, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B)))
+        (!C::NARROW && !make_map(&maps.o, p.out, DV, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32)))
       return cudaErrorInvalidValue;
   }
   const long long state_rows = (long long)a.n_seq * a.H * DK;
