@@ -44,9 +44,10 @@ def _bind(path):
     lib.oracle_fwd_chunked.argtypes = [P, P, P, P, P, D, P, I, I, I, I, I, P, P, I]
     lib.oracle_decode_step.argtypes = [P, P, P, P, D, P, P, I, I, I, I, I]
     lib.oracle_bwd.argtypes = [P, P, P, P, P, D, P, P, P, I, I, I, I, P, P, P, P, I]
+    lib.oracle_self_aug.argtypes = [P, P, P, P, ctypes.c_longlong, I, I, I, P]
     lib.oracle_hardware_threads.argtypes = []
     for f in (lib.oracle_fwd, lib.oracle_fwd_chunked, lib.oracle_decode_step, lib.oracle_bwd,
-              lib.oracle_hardware_threads):
+              lib.oracle_self_aug, lib.oracle_hardware_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -137,6 +138,22 @@ def decode_step(q, k, v, log_lambda, scale, state, nthreads=0, _lib_override=Non
     return o
 
 
+def self_aug(q, k, v, aug, _lib_override=None):
+    """The self-augmentation term ``sigmoid(q_t . (a_h * k_t)) v_t`` for every row (token or
+    sequence) and head, fp64 ``[rows, H, dv]``; add it to :func:`fwd`'s or :func:`decode_step`'s
+    output.  q, k ``[rows, H, dk]``; v ``[rows, H, dv]``; aug ``[H, dk]``."""
+    q, k, v, a = _f32(q), _f32(k), _f32(v), _f32(aug)
+    rows, H, dk, dv = _shapes(q, k, v)
+    if a.shape != (H, dk):
+        raise ValueError("aug must be [H, dk]")
+    out = np.zeros((rows, H, dv), np.float64)
+    rc = (_lib_override or _load()).oracle_self_aug(_ptr(q), _ptr(k), _ptr(v), _ptr(a), rows, H, dk, dv,
+                                                    _ptr(out))
+    if rc:
+        raise ValueError(f"oracle_self_aug rejected its arguments ({rc})")
+    return out
+
+
 def bwd(q, k, v, log_lambda, scale, dO, h0=None, dhT=None, cu_seqlens=None, nthreads=0,
         _lib_override=None):
     """Adjoint of :func:`fwd`.  Returns ``(dq, dk, dv, dh0)`` in fp64."""
@@ -177,6 +194,9 @@ class Variant:
 
     def bwd(self, *a, **kw):
         return bwd(*a, _lib_override=self._lib, **kw)
+
+    def self_aug(self, *a, **kw):
+        return self_aug(*a, _lib_override=self._lib, **kw)
 
 
 def source_path() -> str:

@@ -183,6 +183,33 @@ int oracle_decode_step(const float* q, const float* k, const float* v, const flo
   return 0;
 }
 
+// Self-augmentation (section "i14 and the Laplace 3B architecture", the paragraph after the
+// state readout): each head's output gains a gated copy of the token's own value,
+//     add_t = sigmoid(q_t . (a_h (*) k_t)) * v_t,
+// where (*) is the element-wise product and a_h (aug_balance) is the head's learned rescaling of
+// the key's d_k channels; a = 0 gives sigmoid(0) = 1/2, the half-strength copy of the value the
+// page describes at initialisation.  The equation image is missing from the text; the readings
+// used: the query enters unscaled (the readout's scale is not applied to the gate), a holds one
+// d_k vector per head, and the term is added to the readout o_t.  Rows are tokens of a forward
+// call or sequences of a decode step: q, k [rows, H, dk]; v, add [rows, H, dv]; aug [H, dk].
+int oracle_self_aug(const float* q, const float* k, const float* v, const float* aug, long long rows,
+                    int H, int dk, int dv, double* add) {
+  if (rows < 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+  for (long long t = 0; t < rows; ++t)
+    for (int h = 0; h < H; ++h) {
+      const float* qt = q + ((size_t)t * H + h) * dk;
+      const float* kt = k + ((size_t)t * H + h) * dk;
+      const float* vt = v + ((size_t)t * H + h) * dv;
+      const float* ah = aug + (size_t)h * dk;
+      double g = 0.0;
+      for (int c = 0; c < dk; ++c) g += (double)qt[c] * ((double)ah[c] * (double)kt[c]);
+      const double gate = 1.0 / (1.0 + std::exp(-g));
+      double* out = add + ((size_t)t * H + h) * dv;
+      for (int b = 0; b < dv; ++b) out[b] = gate * (double)vt[b];
+    }
+  return 0;
+}
+
 // Backward of oracle_fwd (the adjoint of the recurrence), given dO = dL/do and dhT = dL/dhT.
 // With G_t = dL/dS_t (all later uses included) and R_t = lambda * G_{t+1} (R_T = dhT):
 //   G_t  = R_t + scale * q_t dO_t^T

@@ -52,6 +52,16 @@ MUTANTS = [
     ("bwd: carry not decayed", "for (size_t e = 0; e < DS; ++e) R[e] = lam * G[e];",
      "for (size_t e = 0; e < DS; ++e) R[e] = G[e];", 0),
     ("bwd: dhT ignored", "    if (dhT) {", "    if (false && dhT) {", 0),
+    ("aug: gate without the balance", "g += (double)qt[c] * ((double)ah[c] * (double)kt[c]);",
+     "g += (double)qt[c] * (double)kt[c];", 0),
+    ("aug: gate uses q twice", "g += (double)qt[c] * ((double)ah[c] * (double)kt[c]);",
+     "g += (double)qt[c] * ((double)ah[c] * (double)qt[c]);", 0),
+    ("aug: sigmoid of the wrong sign", "const double gate = 1.0 / (1.0 + std::exp(-g));",
+     "const double gate = 1.0 / (1.0 + std::exp(g));", 0),
+    ("aug: gate not applied", "for (int b = 0; b < dv; ++b) out[b] = gate * (double)vt[b];",
+     "for (int b = 0; b < dv; ++b) out[b] = (double)vt[b];", 0),
+    ("aug: balance of the wrong head", "const float* ah = aug + (size_t)h * dk;",
+     "const float* ah = aug + (size_t)(H - 1 - h) * dk;", 0),
     ("bwd: forward state missing its decay",
      "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];",
      "S[(size_t)a * dv + b] = S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];", 2),
@@ -67,6 +77,10 @@ PIN_TESTS = [
     pins.test_decode_steps_equal_prefill,
     lambda o: pins.test_backward_matches_finite_differences(o, [6]),
     pins.test_backward_lambda_one_closed_form,
+    pins.test_self_aug_zero_balance_is_half_the_value,
+    pins.test_self_aug_opposite_balances_sum_to_the_value,
+    pins.test_self_aug_single_channel_saturates_by_sign_of_q_times_k,
+    pins.test_self_aug_gate_against_exact_value,
 ]
 
 

@@ -298,3 +298,59 @@ def test_backward_empty_sequence_passes_dhT(oracle_mod):
     _, _, _, dh0 = oracle_mod.bwd(q, k, v, np.log(np.array([0.9], np.float32)), 1.0, dO, dhT=dhT,
                                   cu_seqlens=cu)
     assert np.array_equal(dh0[0], dhT[0].astype(np.float64))
+
+
+# --- self-augmentation term -------------------------------------------------------------------
+# The page (section "i14 and the Laplace 3B architecture", the paragraph after the readout) adds a
+# gated copy of the value, sigmoid(q_t . (a (*) k_t)) v_t, and states that a = 0 gives a
+# half-strength copy of the value.  The pins below use facts of the sigmoid and of the gate's
+# arguments that do not depend on how the oracle evaluates it.
+
+def _aug_case(seed, rows=9, H=2, dk=5, dv=7):
+    q = _rand(seed, 11, (rows, H, dk))
+    k = _rand(seed, 12, (rows, H, dk))
+    v = _rand(seed, 13, (rows, H, dv))
+    a = _rand(seed, 14, (H, dk), 0.7)
+    return q, k, v, a
+
+
+def test_self_aug_zero_balance_is_half_the_value(oracle_mod):
+    q, k, v, _ = _aug_case(21)
+    add = oracle_mod.self_aug(q, k, v, np.zeros((q.shape[1], q.shape[2]), np.float32))
+    assert np.array_equal(add, 0.5 * np.asarray(v, np.float64))
+
+
+def test_self_aug_opposite_balances_sum_to_the_value(oracle_mod):
+    # sigmoid(x) + sigmoid(-x) = 1 for every gate argument x = q . (a * k)
+    q, k, v, a = _aug_case(22)
+    s = oracle_mod.self_aug(q, k, v, a) + oracle_mod.self_aug(q, k, v, -a)
+    assert np.allclose(s, np.asarray(v, np.float64), rtol=0, atol=1e-14)
+
+
+def test_self_aug_single_channel_saturates_by_sign_of_q_times_k(oracle_mod):
+    # a = M e_c on one channel c: the gate argument is M q_c k_c, so for large M the copy is the
+    # whole value where q_c k_c > 0 and nothing where q_c k_c < 0 (per row and head).
+    q, k, v, _ = _aug_case(23, rows=16, H=2, dk=6, dv=3)
+    for c in (0, 4):
+        a = np.zeros((2, 6), np.float32)
+        a[0, c] = 1e4
+        a[1, (c + 1) % 6] = -1e4
+        add = oracle_mod.self_aug(q, k, v, a)
+        for h, ch, sign in ((0, c, 1.0), (1, (c + 1) % 6, -1.0)):
+            prod = sign * np.asarray(q[:, h, ch], np.float64) * np.asarray(k[:, h, ch], np.float64)
+            want = np.where(prod[:, None] > 0, np.asarray(v[:, h], np.float64), 0.0)
+            keep = np.abs(prod) > 1e-2  # stay clear of the gate's middle
+            assert np.allclose(add[keep, h], want[keep], rtol=0, atol=1e-12)
+
+
+def test_self_aug_gate_against_exact_value(oracle_mod):
+    # One row, one head, dk = 2: q . (a * k) = 0.5*2*1 + (-1)*0.25*4 = 1 - 1 = 0 -> gate 1/2;
+    # and with a = (1, 0): 0.5*1*2 = 1 -> gate 1 / (1 + e^-1).
+    q = np.array([[[0.5, -1.0]]], np.float32)
+    k = np.array([[[2.0, 4.0]]], np.float32)
+    v = np.array([[[1.0, -3.0, 8.0]]], np.float32)
+    add = oracle_mod.self_aug(q, k, v, np.array([[1.0, 0.25]], np.float32))
+    assert np.array_equal(add, 0.5 * np.asarray(v, np.float64))
+    add = oracle_mod.self_aug(q, k, v, np.array([[1.0, 0.0]], np.float32))
+    g = 1.0 / (1.0 + np.exp(-1.0))
+    assert np.allclose(add, g * np.asarray(v, np.float64), rtol=1e-15, atol=0)
