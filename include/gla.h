@@ -96,6 +96,21 @@ int gla_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
                   int n_seq, int T, int H, int dk, int dv, int dtype, void* workspace,
                   size_t ws_bytes, gla_stream_t stream);
 
+/* Chunked forward with the self-augmentation step ("Beyond the KV cache", section "i14 and the
+ * Laplace 3B architecture", the paragraph after the state readout): every output row also gains
+ * a gated copy of its own value,
+ *     o_t += sigmoid(q_t . (a_h * k_t)) v_t,
+ * with a_h the head's aug_balance (a learned rescaling of the key's channels; a = 0 gives the
+ * half-strength copy 0.5 v_t).  The query enters the gate unscaled.
+ *   aug          [H, 96] fp32 device (non-NULL, 16-byte aligned); a NULL aug returns GLA_ERR_NULL.
+ *   every other argument, and the results, as in gla_chunk_fwd (hT is not affected: the copy
+ *   adds to the output only).
+ * gla_chunk_bwd differentiates the mixer without this step. */
+int gla_chunk_fwd_aug(const void* q, const void* k, const void* v, const float* log_lambda,
+                      const float* h0, float scale, const float* aug, void* o, float* hT,
+                      const int32_t* cu_seqlens, int n_seq, int T, int H, int dk, int dv, int dtype,
+                      void* workspace, size_t ws_bytes, gla_stream_t stream);
+
 /* Bytes of device workspace that gla_chunk_bwd needs; n_seq, T, H as in that call, packed != 0
  * when cu_seqlens is given, dtype the gla_dtype.  In bf16 mode the workspace holds fp32 partial
  * sums of dq and dk (2 x T_total x H x 96 x 4 bytes) plus the packed schedule; in fp32 mode only
@@ -130,6 +145,14 @@ int gla_chunk_bwd(const void* q, const void* k, const void* v, const float* log_
 int gla_decode_step(const void* q, const void* k, const void* v, const float* log_lambda,
                     float scale, float* state, const int32_t* slot, int pool_rows, void* o, int N,
                     int H, int dk, int dv, int dtype, gla_stream_t stream);
+
+/* One decode step with the self-augmentation step: as gla_decode_step, and the output also gains
+ * sigmoid(q . (a_h * k)) v (see gla_chunk_fwd_aug); aug [H, 96] fp32 device, non-NULL and
+ * 16-byte aligned.  The state update is the same. */
+int gla_decode_step_aug(const void* q, const void* k, const void* v, const float* log_lambda,
+                        float scale, const float* aug, float* state, const int32_t* slot,
+                        int pool_rows, void* o, int N, int H, int dk, int dv, int dtype,
+                        gla_stream_t stream);
 
 /* The forward without any device allocation (no counterpart in the paper).  For callers that
  * cannot allocate device memory per call, such as a serving engine whose memory is all handed to

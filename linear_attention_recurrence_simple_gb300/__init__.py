@@ -27,7 +27,7 @@ __all__ = [
 DK, DV, CHUNK = 96, 192, 128
 GLA_BF16, GLA_F32 = 0, 1
 EXPORTS = ("gla_workspace_bytes", "gla_bwd_workspace_bytes", "gla_chunk_fwd", "gla_chunk_bwd",
-           "gla_decode_step",
+           "gla_decode_step", "gla_chunk_fwd_aug", "gla_decode_step_aug",
            "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
            "gla_status_string")
 NOALLOC_MAX_SEQS = 16384
@@ -75,6 +75,10 @@ def load_library(build: bool = True):
         lib.gla_chunk_fwd_noalloc.restype = I
         lib.gla_decode_step.argtypes = [P, P, P, P, F, P, P, I, P, I, I, I, I, I, P]
         lib.gla_decode_step.restype = I
+        lib.gla_chunk_fwd_aug.argtypes = [P, P, P, P, P, F, P, P, P, P, I, I, I, I, I, I, P, Z, P]
+        lib.gla_chunk_fwd_aug.restype = I
+        lib.gla_decode_step_aug.argtypes = [P, P, P, P, F, P, P, P, I, P, I, I, I, I, I, P]
+        lib.gla_decode_step_aug.restype = I
         lib.gla_get_device_error.argtypes = [P]
         lib.gla_get_device_error.restype = I
         lib.gla_set_wait_limit_ns.argtypes = [U]
@@ -164,8 +168,11 @@ def _workspace(cu_seqlens, n_seq, H, device, workspace):
 
 
 def gla_chunk_fwd(q, k, v, log_lambda, scale=None, h0=None, cu_seqlens=None,
-                  output_final_state: bool = True, o=None, hT=None, workspace=None):
-    """Chunked forward.  Returns ``(o, hT)`` (``hT`` is None if not requested)."""
+                  output_final_state: bool = True, o=None, hT=None, workspace=None, aug=None):
+    """Chunked forward.  Returns ``(o, hT)`` (``hT`` is None if not requested).
+
+    ``aug`` (aug_balance, fp32 ``[H, 96]``) adds the self-augmentation copy
+    ``sigmoid(q_t . (aug[h] * k_t)) v_t`` to each output row (``gla_chunk_fwd_aug``)."""
     lib = load_library()
     dev = q.device
     dt = _dtype_code(q)
@@ -190,11 +197,20 @@ def gla_chunk_fwd(q, k, v, log_lambda, scale=None, h0=None, cu_seqlens=None,
         _need(hT, "hT", torch.float32, dev)
     ws, ws_bytes = _workspace(cu_seqlens, n_seq, H, dev, workspace)
     s = float(DK ** -0.5) if scale is None else float(scale)
+    if aug is not None:
+        _need(aug, "aug", torch.float32, dev)
+        if aug.shape != (H, DK):
+            raise ValueError("aug must be [H, 96]")
     with torch.cuda.device(dev):
-        rc = lib.gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), s, _ptr(o),
-                               _ptr(hT), _ptr(cu_seqlens), n_seq, T, H, DK, DV, dt, _ptr(ws),
-                               ws_bytes, _stream(dev))
-    _check(rc, "gla_chunk_fwd")
+        if aug is None:
+            rc = lib.gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), s, _ptr(o),
+                                   _ptr(hT), _ptr(cu_seqlens), n_seq, T, H, DK, DV, dt, _ptr(ws),
+                                   ws_bytes, _stream(dev))
+        else:
+            rc = lib.gla_chunk_fwd_aug(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), s,
+                                       _ptr(aug), _ptr(o), _ptr(hT), _ptr(cu_seqlens), n_seq, T, H, DK,
+                                       DV, dt, _ptr(ws), ws_bytes, _stream(dev))
+    _check(rc, "gla_chunk_fwd" if aug is None else "gla_chunk_fwd_aug")
     return o, hT
 
 
@@ -267,10 +283,11 @@ def gla_chunk_bwd(q, k, v, log_lambda, dO, scale=None, h0=None, dhT=None, cu_seq
     return dq, dk, dv, dh0
 
 
-def gla_decode_step(q, k, v, log_lambda, state, scale=None, slot=None, o=None):
+def gla_decode_step(q, k, v, log_lambda, state, scale=None, slot=None, o=None, aug=None):
     """One decode step on the state pool ``state [P, H, 96, 192]`` (updated in place).
 
     q, k ``[N, H, 96]``; v ``[N, H, 192]``; ``slot`` ``[N]`` int32 pool rows or None (row n).
+    ``aug`` (fp32 ``[H, 96]``) adds the self-augmentation copy of v (``gla_decode_step_aug``).
     Returns ``o [N, H, 192]``."""
     lib = load_library()
     dev = q.device
@@ -292,10 +309,19 @@ def gla_decode_step(q, k, v, log_lambda, state, scale=None, slot=None, o=None):
         o = torch.empty(v.shape, dtype=v.dtype, device=dev)
     _need(o, "o", v.dtype, dev)
     s = float(DK ** -0.5) if scale is None else float(scale)
+    if aug is not None:
+        _need(aug, "aug", torch.float32, dev)
+        if aug.shape != (H, DK):
+            raise ValueError("aug must be [H, 96]")
     with torch.cuda.device(dev):
-        rc = lib.gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), s, _ptr(state),
-                                 _ptr(slot), state.shape[0], _ptr(o), N, H, DK, DV, dt, _stream(dev))
-    _check(rc, "gla_decode_step")
+        if aug is None:
+            rc = lib.gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), s, _ptr(state),
+                                     _ptr(slot), state.shape[0], _ptr(o), N, H, DK, DV, dt, _stream(dev))
+        else:
+            rc = lib.gla_decode_step_aug(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), s, _ptr(aug),
+                                         _ptr(state), _ptr(slot), state.shape[0], _ptr(o), N, H, DK, DV,
+                                         dt, _stream(dev))
+    _check(rc, "gla_decode_step" if aug is None else "gla_decode_step_aug")
     return o
 
 

@@ -9,7 +9,7 @@ namespace gla {
 cudaError_t launch_decode_step(int dtype_f32, const void* q, const void* k, const void* v,
                                const float* log_lambda, float scale, float* state,
                                const int32_t* slot, int pool_rows, void* o, int N, int H,
-                               unsigned* err, cudaStream_t stream);
+                               const float* aug, unsigned* err, cudaStream_t stream);
 cudaError_t launch_simt_fwd(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_simt_bwd(int dtype_f32, const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream);
@@ -131,10 +131,10 @@ size_t gla_bwd_workspace_bytes(int n_seq, int T, int H, int packed, int dtype) {
   return bytes;
 }
 
-int gla_chunk_fwd(const void* q, const void* k, const void* v, const float* log_lambda,
-                  const float* h0, float scale, void* o, float* hT, const int32_t* cu_seqlens,
-                  int n_seq, int T, int H, int dk, int dv, int dtype, void* workspace,
-                  size_t ws_bytes, gla_stream_t stream) {
+static int chunk_fwd(const void* q, const void* k, const void* v, const float* log_lambda,
+                     const float* h0, float scale, const float* aug, void* o, float* hT,
+                     const int32_t* cu_seqlens, int n_seq, int T, int H, int dk, int dv, int dtype,
+                     void* workspace, size_t ws_bytes, gla_stream_t stream) {
   long long tokens = 0;
   int rc = check_chunk_call(n_seq, T, H, dk, dv, dtype, cu_seqlens, workspace, ws_bytes, &tokens);
   if (rc) return rc;
@@ -142,7 +142,7 @@ int gla_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
   if (!log_lambda) return GLA_ERR_NULL;
   if (tokens > 0 && (!q || !k || !v || !o)) return GLA_ERR_NULL;
   for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)o,
-                        (const void*)h0, (const void*)hT, (const void*)log_lambda})
+                        (const void*)h0, (const void*)hT, (const void*)log_lambda, (const void*)aug})
     if (p && !aligned16(p)) return GLA_ERR_ALIGN;
   int dev;
   unsigned* err;
@@ -156,6 +156,7 @@ int gla_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
   a.v = v;
   a.log_lambda = log_lambda;
   a.h0 = h0;
+  a.aug = aug;
   a.o = o;
   a.hT = hT;
   a.cu_seqlens = cu_seqlens;
@@ -174,6 +175,23 @@ int gla_chunk_fwd(const void* q, const void* k, const void* v, const float* log_
   }
   if (dtype == GLA_F32) return to_status(gla::launch_simt_fwd(a, s));
   return to_status(gla::launch_tc_fwd(a, s));
+}
+
+int gla_chunk_fwd(const void* q, const void* k, const void* v, const float* log_lambda,
+                  const float* h0, float scale, void* o, float* hT, const int32_t* cu_seqlens,
+                  int n_seq, int T, int H, int dk, int dv, int dtype, void* workspace,
+                  size_t ws_bytes, gla_stream_t stream) {
+  return chunk_fwd(q, k, v, log_lambda, h0, scale, nullptr, o, hT, cu_seqlens, n_seq, T, H, dk, dv,
+                   dtype, workspace, ws_bytes, stream);
+}
+
+int gla_chunk_fwd_aug(const void* q, const void* k, const void* v, const float* log_lambda,
+                      const float* h0, float scale, const float* aug, void* o, float* hT,
+                      const int32_t* cu_seqlens, int n_seq, int T, int H, int dk, int dv, int dtype,
+                      void* workspace, size_t ws_bytes, gla_stream_t stream) {
+  if (!aug) return GLA_ERR_NULL;
+  return chunk_fwd(q, k, v, log_lambda, h0, scale, aug, o, hT, cu_seqlens, n_seq, T, H, dk, dv,
+                   dtype, workspace, ws_bytes, stream);
 }
 
 int gla_chunk_bwd(const void* q, const void* k, const void* v, const float* log_lambda,
@@ -236,9 +254,10 @@ int gla_chunk_bwd(const void* q, const void* k, const void* v, const float* log_
   return to_status(gla::launch_tc_bwd(a, acc_q, acc_k, s));
 }
 
-int gla_decode_step(const void* q, const void* k, const void* v, const float* log_lambda,
-                    float scale, float* state, const int32_t* slot, int pool_rows, void* o, int N,
-                    int H, int dk, int dv, int dtype, gla_stream_t stream) {
+static int decode_step(const void* q, const void* k, const void* v, const float* log_lambda,
+                       float scale, const float* aug, float* state, const int32_t* slot,
+                       int pool_rows, void* o, int N, int H, int dk, int dv, int dtype,
+                       gla_stream_t stream) {
   if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_DTYPE;
   if (dk != GLA_DK || dv != GLA_DV) return GLA_ERR_UNSUPPORTED;
   if (N < 0 || H < 1 || pool_rows < 0) return GLA_ERR_SHAPE;
@@ -248,6 +267,7 @@ int gla_decode_step(const void* q, const void* k, const void* v, const float* lo
   for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)o,
                         (const void*)state, (const void*)log_lambda})
     if (!aligned16(p)) return GLA_ERR_ALIGN;
+  if (aug && !aligned16(aug)) return GLA_ERR_ALIGN;
   if (slot && ((uintptr_t)slot & 3u)) return GLA_ERR_ALIGN;
   int dev;
   unsigned* err;
@@ -255,7 +275,23 @@ int gla_decode_step(const void* q, const void* k, const void* v, const float* lo
   int rc = device_state(&dev, &err, &wait_ns);
   if (rc) return rc;
   return to_status(gla::launch_decode_step(dtype == GLA_F32, q, k, v, log_lambda, scale, state, slot,
-                                           pool_rows, o, N, H, err, (cudaStream_t)stream));
+                                           pool_rows, o, N, H, aug, err, (cudaStream_t)stream));
+}
+
+int gla_decode_step(const void* q, const void* k, const void* v, const float* log_lambda,
+                    float scale, float* state, const int32_t* slot, int pool_rows, void* o, int N,
+                    int H, int dk, int dv, int dtype, gla_stream_t stream) {
+  return decode_step(q, k, v, log_lambda, scale, nullptr, state, slot, pool_rows, o, N, H, dk, dv,
+                     dtype, stream);
+}
+
+int gla_decode_step_aug(const void* q, const void* k, const void* v, const float* log_lambda,
+                        float scale, const float* aug, float* state, const int32_t* slot,
+                        int pool_rows, void* o, int N, int H, int dk, int dv, int dtype,
+                        gla_stream_t stream) {
+  if (!aug) return GLA_ERR_NULL;
+  return decode_step(q, k, v, log_lambda, scale, aug, state, slot, pool_rows, o, N, H, dk, dv, dtype,
+                     stream);
 }
 
 int gla_get_device_error(gla_stream_t stream) {

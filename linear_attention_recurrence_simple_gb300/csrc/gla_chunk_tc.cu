@@ -70,7 +70,8 @@
 
 namespace gla {
 
-enum ScanMode { MODE_FWD = 0, MODE_DV = 1, MODE_DQ = 2, MODE_DK = 3 };
+// MODE_FWDA: the forward with the self-augmentation step (see the decay mask).
+enum ScanMode { MODE_FWD = 0, MODE_DV = 1, MODE_DQ = 2, MODE_DK = 3, MODE_FWDA = 4 };
 
 namespace {
 
@@ -81,11 +82,13 @@ template <int MODE>
 struct Cfg {
   static constexpr bool REVERSE = MODE == MODE_DV || MODE == MODE_DK;  // reverse scan, j >= i mask
   static constexpr bool NARROW = MODE == MODE_DQ || MODE == MODE_DK;   // X, Y are 64-wide d_v tiles
+  static constexpr bool FWD = MODE == MODE_FWD || MODE == MODE_FWDA;
+  static constexpr bool AUG = MODE == MODE_FWDA;
   // Warp roles: 16 warps with one epilogue warpgroup (forward), or 20 with the epilogue's state
   // and output parts in two warpgroups (backward scans).  Per-thread registers of each warpgroup
   // after setmaxnreg add up to the launch count times the number of warpgroups (the host checks
   // the compiled count before the first launch: any other split could wait forever).
-  static constexpr bool SPLIT = MODE != MODE_FWD;
+  static constexpr bool SPLIT = !FWD;
   static constexpr int THREADS = SPLIT ? 640 : 512;
   static constexpr int REG_LAUNCH = SPLIT ? 96 : 128;
   static constexpr int REG_CTRL = SPLIT ? 64 : 72, REG_MASK = SPLIT ? 120 : 184, REG_STATE = SPLIT ? 136 : 184;
@@ -130,7 +133,9 @@ struct Smem {
   // contiguous row segments
   static constexpr uint32_t OFF_OST = OFF_SP + SZ_SP;
   static constexpr uint32_t OFF_PW = OFF_OST + (Cfg<MODE>::NARROW ? 4u * RED_WARP_BYTES : SZ_TILE64);
-  static constexpr uint32_t OFF_BAR = OFF_PW + 2 * PW_FLOATS * 4 + 8;  // two tables (per unit parity)
+  // two decay tables (per unit parity), then (self-augmentation) two copies of the head's aug_balance
+  static constexpr uint32_t OFF_AUG = OFF_PW + 2 * PW_FLOATS * 4 + 8;
+  static constexpr uint32_t OFF_BAR = OFF_AUG + (Cfg<MODE>::AUG ? 2 * DK * 4 : 0);
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t OFF_ITEMS = OFF_MISC + 16;  // the CTA's work list (see the kernel)
   static constexpr uint32_t BYTES = OFF_ITEMS + MAX_ITEMS * 32 + 1024;
@@ -715,6 +720,34 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
      }
      for (int it = wi.it0; it < wi.it1; ++it, ++gk) {
       const uint32_t pc = (uint32_t)gk & 1u;
+      // Self-augmentation: row i's output gains sigmoid(q_i . (a_h * k_i)) v_i, which is that
+      // gate added to P's diagonal entry (i, i) before MMA2.  The gate is read from the stage's
+      // q and k rows (held until MMA2 is done), while MMA1 runs.
+      float sig = 0.f;
+      if constexpr (C::AUG) {
+        if (!warp_wait(&bars[B_FULL + (gk & 1)], (uint32_t)(gk >> 1) & 1u, a, abort_flag)) { stop = true; break; }
+        const uint32_t st = sbase + (uint32_t)(gk & 1) * C::SZ_STAGE;
+        const float* av = reinterpret_cast<const float*>(sm + SMM::OFF_AUG) + tbuf * DK;
+        float g = 0.f;
+        // q: columns 0..63 in a 128B-swizzled panel, 64..95 in a 64B-swizzled one; k: two
+        // 128B-swizzled panels.  16-byte piece p of a row holds columns 8p .. 8p + 7.
+#pragma unroll 1
+        for (int p = 0; p < 12; ++p) {
+          const uint32_t qa = p < 8 ? st + C::ST_X + (uint32_t)i * 128u + ((uint32_t)(p ^ (i & 7)) << 4)
+                                    : st + C::ST_X1 + (uint32_t)i * 64u + ((uint32_t)((p - 8) ^ ((i >> 1) & 3)) << 4);
+          const uint32_t ka = st + C::ST_Y + (uint32_t)(p >> 3) * 16384u + (uint32_t)i * 128u +
+                              ((uint32_t)((p & 7) ^ (i & 7)) << 4);
+          const uint4 qv = ld_shared_v4(qa), kv = ld_shared_v4(ka);
+          const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 qf = bf2_to_f2(qw[e]), kf = bf2_to_f2(kw[e]);
+            g = fmaf(qf.x * av[8 * p + 2 * e], kf.x, g);
+            g = fmaf(qf.y * av[8 * p + 2 * e + 1], kf.y, g);
+          }
+        }
+        sig = 1.f / (1.f + expf(-g));
+      }
       if (!warp_wait(&bars[B_A_FULL], pc, a, abort_flag)) { stop = true; break; }
       if (!warp_wait(&bars[B_P_EMPTY], pc ^ 1u, a, abort_flag)) { stop = true; break; }
       tc_fence_after();
@@ -763,7 +796,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
           // diagonal group: the lane's own factors (fixed for the kernel)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float2 pv = mul2(dgf[e], ld_f2(r, 2 * e));
+            float2 pv = mul2(dgf[e], ld_f2(r, 2 * e));
+            if (C::AUG && e == (lane >> 1)) {  // the diagonal entry (column i) carries the gate
+              if (lane & 1)
+                pv.y += sig;
+              else
+                pv.x += sig;
+            }
             pkg[e] = pack_bf16(pv.x, pv.y);
           }
         }
@@ -800,6 +839,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
          pw[d] = pv;
          pws[d] = a.scale * pv;
        }
+       if (C::AUG && t < DK)
+         reinterpret_cast<float*>(sm + SMM::OFF_AUG)[tbuf * DK + t] = a.aug[w.h * DK + t];
      }
      mbar_arrive(&bars[B_TBL_FULL + tbuf]);
      if (!warp_wait(&bars[B_TBL_FULL + tbuf], (uint32_t)(ku >> 1) & 1u, a, abort_flag)) break;
@@ -888,7 +929,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
        if constexpr (DO_STATE) {
 #pragma unroll
          for (int x = 0; x < TN; ++x) S[x] = 0.f;
-         if (MODE == MODE_FWD && w.head) {
+         if (C::FWD && w.head) {
            // (the hand-over tile lands in the state-copy buffer: the last MMA3 must have read it)
            if (gk > 0 && !warp_wait(&bars[B_SP_EMPTY], (uint32_t)(gk - 1) & 1u, a, abort_flag)) { aborted = true; break; }
            // The same tile's CTA of the previous group ran this unit's first chunks and left the
@@ -1072,7 +1113,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
        }
        if (aborted) break;
        if constexpr (DO_STATE) {
-         if (MODE == MODE_FWD && prm.s_out) {
+         if (C::FWD && prm.s_out) {
            // Forward: each thread stores its final-state row straight from registers (no staging,
            // nothing to wait for); a tail piece raises its hand-over flag once every row is visible.
            if (r_ < DK) {
@@ -1101,7 +1142,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
              }
            }
          }
-         if (MODE != MODE_FWD && prm.s_out && r_ < DK) {
+         if (!C::FWD && prm.s_out && r_ < DK) {
            float4* dst = reinterpret_cast<float4*>(prm.s_out + ((long long)srow0 + r_) * DV + col0);
 #pragma unroll
            for (int x = 0; x < TN / 4; ++x) dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
@@ -1213,7 +1254,7 @@ cudaError_t launch_scan(const void* X, const void* Y, const void* Z, const ScanP
       return cudaErrorInvalidValue;
   }
   const long long state_rows = (long long)a.n_seq * a.H * DK;
-  if (MODE == MODE_FWD && p.s_out && !make_state_map(&maps.s, p.s_out, state_rows))
+  if (Cfg<MODE>::FWD && p.s_out && !make_state_map(&maps.s, p.s_out, state_rows))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
@@ -1284,6 +1325,7 @@ cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream) {
       p.epoch = n / FLAG_SETS % 0xFFFFFFFu + 1u;
     }
   }
+  if (a.aug) return launch_scan<MODE_FWDA>(a.q, a.k, a.v, p, stream, max_ctas);
   return launch_scan<MODE_FWD>(a.q, a.k, a.v, p, stream, max_ctas);
 }
 

@@ -24,6 +24,7 @@ struct ChunkArgs {
   const void* dO;          // backward only
   const float* log_lambda;
   const float* h0;         // may be null
+  const float* aug;        // forward only: aug_balance [H, 96] (self-augmentation), or null
   const float* dhT;        // backward only; may be null
   void* o;                 // forward output (or dq in the backward)
   void* dk;                // backward only

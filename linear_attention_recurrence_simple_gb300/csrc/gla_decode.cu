@@ -4,7 +4,9 @@
 // architecture", GLA mixer: S <- lambda_h S + k v^T (rank-1 write of the current key/value,
 // fixed per-head decay), then the readout o = S^T (scale q) queries the updated state.  Section
 // "Optimizing inference on Trainium2": the serving wrapper keeps one fixed page of recurrent state
-// per sequence in a pool, which `slot` indexes here.
+// per sequence in a pool, which `slot` indexes here.  With `aug` (aug_balance, [H, 96]) the
+// output also gains the self-augmentation copy of the value, sigmoid(q . (a_h * k)) v (the
+// paragraph after the readout in the same section; the query enters the gate unscaled).
 //
 // The step is a pure stream over the 72 KB state of each (sequence, head): read once, update,
 // write once.  One CTA of 576 threads owns one state; thread (r, c), r < 12, c < 48, holds
@@ -44,9 +46,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
 decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    const float* __restrict__ log_lambda, float scale, float* __restrict__ state,
                    const int32_t* __restrict__ slot, int pool_rows, T* __restrict__ o, int H,
-                   unsigned* err) {
+                   const float* __restrict__ aug, unsigned* err) {
   __shared__ float s_q[DK];
   __shared__ float s_k[DK];
+  __shared__ float s_gate;
   __shared__ float4 s_part[DEC_RGROUPS][DEC_COLS];
 
   const long long nh = blockIdx.x;  // n * H + h
@@ -92,6 +95,14 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     acc.w = fmaf(qa, x.w, acc.w);
   }
   s_part[r][c] = acc;
+  if (aug && tid < 32) {  // gate = sigmoid(q . (a_h * k)), q unscaled
+    float g = 0.f;
+#pragma unroll
+    for (int d = tid; d < DK; d += 32) g = fmaf(to_f(q[nh * DK + d]) * aug[h * DK + d], s_k[d], g);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) g += __shfl_xor_sync(0xffffffffu, g, off);
+    if (tid == 0) s_gate = 1.f / (1.f + expf(-g));
+  }
   __syncthreads();
   if (tid < DEC_COLS) {
     float4 t = s_part[0][tid];
@@ -103,6 +114,13 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
       t.z += p.z;
       t.w += p.w;
     }
+    if (aug) {
+      const float gate = s_gate;
+      t.x = fmaf(gate, vv.x, t.x);
+      t.y = fmaf(gate, vv.y, t.y);
+      t.z = fmaf(gate, vv.z, t.z);
+      t.w = fmaf(gate, vv.w, t.w);
+    }
     store4(o + nh * DV + 4 * tid, t);
   }
 }
@@ -112,17 +130,17 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
 cudaError_t launch_decode_step(int dtype_f32, const void* q, const void* k, const void* v,
                                const float* log_lambda, float scale, float* state,
                                const int32_t* slot, int pool_rows, void* o, int N, int H,
-                               unsigned* err, cudaStream_t stream) {
+                               const float* aug, unsigned* err, cudaStream_t stream) {
   const long long blocks = (long long)N * H;
   if (blocks == 0) return cudaSuccess;
   if (dtype_f32) {
     decode_step_kernel<float><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
         (const float*)q, (const float*)k, (const float*)v, log_lambda, scale, state, slot,
-        pool_rows, (float*)o, H, err);
+        pool_rows, (float*)o, H, aug, err);
   } else {
     decode_step_kernel<__nv_bfloat16><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
         (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, log_lambda,
-        scale, state, slot, pool_rows, (__nv_bfloat16*)o, H, err);
+        scale, state, slot, pool_rows, (__nv_bfloat16*)o, H, aug, err);
   }
   return cudaGetLastError();
 }

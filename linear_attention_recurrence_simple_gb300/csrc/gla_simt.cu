@@ -85,7 +85,9 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(ChunkArgs a) {
     load_rows(Ks, PK, k, t0, L, a.H, h, DK, 0, DK);
     load_rows(Vs, PT, v, t0, L, a.H, h, DV, col0, FWD_TILE);
     __syncthreads();
-    {  // P[i][j] = scale lambda^(i-j) q_i.k_j for j <= i
+    {  // P[i][j] = scale lambda^(i-j) q_i.k_j for j <= i; with aug_balance the diagonal also
+       // carries the self-augmentation gate sigmoid(q_i . (a_h * k_i)), so that the row's output
+       // gains that multiple of v_i
       const int i = tid / 4;
       for (int m = 0; m < SC / 4; ++m) {
         const int j = (tid % 4) + 4 * m;
@@ -94,6 +96,11 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(ChunkArgs a) {
 #pragma unroll 8
           for (int c = 0; c < DK; ++c) acc = fmaf(Qs[i * PK + c], Ks[j * PK + c], acc);
           acc *= a.scale * pw[i - j];
+          if (a.aug && j == i) {
+            float g = 0.f;
+            for (int c = 0; c < DK; ++c) g = fmaf(Qs[i * PK + c] * a.aug[h * DK + c], Ks[i * PK + c], g);
+            acc += 1.f / (1.f + expf(-g));
+          }
         }
         Ps[i * PT + j] = acc;
       }

@@ -97,6 +97,26 @@ def test_fwd_argument_errors(lib):
     assert _fwd(lib, n=0, q=None, k=None, v=None, o=None, ll=None) == OK
 
 
+def test_aug_argument_errors(lib):
+    P = ctypes.c_void_p
+
+    def fwd_aug(aug=A, dk=96, n=2, o=A):
+        return lib.gla_chunk_fwd_aug(P(A), P(A), P(A), P(A), None, 0.1, P(aug), P(o), None, None, n, 8,
+                                     2, dk, 192, 0, None, 0, None)
+
+    def dec_aug(aug=A, N=4):
+        return lib.gla_decode_step_aug(P(A), P(A), P(A), P(A), 0.1, P(aug), P(A), None, 4, P(A), N, 2,
+                                       96, 192, 0, None)
+    assert fwd_aug(aug=None) == NULL
+    assert fwd_aug(aug=MIS) == ALIGN
+    assert fwd_aug(dk=64) == UNSUP
+    assert fwd_aug(o=None) == NULL
+    assert fwd_aug(n=0) == OK
+    assert dec_aug(aug=None) == NULL
+    assert dec_aug(aug=MIS) == ALIGN
+    assert dec_aug(N=0) == OK
+
+
 def test_bwd_argument_errors(lib):
     P = ctypes.c_void_p
 
