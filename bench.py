@@ -270,6 +270,29 @@ def bench_fwd(torch, gla, wl, dist, args, peaks):
     return res
 
 
+def bench_fwd_aug(torch, gla, wl, dist, args, peaks):
+    """The forward with the self-augmentation step (gla_chunk_fwd_aug) on the same workload;
+    aug_balance ~ N(0, 10^2) spreads the gate over the sigmoid (q, k ~ N(0, 1/96))."""
+    import glasynth as gs
+    w = wl.layer()
+    g = w.device_inputs()
+    aug = torch.from_numpy(gs.normal(11, 9, (H, DK), 10.0)).cuda()
+    o = torch.empty_like(g["v"])
+    hT = torch.empty((w.n_seq, H, DK, DV), dtype=torch.float32, device="cuda")
+    fn = lambda: gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], w.scale, o=o, hT=hT,
+                                   aug=aug)
+    region, per_call = timed(torch, dist, fn, args.steps, args.warmup)
+    region, per_call = dist.max(region), dist.max(per_call)
+    tokens = w.tokens
+    res = {"workload": w.name + " + self-augmentation", "tokens": tokens, "ms_per_step": region,
+           "value": tokens * dist.world / (region / 1e3), "unit": "tokens/s",
+           "roofline": roofline(fwd_bytes(tokens, w.n_seq, False) + H * DK * 4,
+                                fwd_flops(tokens) + tokens * H * 2 * (DK + DV), region / 1e3, peaks),
+           "kernel_ms": per_call, "launches_per_step": 1}
+    del g, o, hT, aug
+    return res
+
+
 def bench_varlen(torch, gla, wl, dist, args, peaks):
     w = wl.varlen()
     g = w.device_inputs()
@@ -307,10 +330,13 @@ def bench_bwd(torch, gla, wl, dist, args, peaks):
     return res
 
 
-def bench_decode(torch, gla, wl, dist, args, peaks):
+def bench_decode(torch, gla, wl, dist, args, peaks, aug=False):
+    """``aug``: the step with the self-augmentation copy of v (gla_decode_step_aug), 16 steps."""
+    import glasynth as gs
     w = wl.DecodeWorkload(seqs=args.decode_seqs, layers=args.decode_layers)
     state = w.device_state()
     ll = torch.from_numpy(w.log_lambda).cuda()
+    a = torch.from_numpy(gs.normal(12, 9, (H, DK), 10.0)).cuda() if aug else None
     steps = [w.device_step(s) for s in range(min(w.steps, 4))]  # 4 distinct token sets, cycled
     o = torch.empty((w.N, H, DV), dtype=torch.bfloat16, device="cuda")
     it = [0]
@@ -318,21 +344,22 @@ def bench_decode(torch, gla, wl, dist, args, peaks):
     def fn():
         b = steps[it[0] % len(steps)]
         it[0] += 1
-        gla.gla_decode_step(b["q"], b["k"], b["v"], ll, state, w.scale, o=o)
-    n = w.steps
+        gla.gla_decode_step(b["q"], b["k"], b["v"], ll, state, w.scale, o=o, aug=a)
+    n = 16 if aug else w.steps
     region, per_call = timed(torch, dist, fn, n, max(args.warmup, 3))
     region, per_call = dist.max(region), dist.max(per_call)
     state_bytes = 2 * w.N * H * DK * DV * 4
     io_bytes = w.N * H * (2 * DK * 2 + 2 * DV * 2)
-    res = {"workload": f"decode {w.seqs} seqs x {w.layers} layers H=16 fp32 state bf16 io", "steps": n,
+    res = {"workload": f"decode {w.seqs} seqs x {w.layers} layers H=16 fp32 state bf16 io"
+                       + (" + self-augmentation" if aug else ""), "steps": n,
            "ms_per_step": region,
            "value": w.seqs * dist.world / (region / 1e3), "unit": "tokens/s",
            "token": "one new token per sequence through all 24 layers",
            "roofline": roofline(state_bytes, 2 * 2 * w.N * H * DK * DV, region / 1e3, peaks),
            "io_bytes_outside_roofline": io_bytes, "launches_per_step": 1}
     res["roofline"]["algorithmic_bytes_note"] = "fp32 state read + write per step"
-    res["roofline"]["traffic"] = profiled_traffic("decode", w.N * H)
-    del state, steps, o
+    res["roofline"]["traffic"] = None if aug else profiled_traffic("decode", w.N * H)
+    del state, steps, o, a
     return res
 
 
@@ -411,7 +438,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--rows", default="fwd,bwd,varlen,decode")
+    ap.add_argument("--rows", default="fwd,bwd,varlen,decode,fwd_aug,decode_aug")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-seqs", type=int, default=1280,
                     help="sequences in the decode pool (1280 = the measured workload)")
@@ -442,6 +469,10 @@ def main():
             out["bwd"] = bench_bwd(torch, gla, wl, dist, args, peaks)
         if "decode" in rows:
             out["decode"] = bench_decode(torch, gla, wl, dist, args, peaks)
+        if "fwd_aug" in rows:
+            out["fwd_aug"] = bench_fwd_aug(torch, gla, wl, dist, args, peaks)
+        if "decode_aug" in rows:
+            out["decode_aug"] = bench_decode(torch, gla, wl, dist, args, peaks, aug=True)
     err = gla.gla_get_device_error()
     clocks = sampler.summary()
     cpu = None

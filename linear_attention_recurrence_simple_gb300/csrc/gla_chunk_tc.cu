@@ -134,7 +134,8 @@ struct Smem {
   static constexpr uint32_t OFF_OST = OFF_SP + SZ_SP;
   static constexpr uint32_t OFF_PW = OFF_OST + (Cfg<MODE>::NARROW ? 4u * RED_WARP_BYTES : SZ_TILE64);
   // two decay tables (per unit parity), then (self-augmentation) two copies of the head's aug_balance
-  static constexpr uint32_t OFF_AUG = OFF_PW + 2 * PW_FLOATS * 4 + 8;
+  static constexpr uint32_t OFF_AUG = Cfg<MODE>::AUG ? (OFF_PW + 2 * PW_FLOATS * 4 + 8 + 15) / 16 * 16
+                                                      : OFF_PW + 2 * PW_FLOATS * 4 + 8;
   static constexpr uint32_t OFF_BAR = OFF_AUG + (Cfg<MODE>::AUG ? 2 * DK * 4 : 0);
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t OFF_ITEMS = OFF_MISC + 16;  // the CTA's work list (see the kernel)
@@ -727,26 +728,28 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       if constexpr (C::AUG) {
         if (!warp_wait(&bars[B_FULL + (gk & 1)], (uint32_t)(gk >> 1) & 1u, a, abort_flag)) { stop = true; break; }
         const uint32_t st = sbase + (uint32_t)(gk & 1) * C::SZ_STAGE;
-        const float* av = reinterpret_cast<const float*>(sm + SMM::OFF_AUG) + tbuf * DK;
-        float g = 0.f;
+        const uint32_t avs = sbase + SMM::OFF_AUG + (uint32_t)tbuf * DK * 4u;
         // q: columns 0..63 in a 128B-swizzled panel, 64..95 in a 64B-swizzled one; k: two
-        // 128B-swizzled panels.  16-byte piece p of a row holds columns 8p .. 8p + 7.
-#pragma unroll 1
+        // 128B-swizzled panels.  16-byte piece p of a row holds columns 8p .. 8p + 7.  The sum
+        // runs in four independent parts.
+        float gp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
         for (int p = 0; p < 12; ++p) {
-          const uint32_t qa = p < 8 ? st + C::ST_X + (uint32_t)i * 128u + ((uint32_t)(p ^ (i & 7)) << 4)
-                                    : st + C::ST_X1 + (uint32_t)i * 64u + ((uint32_t)((p - 8) ^ ((i >> 1) & 3)) << 4);
-          const uint32_t ka = st + C::ST_Y + (uint32_t)(p >> 3) * 16384u + (uint32_t)i * 128u +
-                              ((uint32_t)((p & 7) ^ (i & 7)) << 4);
-          const uint4 qv = ld_shared_v4(qa), kv = ld_shared_v4(ka);
+          const uint4 qv = ld_shared_v4(p < 8 ? st + C::ST_X + (uint32_t)i * 128u + ((uint32_t)(p ^ (i & 7)) << 4)
+                                              : st + C::ST_X1 + (uint32_t)i * 64u + ((uint32_t)((p - 8) ^ ((i >> 1) & 3)) << 4));
+          const uint4 kv = ld_shared_v4(st + C::ST_Y + (uint32_t)(p >> 3) * 16384u + (uint32_t)i * 128u +
+                                        ((uint32_t)((p & 7) ^ (i & 7)) << 4));
+          const uint4 a0 = ld_shared_v4(avs + (uint32_t)p * 32u), a1 = ld_shared_v4(avs + (uint32_t)p * 32u + 16u);
           const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+          const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 qf = bf2_to_f2(qw[e]), kf = bf2_to_f2(kw[e]);
-            g = fmaf(qf.x * av[8 * p + 2 * e], kf.x, g);
-            g = fmaf(qf.y * av[8 * p + 2 * e + 1], kf.y, g);
+            gp[e] = fmaf(qf.x * __uint_as_float(aw[2 * e]), kf.x, gp[e]);
+            gp[e] = fmaf(qf.y * __uint_as_float(aw[2 * e + 1]), kf.y, gp[e]);
           }
         }
-        sig = 1.f / (1.f + expf(-g));
+        sig = 1.f / (1.f + expf(-((gp[0] + gp[1]) + (gp[2] + gp[3]))));
       }
       if (!warp_wait(&bars[B_A_FULL], pc, a, abort_flag)) { stop = true; break; }
       if (!warp_wait(&bars[B_P_EMPTY], pc ^ 1u, a, abort_flag)) { stop = true; break; }
