@@ -45,9 +45,10 @@ def _bind(path):
     lib.oracle_decode_step.argtypes = [P, P, P, P, D, P, P, I, I, I, I, I]
     lib.oracle_bwd.argtypes = [P, P, P, P, P, D, P, P, P, I, I, I, I, P, P, P, P, I]
     lib.oracle_self_aug.argtypes = [P, P, P, P, ctypes.c_longlong, I, I, I, P]
+    lib.oracle_head_norm_gate.argtypes = [P, P, P, P, I, D, ctypes.c_longlong, I, I, P]
     lib.oracle_hardware_threads.argtypes = []
     for f in (lib.oracle_fwd, lib.oracle_fwd_chunked, lib.oracle_decode_step, lib.oracle_bwd,
-              lib.oracle_self_aug, lib.oracle_hardware_threads):
+              lib.oracle_self_aug, lib.oracle_head_norm_gate, lib.oracle_hardware_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -154,6 +155,22 @@ def self_aug(q, k, v, aug, _lib_override=None):
     return out
 
 
+def head_norm_gate(o, g, weight, tier, eps, _lib_override=None):
+    """Per-tier Head RMSNorm of each head's output row and the SiLU(g) gate, fp64
+    ``[rows, H, dv]``.  o, g ``[rows, H, dv]``; weight ``[n_tiers, dv]``; tier ``[H]`` int."""
+    o, g, w = _f32(o), _f32(g), _f32(weight)
+    tr = np.ascontiguousarray(tier, np.int32)
+    if o.ndim != 3 or g.shape != o.shape or w.ndim != 2 or w.shape[1] != o.shape[2] or tr.shape != (o.shape[1],):
+        raise ValueError("expected o, g [rows, H, dv], weight [n_tiers, dv], tier [H]")
+    rows, H, dv = o.shape
+    y = np.zeros((rows, H, dv), np.float64)
+    rc = (_lib_override or _load()).oracle_head_norm_gate(_ptr(o), _ptr(g), _ptr(w), _ptr(tr), w.shape[0],
+                                                          float(eps), rows, H, dv, _ptr(y))
+    if rc:
+        raise ValueError(f"oracle_head_norm_gate rejected its arguments ({rc})")
+    return y
+
+
 def bwd(q, k, v, log_lambda, scale, dO, h0=None, dhT=None, cu_seqlens=None, nthreads=0,
         _lib_override=None):
     """Adjoint of :func:`fwd`.  Returns ``(dq, dk, dv, dh0)`` in fp64."""
@@ -197,6 +214,9 @@ class Variant:
 
     def self_aug(self, *a, **kw):
         return self_aug(*a, _lib_override=self._lib, **kw)
+
+    def head_norm_gate(self, *a, **kw):
+        return head_norm_gate(*a, _lib_override=self._lib, **kw)
 
 
 def source_path() -> str:

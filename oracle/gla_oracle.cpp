@@ -210,6 +210,37 @@ int oracle_self_aug(const float* q, const float* k, const float* v, const float*
   return 0;
 }
 
+// Per-tier Head RMSNorm and SiLU output gate (same section, the end of the paragraph after the
+// readout, and the architecture table's "Head RMSNorm (per tier)"): each head's output row is
+// RMS-normalised, scaled by the gain of the head's decay tier (the heads of a tier share one
+// Head RMSNorm), and gated element-wise by SiLU(g_t), the gate stream of the QKVG projection:
+//     y_{t,h} = o_{t,h} / sqrt(mean_c o_{t,h,c}^2 + eps) (*) w_{tier(h)} (*) SiLU(g_{t,h}),
+//     SiLU(x) = x * sigmoid(x).
+// Readings: the RMS runs over one head's d_v channels; the tier of each head and eps are inputs
+// (the pages state neither).  o, g, y [rows, H, dv]; w [n_tiers, dv]; tier [H].
+int oracle_head_norm_gate(const float* o, const float* g, const float* w, const int32_t* tier,
+                          int n_tiers, double eps, long long rows, int H, int dv, double* y) {
+  if (rows < 0 || H <= 0 || dv <= 0 || n_tiers <= 0 || eps < 0) return -1;
+  for (int h = 0; h < H; ++h)
+    if (tier[h] < 0 || tier[h] >= n_tiers) return -1;
+  for (long long t = 0; t < rows; ++t)
+    for (int h = 0; h < H; ++h) {
+      const float* ot = o + ((size_t)t * H + h) * dv;
+      const float* gt = g + ((size_t)t * H + h) * dv;
+      const float* wt = w + (size_t)tier[h] * dv;
+      double ss = 0.0;
+      for (int c = 0; c < dv; ++c) ss += (double)ot[c] * (double)ot[c];
+      const double inv = 1.0 / std::sqrt(ss / dv + eps);
+      double* yt = y + ((size_t)t * H + h) * dv;
+      for (int c = 0; c < dv; ++c) {
+        const double gc = (double)gt[c];
+        const double silu = gc / (1.0 + std::exp(-gc));
+        yt[c] = (double)ot[c] * inv * (double)wt[c] * silu;
+      }
+    }
+  return 0;
+}
+
 // Backward of oracle_fwd (the adjoint of the recurrence), given dO = dL/do and dhT = dL/dhT.
 // With G_t = dL/dS_t (all later uses included) and R_t = lambda * G_{t+1} (R_T = dhT):
 //   G_t  = R_t + scale * q_t dO_t^T

@@ -62,6 +62,14 @@ MUTANTS = [
      "for (int b = 0; b < dv; ++b) out[b] = (double)vt[b];", 0),
     ("aug: balance of the wrong head", "const float* ah = aug + (size_t)h * dk;",
      "const float* ah = aug + (size_t)(H - 1 - h) * dk;", 0),
+    ("norm: mean square without the division by d_v", "const double inv = 1.0 / std::sqrt(ss / dv + eps);",
+     "const double inv = 1.0 / std::sqrt(ss + eps);", 0),
+    ("norm: eps dropped", "const double inv = 1.0 / std::sqrt(ss / dv + eps);",
+     "const double inv = 1.0 / std::sqrt(ss / dv);", 0),
+    ("norm: sigmoid instead of SiLU", "const double silu = gc / (1.0 + std::exp(-gc));",
+     "const double silu = 1.0 / (1.0 + std::exp(-gc));", 0),
+    ("norm: gain of tier 0 for every head", "const float* wt = w + (size_t)tier[h] * dv;",
+     "const float* wt = w;", 0),
     ("bwd: forward state missing its decay",
      "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];",
      "S[(size_t)a * dv + b] = S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];", 2),
@@ -81,6 +89,10 @@ PIN_TESTS = [
     pins.test_self_aug_opposite_balances_sum_to_the_value,
     pins.test_self_aug_single_channel_saturates_by_sign_of_q_times_k,
     pins.test_self_aug_gate_against_exact_value,
+    pins.test_norm_gate_unit_gain_and_gate_give_unit_rms,
+    pins.test_norm_gate_is_scale_invariant_in_o,
+    pins.test_norm_gate_zero_gate_is_zero_and_tier_gain_scales,
+    pins.test_norm_gate_worked_example,
 ]
 
 

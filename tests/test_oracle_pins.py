@@ -354,3 +354,63 @@ def test_self_aug_gate_against_exact_value(oracle_mod):
     add = oracle_mod.self_aug(q, k, v, np.array([[1.0, 0.0]], np.float32))
     g = 1.0 / (1.0 + np.exp(-1.0))
     assert np.allclose(add, g * np.asarray(v, np.float64), rtol=1e-15, atol=0)
+
+
+# --- per-tier Head RMSNorm and SiLU gate ----------------------------------------------------
+# y = o / sqrt(mean(o^2) + eps) * w_tier(h) * SiLU(g) ("i14 and the Laplace 3B architecture":
+# the per-head outputs pass through a Head RMSNorm per decay tier and are gated by SiLU(g_t)).
+
+def _silu_one():
+    """The gate value x with x * sigmoid(x) = 1, by bisection (SiLU is increasing on x > 0)."""
+    lo, hi = 0.0, 4.0
+    for _ in range(200):
+        mid = 0.5 * (lo + hi)
+        if mid / (1.0 + np.exp(-mid)) < 1.0:
+            lo = mid
+        else:
+            hi = mid
+    return 0.5 * (lo + hi)
+
+
+def _norm_case(seed, rows=6, H=4, dv=8):
+    o = _rand(seed, 31, (rows, H, dv))
+    g = _rand(seed, 32, (rows, H, dv))
+    w = _rand(seed, 33, (2, dv), 0.5) + 1.0
+    tier = np.array([0, 0, 1, 1][:H], np.int32)
+    return o, g, w, tier
+
+
+def test_norm_gate_unit_gain_and_gate_give_unit_rms(oracle_mod):
+    # w = 1 and SiLU(g) = 1 everywhere, eps = 0: every output row has RMS exactly 1
+    o, _, _, tier = _norm_case(41)
+    g = np.full(o.shape, _silu_one(), np.float32)
+    y = oracle_mod.head_norm_gate(o, g, np.ones((2, o.shape[2]), np.float32), tier, 0.0)
+    assert np.allclose(np.sqrt(np.mean(y ** 2, axis=2)), 1.0, rtol=0, atol=1e-6)
+
+
+def test_norm_gate_is_scale_invariant_in_o(oracle_mod):
+    o, g, w, tier = _norm_case(42)
+    y1 = oracle_mod.head_norm_gate(o, g, w, tier, 0.0)
+    y2 = oracle_mod.head_norm_gate(np.float32(4.0) * o, g, w, tier, 0.0)
+    assert np.allclose(y1, y2, rtol=1e-12, atol=0)
+
+
+def test_norm_gate_zero_gate_is_zero_and_tier_gain_scales(oracle_mod):
+    o, g, w, tier = _norm_case(43)
+    assert np.array_equal(oracle_mod.head_norm_gate(o, np.zeros_like(g), w, tier, 1e-6), np.zeros(o.shape))
+    # gains c_0 (tier 0) and c_1 (tier 1): the heads of each tier scale by their tier's gain only
+    base = oracle_mod.head_norm_gate(o, g, np.ones_like(w), tier, 1e-6)
+    y = oracle_mod.head_norm_gate(o, g, np.stack([np.full(w.shape[1], 2.0), np.full(w.shape[1], -3.0)]).astype(np.float32),
+                                  tier, 1e-6)
+    assert np.allclose(y[:, tier == 0], 2.0 * base[:, tier == 0], rtol=1e-14, atol=0)
+    assert np.allclose(y[:, tier == 1], -3.0 * base[:, tier == 1], rtol=1e-14, atol=0)
+
+
+def test_norm_gate_worked_example(oracle_mod):
+    # o = (3, 4): mean square 12.5, eps = 0.5 -> rms 3.6055...; g = (0, 1): SiLU = (0, 1/(1+e^-1))
+    o = np.array([[[3.0, 4.0]]], np.float32)
+    g = np.array([[[0.0, 1.0]]], np.float32)
+    w = np.array([[2.0, 0.5]], np.float32)
+    y = oracle_mod.head_norm_gate(o, g, w, np.array([0], np.int32), 0.5)
+    want = np.array([0.0, 4.0 / np.sqrt(13.0) * 0.5 / (1.0 + np.exp(-1.0))])
+    assert np.allclose(y[0, 0], want, rtol=1e-15, atol=0)
