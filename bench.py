@@ -293,6 +293,29 @@ def bench_fwd_aug(torch, gla, wl, dist, args, peaks):
     return res
 
 
+def bench_norm_gate(torch, gla, wl, dist, args, peaks):
+    """Per-tier Head RMSNorm + SiLU gate (gla_head_norm_gate) on the forward workload's output
+    shape: o and g [8 x 2048, 16, 192] bf16 read once, y written once; four tiers of four heads."""
+    import glasynth as gs
+    w = wl.layer()
+    rows = w.tokens
+    o = torch.from_numpy(gs.normal(13, 1, (rows, H, DV))).cuda().to(torch.bfloat16)
+    g = torch.from_numpy(gs.normal(13, 2, (rows, H, DV), 2.0)).cuda().to(torch.bfloat16)
+    wt = (1.0 + torch.from_numpy(gs.normal(13, 3, (4, DV), 0.3))).cuda()
+    tier = (torch.arange(H, dtype=torch.int32) // 4).cuda()
+    y = torch.empty_like(o)
+    fn = lambda: gla.gla_head_norm_gate(o, g, wt, tier, y=y)
+    region, per_call = timed(torch, dist, fn, args.steps, args.warmup)
+    region, per_call = dist.max(region), dist.max(per_call)
+    byts = 3 * rows * H * DV * 2 + 4 * DV * 4 + H * 4
+    res = {"workload": "head RMSNorm + SiLU gate, 16,384 rows x 16 heads x 192 bf16, 4 tiers",
+           "tokens": rows, "ms_per_step": region, "value": rows * dist.world / (region / 1e3),
+           "unit": "tokens/s", "roofline": roofline(byts, rows * H * DV * 8, region / 1e3, peaks),
+           "kernel_ms": per_call, "launches_per_step": 1}
+    del o, g, wt, tier, y
+    return res
+
+
 def bench_varlen(torch, gla, wl, dist, args, peaks):
     w = wl.varlen()
     g = w.device_inputs()
@@ -438,7 +461,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--rows", default="fwd,bwd,varlen,decode,fwd_aug,decode_aug")
+    ap.add_argument("--rows", default="fwd,bwd,varlen,decode,fwd_aug,norm_gate,decode_aug")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-seqs", type=int, default=1280,
                     help="sequences in the decode pool (1280 = the measured workload)")
@@ -471,6 +494,8 @@ def main():
             out["decode"] = bench_decode(torch, gla, wl, dist, args, peaks)
         if "fwd_aug" in rows:
             out["fwd_aug"] = bench_fwd_aug(torch, gla, wl, dist, args, peaks)
+        if "norm_gate" in rows:
+            out["norm_gate"] = bench_norm_gate(torch, gla, wl, dist, args, peaks)
         if "decode_aug" in rows:
             out["decode_aug"] = bench_decode(torch, gla, wl, dist, args, peaks, aug=True)
     err = gla.gla_get_device_error()

@@ -154,6 +154,22 @@ int gla_decode_step_aug(const void* q, const void* k, const void* v, const float
                         int pool_rows, void* o, int N, int H, int dk, int dv, int dtype,
                         gla_stream_t stream);
 
+/* Per-tier Head RMSNorm and SiLU output gate ("Beyond the KV cache", section "i14 and the
+ * Laplace 3B architecture": the per-head outputs pass through a Head RMSNorm within each decay
+ * tier, then are gated by SiLU(g_t)).  For every row t and head h:
+ *     y[t,h,:] = o[t,h,:] / sqrt(mean_c o[t,h,c]^2 + eps) * weight[tier[h],:] * SiLU(g[t,h,:]),
+ * SiLU(x) = x sigmoid(x); the RMS runs over the head's 192 channels.
+ *   o, g, y      [rows, H, 192], dtype `dtype` (o is a chunked-forward or decode output, g the
+ *                gate stream); y may not alias o or g.
+ *   weight       [n_tiers, 192] fp32 device, the gain of each tier's norm.
+ *   tier         [H] int32 device: the tier of each head; a value outside [0, n_tiers) leaves
+ *                that head's rows untouched and records GLA_ERR_SHAPE in the device error word.
+ *   eps          >= 0, added to the mean square (not stated on the pages).
+ * n_tiers <= 32 and H <= 4096 (else GLA_ERR_UNSUPPORTED).  Pointers 16-byte aligned (tier 4-byte).  Returns GLA_OK once the work is queued on `stream`. */
+int gla_head_norm_gate(const void* o, const void* g, const float* weight, const int32_t* tier,
+                       int n_tiers, float eps, void* y, long long rows, int H, int dv, int dtype,
+                       gla_stream_t stream);
+
 /* The forward without any device allocation (no counterpart in the paper).  For callers that
  * cannot allocate device memory per call, such as a serving engine whose memory is all handed to
  * its own pool at start-up: same arguments and results as gla_chunk_fwd, minus the workspace.

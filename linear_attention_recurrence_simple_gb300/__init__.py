@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "GlaError", "load_library", "library_path", "gla_workspace_bytes", "gla_bwd_workspace_bytes",
     "gla_chunk_fwd",
-    "gla_chunk_bwd", "gla_decode_step", "gla_chunk_fwd_noalloc", "gla_get_device_error",
+    "gla_chunk_bwd", "gla_decode_step", "gla_chunk_fwd_noalloc", "gla_head_norm_gate", "gla_get_device_error",
     "gla_set_wait_limit_ns",
     "gla_status_string", "DK", "DV", "CHUNK", "EXPORTS",
 ]
@@ -27,7 +27,7 @@ __all__ = [
 DK, DV, CHUNK = 96, 192, 128
 GLA_BF16, GLA_F32 = 0, 1
 EXPORTS = ("gla_workspace_bytes", "gla_bwd_workspace_bytes", "gla_chunk_fwd", "gla_chunk_bwd",
-           "gla_decode_step", "gla_chunk_fwd_aug", "gla_decode_step_aug",
+           "gla_decode_step", "gla_chunk_fwd_aug", "gla_decode_step_aug", "gla_head_norm_gate",
            "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
            "gla_status_string")
 NOALLOC_MAX_SEQS = 16384
@@ -79,6 +79,8 @@ def load_library(build: bool = True):
         lib.gla_chunk_fwd_aug.restype = I
         lib.gla_decode_step_aug.argtypes = [P, P, P, P, F, P, P, P, I, P, I, I, I, I, I, P]
         lib.gla_decode_step_aug.restype = I
+        lib.gla_head_norm_gate.argtypes = [P, P, P, P, I, F, P, ctypes.c_longlong, I, I, I, P]
+        lib.gla_head_norm_gate.restype = I
         lib.gla_get_device_error.argtypes = [P]
         lib.gla_get_device_error.restype = I
         lib.gla_set_wait_limit_ns.argtypes = [U]
@@ -323,6 +325,34 @@ def gla_decode_step(q, k, v, log_lambda, state, scale=None, slot=None, o=None, a
                                          dt, _stream(dev))
     _check(rc, "gla_decode_step" if aug is None else "gla_decode_step_aug")
     return o
+
+
+def gla_head_norm_gate(o, g, weight, tier, eps=1e-6, y=None):
+    """Per-tier Head RMSNorm of each head's output row and the SiLU(g) gate.
+
+    o, g ``[..., H, 192]`` (same dtype, bf16 or fp32); weight fp32 ``[n_tiers, 192]``; tier int32
+    ``[H]``.  Returns ``y`` like ``o``."""
+    lib = load_library()
+    dev = o.device
+    dt = _dtype_code(o)
+    _need(o, "o", o.dtype, dev)
+    _need(g, "g", o.dtype, dev)
+    _need(weight, "weight", torch.float32, dev)
+    _need(tier, "tier", torch.int32, dev)
+    if o.dim() < 2 or o.shape[-1] != DV or g.shape != o.shape:
+        raise ValueError("expected o, g [..., H, 192] of one shape")
+    H = o.shape[-2]
+    rows = o.numel() // (H * DV)
+    if weight.dim() != 2 or weight.shape[1] != DV or tier.shape != (H,):
+        raise ValueError("weight must be [n_tiers, 192] and tier [H]")
+    if y is None:
+        y = torch.empty_like(o)
+    _need(y, "y", o.dtype, dev)
+    with torch.cuda.device(dev):
+        rc = lib.gla_head_norm_gate(_ptr(o), _ptr(g), _ptr(weight), _ptr(tier), weight.shape[0], float(eps),
+                                    _ptr(y), rows, H, DV, dt, _stream(dev))
+    _check(rc, "gla_head_norm_gate")
+    return y
 
 
 def gla_get_device_error(device=None) -> int:

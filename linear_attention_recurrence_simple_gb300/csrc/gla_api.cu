@@ -16,6 +16,9 @@ cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_tc_bwd(const ChunkArgs& a, float* acc_q, float* acc_k, cudaStream_t stream);
 size_t tc_bwd_acc_bytes(long long T_total, int H);
 cudaError_t tc_clear_handover(cudaStream_t stream);
+cudaError_t launch_head_norm_gate(int dtype_f32, const void* o, const void* g, const float* w,
+                                  const int32_t* tier, int n_tiers, float eps, void* y, long long rows,
+                                  int H, unsigned* err, cudaStream_t stream);
 }  // namespace gla
 
 namespace {
@@ -292,6 +295,27 @@ int gla_decode_step_aug(const void* q, const void* k, const void* v, const float
   if (!aug) return GLA_ERR_NULL;
   return decode_step(q, k, v, log_lambda, scale, aug, state, slot, pool_rows, o, N, H, dk, dv, dtype,
                      stream);
+}
+
+int gla_head_norm_gate(const void* o, const void* g, const float* weight, const int32_t* tier,
+                       int n_tiers, float eps, void* y, long long rows, int H, int dv, int dtype,
+                       gla_stream_t stream) {
+  if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_DTYPE;
+  if (dv != GLA_DV) return GLA_ERR_UNSUPPORTED;
+  if (rows < 0 || H < 1 || n_tiers < 1 || !(eps >= 0.f) || rows > (1ll << 40)) return GLA_ERR_SHAPE;
+  if (n_tiers > 32 || H > 4096) return GLA_ERR_UNSUPPORTED;  // the kernel's shared-memory copies
+  if (rows == 0) return GLA_OK;
+  if (!o || !g || !weight || !tier || !y) return GLA_ERR_NULL;
+  for (const void* p : {o, g, (const void*)weight, (const void*)y})
+    if (!aligned16(p)) return GLA_ERR_ALIGN;
+  if ((uintptr_t)tier & 3u) return GLA_ERR_ALIGN;
+  int dev;
+  unsigned* err;
+  unsigned long long wait_ns;
+  int rc = device_state(&dev, &err, &wait_ns);
+  if (rc) return rc;
+  return to_status(gla::launch_head_norm_gate(dtype == GLA_F32, o, g, weight, tier, n_tiers, eps, y, rows,
+                                              H, err, (cudaStream_t)stream));
 }
 
 int gla_get_device_error(gla_stream_t stream) {

@@ -117,6 +117,28 @@ def test_aug_argument_errors(lib):
     assert dec_aug(N=0) == OK
 
 
+def test_head_norm_gate_argument_errors(lib):
+    P = ctypes.c_void_p
+
+    def ng(o=A, g=A, w=A, tier=A, nt=2, eps=1e-6, y=A, rows=4, H=2, dv=192, dt=0):
+        return lib.gla_head_norm_gate(P(o), P(g), P(w), P(tier), nt, eps, P(y), rows, H, dv, dt, None)
+    assert ng(dt=5) == DTYPE
+    assert ng(dv=128) == UNSUP
+    assert ng(rows=-1) == SHAPE
+    assert ng(H=0) == SHAPE
+    assert ng(nt=0) == SHAPE
+    assert ng(nt=33) == UNSUP
+    assert ng(H=5000) == UNSUP
+    assert ng(eps=-1.0) == SHAPE
+    assert ng(eps=float("nan")) == SHAPE
+    assert ng(o=None) == NULL
+    assert ng(tier=None) == NULL
+    assert ng(y=MIS) == ALIGN
+    assert ng(w=MIS) == ALIGN
+    assert ng(tier=A + 2) == ALIGN
+    assert ng(rows=0, o=None, y=None) == OK
+
+
 def test_bwd_argument_errors(lib):
     P = ctypes.c_void_p
 
