@@ -46,9 +46,12 @@ def _bind(path):
     lib.oracle_bwd.argtypes = [P, P, P, P, P, D, P, P, P, I, I, I, I, P, P, P, P, I]
     lib.oracle_self_aug.argtypes = [P, P, P, P, ctypes.c_longlong, I, I, I, P]
     lib.oracle_head_norm_gate.argtypes = [P, P, P, P, I, D, ctypes.c_longlong, I, I, P]
+    lib.oracle_decode_step_bf16_state.argtypes = [P, P, P, P, D, P, P, I, I, I, I]
+    lib.oracle_round_to_bf16.argtypes = [P, P, ctypes.c_longlong]
     lib.oracle_hardware_threads.argtypes = []
     for f in (lib.oracle_fwd, lib.oracle_fwd_chunked, lib.oracle_decode_step, lib.oracle_bwd,
-              lib.oracle_self_aug, lib.oracle_head_norm_gate, lib.oracle_hardware_threads):
+              lib.oracle_self_aug, lib.oracle_head_norm_gate, lib.oracle_decode_step_bf16_state,
+              lib.oracle_round_to_bf16, lib.oracle_hardware_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -171,6 +174,31 @@ def head_norm_gate(o, g, weight, tier, eps, _lib_override=None):
     return y
 
 
+def round_to_bf16(x, _lib_override=None):
+    """fp64 values rounded to the nearest bf16 (ties to even), as fp64."""
+    x = np.ascontiguousarray(x, np.float64)
+    y = np.empty_like(x)
+    (_lib_override or _load()).oracle_round_to_bf16(_ptr(x), _ptr(y), x.size)
+    return y
+
+
+def decode_step_bf16_state(q, k, v, log_lambda, scale, state, _lib_override=None):
+    """One decode step with a bf16-stored state: ``state`` (fp64 ``[N, H, dk, dv]`` holding bf16
+    values) is updated in place to the update rounded to bf16; returns ``o`` read out from the
+    update before that rounding."""
+    q, k, v, ll = _f32(q), _f32(k), _f32(v), _f32(log_lambda)
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    if state.dtype != np.float64 or not state.flags.c_contiguous or state.shape != (N, H, dk, dv):
+        raise ValueError("state must be a C-contiguous fp64 [N, H, dk, dv] array")
+    o = np.zeros((N, H, dv), np.float64)
+    rc = (_lib_override or _load()).oracle_decode_step_bf16_state(_ptr(q), _ptr(k), _ptr(v), _ptr(ll), float(scale),
+                                                                  _ptr(state), _ptr(o), N, H, dk, dv)
+    if rc:
+        raise ValueError(f"oracle_decode_step_bf16_state rejected its arguments ({rc})")
+    return o
+
+
 def bwd(q, k, v, log_lambda, scale, dO, h0=None, dhT=None, cu_seqlens=None, nthreads=0,
         _lib_override=None):
     """Adjoint of :func:`fwd`.  Returns ``(dq, dk, dv, dh0)`` in fp64."""
@@ -217,6 +245,12 @@ class Variant:
 
     def head_norm_gate(self, *a, **kw):
         return head_norm_gate(*a, _lib_override=self._lib, **kw)
+
+    def round_to_bf16(self, *a, **kw):
+        return round_to_bf16(*a, _lib_override=self._lib, **kw)
+
+    def decode_step_bf16_state(self, *a, **kw):
+        return decode_step_bf16_state(*a, _lib_override=self._lib, **kw)
 
 
 def source_path() -> str:

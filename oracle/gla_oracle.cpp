@@ -241,6 +241,51 @@ int oracle_head_norm_gate(const float* o, const float* g, const float* w, const 
   return 0;
 }
 
+// A value rounded to the nearest bf16 (8 significant bits, ties to even), fp64 in and out;
+// zeros and non-finite values pass through.  Written from the format's definition.
+double round_to_bf16(double x) {
+  if (x == 0.0 || !std::isfinite(x)) return x;
+  int e;
+  const double m = std::frexp(x, &e);  // x = m 2^e, 0.5 <= |m| < 1
+  const double r = std::nearbyint(std::ldexp(m, 8));  // 8 significant bits; default rounding
+  return std::ldexp(r, e - 8);                         // mode: to nearest, ties to even
+}
+
+// One decode step with the state stored in bf16 (not on the pages: a storage variant that
+// halves the state traffic).  The update and the readout are those of oracle_decode_step,
+// computed from the stored (bf16-valued) state; the readout uses the updated state before it
+// is rounded, and the stored state is the update rounded to bf16.  state holds bf16 values in
+// fp64 and is updated in place; aug may be null (else the self-augmentation term is added).
+int oracle_decode_step_bf16_state(const float* q, const float* k, const float* v, const float* log_lambda,
+                                  double scale, double* state, double* o, int N, int H, int dk, int dv) {
+  if (N < 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;
+  std::vector<double> S((size_t)dk * dv);
+  for (int n = 0; n < N; ++n)
+    for (int h = 0; h < H; ++h) {
+      const double lam = std::exp((double)log_lambda[h]);
+      double* St = state + ((size_t)n * H + h) * dk * dv;
+      const float* kt = k + ((size_t)n * H + h) * dk;
+      const float* vt = v + ((size_t)n * H + h) * dv;
+      const float* qt = q + ((size_t)n * H + h) * dk;
+      for (int a = 0; a < dk; ++a)
+        for (int b = 0; b < dv; ++b)
+          S[(size_t)a * dv + b] = lam * St[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];
+      double* ot = o + ((size_t)n * H + h) * dv;
+      for (int b = 0; b < dv; ++b) {
+        double acc = 0.0;
+        for (int a = 0; a < dk; ++a) acc += S[(size_t)a * dv + b] * (scale * (double)qt[a]);
+        ot[b] = acc;
+      }
+      for (size_t e = 0; e < S.size(); ++e) St[e] = round_to_bf16(S[e]);
+    }
+  return 0;
+}
+
+int oracle_round_to_bf16(const double* x, double* y, long long n) {
+  for (long long i = 0; i < n; ++i) y[i] = round_to_bf16(x[i]);
+  return 0;
+}
+
 // Backward of oracle_fwd (the adjoint of the recurrence), given dO = dL/do and dhT = dL/dhT.
 // With G_t = dL/dS_t (all later uses included) and R_t = lambda * G_{t+1} (R_T = dhT):
 //   G_t  = R_t + scale * q_t dO_t^T

@@ -70,6 +70,12 @@ MUTANTS = [
      "const double silu = 1.0 / (1.0 + std::exp(-gc));", 0),
     ("norm: gain of tier 0 for every head", "const float* wt = w + (size_t)tier[h] * dv;",
      "const float* wt = w;", 0),
+    ("bf16 state: 7 significant bits", "const double r = std::nearbyint(std::ldexp(m, 8));",
+     "const double r = std::nearbyint(std::ldexp(m, 7));", 0),
+    ("bf16 state: truncation instead of rounding", "const double r = std::nearbyint(std::ldexp(m, 8));",
+     "const double r = std::trunc(std::ldexp(m, 8));", 0),
+    ("bf16 state: state stored unrounded", "for (size_t e = 0; e < S.size(); ++e) St[e] = round_to_bf16(S[e]);",
+     "for (size_t e = 0; e < S.size(); ++e) St[e] = S[e];", 0),
     ("bwd: forward state missing its decay",
      "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];",
      "S[(size_t)a * dv + b] = S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];", 2),
@@ -93,6 +99,8 @@ PIN_TESTS = [
     pins.test_norm_gate_is_scale_invariant_in_o,
     pins.test_norm_gate_zero_gate_is_zero_and_tier_gain_scales,
     pins.test_norm_gate_worked_example,
+    pins.test_round_to_bf16_format_facts,
+    pins.test_decode_bf16_state_is_rounded_fp32_step,
 ]
 
 

@@ -414,3 +414,36 @@ def test_norm_gate_worked_example(oracle_mod):
     y = oracle_mod.head_norm_gate(o, g, w, np.array([0], np.int32), 0.5)
     want = np.array([0.0, 4.0 / np.sqrt(13.0) * 0.5 / (1.0 + np.exp(-1.0))])
     assert np.allclose(y[0, 0], want, rtol=1e-15, atol=0)
+
+
+# --- bf16-stored decode state -----------------------------------------------------------------
+# Rounding to bf16 is fixed by the format (8 significant bits, ties to even); the bf16-state step
+# is the fp32-state step followed by that rounding of the stored state.
+
+def test_round_to_bf16_format_facts(oracle_mod):
+    x = np.array([1.0, -3.5, 2.0 ** -40, 1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 1 + 2.0 ** -9,
+                  255.0, 257.0, 0.0, -0.0], np.float64)
+    want = np.array([1.0, -3.5, 2.0 ** -40, 1.0, 1 + 2.0 ** -6, 1.0, 255.0, 256.0, 0.0, 0.0])
+    assert np.array_equal(oracle_mod.round_to_bf16(x), want)
+    r = np.asarray(gs.normal(51, 1, (4096,)), np.float64) * 1e3
+    y = oracle_mod.round_to_bf16(r)
+    assert np.all(np.abs(y - r) <= np.abs(r) * 2.0 ** -8 + 0)   # half an ulp of 8-bit precision
+    assert np.array_equal(oracle_mod.round_to_bf16(y), y)       # idempotent
+    # agrees with the input generator's independent fp32 bit-level rounding on fp32 values
+    r32 = np.asarray(gs.normal(52, 1, (4096,)), np.float32)
+    assert np.array_equal(oracle_mod.round_to_bf16(r32.astype(np.float64)), gs.bf16_round(r32).astype(np.float64))
+
+
+def test_decode_bf16_state_is_rounded_fp32_step(oracle_mod):
+    N, H = 3, 2
+    q = _rand(61, 1, (N, H, 5))
+    k = _rand(61, 2, (N, H, 5))
+    v = _rand(61, 3, (N, H, 7))
+    ll = np.log(np.array([0.9, 0.5], np.float32))
+    s0 = oracle_mod.round_to_bf16(np.asarray(_rand(61, 4, (N, H, 5, 7), 0.5), np.float64))
+    s_full = s0.copy()
+    o_full = oracle_mod.decode_step(q, k, v, ll, 0.3, s_full)
+    s_b = s0.copy()
+    o_b = oracle_mod.decode_step_bf16_state(q, k, v, ll, 0.3, s_b)
+    assert np.allclose(o_b, o_full, rtol=1e-14, atol=1e-15)
+    assert np.array_equal(s_b, oracle_mod.round_to_bf16(s_full))
