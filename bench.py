@@ -353,11 +353,14 @@ def bench_bwd(torch, gla, wl, dist, args, peaks):
     return res
 
 
-def bench_decode(torch, gla, wl, dist, args, peaks, aug=False):
-    """``aug``: the step with the self-augmentation copy of v (gla_decode_step_aug), 16 steps."""
+def bench_decode(torch, gla, wl, dist, args, peaks, aug=False, bf16_state=False):
+    """``aug``: the step with the self-augmentation copy of v (gla_decode_step_aug), 16 steps;
+    ``bf16_state``: the same pool stored in bf16 (gla_decode_step_bf16_state), 16 steps."""
     import glasynth as gs
     w = wl.DecodeWorkload(seqs=args.decode_seqs, layers=args.decode_layers)
     state = w.device_state()
+    if bf16_state:
+        state = state.to(torch.bfloat16)
     ll = torch.from_numpy(w.log_lambda).cuda()
     a = torch.from_numpy(gs.normal(12, 9, (H, DK), 10.0)).cuda() if aug else None
     steps = [w.device_step(s) for s in range(min(w.steps, 4))]  # 4 distinct token sets, cycled
@@ -368,20 +371,21 @@ def bench_decode(torch, gla, wl, dist, args, peaks, aug=False):
         b = steps[it[0] % len(steps)]
         it[0] += 1
         gla.gla_decode_step(b["q"], b["k"], b["v"], ll, state, w.scale, o=o, aug=a)
-    n = 16 if aug else w.steps
+    n = 16 if (aug or bf16_state) else w.steps
     region, per_call = timed(torch, dist, fn, n, max(args.warmup, 3))
     region, per_call = dist.max(region), dist.max(per_call)
-    state_bytes = 2 * w.N * H * DK * DV * 4
+    state_bytes = 2 * w.N * H * DK * DV * (2 if bf16_state else 4)
     io_bytes = w.N * H * (2 * DK * 2 + 2 * DV * 2)
-    res = {"workload": f"decode {w.seqs} seqs x {w.layers} layers H=16 fp32 state bf16 io"
+    res = {"workload": f"decode {w.seqs} seqs x {w.layers} layers H=16 "
+                       + ("bf16" if bf16_state else "fp32") + " state bf16 io"
                        + (" + self-augmentation" if aug else ""), "steps": n,
            "ms_per_step": region,
            "value": w.seqs * dist.world / (region / 1e3), "unit": "tokens/s",
            "token": "one new token per sequence through all 24 layers",
            "roofline": roofline(state_bytes, 2 * 2 * w.N * H * DK * DV, region / 1e3, peaks),
            "io_bytes_outside_roofline": io_bytes, "launches_per_step": 1}
-    res["roofline"]["algorithmic_bytes_note"] = "fp32 state read + write per step"
-    res["roofline"]["traffic"] = None if aug else profiled_traffic("decode", w.N * H)
+    res["roofline"]["algorithmic_bytes_note"] = ("bf16" if bf16_state else "fp32") + " state read + write per step"
+    res["roofline"]["traffic"] = None if (aug or bf16_state) else profiled_traffic("decode", w.N * H)
     del state, steps, o, a
     return res
 
@@ -461,7 +465,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--rows", default="fwd,bwd,varlen,decode,fwd_aug,norm_gate,decode_aug")
+    ap.add_argument("--rows", default="fwd,bwd,varlen,decode,fwd_aug,norm_gate,decode_aug,decode_bf16_state")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-seqs", type=int, default=1280,
                     help="sequences in the decode pool (1280 = the measured workload)")
@@ -498,6 +502,8 @@ def main():
             out["norm_gate"] = bench_norm_gate(torch, gla, wl, dist, args, peaks)
         if "decode_aug" in rows:
             out["decode_aug"] = bench_decode(torch, gla, wl, dist, args, peaks, aug=True)
+        if "decode_bf16_state" in rows:
+            out["decode_bf16_state"] = bench_decode(torch, gla, wl, dist, args, peaks, bf16_state=True)
     err = gla.gla_get_device_error()
     clocks = sampler.summary()
     cpu = None

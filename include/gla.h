@@ -170,6 +170,18 @@ int gla_head_norm_gate(const void* o, const void* g, const float* weight, const 
                        int n_tiers, float eps, void* y, long long rows, int H, int dv, int dtype,
                        gla_stream_t stream);
 
+/* One decode step on a state pool stored in bf16 (no counterpart in the paper: a storage
+ * variant that halves the state stream).  As gla_decode_step (aug NULL) or gla_decode_step_aug
+ * (aug non-NULL), with `state` a [pool_rows, H, 96, 192] bf16 pool: each state is widened to
+ * fp32, updated and read out in fp32 (the readout uses the update before rounding), and written
+ * back rounded to bf16 (to nearest, ties to even).  The rounding error is kept in the state and
+ * carried by later steps (relative 2^-9 per element per step, decayed by lambda), so long decodes
+ * drift from the fp32-state result; the fp32 pool is the reference path. */
+int gla_decode_step_bf16_state(const void* q, const void* k, const void* v, const float* log_lambda,
+                               float scale, const float* aug, void* state, const int32_t* slot,
+                               int pool_rows, void* o, int N, int H, int dk, int dv, int dtype,
+                               gla_stream_t stream);
+
 /* The forward without any device allocation (no counterpart in the paper).  For callers that
  * cannot allocate device memory per call, such as a serving engine whose memory is all handed to
  * its own pool at start-up: same arguments and results as gla_chunk_fwd, minus the workspace.

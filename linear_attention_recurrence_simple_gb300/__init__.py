@@ -28,6 +28,7 @@ DK, DV, CHUNK = 96, 192, 128
 GLA_BF16, GLA_F32 = 0, 1
 EXPORTS = ("gla_workspace_bytes", "gla_bwd_workspace_bytes", "gla_chunk_fwd", "gla_chunk_bwd",
            "gla_decode_step", "gla_chunk_fwd_aug", "gla_decode_step_aug", "gla_head_norm_gate",
+           "gla_decode_step_bf16_state",
            "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
            "gla_status_string")
 NOALLOC_MAX_SEQS = 16384
@@ -80,6 +81,8 @@ def load_library(build: bool = True):
         lib.gla_decode_step_aug.argtypes = [P, P, P, P, F, P, P, P, I, P, I, I, I, I, I, P]
         lib.gla_decode_step_aug.restype = I
         lib.gla_head_norm_gate.argtypes = [P, P, P, P, I, F, P, ctypes.c_longlong, I, I, I, P]
+        lib.gla_decode_step_bf16_state.argtypes = [P, P, P, P, F, P, P, P, I, P, I, I, I, I, I, P]
+        lib.gla_decode_step_bf16_state.restype = I
         lib.gla_head_norm_gate.restype = I
         lib.gla_get_device_error.argtypes = [P]
         lib.gla_get_device_error.restype = I
@@ -290,14 +293,17 @@ def gla_decode_step(q, k, v, log_lambda, state, scale=None, slot=None, o=None, a
 
     q, k ``[N, H, 96]``; v ``[N, H, 192]``; ``slot`` ``[N]`` int32 pool rows or None (row n).
     ``aug`` (fp32 ``[H, 96]``) adds the self-augmentation copy of v (``gla_decode_step_aug``).
-    Returns ``o [N, H, 192]``."""
+    A bf16 ``state`` pool runs ``gla_decode_step_bf16_state`` (the state is rounded to bf16 when
+    it is written back).  Returns ``o [N, H, 192]``."""
     lib = load_library()
     dev = q.device
     dt = _dtype_code(q)
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need(t, name, q.dtype, dev)
     _need(log_lambda, "log_lambda", torch.float32, dev)
-    _need(state, "state", torch.float32, dev)
+    if state.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("state must be float32 or bfloat16")
+    _need(state, "state", state.dtype, dev)
     if q.dim() != 3 or q.shape[2] != DK or k.shape != q.shape or v.shape != (*q.shape[:2], DV):
         raise ValueError("expected q, k [N, H, 96] and v [N, H, 192]")
     N, H = q.shape[:2]
@@ -316,6 +322,12 @@ def gla_decode_step(q, k, v, log_lambda, state, scale=None, slot=None, o=None, a
         if aug.shape != (H, DK):
             raise ValueError("aug must be [H, 96]")
     with torch.cuda.device(dev):
+        if state.dtype == torch.bfloat16:
+            rc = lib.gla_decode_step_bf16_state(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), s, _ptr(aug),
+                                                _ptr(state), _ptr(slot), state.shape[0], _ptr(o), N, H, DK,
+                                                DV, dt, _stream(dev))
+            _check(rc, "gla_decode_step_bf16_state")
+            return o
         if aug is None:
             rc = lib.gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), s, _ptr(state),
                                      _ptr(slot), state.shape[0], _ptr(o), N, H, DK, DV, dt, _stream(dev))

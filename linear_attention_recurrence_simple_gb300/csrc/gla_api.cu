@@ -6,8 +6,8 @@
 #include "gla_common.cuh"
 
 namespace gla {
-cudaError_t launch_decode_step(int dtype_f32, const void* q, const void* k, const void* v,
-                               const float* log_lambda, float scale, float* state,
+cudaError_t launch_decode_step(int dtype_f32, int state_bf16, const void* q, const void* k, const void* v,
+                               const float* log_lambda, float scale, void* state,
                                const int32_t* slot, int pool_rows, void* o, int N, int H,
                                const float* aug, unsigned* err, cudaStream_t stream);
 cudaError_t launch_simt_fwd(const ChunkArgs& a, cudaStream_t stream);
@@ -258,7 +258,7 @@ int gla_chunk_bwd(const void* q, const void* k, const void* v, const float* log_
 }
 
 static int decode_step(const void* q, const void* k, const void* v, const float* log_lambda,
-                       float scale, const float* aug, float* state, const int32_t* slot,
+                       float scale, const float* aug, void* state, int state_bf16, const int32_t* slot,
                        int pool_rows, void* o, int N, int H, int dk, int dv, int dtype,
                        gla_stream_t stream) {
   if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_DTYPE;
@@ -277,14 +277,14 @@ static int decode_step(const void* q, const void* k, const void* v, const float*
   unsigned long long wait_ns;
   int rc = device_state(&dev, &err, &wait_ns);
   if (rc) return rc;
-  return to_status(gla::launch_decode_step(dtype == GLA_F32, q, k, v, log_lambda, scale, state, slot,
-                                           pool_rows, o, N, H, aug, err, (cudaStream_t)stream));
+  return to_status(gla::launch_decode_step(dtype == GLA_F32, state_bf16, q, k, v, log_lambda, scale, state,
+                                           slot, pool_rows, o, N, H, aug, err, (cudaStream_t)stream));
 }
 
 int gla_decode_step(const void* q, const void* k, const void* v, const float* log_lambda,
                     float scale, float* state, const int32_t* slot, int pool_rows, void* o, int N,
                     int H, int dk, int dv, int dtype, gla_stream_t stream) {
-  return decode_step(q, k, v, log_lambda, scale, nullptr, state, slot, pool_rows, o, N, H, dk, dv,
+  return decode_step(q, k, v, log_lambda, scale, nullptr, state, 0, slot, pool_rows, o, N, H, dk, dv,
                      dtype, stream);
 }
 
@@ -293,7 +293,15 @@ int gla_decode_step_aug(const void* q, const void* k, const void* v, const float
                         int pool_rows, void* o, int N, int H, int dk, int dv, int dtype,
                         gla_stream_t stream) {
   if (!aug) return GLA_ERR_NULL;
-  return decode_step(q, k, v, log_lambda, scale, aug, state, slot, pool_rows, o, N, H, dk, dv, dtype,
+  return decode_step(q, k, v, log_lambda, scale, aug, state, 0, slot, pool_rows, o, N, H, dk, dv, dtype,
+                     stream);
+}
+
+int gla_decode_step_bf16_state(const void* q, const void* k, const void* v, const float* log_lambda,
+                               float scale, const float* aug, void* state, const int32_t* slot,
+                               int pool_rows, void* o, int N, int H, int dk, int dv, int dtype,
+                               gla_stream_t stream) {
+  return decode_step(q, k, v, log_lambda, scale, aug, state, 1, slot, pool_rows, o, N, H, dk, dv, dtype,
                      stream);
 }
 

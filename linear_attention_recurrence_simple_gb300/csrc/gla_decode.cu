@@ -7,6 +7,9 @@
 // per sequence in a pool, which `slot` indexes here.  With `aug` (aug_balance, [H, 96]) the
 // output also gains the self-augmentation copy of the value, sigmoid(q . (a_h * k)) v (the
 // paragraph after the readout in the same section; the query enters the gate unscaled).
+// The state may also be stored in bf16 (not on the pages: a storage variant that halves the
+// stream): it is read and widened to fp32, updated and read out in fp32, and rounded to bf16 (to
+// nearest, ties to even) when it is written back.
 //
 // The step is a pure stream over the 72 KB state of each (sequence, head): read once, update,
 // write once.  One CTA of 576 threads owns one state; thread (r, c), r < 12, c < 48, holds
@@ -34,6 +37,23 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
   return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 __device__ __forceinline__ void store4(float* p, float4 x) { *reinterpret_cast<float4*>(p) = x; }
+// State vectors (4 consecutive columns) with the streaming cache hint: fp32 storage as float4,
+// bf16 storage as uint2 (four bf16).
+template <class ST> struct StateVec;
+template <> struct StateVec<float> { using type = float4; };
+template <> struct StateVec<__nv_bfloat16> { using type = uint2; };
+__device__ __forceinline__ float4 load_state(const float4* p) { return __ldcs(p); }
+__device__ __forceinline__ float4 load_state(const uint2* p) {
+  const uint2 u = __ldcs(p);
+  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ void store_state(float4* p, float4 x) { __stcs(p, x); }
+__device__ __forceinline__ void store_state(uint2* p, float4 x) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y), b = __floats2bfloat162_rn(x.z, x.w);
+  __stcs(p, make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b)));
+}
 __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 x) {
   Bf16x4 r;
   r.a = __floats2bfloat162_rn(x.x, x.y);
@@ -41,10 +61,10 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 x) {
   *reinterpret_cast<Bf16x4*>(p) = r;
 }
 
-template <class T>
+template <class T, class ST>
 __global__ void __launch_bounds__(DEC_THREADS, 2)
 decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                   const float* __restrict__ log_lambda, float scale, float* __restrict__ state,
+                   const float* __restrict__ log_lambda, float scale, ST* __restrict__ state,
                    const int32_t* __restrict__ slot, int pool_rows, T* __restrict__ o, int H,
                    const float* __restrict__ aug, unsigned* err) {
   __shared__ float s_q[DK];
@@ -64,11 +84,12 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     if (tid == 0) raise_error(err, ERR_SHAPE);
     return;
   }
-  float4* S = reinterpret_cast<float4*>(state + ((long long)row * H + h) * (DK * DV));
+  using SV = typename StateVec<ST>::type;
+  SV* S = reinterpret_cast<SV*>(state + ((long long)row * H + h) * (DK * DV));
 
   float4 s[DEC_ROWS];
 #pragma unroll
-  for (int i = 0; i < DEC_ROWS; ++i) s[i] = __ldcs(S + (r + DEC_RGROUPS * i) * DEC_COLS + c);
+  for (int i = 0; i < DEC_ROWS; ++i) s[i] = load_state(S + (r + DEC_RGROUPS * i) * DEC_COLS + c);
 
   if (tid < DK) {
     s_q[tid] = scale * to_f(q[nh * DK + tid]);
@@ -88,7 +109,7 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     x.y = fmaf(lam, x.y, ka * vv.y);
     x.z = fmaf(lam, x.z, ka * vv.z);
     x.w = fmaf(lam, x.w, ka * vv.w);
-    __stcs(S + a * DEC_COLS + c, x);
+    store_state(S + a * DEC_COLS + c, x);
     acc.x = fmaf(qa, x.x, acc.x);
     acc.y = fmaf(qa, x.y, acc.y);
     acc.z = fmaf(qa, x.z, acc.z);
@@ -127,20 +148,29 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
 
 }  // namespace
 
-cudaError_t launch_decode_step(int dtype_f32, const void* q, const void* k, const void* v,
-                               const float* log_lambda, float scale, float* state,
+cudaError_t launch_decode_step(int dtype_f32, int state_bf16, const void* q, const void* k, const void* v,
+                               const float* log_lambda, float scale, void* state,
                                const int32_t* slot, int pool_rows, void* o, int N, int H,
                                const float* aug, unsigned* err, cudaStream_t stream) {
   const long long blocks = (long long)N * H;
   if (blocks == 0) return cudaSuccess;
-  if (dtype_f32) {
-    decode_step_kernel<float><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
-        (const float*)q, (const float*)k, (const float*)v, log_lambda, scale, state, slot,
+  using BF = __nv_bfloat16;
+  if (dtype_f32 && !state_bf16) {
+    decode_step_kernel<float, float><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
+        (const float*)q, (const float*)k, (const float*)v, log_lambda, scale, (float*)state, slot,
         pool_rows, (float*)o, H, aug, err);
+  } else if (dtype_f32) {
+    decode_step_kernel<float, BF><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
+        (const float*)q, (const float*)k, (const float*)v, log_lambda, scale, (BF*)state, slot,
+        pool_rows, (float*)o, H, aug, err);
+  } else if (!state_bf16) {
+    decode_step_kernel<BF, float><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
+        (const BF*)q, (const BF*)k, (const BF*)v, log_lambda, scale, (float*)state, slot, pool_rows,
+        (BF*)o, H, aug, err);
   } else {
-    decode_step_kernel<__nv_bfloat16><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
-        (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, log_lambda,
-        scale, state, slot, pool_rows, (__nv_bfloat16*)o, H, aug, err);
+    decode_step_kernel<BF, BF><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
+        (const BF*)q, (const BF*)k, (const BF*)v, log_lambda, scale, (BF*)state, slot, pool_rows,
+        (BF*)o, H, aug, err);
   }
   return cudaGetLastError();
 }

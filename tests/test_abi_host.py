@@ -139,6 +139,20 @@ def test_head_norm_gate_argument_errors(lib):
     assert ng(rows=0, o=None, y=None) == OK
 
 
+def test_decode_bf16_state_argument_errors(lib):
+    P = ctypes.c_void_p
+
+    def dec(state=A, N=4, dk=96, dt=0, aug=None):
+        return lib.gla_decode_step_bf16_state(P(A), P(A), P(A), P(A), 0.1, P(aug), P(state), None, 4, P(A),
+                                              N, 2, dk, 192, dt, None)
+    assert dec(dt=4) == DTYPE
+    assert dec(dk=32) == UNSUP
+    assert dec(state=None) == NULL
+    assert dec(state=MIS) == ALIGN
+    assert dec(aug=MIS) == ALIGN
+    assert dec(N=0) == OK
+
+
 def test_bwd_argument_errors(lib):
     P = ctypes.c_void_p
 

@@ -108,3 +108,36 @@ def test_decode_workload_sampled_64_steps():
     assert worst <= BF16_TOL
     sg = state[ri, hi].cpu().numpy()
     assert rel_err(sg, ref[:, 0]) <= 1e-4
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+@pytest.mark.parametrize("with_aug", [False, True])
+def test_decode_bf16_state_matches_oracle(bf16, with_aug):
+    """bf16-stored state pool: each step against the oracle's step with the state rounded to bf16
+    on write-back (the readout from the update before rounding); the pool itself against the
+    oracle's rounded state (bf16 values: half a bf16 ulp of allowance).  The bar is the bf16 one
+    for either i/o dtype: the kernel rounds its fp32 update and the oracle its fp64 update, so a
+    value within an fp32 rounding of a bf16 tie may round the other way (one bf16 ulp, 2^-8
+    relative, in that state element), which the next readouts carry; 1e-4 is the all-fp32 bar."""
+    import torch
+    N, H, steps = 5, 3, 10
+    rnd = gs.bf16_round if bf16 else (lambda x: x)
+    dt = torch.bfloat16 if bf16 else torch.float32
+    ll = gs.laplace_log_lambda(H)
+    aug = gs.normal(41, 9, (H, 96), 10.0) if with_aug else None
+    s0 = gs.bf16_round(gs.normal(41, 7, (N, H, 96, 192), 0.1))
+    state = torch.from_numpy(s0).cuda().to(torch.bfloat16)
+    ref_state = s0.astype(np.float64).copy()
+    tol = BF16_TOL
+    for t in range(steps):
+        q = rnd(gs.normal(41, 100 + 3 * t, (N, H, 96), 1 / np.sqrt(96)))
+        k = rnd(gs.normal(41, 101 + 3 * t, (N, H, 96), 1 / np.sqrt(96)))
+        v = rnd(gs.normal(41, 102 + 3 * t, (N, H, 192)))
+        o = gla.gla_decode_step(torch.from_numpy(q).cuda().to(dt), torch.from_numpy(k).cuda().to(dt),
+                                torch.from_numpy(v).cuda().to(dt), torch.from_numpy(ll).cuda(), state,
+                                float(gs.SCALE), aug=None if aug is None else torch.from_numpy(aug).cuda())
+        o_ref = oracle.decode_step_bf16_state(q, k, v, ll, float(gs.SCALE), ref_state)
+        if aug is not None:
+            o_ref = o_ref + oracle.self_aug(q, k, v, aug)
+        assert rel_err(o.float().cpu().numpy(), o_ref, bf16_out=bf16) <= tol, t
+        assert rel_err(state.float().cpu().numpy(), ref_state, bf16_out=True) <= BF16_TOL, t
