@@ -124,3 +124,22 @@ def test_decode_aug_steps_match_oracle(bf16):
         tol = BF16_TOL if bf16 else F32_TOL
         assert rel_err(o.float().cpu().numpy(), o_ref, bf16_out=bf16) <= tol, t
     assert rel_err(state.cpu().numpy(), ref_state) <= 1e-5
+
+
+def test_fwd_aug_layer_workload_sampled():
+    """B=8, T=2048, H=16 bf16 with aug_balance (the benchmark's augmented forward), 5 sampled
+    (sequence, head) units against the oracle's forward plus its self-augmentation term."""
+    from glasynth import workloads as wl
+    w = wl.layer()
+    g = w.device_inputs()
+    aug = gs.normal(11, 9, (16, 96), 10.0)   # as the benchmark row
+    o, hT = gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], w.scale,
+                              aug=torch.from_numpy(aug).cuda())
+    torch.cuda.synchronize()
+    for n, h in [(0, 0), (7, 15), (3, 5), (5, 14), (2, 9)]:
+        u = w.host_unit(n, h)
+        o_ref, hT_ref = oracle.fwd(u["q"], u["k"], u["v"], u["log_lambda"], w.scale, h0=u["h0"])
+        o_ref = o_ref + oracle.self_aug(u["q"], u["k"], u["v"], aug[h:h + 1])
+        og = o[n, :, h].float().cpu().numpy()
+        assert rel_err(og, o_ref[:, 0], bf16_out=True) <= BF16_TOL, (n, h)
+        assert rel_err(hT[n, h].cpu().numpy(), hT_ref[0, 0]) <= BF16_TOL, (n, h)

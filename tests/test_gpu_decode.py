@@ -141,3 +141,34 @@ def test_decode_bf16_state_matches_oracle(bf16, with_aug):
             o_ref = o_ref + oracle.self_aug(q, k, v, aug)
         assert rel_err(o.float().cpu().numpy(), o_ref, bf16_out=bf16) <= tol, t
         assert rel_err(state.float().cpu().numpy(), ref_state, bf16_out=True) <= BF16_TOL, t
+
+
+def test_decode_bf16_state_workload_sampled():
+    """The benchmark's pool (1,280 sequences x 24 layers x 16 heads) stored in bf16, 16 steps as
+    benchmarked; 8 sampled (pool row, head) states followed by the oracle's rounded step."""
+    import torch
+    w = wl.DecodeWorkload()
+    state = w.device_state().to(torch.bfloat16)
+    ll = torch.from_numpy(w.log_lambda).cuda()
+    rng = np.random.default_rng(3)
+    rows = [(int(r), int(h)) for r, h in zip(rng.integers(0, w.N, 6), rng.integers(0, w.H, 6))]
+    rows += [(0, 0), (w.N - 1, w.H - 1)]
+    ref = oracle.round_to_bf16(w.host_state(rows).astype(np.float64))[:, None]
+    bufs = w.device_step(0)
+    ri = torch.tensor([r for r, _ in rows], device="cuda")
+    hi = torch.tensor([h for _, h in rows], device="cuda")
+    worst = 0.0
+    for step in range(16):
+        w.device_step(step, out=bufs)
+        o = gla.gla_decode_step(bufs["q"], bufs["k"], bufs["v"], ll, state, w.scale)
+        og = o[ri, hi].float().cpu().numpy()
+        q, k, v = w.host_step(step, rows)
+        lls = np.array([w.log_lambda[h] for _, h in rows], np.float32)
+        o_ref = np.stack([oracle.decode_step_bf16_state(q[i:i + 1, None], k[i:i + 1, None], v[i:i + 1, None],
+                                                        lls[i:i + 1], w.scale, ref[i:i + 1])[0, 0]
+                          for i in range(len(rows))])
+        worst = max(worst, rel_err(og, o_ref, bf16_out=True))
+    assert worst <= BF16_TOL
+    sg = state[ri, hi].float().cpu().numpy()
+    assert rel_err(sg, ref[:, 0], bf16_out=True) <= BF16_TOL
+    del state

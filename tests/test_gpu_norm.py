@@ -80,3 +80,18 @@ def test_forward_then_norm_gate_end_to_end():
                                torch.from_numpy(w).cuda(), torch.from_numpy(tier).cuda())
     ref = oracle.head_norm_gate(flat(o, False), g, w, tier, 1e-6)
     assert rel_err(flat(y, False), ref, bf16_out=True) <= BF16_TOL
+
+
+def test_head_norm_gate_benchmark_size_in_full():
+    """16,384 rows x 16 heads x 192 bf16, four tiers (the benchmark row's shape and inputs),
+    compared in full (the oracle is a single pass)."""
+    rows, H = 16384, 16
+    o = gs.bf16_round(gs.normal(13, 1, (rows, H, 192)))
+    g = gs.bf16_round(gs.normal(13, 2, (rows, H, 192), 2.0))
+    w = (1.0 + gs.normal(13, 3, (4, 192), 0.3)).astype(np.float32)
+    tier = (np.arange(H) // 4).astype(np.int32)
+    y = gla.gla_head_norm_gate(torch.from_numpy(o).cuda().to(torch.bfloat16),
+                               torch.from_numpy(g).cuda().to(torch.bfloat16), torch.from_numpy(w).cuda(),
+                               torch.from_numpy(tier).cuda())
+    ref = oracle.head_norm_gate(o, g, w, tier, 1e-6)
+    assert rel_err(y.float().cpu().numpy(), ref, bf16_out=True) <= BF16_TOL
