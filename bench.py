@@ -316,6 +316,40 @@ def bench_norm_gate(torch, gla, wl, dist, args, peaks):
     return res
 
 
+def bench_fwd_split(torch, gla, wl, dist, args, peaks):
+    """One long sequence (131,072 tokens, H=16, bf16): the sequence-split forward
+    (gla_chunk_fwd_split, 32-chunk segments) against the plain packed forward, whose 48 units
+    (16 heads x 3 d_v tiles) each run 1,024 chunks on one SM."""
+    import glasynth as gs
+    T = 131072
+    q = torch.from_numpy(gs.normal(14, 1, (T, H, DK), DK ** -0.5)).cuda().to(torch.bfloat16)
+    k = torch.from_numpy(gs.normal(14, 2, (T, H, DK), DK ** -0.5)).cuda().to(torch.bfloat16)
+    v = torch.from_numpy(gs.normal(14, 3, (T, H, DV))).cuda().to(torch.bfloat16)
+    ll = torch.from_numpy(gs.laplace_log_lambda(H)).cuda()
+    o = torch.empty_like(v)
+    hT = torch.empty((1, H, DK, DV), dtype=torch.float32, device="cuda")
+    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    ws_plain = torch.empty(gla.gla_workspace_bytes(1, H), dtype=torch.uint8, device="cuda")
+    scale = DK ** -0.5
+    plain = lambda: gla.gla_chunk_fwd(q, k, v, ll, scale, cu_seqlens=cu, o=o, hT=hT, workspace=ws_plain)
+    p_region, _ = timed(torch, dist, plain, max(3, args.steps // 4), args.warmup)
+    import numpy as np
+    cu_h = np.array([0, T], np.int32)
+    ws = torch.empty(gla.load_library().gla_split_workspace_bytes(cu_h.ctypes.data_as(__import__("ctypes").c_void_p),
+                                                                  1, H, 32), dtype=torch.uint8, device="cuda")
+    split = lambda: gla.gla_chunk_fwd_split(q, k, v, ll, [T], seg_chunks=32, scale=scale, o=o, hT=hT,
+                                            workspace=ws)
+    region, per_call = timed(torch, dist, split, max(3, args.steps // 4), args.warmup)
+    region, p_region = dist.max(region), dist.max(p_region)
+    res = {"workload": "one sequence of 131,072 tokens, H=16, bf16, 32-chunk segments", "tokens": T,
+           "ms_per_step": region, "value": T * dist.world / (region / 1e3), "unit": "tokens/s",
+           "plain_forward_ms": p_region,
+           "roofline": roofline(fwd_bytes(T, 1, False), fwd_flops(T), region / 1e3, peaks),
+           "launches_per_step": 5}
+    del q, k, v, o, hT, ws, ws_plain
+    return res
+
+
 def bench_varlen(torch, gla, wl, dist, args, peaks):
     w = wl.varlen()
     g = w.device_inputs()
@@ -465,7 +499,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--rows", default="fwd,bwd,varlen,decode,fwd_aug,norm_gate,decode_aug,decode_bf16_state")
+    ap.add_argument("--rows", default="fwd,bwd,varlen,decode,fwd_aug,norm_gate,decode_aug,decode_bf16_state,"
+                    "fwd_split")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-seqs", type=int, default=1280,
                     help="sequences in the decode pool (1280 = the measured workload)")
@@ -498,6 +533,8 @@ def main():
             out["decode"] = bench_decode(torch, gla, wl, dist, args, peaks)
         if "fwd_aug" in rows:
             out["fwd_aug"] = bench_fwd_aug(torch, gla, wl, dist, args, peaks)
+        if "fwd_split" in rows:
+            out["fwd_split"] = bench_fwd_split(torch, gla, wl, dist, args, peaks)
         if "norm_gate" in rows:
             out["norm_gate"] = bench_norm_gate(torch, gla, wl, dist, args, peaks)
         if "decode_aug" in rows:

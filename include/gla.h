@@ -182,6 +182,32 @@ int gla_decode_step_bf16_state(const void* q, const void* k, const void* v, cons
                                int pool_rows, void* o, int N, int H, int dk, int dv, int dtype,
                                gla_stream_t stream);
 
+/* Sequence-split forward for long sequences (no counterpart in the paper).  A sequence's work
+ * otherwise sits on one CTA per (head, 64-column tile of d_v), so one long sequence among few
+ * keeps most SMs idle.  Here each sequence is cut into segments of at most seg_chunks chunks
+ * (128 tokens each), and the forward runs in three steps: every segment from a zero state (its
+ * final state U_i), a scan per (sequence, head) that chains them (S_in of the next segment =
+ * lambda^(L_i) S_in + U_i; hT after the last), and every segment again from its S_in, writing o.
+ * Same results as gla_chunk_fwd (the sums are only reassociated), about twice its reads of q, k
+ * and v; worth it when the longest sequences dominate the call.
+ *   cu_seqlens_host  [n_seq + 1] host array of packed offsets (cu_seqlens_host[0] = 0,
+ *                    non-decreasing, cu_seqlens_host[n_seq] = T): the segments are planned on the
+ *                    host, so no device offsets are needed (a fixed-length batch passes 0, T,
+ *                    2T, ... with T = n_seq * T_seq and the [n_seq, T_seq, H, d] layout).
+ *   aug              NULL, or aug_balance [H, 96] (the self-augmentation step of gla_chunk_fwd_aug).
+ *   seg_chunks       >= 1, chunks per segment.
+ *   workspace        >= gla_split_workspace_bytes(cu_seqlens_host, n_seq, H, seg_chunks) bytes,
+ *                    256-byte aligned: the plan, the segment states (two fp32 [segments, H, 96,
+ *                    192] arrays) and the packed schedule.
+ * Every other argument as in gla_chunk_fwd.  The plan is copied to the device with pageable
+ * host-to-device copies (which may wait for the stream's earlier work). */
+size_t gla_split_workspace_bytes(const int32_t* cu_seqlens_host, int n_seq, int H, int seg_chunks);
+int gla_chunk_fwd_split(const void* q, const void* k, const void* v, const float* log_lambda,
+                        const float* h0, float scale, const float* aug, void* o, float* hT,
+                        const int32_t* cu_seqlens_host, int n_seq, int T, int H, int dk, int dv,
+                        int dtype, int seg_chunks, void* workspace, size_t ws_bytes,
+                        gla_stream_t stream);
+
 /* The forward without any device allocation (no counterpart in the paper).  For callers that
  * cannot allocate device memory per call, such as a serving engine whose memory is all handed to
  * its own pool at start-up: same arguments and results as gla_chunk_fwd, minus the workspace.

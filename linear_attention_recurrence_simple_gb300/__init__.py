@@ -19,7 +19,8 @@ import torch
 __all__ = [
     "GlaError", "load_library", "library_path", "gla_workspace_bytes", "gla_bwd_workspace_bytes",
     "gla_chunk_fwd",
-    "gla_chunk_bwd", "gla_decode_step", "gla_chunk_fwd_noalloc", "gla_head_norm_gate", "gla_get_device_error",
+    "gla_chunk_bwd", "gla_decode_step", "gla_chunk_fwd_noalloc", "gla_head_norm_gate", "gla_chunk_fwd_split",
+    "gla_get_device_error",
     "gla_set_wait_limit_ns",
     "gla_status_string", "DK", "DV", "CHUNK", "EXPORTS",
 ]
@@ -28,7 +29,7 @@ DK, DV, CHUNK = 96, 192, 128
 GLA_BF16, GLA_F32 = 0, 1
 EXPORTS = ("gla_workspace_bytes", "gla_bwd_workspace_bytes", "gla_chunk_fwd", "gla_chunk_bwd",
            "gla_decode_step", "gla_chunk_fwd_aug", "gla_decode_step_aug", "gla_head_norm_gate",
-           "gla_decode_step_bf16_state",
+           "gla_decode_step_bf16_state", "gla_split_workspace_bytes", "gla_chunk_fwd_split",
            "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
            "gla_status_string")
 NOALLOC_MAX_SEQS = 16384
@@ -83,6 +84,10 @@ def load_library(build: bool = True):
         lib.gla_head_norm_gate.argtypes = [P, P, P, P, I, F, P, ctypes.c_longlong, I, I, I, P]
         lib.gla_decode_step_bf16_state.argtypes = [P, P, P, P, F, P, P, P, I, P, I, I, I, I, I, P]
         lib.gla_decode_step_bf16_state.restype = I
+        lib.gla_split_workspace_bytes.argtypes = [P, I, I, I]
+        lib.gla_split_workspace_bytes.restype = Z
+        lib.gla_chunk_fwd_split.argtypes = [P, P, P, P, P, F, P, P, P, P, I, I, I, I, I, I, I, P, Z, P]
+        lib.gla_chunk_fwd_split.restype = I
         lib.gla_head_norm_gate.restype = I
         lib.gla_get_device_error.argtypes = [P]
         lib.gla_get_device_error.restype = I
@@ -337,6 +342,59 @@ def gla_decode_step(q, k, v, log_lambda, state, scale=None, slot=None, o=None, a
                                          dt, _stream(dev))
     _check(rc, "gla_decode_step" if aug is None else "gla_decode_step_aug")
     return o
+
+
+def gla_chunk_fwd_split(q, k, v, log_lambda, lengths, seg_chunks=32, scale=None, h0=None, aug=None,
+                        output_final_state: bool = True, o=None, hT=None, workspace=None):
+    """Sequence-split forward (``gla_chunk_fwd_split``) for long sequences.
+
+    ``lengths``: the sequences' token counts (host ints); q, k ``[T_total, H, 96]``, v
+    ``[T_total, H, 192]`` packed in that order (a fixed-length batch may pass ``[B, T, H, d]``
+    tensors with ``lengths = [T] * B``).  Segments hold at most ``seg_chunks`` chunks of 128
+    tokens.  Returns ``(o, hT)`` like :func:`gla_chunk_fwd`."""
+    import numpy as np
+    lib = load_library()
+    dev = q.device
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, q.dtype, dev)
+    _need(log_lambda, "log_lambda", torch.float32, dev)
+    cu = np.zeros(len(lengths) + 1, np.int32)
+    cu[1:] = np.cumsum(np.asarray(lengths, np.int64))
+    n_seq, H = len(lengths), q.shape[-2]
+    T = int(cu[-1])
+    if q.numel() != T * H * DK or k.shape != q.shape or v.numel() != T * H * DV or q.shape[-1] != DK:
+        raise ValueError("q, k, v must hold sum(lengths) tokens of H heads")
+    if log_lambda.numel() != H:
+        raise ValueError("log_lambda must have H entries")
+    if h0 is not None:
+        _need(h0, "h0", torch.float32, dev)
+        if h0.shape != (n_seq, H, DK, DV):
+            raise ValueError("h0 must be [n_seq, H, 96, 192]")
+    if aug is not None:
+        _need(aug, "aug", torch.float32, dev)
+        if aug.shape != (H, DK):
+            raise ValueError("aug must be [H, 96]")
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    _need(o, "o", v.dtype, dev)
+    if output_final_state and hT is None:
+        hT = torch.empty((n_seq, H, DK, DV), dtype=torch.float32, device=dev)
+    if hT is not None:
+        _need(hT, "hT", torch.float32, dev)
+    cu_p = cu.ctypes.data_as(ctypes.c_void_p)
+    need = lib.gla_split_workspace_bytes(cu_p, n_seq, H, int(seg_chunks))
+    if need == 0 and n_seq > 0:
+        raise ValueError("bad lengths or seg_chunks")
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    s = float(DK ** -0.5) if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        rc = lib.gla_chunk_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), s, _ptr(aug),
+                                     _ptr(o), _ptr(hT), cu_p, n_seq, T, H, DK, DV, dt, int(seg_chunks),
+                                     _ptr(workspace), workspace.numel(), _stream(dev))
+    _check(rc, "gla_chunk_fwd_split")
+    return o, hT
 
 
 def gla_head_norm_gate(o, g, weight, tier, eps=1e-6, y=None):

@@ -153,6 +153,31 @@ def test_decode_bf16_state_argument_errors(lib):
     assert dec(N=0) == OK
 
 
+def test_split_argument_errors(lib):
+    import numpy as np
+    P = ctypes.c_void_p
+    cu = np.array([0, 300, 300, 1000], np.int32)
+    cp = cu.ctypes.data_as(P)
+    need = lib.gla_split_workspace_bytes(cp, 3, 2, 2)
+    assert need > 0
+    assert lib.gla_split_workspace_bytes(None, 3, 2, 2) == 0
+    assert lib.gla_split_workspace_bytes(cp, 3, 2, 0) == 0
+
+    def sp(cu_p=cp, n=3, T=1000, seg=2, ws=A, wsb=None, dk=96):
+        return lib.gla_chunk_fwd_split(P(A), P(A), P(A), P(A), None, 0.1, None, P(A), None, cu_p, n, T, 2, dk,
+                                       192, 0, seg, P(ws), need if wsb is None else wsb, None)
+    assert sp(dk=64) == UNSUP
+    assert sp(seg=0) == SHAPE
+    assert sp(cu_p=None) == NULL
+    assert sp(T=999) == SHAPE                     # cu[n_seq] must equal T
+    bad = np.array([0, 300, 200, 1000], np.int32)
+    assert sp(cu_p=bad.ctypes.data_as(P)) == SHAPE  # offsets must not decrease
+    assert sp(ws=None) == WS
+    assert sp(wsb=need - 1) == WS
+    assert sp(ws=A + 16) == ALIGN                 # 256-byte aligned workspace
+    assert sp(n=0) == OK
+
+
 def test_bwd_argument_errors(lib):
     P = ctypes.c_void_p
 
