@@ -70,8 +70,10 @@
 
 namespace gla {
 
-// MODE_FWDA: the forward with the self-augmentation step (see the decay mask).
-enum ScanMode { MODE_FWD = 0, MODE_DV = 1, MODE_DQ = 2, MODE_DK = 3, MODE_FWDA = 4 };
+// MODE_FWDA: the forward with the self-augmentation step (see the decay mask).  MODE_FWDS: the
+// forward's final states only (no outputs): the producer loads k and the v tile, MMA4 and the
+// epilogue's state update run, everything that builds outputs is left out.
+enum ScanMode { MODE_FWD = 0, MODE_DV = 1, MODE_DQ = 2, MODE_DK = 3, MODE_FWDA = 4, MODE_FWDS = 5 };
 
 namespace {
 
@@ -82,8 +84,9 @@ template <int MODE>
 struct Cfg {
   static constexpr bool REVERSE = MODE == MODE_DV || MODE == MODE_DK;  // reverse scan, j >= i mask
   static constexpr bool NARROW = MODE == MODE_DQ || MODE == MODE_DK;   // X, Y are 64-wide d_v tiles
-  static constexpr bool FWD = MODE == MODE_FWD || MODE == MODE_FWDA;
+  static constexpr bool FWD = MODE == MODE_FWD || MODE == MODE_FWDA || MODE == MODE_FWDS;
   static constexpr bool AUG = MODE == MODE_FWDA;
+  static constexpr bool STATES = MODE == MODE_FWDS;
   // Warp roles: 16 warps with one epilogue warpgroup (forward), or 20 with the epilogue's state
   // and output parts in two warpgroups (backward scans).  Per-thread registers of each warpgroup
   // after setmaxnreg add up to the launch count times the number of warpgroups (the host checks
@@ -454,9 +457,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == B_EMPTY || i == B_EMPTY + 1) cnt = 3;
+      if (i == B_EMPTY || i == B_EMPTY + 1) cnt = C::STATES ? 1 : 3;  // the MMA issuers that read a stage
       if (i == B_TBL_FULL || i == B_TBL_FULL + 1) cnt = 128;   // the Z4 warps write a unit's table
-      if (i == B_TBL_EMPTY || i == B_TBL_EMPTY + 1) cnt = C::SPLIT ? 512 : 384;  // its reader warps
+      if (i == B_TBL_EMPTY || i == B_TBL_EMPTY + 1) cnt = C::SPLIT ? 512 : (C::STATES ? 256 : 384);  // its readers
       if (i == B_O_FULL) cnt = 2;
       if (i == B_ST_FULL) cnt = 128;  // the epilogue threads' final-state rows are visible (tail piece)
       if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_P_HALF || i == B_U_EMPTY || i == B_SP_FULL ||
@@ -547,7 +550,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
         if (!mbar_wait(&bars[B_EMPTY + s], ph ^ 1u, a.wait_ns, abort_flag)) { stop = true; break; }
         const uint32_t st = sbase + (uint32_t)s * C::SZ_STAGE;
         uint64_t* full = &bars[B_FULL + s];
-        mbar_expect_tx(full, C::SZ_STAGE);
+        mbar_expect_tx(full, C::STATES ? C::SZ_STAGE - 24576u : C::SZ_STAGE);  // (no q: 24 KB)
         const int tok = (int)(w.tb + (long long)c * CHUNK);
         if (C::NARROW) {
           tma_load_3d(st + C::ST_X, &maps.x, full, col0, h, tok);
@@ -555,8 +558,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
           tma_load_3d(st + C::ST_Z, &maps.z, full, 0, h, tok);
           tma_load_3d(st + C::ST_Z + 16384u, &maps.z, full, 64, h, tok);
         } else {
-          tma_load_3d(st + C::ST_X, &maps.x, full, 0, h, tok);
-          tma_load_3d(st + C::ST_X1, &maps.x1, full, 64, h, tok);
+          if (!C::STATES) {
+            tma_load_3d(st + C::ST_X, &maps.x, full, 0, h, tok);
+            tma_load_3d(st + C::ST_X1, &maps.x1, full, 64, h, tok);
+          }
           tma_load_3d(st + C::ST_Y, &maps.y, full, 0, h, tok);
           tma_load_3d(st + C::ST_Y + 16384u, &maps.y, full, 64, h, tok);
           tma_load_3d(st + C::ST_Z, &maps.z, full, col0, h, tok);
@@ -571,8 +576,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
             tma_prefetch_3d(&maps.z, 0, h, tp);
             tma_prefetch_3d(&maps.z, 64, h, tp);
           } else {
-            tma_prefetch_3d(&maps.x, 0, h, tp);
-            tma_prefetch_3d(&maps.x1, 64, h, tp);
+            if (!C::STATES) {
+              tma_prefetch_3d(&maps.x, 0, h, tp);
+              tma_prefetch_3d(&maps.x1, 64, h, tp);
+            }
             tma_prefetch_3d(&maps.y, 0, h, tp);
             tma_prefetch_3d(&maps.y, 64, h, tp);
             tma_prefetch_3d(&maps.z, col0, h, tp);
@@ -601,7 +608,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       //   state copy: MN-major [hi | lo] (wide) or K-major (narrow)
       const SDesc dvt = sdesc(sbase + SMM::OFF_VT, SZ_TILE64, 1024, LAYOUT_SW128);
       int gk = 0;
-      bool stop = false;
+      bool stop = C::STATES && warp != 2;  // states only: MMA4 alone
       for (int u = 0; u < n_items && !stop; ++u) {
        const Unit wi = unit_at(u);
        for (int it = wi.it0; it < wi.it1; ++it, ++gk) {
@@ -689,6 +696,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
   } else if (warp < 8) {
     // ------------------------------------------------------------------ decay mask
     setmaxnreg_inc<C::REG_MASK>();
+    if constexpr (!C::STATES) {
     const int i = threadIdx.x - 128;  // query row = tensor-memory lane
     const int q = warp & 3;           // this warp's lanes are rows 32q .. 32q + 31
     const uint32_t lane_addr = tmem + ((uint32_t)(q << 5) << 16);
@@ -821,6 +829,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       mbar_arrive(&bars[B_P_FULL]);
      }
      mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
+    }
     }
   } else if (warp >= 12 && warp < 16) {
     // ------------------------------------------------------------------ weighted Z4 (hi and lo)
@@ -1014,13 +1023,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
             tc_fence_before();
             mbar_arrive(&bars[B_U_EMPTY]);
           }
-          if (it + 1 < w.it1) {  // after MMA3 of this chunk has read the previous copy
+          if (!C::STATES && it + 1 < w.it1) {  // after MMA3 of this chunk has read the previous copy
             if (g >= 0 && !warp_wait(&bars[B_SP_EMPTY], pc, a, abort_flag)) { aborted = true; break; }
             write_sprev();
           }
         }
         if (it < w.it0) continue;
-        if constexpr (DO_OUT) {
+        if constexpr (DO_OUT && !C::STATES) {
           // out row = O_intra + g * O_inter;  g = s lambda^(i+1) (forward scans) or lambda^(L-1-i)
           if (!warp_wait(&bars[B_O_FULL], pc, a, abort_flag)) { aborted = true; break; }
           tc_fence_after();
@@ -1253,7 +1262,7 @@ cudaError_t launch_scan(const void* X, const void* Y, const void* Z, const ScanP
         (!C::NARROW && !make_map(&maps.x1, X, DK, a.H, T_total, 32, CU_TENSOR_MAP_SWIZZLE_64B)) ||
         !make_map(&maps.y, Y, dx, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.z, Z, dz, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        (!C::NARROW && !make_map(&maps.o, p.out, DV, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32)))
+        (!C::NARROW && !C::STATES && !make_map(&maps.o, p.out, DV, a.H, T_total, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32)))
       return cudaErrorInvalidValue;
   }
   const long long state_rows = (long long)a.n_seq * a.H * DK;
@@ -1330,6 +1339,17 @@ cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream) {
   }
   if (a.aug) return launch_scan<MODE_FWDA>(a.q, a.k, a.v, p, stream, max_ctas);
   return launch_scan<MODE_FWD>(a.q, a.k, a.v, p, stream, max_ctas);
+}
+
+// The forward's final states only (hT; no outputs), one CTA per unit.  Refused (an error) when
+// the states-only kernel did not compile to the register count its role split needs.
+cudaError_t launch_tc_fwd_states(const ChunkArgs& a, cudaStream_t stream) {
+  ScanParams p;
+  p.a = a;
+  p.s0 = a.h0;
+  p.s_out = a.hT;
+  p.out = nullptr;
+  return launch_scan<MODE_FWDS>(a.q, a.k, a.v, p, stream, 0);
 }
 
 // After a wait gave up, a hand-over flag may have been left raised; lower them all.

@@ -3,15 +3,16 @@
 // "Beyond the KV cache", section "Challenge 1": within a chunk the work is parallel and only the
 // state's advance from chunk to chunk is sequential.  A sequence's chunks therefore split into
 // segments whose work runs in parallel once each segment knows the state it starts from:
-//   1. every segment runs the chunked forward from a zero state; its final state is
-//      U_i = sum_j lambda^(L_i-1-j) k_j v_j^T over the segment's L_i tokens;
+//   1. every segment runs the chunked forward from a zero state, final states only (bf16: the
+//      tensor-core scan's states-only mode, which loads k and v and runs the state update
+//      alone); its final state is U_i = sum_j lambda^(L_i-1-j) k_j v_j^T over its L_i tokens;
 //   2. a short scan per (sequence, head) chains them: S_in[first] = h0,
 //      S_in[i+1] = lambda^(L_i) S_in[i] + U_i, and hT = lambda^(L_last) S_in[last] + U_last;
 //   3. every segment runs the chunked forward again from S_in[i], writing the outputs.
 // A sequence whose chunks sit on one CTA (one unit per (sequence, head, d_v tile)) then spreads
-// over as many CTAs as it has segments, at the price of a second pass over q, k, v (step 1 also
-// writes outputs, which step 3 overwrites).  The host plans the segments from a host copy of the
-// sequence offsets; the device arrays it needs go into the caller's workspace.
+// over as many CTAs as it has segments, at the price of a second pass over k and v (in fp32 mode
+// step 1 is the full forward, whose outputs step 3 overwrites).  The host plans the segments from
+// a host copy of the sequence offsets; the device arrays it needs go into the caller's workspace.
 #include <algorithm>
 #include <vector>
 
@@ -19,6 +20,10 @@
 #include "gla_common.cuh"
 
 namespace gla {
+int current_device_state(unsigned** err, unsigned long long* wait_ns);
+cudaError_t launch_lpt_order(const int32_t* cu_seqlens, int n_seq, int32_t* order, cudaStream_t stream);
+cudaError_t launch_tc_fwd_states(const ChunkArgs& a, cudaStream_t stream);
+
 namespace {
 
 constexpr int SPLIT_THREADS = 256;
@@ -134,10 +139,38 @@ int gla_chunk_fwd_split(const void* q, const void* k, const void* v, const float
       cudaMemcpyAsync(seg_first, plan.seg_first.data(), plan.seg_first.size() * sizeof(int32_t),
                       cudaMemcpyHostToDevice, s) != cudaSuccess)
     return GLA_ERR_LAUNCH;
-  // 1. segment states from zero (the outputs written here are overwritten by step 3)
-  rc = gla_chunk_fwd(q, k, v, log_lambda, nullptr, scale, o, U, seg_cu, plan.M, T, H, dk, dv, dtype,
-                     ws + l.lpt, l.U - l.lpt, stream);
-  if (rc) return rc;
+  // 1. segment states from zero
+  bool states_done = false;
+  if (dtype == GLA_BF16) {
+    for (const void* p : {q, k, v, (const void*)o, (const void*)log_lambda})
+      if (((uintptr_t)p & 15u) != 0) return GLA_ERR_ALIGN;
+    unsigned* err;
+    unsigned long long wait_ns;
+    if ((rc = gla::current_device_state(&err, &wait_ns)) != GLA_OK) return rc;
+    int32_t* order = (int32_t*)(ws + l.lpt + 256);
+    if (gla::launch_lpt_order(seg_cu, plan.M, order, s) != cudaSuccess) return GLA_ERR_LAUNCH;
+    gla::ChunkArgs a = {};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.log_lambda = log_lambda;
+    a.hT = U;
+    a.cu_seqlens = seg_cu;
+    a.order = order;
+    a.scale = scale;
+    a.n_seq = plan.M;
+    a.T = T;
+    a.H = H;
+    a.err = err;
+    a.wait_ns = wait_ns;
+    states_done = gla::launch_tc_fwd_states(a, s) == cudaSuccess;
+    if (!states_done) (void)cudaGetLastError();  // refused: the full forward below instead
+  }
+  if (!states_done) {  // (the outputs written here are overwritten by step 3)
+    rc = gla_chunk_fwd(q, k, v, log_lambda, nullptr, scale, o, U, seg_cu, plan.M, T, H, dk, dv, dtype,
+                       ws + l.lpt, l.U - l.lpt, stream);
+    if (rc) return rc;
+  }
   // 2. chain the segment states
   gla::split_scan_kernel<<<(unsigned)((long long)n_seq * H * 4), gla::SPLIT_THREADS, 0, s>>>(
       U, h0, seg_cu, seg_first, log_lambda, S_in, hT, H);
