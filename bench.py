@@ -318,8 +318,8 @@ def bench_norm_gate(torch, gla, wl, dist, args, peaks):
 
 def bench_fwd_split(torch, gla, wl, dist, args, peaks):
     """One long sequence (131,072 tokens, H=16, bf16): the sequence-split forward
-    (gla_chunk_fwd_split, 32-chunk segments) against the plain packed forward, whose 48 units
-    (16 heads x 3 d_v tiles) each run 1,024 chunks on one SM."""
+    (gla_chunk_fwd_split, segment length chosen by the library) against the plain packed forward,
+    whose 48 units (16 heads x 3 d_v tiles) each run 1,024 chunks on one SM."""
     import glasynth as gs
     T = 131072
     q = torch.from_numpy(gs.normal(14, 1, (T, H, DK), DK ** -0.5)).cuda().to(torch.bfloat16)
@@ -335,13 +335,15 @@ def bench_fwd_split(torch, gla, wl, dist, args, peaks):
     p_region, _ = timed(torch, dist, plain, max(3, args.steps // 4), args.warmup)
     import numpy as np
     cu_h = np.array([0, T], np.int32)
+    seg = gla.gla_split_choose_seg_chunks([T], H)
     ws = torch.empty(gla.load_library().gla_split_workspace_bytes(cu_h.ctypes.data_as(__import__("ctypes").c_void_p),
-                                                                  1, H, 32), dtype=torch.uint8, device="cuda")
-    split = lambda: gla.gla_chunk_fwd_split(q, k, v, ll, [T], seg_chunks=32, scale=scale, o=o, hT=hT,
+                                                                  1, H, 0), dtype=torch.uint8, device="cuda")
+    split = lambda: gla.gla_chunk_fwd_split(q, k, v, ll, [T], seg_chunks=0, scale=scale, o=o, hT=hT,
                                             workspace=ws)
     region, per_call = timed(torch, dist, split, max(3, args.steps // 4), args.warmup)
     region, p_region = dist.max(region), dist.max(p_region)
-    res = {"workload": "one sequence of 131,072 tokens, H=16, bf16, 32-chunk segments", "tokens": T,
+    res = {"workload": f"one sequence of 131,072 tokens, H=16, bf16, {seg}-chunk segments (seg_chunks=0)",
+           "tokens": T, "seg_chunks": seg,
            "ms_per_step": region, "value": T * dist.world / (region / 1e3), "unit": "tokens/s",
            "plain_forward_ms": p_region,
            "roofline": roofline(fwd_bytes(T, 1, False), fwd_flops(T), region / 1e3, peaks),

@@ -195,13 +195,23 @@ int gla_decode_step_bf16_state(const void* q, const void* k, const void* v, cons
  *                    host, so no device offsets are needed (a fixed-length batch passes 0, T,
  *                    2T, ... with T = n_seq * T_seq and the [n_seq, T_seq, H, d] layout).
  *   aug              NULL, or aug_balance [H, 96] (the self-augmentation step of gla_chunk_fwd_aug).
- *   seg_chunks       >= 1, chunks per segment.
+ *   seg_chunks       >= 1, chunks per segment; 0: chosen by gla_split_choose_seg_chunks.  When
+ *                    every sequence fits one segment the call is gla_chunk_fwd (or _aug).
  *   workspace        >= gla_split_workspace_bytes(cu_seqlens_host, n_seq, H, seg_chunks) bytes,
  *                    256-byte aligned: the plan, the segment states (two fp32 [segments, H, 96,
  *                    192] arrays) and the packed schedule.
  * Every other argument as in gla_chunk_fwd.  The plan is copied to the device with pageable
- * host-to-device copies (which may wait for the stream's earlier work). */
+ * host-to-device copies (which may wait for the stream's earlier work).
+ * gla_split_workspace_bytes returns 0 for a NULL cu_seqlens_host, n_seq < 0, H < 1, seg_chunks
+ * < 0 or decreasing offsets.
+ * gla_split_choose_seg_chunks: the segment length that seg_chunks = 0 uses, from a cost model of
+ * the packed forward (one CTA per (segment, head, d_v tile) unit on each of 152 SMs, longest
+ * units first, a unit costing its chunks plus a start-up cost; the split's two passes against the
+ * plain forward's one), over lengths that cut the longest sequence into 2 .. 64 equal parts.
+ * Returns 0 when no split is estimated faster, GLA_ERR_NULL / GLA_ERR_SHAPE on bad arguments.
+ * Host only (no device needed). */
 size_t gla_split_workspace_bytes(const int32_t* cu_seqlens_host, int n_seq, int H, int seg_chunks);
+int gla_split_choose_seg_chunks(const int32_t* cu_seqlens_host, int n_seq, int H);
 int gla_chunk_fwd_split(const void* q, const void* k, const void* v, const float* log_lambda,
                         const float* h0, float scale, const float* aug, void* o, float* hT,
                         const int32_t* cu_seqlens_host, int n_seq, int T, int H, int dk, int dv,

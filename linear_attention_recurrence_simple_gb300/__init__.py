@@ -20,7 +20,7 @@ __all__ = [
     "GlaError", "load_library", "library_path", "gla_workspace_bytes", "gla_bwd_workspace_bytes",
     "gla_chunk_fwd",
     "gla_chunk_bwd", "gla_decode_step", "gla_chunk_fwd_noalloc", "gla_head_norm_gate", "gla_chunk_fwd_split",
-    "gla_get_device_error",
+    "gla_split_choose_seg_chunks", "gla_get_device_error",
     "gla_set_wait_limit_ns",
     "gla_status_string", "DK", "DV", "CHUNK", "EXPORTS",
 ]
@@ -30,7 +30,7 @@ GLA_BF16, GLA_F32 = 0, 1
 EXPORTS = ("gla_workspace_bytes", "gla_bwd_workspace_bytes", "gla_chunk_fwd", "gla_chunk_bwd",
            "gla_decode_step", "gla_chunk_fwd_aug", "gla_decode_step_aug", "gla_head_norm_gate",
            "gla_decode_step_bf16_state", "gla_split_workspace_bytes", "gla_chunk_fwd_split",
-           "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
+           "gla_split_choose_seg_chunks", "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
            "gla_status_string")
 NOALLOC_MAX_SEQS = 16384
 
@@ -88,6 +88,8 @@ def load_library(build: bool = True):
         lib.gla_split_workspace_bytes.restype = Z
         lib.gla_chunk_fwd_split.argtypes = [P, P, P, P, P, F, P, P, P, P, I, I, I, I, I, I, I, P, Z, P]
         lib.gla_chunk_fwd_split.restype = I
+        lib.gla_split_choose_seg_chunks.argtypes = [P, I, I]
+        lib.gla_split_choose_seg_chunks.restype = I
         lib.gla_head_norm_gate.restype = I
         lib.gla_get_device_error.argtypes = [P]
         lib.gla_get_device_error.restype = I
@@ -344,14 +346,32 @@ def gla_decode_step(q, k, v, log_lambda, state, scale=None, slot=None, o=None, a
     return o
 
 
-def gla_chunk_fwd_split(q, k, v, log_lambda, lengths, seg_chunks=32, scale=None, h0=None, aug=None,
+def _host_offsets(lengths):
+    import numpy as np
+    cu = np.zeros(len(lengths) + 1, np.int32)
+    cu[1:] = np.cumsum(np.asarray(lengths, np.int64))
+    return cu
+
+
+def gla_split_choose_seg_chunks(lengths, H):
+    """Chunks per segment that ``gla_chunk_fwd_split(..., seg_chunks=0)`` uses for these sequence
+    lengths and H heads; 0 when every sequence stays one segment (the plain forward)."""
+    cu = _host_offsets(lengths)
+    rc = load_library().gla_split_choose_seg_chunks(cu.ctypes.data_as(ctypes.c_void_p), len(lengths), int(H))
+    if rc < 0:
+        _check(rc, "gla_split_choose_seg_chunks")
+    return rc
+
+
+def gla_chunk_fwd_split(q, k, v, log_lambda, lengths, seg_chunks=0, scale=None, h0=None, aug=None,
                         output_final_state: bool = True, o=None, hT=None, workspace=None):
     """Sequence-split forward (``gla_chunk_fwd_split``) for long sequences.
 
     ``lengths``: the sequences' token counts (host ints); q, k ``[T_total, H, 96]``, v
     ``[T_total, H, 192]`` packed in that order (a fixed-length batch may pass ``[B, T, H, d]``
     tensors with ``lengths = [T] * B``).  Segments hold at most ``seg_chunks`` chunks of 128
-    tokens.  Returns ``(o, hT)`` like :func:`gla_chunk_fwd`."""
+    tokens; 0 lets the library choose (:func:`gla_split_choose_seg_chunks`), which may keep every
+    sequence whole.  Returns ``(o, hT)`` like :func:`gla_chunk_fwd`."""
     import numpy as np
     lib = load_library()
     dev = q.device

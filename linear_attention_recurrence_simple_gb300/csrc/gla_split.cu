@@ -57,14 +57,101 @@ struct SplitPlan {
   int M = 0;
 };
 
-// Segments of at most seg_chunks chunks (chunk-aligned within each sequence); an empty sequence
-// keeps one empty segment, which passes h0 through.
-int plan_split(const int32_t* cu, int n_seq, int seg_chunks, SplitPlan* p) {
+// Cost model of the automatic segment length (seg_chunks = 0).  The packed forward runs one CTA
+// per unit, (segment, head, d_v tile), one CTA per SM, longest units first; a unit takes its
+// chunk count plus a start-up cost, in chunk times.  The split runs two such passes (the
+// states-only pass at about three quarters of the full one), the plain forward one.  Costs are
+// kept in quarter chunk times (integers).
+constexpr int PLAN_SMS = 152;             // SMs of a GB300
+constexpr long long UNIT_OVERHEAD = 12;   // 3 chunk times per unit: pipeline fill and drain
+constexpr long long SPLIT_PASSES_X4 = 7;  // both passes of the split: 7/4 of a full pass
+
+using UnitGroups = std::vector<std::pair<int, long long>>;  // (chunks, units), any order
+
+// Estimated makespan of units placed longest-first on PLAN_SMS SMs, each on the least loaded.
+// A full round of PLAN_SMS equal units puts one on every SM, and the r < PLAN_SMS left over go
+// to the r least loaded SMs (exact while the loads differ by less than one unit): the loads stay
+// sorted by merging the r raised entries back into the rest.
+long long lpt_makespan(UnitGroups g) {
+  std::sort(g.begin(), g.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
+  long long load[PLAN_SMS] = {}, tmp[PLAN_SMS];
+  long long base = 0;
+  for (size_t i = 0; i < g.size();) {
+    long long count = 0;
+    const int len = g[i].first;
+    for (; i < g.size() && g[i].first == len; ++i) count += g[i].second;
+    const long long cost = 4ll * len + UNIT_OVERHEAD;
+    base += count / PLAN_SMS * cost;
+    const int r = (int)(count % PLAN_SMS);
+    if (r == 0) continue;
+    for (int i = 0; i < r; ++i) load[i] += cost;
+    std::merge(load, load + r, load + r, load + PLAN_SMS, tmp);
+    std::copy(tmp, tmp + PLAN_SMS, load);
+  }
+  return base + load[PLAN_SMS - 1];
+}
+
+// Chunks per segment for seg_chunks = 0: the plain forward's estimate against the split's for
+// segment lengths that cut the longest sequence into 2 .. 64 equal parts; 0 when no split is
+// estimated faster (every sequence then stays one segment).
+int choose_seg_chunks(const int32_t* cu, int n_seq, int H) {
+  const long long units = 3ll * H;  // (head, d_v tile) units per segment
+  std::vector<int> c(n_seq);
+  int c_max = 0;
+  long long chunks = 0, segs = 0;
+  UnitGroups plain;
+  for (int n = 0; n < n_seq; ++n) {
+    c[n] = (int)(((long long)cu[n + 1] - cu[n] + GLA_CHUNK - 1) / GLA_CHUNK);
+    c_max = std::max(c_max, c[n]);
+    if (c[n] > 0) {
+      plain.push_back({c[n], units});
+      chunks += c[n];
+      ++segs;
+    }
+  }
+  if (c_max < 2) return 0;
+  long long best = lpt_makespan(plain);
+  // A pass over segs' segments takes at least an even spread of all their costs over the SMs.
+  auto bound = [&](long long n_segs) {
+    return SPLIT_PASSES_X4 * ((units * (4 * chunks + n_segs * UNIT_OVERHEAD)) / PLAN_SMS) / 4;
+  };
+  if (bound(segs) >= best) return 0;
+  int best_len = 0, prev = 0;
+  UnitGroups g;
+  for (int parts = 2; parts <= std::min(c_max, 64); ++parts) {
+    const int len = (c_max + parts - 1) / parts;
+    if (len == prev) continue;
+    prev = len;
+    long long n_segs = 0;
+    g.clear();
+    for (int n = 0; n < n_seq; ++n) {
+      if (c[n] >= len) g.push_back({len, units * (c[n] / len)});
+      if (c[n] % len) g.push_back({c[n] % len, units});
+      n_segs += (c[n] + len - 1) / len;
+    }
+    if (bound(n_segs) >= best || SPLIT_PASSES_X4 * (4ll * len + UNIT_OVERHEAD) / 4 >= best) continue;
+    const long long t = SPLIT_PASSES_X4 * lpt_makespan(g) / 4;
+    if (t < best) {
+      best = t;
+      best_len = len;
+    }
+  }
+  return best_len;
+}
+
+// Segments of at most seg_chunks chunks (chunk-aligned within each sequence; 0: chosen by
+// choose_seg_chunks); an empty sequence keeps one empty segment, which passes h0 through.
+int plan_split(const int32_t* cu, int n_seq, int H, int seg_chunks, SplitPlan* p) {
+  for (int n = 0; n < n_seq; ++n)
+    if (cu[n + 1] < cu[n]) return GLA_ERR_SHAPE;
+  if (seg_chunks == 0) {
+    seg_chunks = choose_seg_chunks(cu, n_seq, H);
+    if (seg_chunks == 0) seg_chunks = 1 << 24;  // one segment per sequence
+  }
   p->seg_cu.assign(1, cu[0]);
   p->seg_first.assign(1, 0);
   for (int n = 0; n < n_seq; ++n) {
     const long long a = cu[n], b = cu[n + 1];
-    if (b < a) return GLA_ERR_SHAPE;
     const long long step = (long long)seg_chunks * GLA_CHUNK;
     if (b == a) {
       p->seg_cu.push_back((int32_t)b);
@@ -84,6 +171,7 @@ struct SplitLayout {
   size_t seg_cu, seg_first, lpt, U, S_in, total;
 };
 
+// With one segment per sequence (M == n_seq) the call is the plain forward: no segment states.
 SplitLayout split_layout(int M, int n_seq, int H) {
   SplitLayout l;
   const size_t state = (size_t)M * H * DK * DV * sizeof(float);
@@ -92,7 +180,7 @@ SplitLayout split_layout(int M, int n_seq, int H) {
   l.lpt = l.seg_first + align256((size_t)(n_seq + 1) * sizeof(int32_t));
   l.U = l.lpt + align256(gla_workspace_bytes(M, H));
   l.S_in = l.U + align256(state);
-  l.total = l.S_in + align256(state);
+  l.total = M == n_seq ? l.U : l.S_in + align256(state);
   return l;
 }
 
@@ -102,10 +190,18 @@ SplitLayout split_layout(int M, int n_seq, int H) {
 extern "C" {
 
 size_t gla_split_workspace_bytes(const int32_t* cu_seqlens_host, int n_seq, int H, int seg_chunks) {
-  if (!cu_seqlens_host || n_seq < 0 || H < 1 || seg_chunks < 1) return 0;
+  if (!cu_seqlens_host || n_seq < 0 || H < 1 || seg_chunks < 0) return 0;
   gla::SplitPlan plan;
-  if (gla::plan_split(cu_seqlens_host, n_seq, seg_chunks, &plan) != GLA_OK) return 0;
+  if (gla::plan_split(cu_seqlens_host, n_seq, H, seg_chunks, &plan) != GLA_OK) return 0;
   return gla::split_layout(plan.M, n_seq, H).total;
+}
+
+int gla_split_choose_seg_chunks(const int32_t* cu_seqlens_host, int n_seq, int H) {
+  if (!cu_seqlens_host) return GLA_ERR_NULL;
+  if (n_seq < 0 || H < 1) return GLA_ERR_SHAPE;
+  for (int n = 0; n < n_seq; ++n)
+    if (cu_seqlens_host[n + 1] < cu_seqlens_host[n]) return GLA_ERR_SHAPE;
+  return gla::choose_seg_chunks(cu_seqlens_host, n_seq, H);
 }
 
 int gla_chunk_fwd_split(const void* q, const void* k, const void* v, const float* log_lambda,
@@ -115,12 +211,12 @@ int gla_chunk_fwd_split(const void* q, const void* k, const void* v, const float
                         gla_stream_t stream) {
   if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_DTYPE;
   if (dk != GLA_DK || dv != GLA_DV) return GLA_ERR_UNSUPPORTED;
-  if (n_seq < 0 || T < 0 || H < 1 || seg_chunks < 1) return GLA_ERR_SHAPE;
+  if (n_seq < 0 || T < 0 || H < 1 || seg_chunks < 0) return GLA_ERR_SHAPE;
   if (n_seq == 0) return GLA_OK;
   if (!cu_seqlens_host) return GLA_ERR_NULL;
   if (cu_seqlens_host[0] != 0 || cu_seqlens_host[n_seq] != T) return GLA_ERR_SHAPE;
   gla::SplitPlan plan;
-  int rc = gla::plan_split(cu_seqlens_host, n_seq, seg_chunks, &plan);
+  int rc = gla::plan_split(cu_seqlens_host, n_seq, H, seg_chunks, &plan);
   if (rc) return rc;
   if ((long long)plan.M * H * GLA_DK >= (1ll << 31)) return GLA_ERR_SHAPE;
   const gla::SplitLayout l = gla::split_layout(plan.M, n_seq, H);
@@ -139,6 +235,13 @@ int gla_chunk_fwd_split(const void* q, const void* k, const void* v, const float
       cudaMemcpyAsync(seg_first, plan.seg_first.data(), plan.seg_first.size() * sizeof(int32_t),
                       cudaMemcpyHostToDevice, s) != cudaSuccess)
     return GLA_ERR_LAUNCH;
+  if (plan.M == n_seq) {  // one segment per sequence: the plain forward
+    if (aug)
+      return gla_chunk_fwd_aug(q, k, v, log_lambda, h0, scale, aug, o, hT, seg_cu, n_seq, T, H, dk, dv,
+                               dtype, ws + l.lpt, l.U - l.lpt, stream);
+    return gla_chunk_fwd(q, k, v, log_lambda, h0, scale, o, hT, seg_cu, n_seq, T, H, dk, dv, dtype,
+                         ws + l.lpt, l.U - l.lpt, stream);
+  }
   // 1. segment states from zero
   bool states_done = false;
   if (dtype == GLA_BF16) {

@@ -161,13 +161,14 @@ def test_split_argument_errors(lib):
     need = lib.gla_split_workspace_bytes(cp, 3, 2, 2)
     assert need > 0
     assert lib.gla_split_workspace_bytes(None, 3, 2, 2) == 0
-    assert lib.gla_split_workspace_bytes(cp, 3, 2, 0) == 0
+    assert lib.gla_split_workspace_bytes(cp, 3, 2, -1) == 0
+    assert lib.gla_split_workspace_bytes(cp, 3, 2, 0) > 0      # 0: the library chooses
 
     def sp(cu_p=cp, n=3, T=1000, seg=2, ws=A, wsb=None, dk=96):
         return lib.gla_chunk_fwd_split(P(A), P(A), P(A), P(A), None, 0.1, None, P(A), None, cu_p, n, T, 2, dk,
                                        192, 0, seg, P(ws), need if wsb is None else wsb, None)
     assert sp(dk=64) == UNSUP
-    assert sp(seg=0) == SHAPE
+    assert sp(seg=-1) == SHAPE
     assert sp(cu_p=None) == NULL
     assert sp(T=999) == SHAPE                     # cu[n_seq] must equal T
     bad = np.array([0, 300, 200, 1000], np.int32)
@@ -176,6 +177,34 @@ def test_split_argument_errors(lib):
     assert sp(wsb=need - 1) == WS
     assert sp(ws=A + 16) == ALIGN                 # 256-byte aligned workspace
     assert sp(n=0) == OK
+
+
+def test_split_choice_of_segment_length(lib):
+    """The automatic segment length: one long sequence among few is cut (into pieces that fill
+    whole waves of 152 SMs better than the plain forward's one CTA per unit), a batch whose units
+    already outnumber the SMs several times over is not, and neither is anything too short."""
+    import numpy as np
+    from glasynth import varlen_lengths
+    P = ctypes.c_void_p
+
+    def choose(lens, H=16):
+        cu = np.zeros(len(lens) + 1, np.int32)
+        cu[1:] = np.cumsum(lens)
+        return lib.gla_split_choose_seg_chunks(cu.ctypes.data_as(P), len(lens), H)
+    L = choose([131072])              # 1,024 chunks on 48 units: cut
+    assert 16 <= L <= 128
+    assert choose([131072, 2048, 4096]) > 0   # one long sequence with short ones: cut
+    assert choose([131072] * 4) == 0  # 192 units of 1,024 chunks: two passes cost more than the
+                                      # plain forward's second wave
+    assert choose([int(x) for x in varlen_lengths(3, 32, 128, 16384)]) == 0   # balanced by ordering
+    assert choose([2048] * 8) == 0    # 384 units of 16 chunks
+    assert choose([128]) == 0         # one chunk
+    assert choose([]) == 0
+    assert choose([0, 0]) == 0
+    assert lib.gla_split_choose_seg_chunks(None, 1, 16) == NULL
+    bad = np.array([0, 300, 200], np.int32)
+    assert lib.gla_split_choose_seg_chunks(bad.ctypes.data_as(P), 2, 16) == SHAPE
+    assert lib.gla_split_choose_seg_chunks(bad.ctypes.data_as(P), 1, 0) == SHAPE
 
 
 def test_bwd_argument_errors(lib):

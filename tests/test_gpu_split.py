@@ -87,3 +87,35 @@ def test_split_one_segment_per_sequence_matches_plain_forward_bitwise():
                                 cu_seqlens=g["cu_seqlens"])
     assert torch.equal(o, o2)
     assert rel_err(hT.cpu().numpy(), hT2.cpu().numpy()) <= 1e-6
+
+
+def test_split_automatic_segment_length_cuts_a_long_sequence():
+    """seg_chunks = 0 on one long sequence with short ones: the library cuts it (the chosen length
+    is below the longest sequence's 157 chunks) and the result still matches the oracle."""
+    lens = [20000, 300, 0]
+    H = 4
+    L = gla.gla_split_choose_seg_chunks(lens, H)
+    assert 1 <= L < 157
+    d = host_chunk_inputs(1150, lens, H, True, with_h0=True, packed=True)
+    d["scale"] = float(gs.SCALE)
+    g = to_device(d, True, packed=True)
+    o, hT = gla.gla_chunk_fwd_split(g["q"], g["k"], g["v"], g["log_lambda"], lens, scale=d["scale"],
+                                    h0=g["h0"])
+    _check(d, o, hT, BF16_TOL)
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_split_automatic_on_a_balanced_batch_is_the_plain_forward(bf16):
+    """seg_chunks = 0 where no split pays off (more units than SMs several times over, none much
+    longer than the rest): the call is gla_chunk_fwd, bit for bit."""
+    lens = [640] * 10 + [300, 129, 0]
+    assert gla.gla_split_choose_seg_chunks(lens, 8) == 0
+    d = host_chunk_inputs(1160, lens, 8, bf16, with_h0=True, packed=True)
+    d["scale"] = float(gs.SCALE)
+    g = to_device(d, bf16, packed=True)
+    o, hT = gla.gla_chunk_fwd_split(g["q"], g["k"], g["v"], g["log_lambda"], lens, scale=d["scale"],
+                                    h0=g["h0"])
+    o2, hT2 = gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], d["scale"], h0=g["h0"],
+                                cu_seqlens=g["cu_seqlens"])
+    assert torch.equal(o, o2)
+    assert torch.equal(hT, hT2)
