@@ -27,27 +27,44 @@ cudaError_t launch_tc_fwd_states(const ChunkArgs& a, cudaStream_t stream);
 namespace {
 
 constexpr int SPLIT_THREADS = 256;
+constexpr int STATE4 = DK * DV / 4;            // float4 entries of one state
+constexpr int SCAN_CTAS_PER_STATE = STATE4 / SPLIT_THREADS;  // 18
+static_assert(STATE4 % SPLIT_THREADS == 0, "a state is a whole number of CTAs");
+constexpr int SCAN_AHEAD = 4;                  // segments whose loads are issued together
 
-// One CTA per (sequence, head) and quarter of the 96 x 192 state: walks the sequence's segments
-// in order (step 2 above).  seg_first[n] .. seg_first[n + 1] - 1 are sequence n's segments.
+// One thread per 4 consecutive entries of one (sequence, head)'s 96 x 192 state: walks the
+// sequence's segments in order (step 2 above), issuing the loads of SCAN_AHEAD segments before
+// their links of the chain.  seg_first[n] .. seg_first[n + 1] - 1 are sequence n's segments.
 __global__ void __launch_bounds__(SPLIT_THREADS)
-split_scan_kernel(const float* __restrict__ U, const float* __restrict__ h0, const int32_t* __restrict__ seg_cu,
-                  const int32_t* __restrict__ seg_first, const float* __restrict__ log_lambda, float* __restrict__ S_in,
-                  float* __restrict__ hT, int H) {
-  constexpr int STATE = DK * DV, PART = STATE / 4;
-  const int nh = blockIdx.x / 4, part = blockIdx.x % 4;
-  const int n = nh / H, h = nh % H;
+split_scan_kernel(const float4* __restrict__ U, const float4* __restrict__ h0, const int32_t* __restrict__ seg_cu,
+                  const int32_t* __restrict__ seg_first, const float* __restrict__ log_lambda,
+                  float4* __restrict__ S_in, float4* __restrict__ hT, int H) {
+  const long long nh = blockIdx.x / SCAN_CTAS_PER_STATE;
+  const int e = (int)(blockIdx.x % SCAN_CTAS_PER_STATE) * SPLIT_THREADS + (int)threadIdx.x;
+  const int n = (int)(nh / H), h = (int)(nh % H);
   const float ll = log_lambda[h];
   const int i0 = seg_first[n], i1 = seg_first[n + 1];
-  for (int e = part * PART + (int)threadIdx.x; e < (part + 1) * PART; e += SPLIT_THREADS) {
-    float s = h0 ? h0[(long long)nh * STATE + e] : 0.f;
-    for (int i = i0; i < i1; ++i) {
-      const long long at = ((long long)i * H + h) * STATE + e;
-      S_in[at] = s;
-      s = fmaf(expf((float)(seg_cu[i + 1] - seg_cu[i]) * ll), s, U[at]);
+  float4 s = h0 ? h0[nh * STATE4 + e] : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = i0; i < i1; i += SCAN_AHEAD) {
+    float4 u[SCAN_AHEAD];
+    float d[SCAN_AHEAD];
+#pragma unroll
+    for (int j = 0; j < SCAN_AHEAD; ++j) {
+      if (i + j < i1) {
+        u[j] = U[((long long)(i + j) * H + h) * STATE4 + e];
+        d[j] = expf((float)(seg_cu[i + j + 1] - seg_cu[i + j]) * ll);
+      }
     }
-    if (hT) hT[(long long)nh * STATE + e] = s;
+#pragma unroll
+    for (int j = 0; j < SCAN_AHEAD; ++j) {
+      if (i + j < i1) {
+        S_in[((long long)(i + j) * H + h) * STATE4 + e] = s;
+        s = make_float4(fmaf(d[j], s.x, u[j].x), fmaf(d[j], s.y, u[j].y), fmaf(d[j], s.z, u[j].z),
+                        fmaf(d[j], s.w, u[j].w));
+      }
+    }
   }
+  if (hT) hT[nh * STATE4 + e] = s;
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -223,6 +240,9 @@ int gla_chunk_fwd_split(const void* q, const void* k, const void* v, const float
   if (!workspace || ws_bytes < l.total) return GLA_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 255u) != 0) return GLA_ERR_ALIGN;
   if (!log_lambda || (T > 0 && (!q || !k || !v || !o))) return GLA_ERR_NULL;
+  for (const void* p : {q, k, v, (const void*)o, (const void*)log_lambda, (const void*)h0, (const void*)hT,
+                        (const void*)aug})
+    if (((uintptr_t)p & 15u) != 0) return GLA_ERR_ALIGN;
   char* ws = (char*)workspace;
   int32_t* seg_cu = (int32_t*)(ws + l.seg_cu);
   int32_t* seg_first = (int32_t*)(ws + l.seg_first);
@@ -245,8 +265,6 @@ int gla_chunk_fwd_split(const void* q, const void* k, const void* v, const float
   // 1. segment states from zero
   bool states_done = false;
   if (dtype == GLA_BF16) {
-    for (const void* p : {q, k, v, (const void*)o, (const void*)log_lambda})
-      if (((uintptr_t)p & 15u) != 0) return GLA_ERR_ALIGN;
     unsigned* err;
     unsigned long long wait_ns;
     if ((rc = gla::current_device_state(&err, &wait_ns)) != GLA_OK) return rc;
@@ -275,8 +293,9 @@ int gla_chunk_fwd_split(const void* q, const void* k, const void* v, const float
     if (rc) return rc;
   }
   // 2. chain the segment states
-  gla::split_scan_kernel<<<(unsigned)((long long)n_seq * H * 4), gla::SPLIT_THREADS, 0, s>>>(
-      U, h0, seg_cu, seg_first, log_lambda, S_in, hT, H);
+  gla::split_scan_kernel<<<(unsigned)((long long)n_seq * H * gla::SCAN_CTAS_PER_STATE), gla::SPLIT_THREADS, 0,
+                           s>>>((const float4*)U, (const float4*)h0, seg_cu, seg_first, log_lambda,
+                                (float4*)S_in, (float4*)hT, H);
   if (cudaGetLastError() != cudaSuccess) return GLA_ERR_LAUNCH;
   // 3. the outputs, each segment from its starting state
   if (aug)
