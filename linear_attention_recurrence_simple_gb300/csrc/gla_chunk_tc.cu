@@ -607,7 +607,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       //   Y: K-major (wide: two 128B panels);  Z, K4, weighted Z4: MN-major
       //   state copy: MN-major [hi | lo] (wide) or K-major (narrow)
       const SDesc dvt = sdesc(sbase + SMM::OFF_VT, SZ_TILE64, 1024, LAYOUT_SW128);
-      int gk = 0;
+      int gk = 0, nu = 0;  // chunks; units with chunks (states only: one U per unit)
       bool stop = C::STATES && warp != 2;  // states only: MMA4 alone
       for (int u = 0; u < n_items && !stop; ++u) {
        const Unit wi = unit_at(u);
@@ -675,17 +675,21 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
           umma_commit(&bars[B_EMPTY + s]);
         } else {
           if (!mbar_wait(&bars[B_VT_FULL], pc, a.wait_ns, abort_flag)) { stop = true; break; }
-          if (!mbar_wait(&bars[B_U_EMPTY], pc ^ 1u, a.wait_ns, abort_flag)) { stop = true; break; }
+          // states only: U accumulates over the unit's chunks, read once after the last
+          const bool u_first = !C::STATES || it == wi.it0, u_last = !C::STATES || it + 1 == wi.it1;
+          if (u_first && !mbar_wait(&bars[B_U_EMPTY], (C::STATES ? (uint32_t)nu & 1u : pc) ^ 1u, a.wait_ns,
+                                    abort_flag)) { stop = true; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma(tmem + C::TM_U, sdesc(st + C::ST_K4, 16384, 1024, LAYOUT_SW128) + (uint32_t)kk * 2048u,
-                 dvt + (uint32_t)kk * 2048u, ID_U, kk > 0);
-          umma_commit(&bars[B_U_FULL]);
+                 dvt + (uint32_t)kk * 2048u, ID_U, kk > 0 || !u_first);
+          if (u_last) umma_commit(&bars[B_U_FULL]);
           umma_commit(&bars[B_VT_EMPTY]);
           umma_commit(&bars[B_EMPTY + s]);
         }
        }
+       if (C::STATES) nu += wi.it1 > wi.it0;
       }
       // All MMAs (and their barrier arrivals) finish before tensor memory is released.
       uint64_t* drain = &bars[B_DRAIN + (warp - 1)];
@@ -868,7 +872,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       uint8_t* zlo = sm + SMM::OFF_VT + SZ_TILE64;
       {  // Z4t row j = w_j z_j; w_j = 0 past the sequence end
         const int j = t;
-        const float wj = j < L ? (C::REVERSE ? pws[j + 1] : pw[L - 1 - j]) : 0.f;
+        float wj = j < L ? (C::REVERSE ? pws[j + 1] : pw[L - 1 - j]) : 0.f;
+        // states only: weights relative to the unit's end (lambda^(len - 1 - position)), so that
+        // MMA4 accumulates the whole unit's update in tensor memory
+        if constexpr (C::STATES) wj *= expf((float)(w.len - c * CHUNK - L) * a.log_lambda[w.h]);
         const float2 f = make_float2(wj, wj);
 #pragma unroll 1
         for (int p = 0; p < 8; ++p) {
@@ -930,7 +937,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       bool aborted = false;
       bool head_pending = false;  // a head piece's state load is in flight (thread r_ = 0)
       int nst = 0;  // full chunks stored through the staging tile
-      int gk = 0, ku = 0;
+      int gk = 0, ku = 0, nu = 0;  // nu: units with chunks (states only: one U per unit)
       for (int u = 0; u < n_items && !aborted; ++u, ++ku) {
        const Unit w = unit_at(u);
        const int h = w.h, col0 = w.tile * TN, nc = w.nc, tbuf = ku & 1;
@@ -1003,11 +1010,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
         const int c = it < w.it0 ? 0 : (C::REVERSE ? nc - 1 - it : it);
         const int L = min(CHUNK, w.len - c * CHUNK);
         if constexpr (DO_STATE) {
-          if (it >= w.it0) {
-            // state <- lambda^L state + U_hi + U_lo
-            if (!warp_wait(&bars[B_U_FULL], pc, a, abort_flag)) { aborted = true; break; }
+          if (it >= w.it0 && (!C::STATES || it + 1 == w.it1)) {
+            // state <- lambda^L state + U_hi + U_lo (states only: once per unit, L = its length)
+            if (!warp_wait(&bars[B_U_FULL], C::STATES ? (uint32_t)nu & 1u : pc, a, abort_flag)) { aborted = true; break; }
             tc_fence_after();
-            const float lamL = pw[L];
+            const float lamL = C::STATES ? expf((float)w.len * a.log_lambda[h]) : pw[L];
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
               uint32_t u[32];  // [0, 16): hi columns, [16, 32): lo columns of this quarter
@@ -1124,6 +1131,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
         }
        }
        if (aborted) break;
+       nu += w.it1 > w.it0;
        if constexpr (DO_STATE) {
          if (C::FWD && prm.s_out) {
            // Forward: each thread stores its final-state row straight from registers (no staging,
@@ -1344,6 +1352,9 @@ cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream) {
 // The forward's final states only (hT; no outputs), one CTA per unit.  Refused (an error) when
 // the states-only kernel did not compile to the register count its role split needs.
 cudaError_t launch_tc_fwd_states(const ChunkArgs& a, cudaStream_t stream) {
+  // packed sequences only: one CTA per whole unit (the states-only weights are relative to the
+  // unit's end, so a unit is never split into pieces)
+  if (!a.cu_seqlens) return cudaErrorInvalidValue;
   ScanParams p;
   p.a = a;
   p.s0 = a.h0;
