@@ -169,6 +169,29 @@ def test_resume_from_final_state(oracle_mod):
     assert _relerr(oa, o[:19]) < 1e-15
 
 
+@pytest.mark.parametrize("cuts", [[19], [1, 2, 30], [10, 20, 30, 40]])
+def test_segment_states_chain_to_the_final_state(oracle_mod, cuts):
+    """The sequence-split forward's algebra: each segment's final state from a ZERO state, U_i,
+    chained as S_in[0] = h0, S_in[i+1] = lam^(L_i) S_in[i] + U_i, gives every segment's starting
+    state (the last link is hT), and the segments run from those states give the unsplit
+    outputs.  Checked against the closed form for hT and the unsplit oracle for the outputs."""
+    q, k, v, h0, ll = _case(16, 50)
+    s = 0.5
+    o, hT = oracle_mod.fwd(q, k, v, ll, s, h0=h0)
+    _, hT_closed = _closed_form(q, k, v, ll, s, h0)
+    lam = np.exp(ll.astype(np.float64))
+    bounds = [0] + list(cuts) + [50]
+    S = np.asarray(h0, np.float64)
+    outs = []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        oi, _ = oracle_mod.fwd(q[a:b], k[a:b], v[a:b], ll, s, h0=S.astype(np.float32))
+        outs.append(oi)
+        _, U = oracle_mod.fwd(q[a:b], k[a:b], v[a:b], ll, s)
+        S = (lam ** (b - a))[None, :, None, None] * S + U
+    assert _relerr(S, hT_closed) < 1e-12
+    assert _relerr(np.concatenate(outs), o) < 1e-6   # (segment starts rounded to fp32 h0)
+
+
 @pytest.mark.parametrize("C", [1, 7, 64, 128, 200])
 def test_chunk_size_invariance(oracle_mod, C):
     q, k, v, h0, ll = _case(7, 200, dk=6, dv=4)
