@@ -294,6 +294,36 @@ def test_backward_matches_finite_differences(oracle_mod, lens):
             assert abs(fd - g[idx]) <= 1e-9 * max(1.0, abs(fd)), (name, idx, fd, g[idx])
 
 
+@pytest.mark.parametrize("lens", [[40], [17, 0, 33, 1]])
+def test_backward_adjoint_identity_random_directions(oracle_mod, lens):
+    """The forward is linear in each of q, k, v, h0 alone (the others fixed), so for a random
+    direction d of one of them the loss L = <dO, o> + <dhT, hT> changes by exactly
+    L(x + d) - L(x) = <dx, d>: the backward is the adjoint of the forward.  Full-size random
+    directions (every element at once), real-valued inputs, longer sequences than the
+    finite-difference pin."""
+    cu = gs.cu_seqlens_of(lens)
+    T, H, dk, dv = int(cu[-1]), 3, 5, 7
+    n = len(lens)
+    x = {"q": _rand(30, 1, (T, H, dk)), "k": _rand(30, 2, (T, H, dk)), "v": _rand(30, 3, (T, H, dv)),
+         "h0": _rand(30, 4, (n, H, dk, dv), 0.5)}
+    dO = _rand(30, 5, (T, H, dv))
+    dhT = _rand(30, 6, (n, H, dk, dv), 0.3)
+    ll = np.log(np.array([0.9, 0.6, 0.99], np.float32))
+    s = 0.37
+    grads = dict(zip(("q", "k", "v", "h0"),
+                     oracle_mod.bwd(x["q"], x["k"], x["v"], ll, s, dO, h0=x["h0"], dhT=dhT, cu_seqlens=cu)))
+    base = _loss(oracle_mod, x["q"], x["k"], x["v"], ll, s, x["h0"], dO, dhT, cu)
+    for i, name in enumerate(("q", "k", "v", "h0")):
+        d = _rand(31, 10 + i, x[name].shape)
+        args = dict(x)
+        shifted = (np.asarray(x[name], np.float64) + np.asarray(d, np.float64)).astype(np.float32)
+        d_eff = shifted.astype(np.float64) - np.asarray(x[name], np.float64)  # the step actually taken
+        args[name] = shifted
+        change = _loss(oracle_mod, args["q"], args["k"], args["v"], ll, s, args["h0"], dO, dhT, cu) - base
+        pred = float(np.sum(np.asarray(grads[name], np.float64) * d_eff))
+        assert abs(change - pred) <= 1e-9 * max(1.0, abs(pred)), (name, change, pred)
+
+
 def test_backward_lambda_one_closed_form(oracle_mod):
     """lambda = 1: G_t = dhT + s sum_{u>=t} q_u dO_u^T, so dk_t = G_t v_t and dv_t = G_t^T k_t;
     dq_t = s (h0 + sum_{j<=t} k_j v_j^T) dO_t."""
