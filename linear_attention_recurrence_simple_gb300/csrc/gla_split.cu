@@ -4,15 +4,17 @@
 // state's advance from chunk to chunk is sequential.  A sequence's chunks therefore split into
 // segments whose work runs in parallel once each segment knows the state it starts from:
 //   1. every segment runs the chunked forward from a zero state, final states only (bf16: the
-//      tensor-core scan's states-only mode, which loads k and v and runs the state update
-//      alone); its final state is U_i = sum_j lambda^(L_i-1-j) k_j v_j^T over its L_i tokens;
+//      tensor-core scan's states-only mode, which loads k and v and accumulates the weighted
+//      products in tensor memory); its final state is U_i = sum_j lambda^(L_i-1-j) k_j v_j^T
+//      over its L_i tokens;
 //   2. a short scan per (sequence, head) chains them: S_in[first] = h0,
 //      S_in[i+1] = lambda^(L_i) S_in[i] + U_i, and hT = lambda^(L_last) S_in[last] + U_last;
 //   3. every segment runs the chunked forward again from S_in[i], writing the outputs.
 // A sequence whose chunks sit on one CTA (one unit per (sequence, head, d_v tile)) then spreads
 // over as many CTAs as it has segments, at the price of a second pass over k and v (in fp32 mode
 // step 1 is the full forward, whose outputs step 3 overwrites).  The host plans the segments from
-// a host copy of the sequence offsets; the device arrays it needs go into the caller's workspace.
+// a host copy of the sequence offsets (seg_chunks = 0: the length from a cost model of the packed
+// forward, or no split at all); the device arrays it needs go into the caller's workspace.
 #include <algorithm>
 #include <vector>
 
