@@ -201,6 +201,15 @@ def test_split_choice_of_segment_length(lib):
     assert choose([128]) == 0         # one chunk
     assert choose([]) == 0
     assert choose([0, 0]) == 0
+    # workspace: a batch the library keeps whole needs no segment states (two fp32 state arrays
+    # per segment otherwise)
+    lens = [2048] * 8
+    cu = np.zeros(9, np.int32)
+    cu[1:] = np.cumsum(lens)
+    cp = cu.ctypes.data_as(P)
+    whole, cut = lib.gla_split_workspace_bytes(cp, 8, 16, 0), lib.gla_split_workspace_bytes(cp, 8, 16, 4)
+    assert 0 < whole < 8 * 16 * 96 * 192 * 4
+    assert cut >= 2 * 4 * 8 * 16 * 96 * 192 * 4   # 4 segments per sequence, U and S_in
     assert lib.gla_split_choose_seg_chunks(None, 1, 16) == NULL
     bad = np.array([0, 300, 200], np.int32)
     assert lib.gla_split_choose_seg_chunks(bad.ctypes.data_as(P), 2, 16) == SHAPE
