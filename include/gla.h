@@ -41,6 +41,9 @@
  *     gla_get_device_error() reports.
  *   - Empty work is valid: n_seq = 0, T = 0 or sequences of length 0 launch nothing for them;
  *     a length-0 sequence gives hT = h0 (zeros if h0 is NULL) and dh0 = dhT.
+ *   - The library looks up the device addresses of its own device variables (the error word,
+ *     the hand-over flags, the array of gla_chunk_fwd_noalloc) once per device and keeps them, so
+ *     resetting a device (cudaDeviceReset) after the library's first call on it is not supported.
  */
 #ifndef GLA_H_
 #define GLA_H_
@@ -223,7 +226,9 @@ int gla_chunk_fwd_split(const void* q, const void* k, const void* v, const float
  * its own pool at start-up: same arguments and results as gla_chunk_fwd, minus the workspace.
  * The longest-first schedule of packed sequences lives instead in a library-owned device array of
  * GLA_NOALLOC_MAX_SEQS int32 (64 KB), kept by every GPU that loads the library until exit.
- *   n_seq > GLA_NOALLOC_MAX_SEQS with cu_seqlens returns GLA_ERR_WORKSPACE (nothing launched).
+ *   Arguments are checked as in gla_chunk_fwd (the same status codes, including GLA_ERR_SHAPE for
+ *   n_seq * H * 96 or the token count at 2^31 or beyond); then n_seq > GLA_NOALLOC_MAX_SEQS with
+ *   cu_seqlens returns GLA_ERR_WORKSPACE (nothing launched).
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress); make
  *   that first call before any stream capture on the device.
  *   Calls share the array: calls that overlap on the GPU (unordered streams) race on it.  Calls
@@ -235,7 +240,9 @@ int gla_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
                           int dtype, gla_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the current device's sticky error word:
- * GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_SHAPE; GLA_ERR_LAUNCH if the stream itself failed. */
+ * GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_SHAPE; GLA_ERR_LAUNCH if the stream itself failed.
+ * There is one word per device, shared by every caller of the library on that device: the first
+ * fault recorded since the last read is kept, and whichever caller reads next sees and clears it. */
 int gla_get_device_error(gla_stream_t stream);
 
 /* Upper bound, in nanoseconds, of every device-side wait on an mbarrier (default 2e9).  A wait

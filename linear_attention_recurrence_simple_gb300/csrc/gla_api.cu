@@ -16,6 +16,8 @@ cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_tc_bwd(const ChunkArgs& a, float* acc_q, float* acc_k, cudaStream_t stream);
 size_t tc_bwd_acc_bytes(long long T_total, int H);
 cudaError_t tc_clear_handover(cudaStream_t stream);
+int check_chunk_sizes(int n_seq, int T, int H, int dk, int dv, int dtype, const int32_t* cu_seqlens,
+                      long long* tokens);
 cudaError_t launch_head_norm_gate(int dtype_f32, const void* o, const void* g, const float* w,
                                   const int32_t* tier, int n_tiers, float eps, void* y, long long rows,
                                   int H, unsigned* err, cudaStream_t stream);
@@ -81,14 +83,9 @@ int device_state(int* dev_out, unsigned** err_out, unsigned long long* wait_out)
 // Checks shared by the forward and backward; fills the sequence/schedule part of `a`.
 int check_chunk_call(int n_seq, int T, int H, int dk, int dv, int dtype, const int32_t* cu_seqlens,
                      void* workspace, size_t ws_bytes, long long* tokens) {
-  if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_DTYPE;
-  if (dk != GLA_DK || dv != GLA_DV) return GLA_ERR_UNSUPPORTED;
-  if (n_seq < 0 || T < 0 || H < 1) return GLA_ERR_SHAPE;
-  *tokens = cu_seqlens ? (long long)T : (long long)n_seq * T;
-  // state rows (sequence, head, d_k row), work units and token coordinates are 32-bit on the device
-  if ((long long)n_seq * H * GLA_DK >= (1ll << 31) || *tokens >= (1ll << 31)) return GLA_ERR_SHAPE;
+  const int rc = gla::check_chunk_sizes(n_seq, T, H, dk, dv, dtype, cu_seqlens, tokens);
+  if (rc) return rc;
   if (cu_seqlens) {
-    if ((uintptr_t)cu_seqlens & 3u) return GLA_ERR_ALIGN;
     if (n_seq > 0) {
       if (!workspace) return GLA_ERR_WORKSPACE;
       if (ws_bytes < gla_workspace_bytes(n_seq, H)) return GLA_ERR_WORKSPACE;
@@ -103,6 +100,20 @@ int to_status(cudaError_t e) { return e == cudaSuccess ? GLA_OK : GLA_ERR_LAUNCH
 }  // namespace
 
 namespace gla {
+// Size, dtype and layout checks of every chunked call (with or without a workspace): dtype,
+// d_k / d_v, non-negative sizes, the 32-bit limits of the device indexing (state rows (sequence,
+// head, d_k row), work units and token coordinates), and the alignment of cu_seqlens.  Sets the
+// token count.
+int check_chunk_sizes(int n_seq, int T, int H, int dk, int dv, int dtype, const int32_t* cu_seqlens,
+                      long long* tokens) {
+  if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_DTYPE;
+  if (dk != GLA_DK || dv != GLA_DV) return GLA_ERR_UNSUPPORTED;
+  if (n_seq < 0 || T < 0 || H < 1) return GLA_ERR_SHAPE;
+  *tokens = cu_seqlens ? (long long)T : (long long)n_seq * T;
+  if ((long long)n_seq * H * GLA_DK >= (1ll << 31) || *tokens >= (1ll << 31)) return GLA_ERR_SHAPE;
+  if (cu_seqlens && ((uintptr_t)cu_seqlens & 3u)) return GLA_ERR_ALIGN;
+  return GLA_OK;
+}
 // Internal accessors for the allocation-free entry point (gla_noalloc.cu); the entry points
 // above do not go through them.
 int current_device_state(unsigned** err, unsigned long long* wait_ns) {

@@ -20,6 +20,8 @@ cudaError_t launch_simt_fwd(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_lpt_order(const int32_t* cu_seqlens, int n_seq, int32_t* order, cudaStream_t stream);
 int current_device_state(unsigned** err, unsigned long long* wait_ns);
+int check_chunk_sizes(int n_seq, int T, int H, int dk, int dv, int dtype, const int32_t* cu_seqlens,
+                      long long* tokens);
 }  // namespace gla
 
 namespace {
@@ -53,21 +55,20 @@ extern "C" int gla_chunk_fwd_noalloc(const void* q, const void* k, const void* v
                                      const float* h0, float scale, void* o, float* hT,
                                      const int32_t* cu_seqlens, int n_seq, int T, int H, int dk, int dv,
                                      int dtype, gla_stream_t stream) {
-  if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_DTYPE;
-  if (dk != GLA_DK || dv != GLA_DV) return GLA_ERR_UNSUPPORTED;
-  if (n_seq < 0 || T < 0 || H < 1) return GLA_ERR_SHAPE;
+  // the same size checks as gla_chunk_fwd (the device indexing is 32-bit)
+  long long tokens = 0;
+  int rc = gla::check_chunk_sizes(n_seq, T, H, dk, dv, dtype, cu_seqlens, &tokens);
+  if (rc) return rc;
   if (cu_seqlens && n_seq > GLA_NOALLOC_MAX_SEQS) return GLA_ERR_WORKSPACE;
   if (n_seq == 0) return GLA_OK;
-  const long long tokens = cu_seqlens ? (long long)T : (long long)n_seq * T;
   if (!log_lambda) return GLA_ERR_NULL;
   if (tokens > 0 && (!q || !k || !v || !o)) return GLA_ERR_NULL;
-  if (cu_seqlens && ((uintptr_t)cu_seqlens & 3u)) return GLA_ERR_ALIGN;
   for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)o,
                         (const void*)h0, (const void*)hT, (const void*)log_lambda})
     if (p && !aligned16(p)) return GLA_ERR_ALIGN;
   unsigned* err;
   unsigned long long wait_ns;
-  int rc = gla::current_device_state(&err, &wait_ns);
+  rc = gla::current_device_state(&err, &wait_ns);
   if (rc) return rc;
 
   gla::ChunkArgs a = {};

@@ -274,3 +274,34 @@ def test_python_binding_rejects_cpu_tensors():
     v = torch.zeros(1, 8, 2, 192)
     with pytest.raises(ValueError):
         gla.gla_chunk_fwd(q, q, v, torch.zeros(2))
+
+
+def test_noalloc_argument_errors(lib):
+    """The allocation-free forward runs the same argument and size checks as gla_chunk_fwd, before
+    anything is launched, including the 32-bit limits of the device indexing."""
+    P = ctypes.c_void_p
+
+    def na(q=A, k=A, v=A, ll=A, h0=None, o=A, hT=None, cu=None, n=2, T=8, H=2, dk=96, dv=192, dt=0):
+        return lib.gla_chunk_fwd_noalloc(P(q), P(k), P(v), P(ll), P(h0), 0.1, P(o), P(hT), P(cu), n, T,
+                                         H, dk, dv, dt, None)
+    assert na(dt=9) == DTYPE
+    assert na(dk=64) == UNSUP
+    assert na(dv=96) == UNSUP
+    assert na(n=-1) == SHAPE
+    assert na(T=-1) == SHAPE
+    assert na(H=0) == SHAPE
+    # n_seq * H * 96 state rows, or the token count, at 2^31 or beyond: refused, as in gla_chunk_fwd
+    assert na(n=1 << 20, T=1, H=32) == SHAPE
+    assert _fwd(lib, n=1 << 20, T=1, H=32) == SHAPE
+    assert na(n=1 << 16, T=1 << 15, H=1) == SHAPE
+    assert _fwd(lib, n=1 << 16, T=1 << 15, H=1) == SHAPE
+    assert na(cu=A, n=1 << 22, T=100, H=8) == SHAPE     # the size check comes before the array limit
+    assert na(q=None) == NULL
+    assert na(ll=None) == NULL
+    assert na(o=None) == NULL
+    assert na(v=MIS) == ALIGN
+    assert na(h0=MIS) == ALIGN
+    assert na(hT=MIS) == ALIGN
+    assert na(cu=A + 2, n=3, T=20) == ALIGN
+    assert na(n=0) == OK
+    assert na(n=0, q=None, k=None, v=None, o=None, ll=None) == OK
