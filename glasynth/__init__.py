@@ -11,11 +11,23 @@ Generator (the "published definition" both sides implement):
   OOPSLA 2014; the finaliser constants are those of Vigna's public-domain C version).
   Output ``i`` (0-based) of the stream seeded with ``key`` is ``mix64(key + (i + 1) * GAMMA)``.
 * Stream key of tensor ``tid`` under run seed ``seed``: ``mix64((seed * 2**16 + tid + 1) * GAMMA)``.
-* Normal variate (approximate): the four 16-bit fields of one 64-bit output are summed
-  (Irwin-Hall with n = 4 discrete uniforms), centred and scaled in fp32:
-  ``x = (float(sum) - 131070.0f) * c``, ``c = fp32(sigma / sqrt(4 * (65536**2 - 1) / 12))``.
-  Every step is exact or a single IEEE fp32 rounding, so host and device agree bit for bit.
-  The distribution has mean 0, standard deviation sigma, and tails cut at 3.46 sigma.
+* Normal variate (Box-Muller; Box and Muller, "A note on the generation of random normal
+  deviates", Ann. Math. Statist. 1958): from one 64-bit output x, a = x >> 32 and b = x mod 2^32,
+  u1 = (a + 1/2) / 2^32 in (0, 1), u2 = b / 2^32 in [0, 1), and
+  ``z = sqrt(-2 ln u1) * cos(2 pi u2)``, ``value = fp32(z * sigma)``.  Only the cosine half of the
+  pair is used, so element i of a tensor is a function of output i alone.  Tails reach
+  sqrt(-2 ln(2^-33)) = 6.77 sigma.  The logarithm and cosine are not library calls but the
+  series below, evaluated in fp64 with IEEE-rounded +, -, x, / and sqrt only, in one fixed
+  order, so that numpy here and the CUDA kernel give the same bits:
+    ln u1 = (e - 32) ln 2 + ln m, with a + 1/2 = 2^e m, m in [1/sqrt 2, sqrt 2], and
+    ln m = 2 t (1 + t^2/3 + t^4/5 + ... + t^20/21), t = (m - 1)/(m + 1), |t| <= 0.1716
+    (the atanh series; truncation below 1e-17 relative);
+    2 pi u2 = n pi/2 + phi with 4 u2 = n + f, n = floor(4 u2 + 1/2), |f| <= 1/2, phi = f pi/2, and
+    cos phi, sin phi by their Taylor series through phi^20/20!, phi^21/21! (|phi| <= pi/4;
+    truncation below 1e-20); cos(2 pi u2) is cos phi, -sin phi, -cos phi, sin phi for n mod 4 =
+    0, 1, 2, 3.  The series coefficients 1/(2j+1) and +-1/k! are correctly rounded doubles (k! is
+    exact in fp64 for k <= 22).  The result agrees with the exact Box-Muller value to about 1e-15
+    relative before the final fp32 rounding.
 * bf16 inputs are the fp32 variates rounded to nearest-even.
 * Uniform integers in [lo, hi]: ``lo + u64 % (hi - lo + 1)``.
 """
@@ -23,12 +35,20 @@ from __future__ import annotations
 
 import numpy as np
 
+import math
+
 GAMMA = 0x9E3779B97F4A7C15
 _M1 = 0xBF58476D1CE4E5B9
 _M2 = 0x94D049BB133111EB
 _MASK = (1 << 64) - 1
-IH4_SD = float(np.sqrt(4.0 * (65536.0 ** 2 - 1.0) / 12.0))
-IH4_MEAN = 131070.0
+
+# fp64 constants of the Box-Muller evaluation (the CUDA kernel uses the same values)
+LN2 = 0.6931471805599453      # ln 2, rounded to double
+PIO2 = 1.5707963267948966     # pi / 2, rounded to double
+SQRT2 = 1.4142135623730951    # sqrt 2, rounded to double
+LOG_C = tuple(1.0 / (2 * j + 1) for j in range(11))                            # atanh series
+COS_C = tuple((-1) ** j / float(math.factorial(2 * j)) for j in range(11))      # cos Taylor
+SIN_C = tuple((-1) ** j / float(math.factorial(2 * j + 1)) for j in range(11))  # sin Taylor
 
 # Tensor ids of the streams.  A config's run seed picks the stream family.
 TID = {
@@ -71,22 +91,54 @@ def u64(seed: int, tid: int, count: int, start: int = 0) -> np.ndarray:
     return u64_at(seed, tid, np.arange(start, start + count, dtype=np.uint64))
 
 
-def ih4_scale(sigma: float) -> np.float32:
-    """The fp32 constant ``c`` that both sides multiply by."""
-    return np.float32(sigma / IH4_SD)
+def _horner(coef, s):
+    p = np.full_like(s, coef[-1])
+    for c in coef[-2::-1]:
+        p = p * s + c
+    return p
 
 
-def _ih4(x: np.ndarray, sigma: float) -> np.ndarray:
-    m = np.uint64(0xFFFF)
-    s = ((x & m) + ((x >> np.uint64(16)) & m) + ((x >> np.uint64(32)) & m)
-         + ((x >> np.uint64(48)) & m))
-    return ((s.astype(np.float32) - np.float32(IH4_MEAN)) * ih4_scale(sigma)).astype(np.float32)
+def ln_u1(a: np.ndarray) -> np.ndarray:
+    """ln((a + 1/2) / 2^32) for 32-bit integers a, by the atanh series (see the module text)."""
+    y = a.astype(np.float64) + 0.5
+    mant, ex = np.frexp(y)                       # y = mant 2^ex, mant in [1/2, 1): exact
+    m = mant * 2.0
+    e = ex.astype(np.int64) - 1
+    big = m > SQRT2
+    m = np.where(big, m * 0.5, m)
+    e = np.where(big, e + 1, e)
+    t = (m - 1.0) / (m + 1.0)
+    lnm = (2.0 * t) * _horner(LOG_C, t * t)
+    return (e - 32).astype(np.float64) * LN2 + lnm
+
+
+def cos_2pi(b: np.ndarray) -> np.ndarray:
+    """cos(2 pi b / 2^32) for 32-bit integers b, by quadrant reduction and Taylor series."""
+    w = b.astype(np.float64) * (2.0 ** -30)      # 4 u2, exact
+    n = np.floor(w + 0.5)
+    phi = (w - n) * PIO2
+    s = phi * phi
+    c = _horner(COS_C, s)
+    sn = phi * _horner(SIN_C, s)
+    q = n.astype(np.int64) & 3
+    return np.where(q == 0, c, np.where(q == 1, -sn, np.where(q == 2, -c, sn)))
+
+
+def _box_muller(x: np.ndarray, sigma: float) -> np.ndarray:
+    a = x >> np.uint64(32)
+    b = x & np.uint64(0xFFFFFFFF)
+    z = np.sqrt(-2.0 * ln_u1(a)) * cos_2pi(b)
+    return (z * float(sigma)).astype(np.float32)
 
 
 def normal(seed: int, tid: int, shape, sigma: float = 1.0, start: int = 0) -> np.ndarray:
-    """fp32 approximate-normal variates, elements ``start ..`` of the stream, in C order."""
+    """fp32 N(0, sigma^2) variates (Box-Muller), elements ``start ..`` of the stream, in C order."""
     count = int(np.prod(shape, dtype=np.int64))
-    return _ih4(u64(seed, tid, count, start), sigma).reshape(shape)
+    out = np.empty(count, np.float32)
+    step = 1 << 22                               # bounded temporaries for large tensors
+    for i in range(0, count, step):
+        out[i:i + step] = _box_muller(u64(seed, tid, min(step, count - i), start + i), sigma)
+    return out.reshape(shape)
 
 
 def normal_rows(seed: int, tid: int, row_shape, rows, sigma: float = 1.0) -> np.ndarray:
@@ -96,7 +148,7 @@ def normal_rows(seed: int, tid: int, row_shape, rows, sigma: float = 1.0) -> np.
     row_len = int(np.prod(row_shape, dtype=np.int64))
     rows = np.asarray(rows, dtype=np.uint64)
     idx = rows[:, None] * np.uint64(row_len) + np.arange(row_len, dtype=np.uint64)[None, :]
-    return _ih4(u64_at(seed, tid, idx), sigma).reshape((len(rows),) + tuple(row_shape))
+    return _box_muller(u64_at(seed, tid, idx), sigma).reshape((len(rows),) + tuple(row_shape))
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:

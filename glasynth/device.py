@@ -12,7 +12,7 @@ import threading
 
 import torch
 
-from . import ih4_scale, stream_key
+from . import stream_key
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "synth_gen.cu")
@@ -38,7 +38,7 @@ def _load():
             lib = ctypes.CDLL(build())
             lib.glasynth_fill_normal.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong,
                                                  ctypes.c_ulonglong, ctypes.c_ulonglong,
-                                                 ctypes.c_float, ctypes.c_void_p]
+                                                 ctypes.c_double, ctypes.c_void_p]
             lib.glasynth_fill_normal.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -51,7 +51,7 @@ def fill_normal_(t: torch.Tensor, seed: int, tid: int, sigma: float = 1.0, start
     with torch.cuda.device(t.device):
         rc = _load().glasynth_fill_normal(
             ctypes.c_void_p(t.data_ptr()), int(t.dtype == torch.bfloat16), t.numel(), int(start),
-            stream_key(seed, tid), float(ih4_scale(sigma)),
+            stream_key(seed, tid), float(sigma),
             ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream))
     if rc:
         raise RuntimeError("glasynth_fill_normal launch failed")

@@ -10,8 +10,8 @@ any sampled slice regenerable bit-for-bit on the host for the oracle.
             bf16 q, k, v as in `layer`; seed 3
   bwd       `layer` shapes; dO ~ N(0,1) bf16, dhT ~ N(0, 0.01) fp32; seed 4
 
-"N(0, s)" is read with s the standard deviation; the variates are the Irwin-Hall(4)
-approximation documented in :mod:`glasynth`.  No part of the GLA arithmetic is here.
+"N(0, s)" is read with s the standard deviation; the variates are Box-Muller normals (tails
+to 6.77 sigma), documented in :mod:`glasynth`.  No part of the GLA arithmetic is here.
 """
 from __future__ import annotations
 

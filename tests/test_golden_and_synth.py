@@ -41,8 +41,42 @@ def test_generator_moments():
     x = gs.normal(0, 1, (1 << 20,), sigma=0.1).astype(np.float64)
     assert abs(x.mean()) < 1e-3
     assert abs(x.std() - 0.1) < 1e-3
-    # Irwin-Hall(4) support: |x| <= 2 * 65535 * c
-    assert np.max(np.abs(x)) <= 3.47 * 0.1
+    z = x / 0.1
+    assert abs(np.mean(z ** 3)) < 0.02            # symmetric
+    assert abs(np.mean(z ** 4) - 3.0) < 0.05      # normal kurtosis (Irwin-Hall(4) would give 2.7)
+
+
+def test_generator_is_gaussian_in_distribution_and_tails():
+    """Empirical CDF against the normal CDF (Kolmogorov-Smirnov distance; at n = 2^22 the 1 % point
+    is 1.63 / sqrt(n) = 8e-4), and the tail mass beyond 4 and 5 sigma against 2 (1 - Phi(x)).
+    A generator with cut tails (Irwin-Hall(4) ends at 3.46 sigma) fails the tail checks."""
+    import math
+    n = 1 << 22
+    z = np.sort(gs.normal(3, 7, (n,)).astype(np.float64))
+    phi = 0.5 * (1.0 + np.array([math.erf(t / math.sqrt(2.0)) for t in z[::64]]))
+    ecdf_hi = (np.arange(0, n, 64) + 1) / n
+    ecdf_lo = np.arange(0, n, 64) / n
+    ks = max(np.max(ecdf_hi - phi), np.max(phi - ecdf_lo))
+    assert ks < 1.63 / math.sqrt(n) + 64 / n, ks
+    for t, lo, hi in ((4.0, 0.7, 1.3), (5.0, 0.3, 2.2)):
+        expect = n * math.erfc(t / math.sqrt(2.0))
+        got = int(np.sum(np.abs(z) > t))
+        assert lo * expect <= got <= hi * expect, (t, got, expect)
+    assert np.max(np.abs(z)) > 5.0
+
+
+def test_generator_series_against_library_log_and_cos():
+    """The series-evaluated logarithm and cosine (written so that host and device agree bit for
+    bit) against numpy's log and cos, and at points where the value is exact."""
+    a = np.concatenate([np.arange(0, 1 << 32, 65521, dtype=np.uint64),
+                        np.array([0, 1, 2, (1 << 31) - 1, 1 << 31, (1 << 32) - 1], np.uint64)])
+    ref = np.log((a.astype(np.float64) + 0.5) / 2.0 ** 32)
+    assert np.max(np.abs(gs.ln_u1(a) - ref) / np.abs(ref)) < 2e-15
+    c = gs.cos_2pi(a)
+    assert np.max(np.abs(c - np.cos(2.0 * np.pi * (a.astype(np.float64) / 2.0 ** 32)))) < 2e-15
+    q = np.array([0, 1 << 30, 1 << 31, 3 << 30], np.uint64)   # angles 0, pi/2, pi, 3 pi/2
+    assert list(gs.cos_2pi(q)) == [1.0, 0.0, -1.0, 0.0]
+    assert gs.ln_u1(np.array([(1 << 31) - 1], np.uint64))[0] == pytest.approx(np.log(0.5), abs=3e-10)
 
 
 def test_splitmix64_reference_values():
