@@ -126,7 +126,7 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
 
 
-def _need(t: torch.Tensor, name: str, dtype=None, device=None):
+def _need(t: torch.Tensor, name: str, dtype=None, device=None, numel=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
@@ -137,6 +137,8 @@ def _need(t: torch.Tensor, name: str, dtype=None, device=None):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if device is not None and t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} has {t.numel()} elements, expected {numel}")
 
 
 def _layout(q, k, v, cu_seqlens):
@@ -202,11 +204,11 @@ def gla_chunk_fwd(q, k, v, log_lambda, scale=None, h0=None, cu_seqlens=None,
             raise ValueError("h0 must be [n_seq, H, 96, 192]")
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=dev)
-    _need(o, "o", v.dtype, dev)
+    _need(o, "o", v.dtype, dev, v.numel())
     if output_final_state and hT is None:
         hT = torch.empty((n_seq, H, DK, DV), dtype=torch.float32, device=dev)
     if hT is not None:
-        _need(hT, "hT", torch.float32, dev)
+        _need(hT, "hT", torch.float32, dev, n_seq * H * DK * DV)
     ws, ws_bytes = _workspace(cu_seqlens, n_seq, H, dev, workspace)
     s = float(DK ** -0.5) if scale is None else float(scale)
     if aug is not None:
@@ -244,12 +246,12 @@ def gla_chunk_fwd_noalloc(q, k, v, log_lambda, scale=None, h0=None, cu_seqlens=N
         _need(cu_seqlens, "cu_seqlens", torch.int32, dev)
     n_seq, T, H = _layout(q, k, v, cu_seqlens)
     if h0 is not None:
-        _need(h0, "h0", torch.float32, dev)
+        _need(h0, "h0", torch.float32, dev, n_seq * H * DK * DV)
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=dev)
-    _need(o, "o", v.dtype, dev)
+    _need(o, "o", v.dtype, dev, v.numel())
     if hT is not None:
-        _need(hT, "hT", torch.float32, dev)
+        _need(hT, "hT", torch.float32, dev, n_seq * H * DK * DV)
     s = float(DK ** -0.5) if scale is None else float(scale)
     with torch.cuda.device(dev):
         rc = lib.gla_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), s,
@@ -260,8 +262,10 @@ def gla_chunk_fwd_noalloc(q, k, v, log_lambda, scale=None, h0=None, cu_seqlens=N
 
 
 def gla_chunk_bwd(q, k, v, log_lambda, dO, scale=None, h0=None, dhT=None, cu_seqlens=None,
-                  need_dh0: bool = True, workspace=None):
-    """Chunked backward.  Returns ``(dq, dk, dv, dh0)`` (``dh0`` None if not requested)."""
+                  need_dh0: bool = True, workspace=None, dq=None, dk=None, dv=None, dh0=None):
+    """Chunked backward.  Returns ``(dq, dk, dv, dh0)`` (``dh0`` None if not requested).
+    ``dq``, ``dk``, ``dv``, ``dh0``: optional preallocated outputs (contiguous, sized like q, k, v
+    and [n_seq, H, 96, 192] fp32)."""
     lib = load_library()
     dev = q.device
     dt = _dtype_code(q)
@@ -278,10 +282,15 @@ def gla_chunk_bwd(q, k, v, log_lambda, dO, scale=None, h0=None, dhT=None, cu_seq
             _need(t, name, torch.float32, dev)
             if t.shape != (n_seq, H, DK, DV):
                 raise ValueError(f"{name} must be [n_seq, H, 96, 192]")
-    dq = torch.empty(q.shape, dtype=q.dtype, device=dev)
-    dk = torch.empty(k.shape, dtype=k.dtype, device=dev)
-    dv = torch.empty(v.shape, dtype=v.dtype, device=dev)
-    dh0 = torch.empty((n_seq, H, DK, DV), dtype=torch.float32, device=dev) if need_dh0 else None
+    dq = torch.empty(q.shape, dtype=q.dtype, device=dev) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=k.dtype, device=dev) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=v.dtype, device=dev) if dv is None else dv
+    if dh0 is None and need_dh0:
+        dh0 = torch.empty((n_seq, H, DK, DV), dtype=torch.float32, device=dev)
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _need(t, name, q.dtype, dev, ref.numel())
+    if dh0 is not None:
+        _need(dh0, "dh0", torch.float32, dev, n_seq * H * DK * DV)
     need = gla_bwd_workspace_bytes(n_seq, T, H, cu_seqlens is not None, dt)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -322,7 +331,7 @@ def gla_decode_step(q, k, v, log_lambda, state, scale=None, slot=None, o=None, a
             raise ValueError("slot must be [N]")
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=dev)
-    _need(o, "o", v.dtype, dev)
+    _need(o, "o", v.dtype, dev, v.numel())
     s = float(DK ** -0.5) if scale is None else float(scale)
     if aug is not None:
         _need(aug, "aug", torch.float32, dev)
@@ -388,7 +397,7 @@ def gla_chunk_fwd_split(q, k, v, log_lambda, lengths, seg_chunks=0, scale=None, 
     if log_lambda.numel() != H:
         raise ValueError("log_lambda must have H entries")
     if h0 is not None:
-        _need(h0, "h0", torch.float32, dev)
+        _need(h0, "h0", torch.float32, dev, n_seq * H * DK * DV)
         if h0.shape != (n_seq, H, DK, DV):
             raise ValueError("h0 must be [n_seq, H, 96, 192]")
     if aug is not None:
@@ -397,11 +406,11 @@ def gla_chunk_fwd_split(q, k, v, log_lambda, lengths, seg_chunks=0, scale=None, 
             raise ValueError("aug must be [H, 96]")
     if o is None:
         o = torch.empty(v.shape, dtype=v.dtype, device=dev)
-    _need(o, "o", v.dtype, dev)
+    _need(o, "o", v.dtype, dev, v.numel())
     if output_final_state and hT is None:
         hT = torch.empty((n_seq, H, DK, DV), dtype=torch.float32, device=dev)
     if hT is not None:
-        _need(hT, "hT", torch.float32, dev)
+        _need(hT, "hT", torch.float32, dev, n_seq * H * DK * DV)
     cu_p = cu.ctypes.data_as(ctypes.c_void_p)
     need = lib.gla_split_workspace_bytes(cu_p, n_seq, H, int(seg_chunks))
     if need == 0 and n_seq > 0:

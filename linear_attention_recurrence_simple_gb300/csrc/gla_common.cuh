@@ -53,11 +53,16 @@ __device__ __forceinline__ void raise_error(unsigned* word, unsigned code) {
   atomicCAS(word, 0u, code);
 }
 
-// Token range [begin, end) of sequence n.
+// Token range [begin, end) of sequence n.  Packed offsets are read on the device, so they are
+// clamped here to 0 <= begin <= end <= T (the packed total), which keeps every access inside the
+// caller's buffers whatever the offsets hold; an offset that needed clamping (decreasing, negative
+// or past T) records ERR_SHAPE in the error word.
 __device__ __forceinline__ void seq_range(const ChunkArgs& a, int n, long long& begin, long long& end) {
   if (a.cu_seqlens) {
-    begin = a.cu_seqlens[n];
-    end = a.cu_seqlens[n + 1];
+    const long long b = a.cu_seqlens[n], e = a.cu_seqlens[n + 1];
+    begin = min(max(b, 0ll), (long long)a.T);
+    end = min(max(e, begin), (long long)a.T);
+    if (begin != b || end != e) raise_error(a.err, ERR_SHAPE);
   } else {
     begin = (long long)n * a.T;
     end = begin + a.T;

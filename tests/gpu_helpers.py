@@ -15,19 +15,38 @@ def half_ulp_bf16(ref):
     return np.where(a > 0, np.exp2(e - 8), 0.0)
 
 
+class RelErr(float):
+    """The bounded figure (a float, compared against the bar) that also carries the raw
+    max |x - ref| / rms(ref) without the half-ulp allowance; formatting shows both, so a
+    failure message tells how far the plain error sits from the bar."""
+
+    def __new__(cls, value, raw):
+        obj = super().__new__(cls, value)
+        obj.raw = raw
+        return obj
+
+    def __format__(self, spec):
+        return f"{float(self):{spec or '.3e'}} (raw {self.raw:{spec or '.3e'}})"
+
+    def __repr__(self):
+        return format(self, ".3e")
+
+
 def rel_err(x, ref, bf16_out=False):
     """max |x - ref| / rms(ref).  For outputs stored in bf16 (``bf16_out``), each element's error
     is first reduced by half a bf16 ulp of ref: the rounding that even the exact answer takes
-    when stored in the output's format, which the bound is not meant to measure."""
+    when stored in the output's format, which the bound is not meant to measure.  The result
+    (a float) also carries the raw figure, shown when formatted."""
     x = np.asarray(x, np.float64)
     ref = np.asarray(ref, np.float64)
     if ref.size == 0:
-        return 0.0
-    rms = np.sqrt(np.mean(ref ** 2))
+        return RelErr(0.0, 0.0)
+    rms = max(float(np.sqrt(np.mean(ref ** 2))), 1e-30)
     d = np.abs(x - ref)
+    raw = float(np.max(d) / rms)
     if bf16_out:
         d = np.maximum(d - half_ulp_bf16(ref), 0.0)
-    return float(np.max(d) / max(rms, 1e-30))
+    return RelErr(float(np.max(d) / rms), raw)
 
 
 def host_chunk_inputs(seed, lengths, H, bf16, with_h0, packed, log_lambda=None, grad=False,
