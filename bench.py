@@ -147,12 +147,14 @@ class Dist:
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.device = "cpu"
 
     def init(self, backend):
         if self.world > 1:
             import torch.distributed as dist
             dist.init_process_group(backend=backend)
             self.pg = dist
+            self.device = "cuda" if backend == "nccl" else "cpu"
 
     def barrier(self):
         if self.pg:
@@ -161,8 +163,7 @@ class Dist:
     def max(self, x):
         if not self.pg:
             return x
-        t = self.torch.tensor([x], dtype=self.torch.float64,
-                              device="cuda" if self.torch.cuda.is_available() else "cpu")
+        t = self.torch.tensor([x], dtype=self.torch.float64, device=self.device)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
@@ -205,17 +206,32 @@ def timed(torch, dist, fn, steps, warmup):
     return region, per_call
 
 
+# GB300 datasheet figures (nominal, per GPU): HBM3e bandwidth and dense bf16 tensor throughput.
+# The roofline's `frac` is against the measured copy bandwidth / cuBLAS throughput of
+# MEASURED_PEAKS.json; `frac_of_datasheet` is the same achieved figure against these.
+DATASHEET = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
+
+
 def roofline(bytes_, flops, secs, peaks, bound="hbm"):
     if bound == "hbm":
         ach = bytes_ / secs / 1e9
         return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                "peak_source": peaks["source"] + " copy bandwidth",
+                "frac_of_datasheet": round(ach / DATASHEET["hbm_gbs"], 4),
+                "datasheet_peak": DATASHEET["hbm_gbs"],
                 "algorithmic_bytes": int(bytes_), "flops": int(flops),
-                "tensor_frac": round(flops / secs / 1e12 / peaks["bf16_tflops"], 4),
-                "peak_source": peaks["source"]}
+                "tensor_frac": round(flops / secs / 1e12 / peaks["bf16_tflops"], 4)}
     ach = flops / secs / 1e12
     return {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
-            "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": None}
+            "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": None,
+            "frac_of_datasheet": round(ach / DATASHEET["bf16_tflops"], 4),
+            "datasheet_peak": DATASHEET["bf16_tflops"]}
+
+
+def bwd_bytes(tokens, n_seq):
+    """q, k, v, dO read and dq, dk, dv written once each (bf16), plus dhT read and dh0 written."""
+    return tokens * H * (4 * DK + 3 * DV) * 2 + 2 * n_seq * H * DK * DV * 4
 
 
 def fwd_bytes(tokens, n_seq, with_h0):
@@ -379,12 +395,12 @@ def bench_bwd(torch, gla, wl, dist, args, peaks):
     region, per_call = timed(torch, dist, fn, args.steps, args.warmup)
     region, per_call = dist.max(region), dist.max(per_call)
     tokens = w.tokens
-    byts = tokens * H * (4 * DK * 2 + 4 * DV * 2) + 2 * w.n_seq * H * DK * DV * 4
+    byts = bwd_bytes(tokens, w.n_seq)
     flops = tokens * H * 2 * (128 * DV + 128 * DK + 2 * DK * DV      # dq scan
                               + 128 * DV + 128 * DK + 128 * DK + 128 * DV + 4 * DK * DV)  # dk, dv scan
     res = {"workload": w.name, "tokens": tokens, "ms_per_step": region,
            "value": tokens * dist.world / (region / 1e3), "unit": "tokens/s",
-           "roofline": roofline(byts, flops, region / 1e3, peaks), "launches_per_step": 4}
+           "roofline": roofline(byts, flops, region / 1e3, peaks), "launches_per_step": 5}
     del g
     return res
 
@@ -495,6 +511,50 @@ def run_reference(args):
     return 0
 
 
+def free_port():
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def launch_ranks(args):
+    """`--gpus N` without a launcher around it: run this script as N ranks, one per GPU, under
+    torch.distributed.run on 127.0.0.1 (the same command line a scaling driver uses).  Returns
+    the launcher's exit status, or None when this process is already a rank (or N = 1)."""
+    world = os.environ.get("WORLD_SIZE")
+    if world is not None:
+        if int(world) != args.gpus:
+            raise SystemExit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}: the launcher and "
+                             f"the flag disagree on the number of ranks")
+        return None
+    if args.gpus <= 1:
+        return None
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+           f"--master-port={free_port()}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
+def run_launcher_check(args):
+    """`--launcher-check`: exercises the rank launch, the barrier and the max-over-ranks timing on
+    CPU ranks (gloo) with no GPU and no GLA work; prints a line that says so (no metric value).
+    Used by the CPU tests of the multi-rank path."""
+    import torch
+    dist = Dist(torch)
+    dist.init("gloo")
+    dist.barrier()
+    t0 = time.perf_counter()
+    time.sleep(0.001 * (dist.rank + 1))
+    dist.barrier()
+    secs = dist.max(time.perf_counter() - t0)
+    if dist.rank == 0:
+        print(json.dumps({"launcher_check": True, "n_gpus": dist.world, "value": None,
+                          "max_rank_seconds": secs}), flush=True)
+    dist.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -507,10 +567,16 @@ def main():
     ap.add_argument("--decode-seqs", type=int, default=1280,
                     help="sequences in the decode pool (1280 = the measured workload)")
     ap.add_argument("--decode-layers", type=int, default=24)
+    ap.add_argument("--launcher-check", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         return run_reference(args)
+    rc = launch_ranks(args)
+    if rc is not None:
+        return rc
+    if args.launcher_check:
+        return run_launcher_check(args)
 
     import torch
 
@@ -554,7 +620,7 @@ def main():
             "metric": METRIC, "value": f.get("value"), "unit": "tokens/s", "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": f.get("ms_per_step"),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic: seeded SplitMix64 / Irwin-Hall(4) normal inputs, no dataset",
+            "data": "synthetic: seeded SplitMix64 / Box-Muller normal inputs, no dataset",
             "config": {"workload": f.get("workload"), "B": 8, "T": 2048, "H": H, "dk": DK, "dv": DV,
                        "chunk": 128, "accumulate": "fp32 state and accumulation",
                        "l2": "no flush: inputs of each call (201 MB) exceed the 129 MB L2",
@@ -564,6 +630,13 @@ def main():
             "clocks": clocks, "cpu_baseline": cpu, "device_error": err,
             "rows": {k: v for k, v in out.items() if k != "fwd"},
         }
+        # one compact entry per row, last on the line (ms per step, tokens/s, bytes counted,
+        # fraction of the measured peak and of the datasheet peak)
+        line["rows_summary"] = {
+            k: {"ms": round(v["ms_per_step"], 4), "tok_s": round(v["value"], 1),
+                "bytes": v["roofline"].get("algorithmic_bytes"), "frac": v["roofline"]["frac"],
+                "frac_ds": v["roofline"].get("frac_of_datasheet")}
+            for k, v in out.items()}
         print(json.dumps(line), flush=True)
     dist.close()
     return 0

@@ -255,7 +255,8 @@ double round_to_bf16(double x) {
 // halves the state traffic).  The update and the readout are those of oracle_decode_step,
 // computed from the stored (bf16-valued) state; the readout uses the updated state before it
 // is rounded, and the stored state is the update rounded to bf16.  state holds bf16 values in
-// fp64 and is updated in place; aug may be null (else the self-augmentation term is added).
+// fp64 and is updated in place.  (The self-augmentation term does not touch the state: a
+// caller adds oracle_self_aug's output to o.)
 int oracle_decode_step_bf16_state(const float* q, const float* k, const float* v, const float* log_lambda,
                                   double scale, double* state, double* o, int N, int H, int dk, int dv) {
   if (N < 0 || H <= 0 || dk <= 0 || dv <= 0) return -1;

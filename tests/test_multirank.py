@@ -43,3 +43,34 @@ def test_two_rank_max_and_aggregate():
     assert res[0][0] == res[1][0] == 2.5                       # max over ranks
     assert res[0][1] == pytest.approx(2 * 16384 / 2.5e-3)      # summed tokens / slowest time
     assert {res[0][2], res[1][2]} == {0, 1} and res[0][3] == 2
+
+
+def _bench_cmd(*extra):
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    return [sys.executable, os.path.join(root, "bench.py"), *extra], root
+
+
+def test_bench_gpus_flag_launches_that_many_ranks():
+    """`bench.py --gpus 2` with no launcher around it starts two ranks itself (torch.distributed.run
+    on 127.0.0.1); the launcher check runs the barrier and the max over ranks on CPU (gloo) and
+    reports the world size it saw."""
+    import json
+    import subprocess
+    cmd, root = _bench_cmd("--gpus", "2", "--launcher-check")
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=240, env=env, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout        # rank 0 alone prints
+    rec = json.loads(lines[0])
+    assert rec["n_gpus"] == 2 and rec["launcher_check"] is True
+    assert rec["max_rank_seconds"] >= 0.002  # the slower rank's time
+
+
+def test_bench_refuses_disagreeing_world_size():
+    import subprocess
+    cmd, root = _bench_cmd("--gpus", "2", "--launcher-check")
+    env = dict(os.environ, WORLD_SIZE="3", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=120, env=env, cwd=root)
+    assert r.returncode != 0 and "disagree" in r.stderr
