@@ -405,9 +405,12 @@ def bench_bwd(torch, gla, wl, dist, args, peaks):
     return res
 
 
-def bench_decode(torch, gla, wl, dist, args, peaks, aug=False, bf16_state=False):
+def bench_decode(torch, gla, wl, dist, args, peaks, aug=False, bf16_state=False, norm_gate=False):
     """``aug``: the step with the self-augmentation copy of v (gla_decode_step_aug), 16 steps;
-    ``bf16_state``: the same pool stored in bf16 (gla_decode_step_bf16_state), 16 steps."""
+    ``bf16_state``: the same pool stored in bf16 (gla_decode_step_bf16_state), 16 steps;
+    ``norm_gate``: the step with the per-tier Head RMSNorm + SiLU gate fused into its epilogue
+    (gla_decode_step_norm_gate: y instead of o, a gate stream g per step, four tiers of four
+    heads), 16 steps."""
     import glasynth as gs
     w = wl.DecodeWorkload(seqs=args.decode_seqs, layers=args.decode_layers)
     state = w.device_state()
@@ -418,26 +421,39 @@ def bench_decode(torch, gla, wl, dist, args, peaks, aug=False, bf16_state=False)
     steps = [w.device_step(s) for s in range(min(w.steps, 4))]  # 4 distinct token sets, cycled
     o = torch.empty((w.N, H, DV), dtype=torch.bfloat16, device="cuda")
     it = [0]
+    if norm_gate:
+        from glasynth.device import normal as dnormal
+        gs_ = [dnormal((w.N, H, DV), 12, 40 + i, 2.0) for i in range(len(steps))]
+        wt = (1.0 + torch.from_numpy(gs.normal(12, 41, (4, DV), 0.3))).cuda()
+        tier = (torch.arange(H, dtype=torch.int32) // 4).cuda()
 
     def fn():
-        b = steps[it[0] % len(steps)]
+        i = it[0] % len(steps)
+        b = steps[i]
         it[0] += 1
-        gla.gla_decode_step(b["q"], b["k"], b["v"], ll, state, w.scale, o=o, aug=a)
-    n = 16 if (aug or bf16_state) else w.steps
+        if norm_gate:
+            gla.gla_decode_step_norm_gate(b["q"], b["k"], b["v"], ll, state, gs_[i], wt, tier, scale=w.scale,
+                                          y=o)
+        else:
+            gla.gla_decode_step(b["q"], b["k"], b["v"], ll, state, w.scale, o=o, aug=a)
+    n = 16 if (aug or bf16_state or norm_gate) else w.steps
     region, per_call = timed(torch, dist, fn, n, max(args.warmup, 3))
     region, per_call = dist.max(region), dist.max(per_call)
     state_bytes = 2 * w.N * H * DK * DV * (2 if bf16_state else 4)
     io_bytes = w.N * H * (2 * DK * 2 + 2 * DV * 2)
     res = {"workload": f"decode {w.seqs} seqs x {w.layers} layers H=16 "
                        + ("bf16" if bf16_state else "fp32") + " state bf16 io"
-                       + (" + self-augmentation" if aug else ""), "steps": n,
+                       + (" + self-augmentation" if aug else "")
+                       + (" + fused head RMSNorm/SiLU gate (y out)" if norm_gate else ""), "steps": n,
            "ms_per_step": region,
            "value": w.seqs * dist.world / (region / 1e3), "unit": "tokens/s",
            "token": "one new token per sequence through all 24 layers",
            "roofline": roofline(state_bytes, 2 * 2 * w.N * H * DK * DV, region / 1e3, peaks),
            "io_bytes_outside_roofline": io_bytes, "launches_per_step": 1}
     res["roofline"]["algorithmic_bytes_note"] = ("bf16" if bf16_state else "fp32") + " state read + write per step"
-    res["roofline"]["traffic"] = None if (aug or bf16_state) else profiled_traffic("decode", w.N * H)
+    if norm_gate:
+        res["io_bytes_outside_roofline"] += w.N * H * DV * 2
+    res["roofline"]["traffic"] = None if (aug or bf16_state or norm_gate) else profiled_traffic("decode", w.N * H)
     del state, steps, o, a
     return res
 
@@ -562,7 +578,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--rows", default="fwd,bwd,varlen,decode,fwd_aug,norm_gate,decode_aug,decode_bf16_state,"
-                    "fwd_split")
+                    "fwd_split,decode_norm_gate")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-seqs", type=int, default=1280,
                     help="sequences in the decode pool (1280 = the measured workload)")
@@ -609,6 +625,8 @@ def main():
             out["decode_aug"] = bench_decode(torch, gla, wl, dist, args, peaks, aug=True)
         if "decode_bf16_state" in rows:
             out["decode_bf16_state"] = bench_decode(torch, gla, wl, dist, args, peaks, bf16_state=True)
+        if "decode_norm_gate" in rows:
+            out["decode_norm_gate"] = bench_decode(torch, gla, wl, dist, args, peaks, norm_gate=True)
     err = gla.gla_get_device_error()
     clocks = sampler.summary()
     cpu = None

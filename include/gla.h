@@ -173,6 +173,28 @@ int gla_head_norm_gate(const void* o, const void* g, const float* weight, const 
                        int n_tiers, float eps, void* y, long long rows, int H, int dv, int dtype,
                        gla_stream_t stream);
 
+/* One decode step whose readout goes straight through the per-tier Head RMSNorm and the SiLU
+ * output gate ("Beyond the KV cache", section "i14 and the Laplace 3B architecture": the per-head
+ * outputs pass through a Head RMSNorm within each decay tier, then the SiLU(g_t) gate; heads are
+ * grouped into tiers that share a norm, section "Decay schedule's reach").  The state update is
+ * that of gla_decode_step (aug NULL) or gla_decode_step_aug (aug non-NULL) on an fp32 pool; the
+ * readout o (fp32, before any rounding) is not stored but normalised and gated in the same
+ * kernel, and
+ *     y[n,h,:] = o / sqrt(mean_c o_c^2 + eps) * weight[tier[h],:] * SiLU(g[n,h,:])
+ * is written, as gla_head_norm_gate would compute from o.
+ *   g            [N, H, 192] gate stream, dtype `dtype`, 16-byte aligned.
+ *   weight       [n_tiers, 192] fp32, 16-byte aligned; tier [H] int32 (4-byte aligned).  A tier
+ *                outside [0, n_tiers) leaves that head's y untouched (the state is still updated)
+ *                and records GLA_ERR_SHAPE in the device error word.
+ *   eps          >= 0; n_tiers >= 1 (else GLA_ERR_SHAPE).
+ *   y            [N, H, 192] output, dtype `dtype`; may not alias g.
+ * Every other argument as in gla_decode_step_aug. */
+int gla_decode_step_norm_gate(const void* q, const void* k, const void* v, const float* log_lambda,
+                              float scale, const float* aug, float* state, const int32_t* slot,
+                              int pool_rows, const void* g, const float* weight, const int32_t* tier,
+                              int n_tiers, float eps, void* y, int N, int H, int dk, int dv, int dtype,
+                              gla_stream_t stream);
+
 /* One decode step on a state pool stored in bf16 (no counterpart in the paper: a storage
  * variant that halves the state stream).  As gla_decode_step (aug NULL) or gla_decode_step_aug
  * (aug non-NULL), with `state` a [pool_rows, H, 96, 192] bf16 pool: each state is widened to

@@ -30,6 +30,7 @@ GLA_BF16, GLA_F32 = 0, 1
 EXPORTS = ("gla_workspace_bytes", "gla_bwd_workspace_bytes", "gla_chunk_fwd", "gla_chunk_bwd",
            "gla_decode_step", "gla_chunk_fwd_aug", "gla_decode_step_aug", "gla_head_norm_gate",
            "gla_decode_step_bf16_state", "gla_split_workspace_bytes", "gla_chunk_fwd_split",
+           "gla_decode_step_norm_gate",
            "gla_split_choose_seg_chunks", "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
            "gla_status_string")
 NOALLOC_MAX_SEQS = 16384
@@ -84,6 +85,8 @@ def load_library(build: bool = True):
         lib.gla_head_norm_gate.argtypes = [P, P, P, P, I, F, P, ctypes.c_longlong, I, I, I, P]
         lib.gla_decode_step_bf16_state.argtypes = [P, P, P, P, F, P, P, P, I, P, I, I, I, I, I, P]
         lib.gla_decode_step_bf16_state.restype = I
+        lib.gla_decode_step_norm_gate.argtypes = [P, P, P, P, F, P, P, P, I, P, P, P, I, F, P, I, I, I, I, I, P]
+        lib.gla_decode_step_norm_gate.restype = I
         lib.gla_split_workspace_bytes.argtypes = [P, I, I, I]
         lib.gla_split_workspace_bytes.restype = Z
         lib.gla_chunk_fwd_split.argtypes = [P, P, P, P, P, F, P, P, P, P, I, I, I, I, I, I, I, P, Z, P]
@@ -353,6 +356,47 @@ def gla_decode_step(q, k, v, log_lambda, state, scale=None, slot=None, o=None, a
                                          dt, _stream(dev))
     _check(rc, "gla_decode_step" if aug is None else "gla_decode_step_aug")
     return o
+
+
+def gla_decode_step_norm_gate(q, k, v, log_lambda, state, g, weight, tier, scale=None, slot=None,
+                              eps=1e-6, y=None, aug=None):
+    """One decode step (fp32 state pool, updated in place) whose readout goes straight through the
+    per-tier Head RMSNorm and the SiLU(g) gate: returns ``y [N, H, 192]``,
+    ``y = o / sqrt(mean(o^2) + eps) * weight[tier[h]] * SiLU(g)`` with o the step's readout (plus
+    the self-augmentation copy when ``aug`` is given).  ``g`` ``[N, H, 192]`` (dtype of q),
+    ``weight`` fp32 ``[n_tiers, 192]``, ``tier`` int32 ``[H]``."""
+    lib = load_library()
+    dev = q.device
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, q.dtype, dev)
+    _need(log_lambda, "log_lambda", torch.float32, dev)
+    _need(state, "state", torch.float32, dev)
+    if q.dim() != 3 or q.shape[2] != DK or k.shape != q.shape or v.shape != (*q.shape[:2], DV):
+        raise ValueError("expected q, k [N, H, 96] and v [N, H, 192]")
+    N, H = q.shape[:2]
+    if state.dim() != 4 or state.shape[1:] != (H, DK, DV):
+        raise ValueError("state must be [P, H, 96, 192]")
+    _need(g, "g", q.dtype, dev, v.numel())
+    _need(weight, "weight", torch.float32, dev)
+    _need(tier, "tier", torch.int32, dev, H)
+    if weight.dim() != 2 or weight.shape[1] != DV:
+        raise ValueError("weight must be [n_tiers, 192]")
+    if slot is not None:
+        _need(slot, "slot", torch.int32, dev, N)
+    if aug is not None:
+        _need(aug, "aug", torch.float32, dev, H * DK)
+    if y is None:
+        y = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    _need(y, "y", v.dtype, dev, v.numel())
+    s = float(DK ** -0.5) if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        rc = lib.gla_decode_step_norm_gate(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), s, _ptr(aug),
+                                           _ptr(state), _ptr(slot), state.shape[0], _ptr(g), _ptr(weight),
+                                           _ptr(tier), weight.shape[0], float(eps), _ptr(y), N, H, DK, DV,
+                                           dt, _stream(dev))
+    _check(rc, "gla_decode_step_norm_gate")
+    return y
 
 
 def _host_offsets(lengths):

@@ -9,7 +9,8 @@ namespace gla {
 cudaError_t launch_decode_step(int dtype_f32, int state_bf16, const void* q, const void* k, const void* v,
                                const float* log_lambda, float scale, void* state,
                                const int32_t* slot, int pool_rows, void* o, int N, int H,
-                               const float* aug, unsigned* err, cudaStream_t stream);
+                               const float* aug, unsigned* err, cudaStream_t stream,
+                               const DecodeNormGate* ngp);
 cudaError_t launch_simt_fwd(const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_simt_bwd(int dtype_f32, const ChunkArgs& a, cudaStream_t stream);
 cudaError_t launch_tc_fwd(const ChunkArgs& a, cudaStream_t stream);
@@ -271,7 +272,7 @@ int gla_chunk_bwd(const void* q, const void* k, const void* v, const float* log_
 static int decode_step(const void* q, const void* k, const void* v, const float* log_lambda,
                        float scale, const float* aug, void* state, int state_bf16, const int32_t* slot,
                        int pool_rows, void* o, int N, int H, int dk, int dv, int dtype,
-                       gla_stream_t stream) {
+                       gla_stream_t stream, const gla::DecodeNormGate* ngp = nullptr) {
   if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_DTYPE;
   if (dk != GLA_DK || dv != GLA_DV) return GLA_ERR_UNSUPPORTED;
   if (N < 0 || H < 1 || pool_rows < 0) return GLA_ERR_SHAPE;
@@ -289,7 +290,7 @@ static int decode_step(const void* q, const void* k, const void* v, const float*
   int rc = device_state(&dev, &err, &wait_ns);
   if (rc) return rc;
   return to_status(gla::launch_decode_step(dtype == GLA_F32, state_bf16, q, k, v, log_lambda, scale, state,
-                                           slot, pool_rows, o, N, H, aug, err, (cudaStream_t)stream));
+                                           slot, pool_rows, o, N, H, aug, err, (cudaStream_t)stream, ngp));
 }
 
 int gla_decode_step(const void* q, const void* k, const void* v, const float* log_lambda,
@@ -314,6 +315,24 @@ int gla_decode_step_bf16_state(const void* q, const void* k, const void* v, cons
                                gla_stream_t stream) {
   return decode_step(q, k, v, log_lambda, scale, aug, state, 1, slot, pool_rows, o, N, H, dk, dv, dtype,
                      stream);
+}
+
+int gla_decode_step_norm_gate(const void* q, const void* k, const void* v, const float* log_lambda,
+                              float scale, const float* aug, float* state, const int32_t* slot,
+                              int pool_rows, const void* g, const float* weight, const int32_t* tier,
+                              int n_tiers, float eps, void* y, int N, int H, int dk, int dv, int dtype,
+                              gla_stream_t stream) {
+  if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_DTYPE;
+  if (dk != GLA_DK || dv != GLA_DV) return GLA_ERR_UNSUPPORTED;
+  if (n_tiers < 1 || !(eps >= 0.f)) return GLA_ERR_SHAPE;
+  if (N > 0) {
+    if (!g || !weight || !tier) return GLA_ERR_NULL;
+    if (!aligned16(g) || !aligned16(weight)) return GLA_ERR_ALIGN;
+    if ((uintptr_t)tier & 3u) return GLA_ERR_ALIGN;
+  }
+  const gla::DecodeNormGate ng = {g, weight, tier, n_tiers, eps};
+  return decode_step(q, k, v, log_lambda, scale, aug, state, 0, slot, pool_rows, y, N, H, dk, dv, dtype,
+                     stream, &ng);
 }
 
 int gla_head_norm_gate(const void* o, const void* g, const float* weight, const int32_t* tier,

@@ -40,6 +40,16 @@ struct ChunkArgs {
   unsigned long long wait_ns;  // limit of every bounded wait
 };
 
+// The decode step's fused per-tier Head RMSNorm + SiLU gate: g [N, H, 192] (dtype of o), the
+// tier gains weight [n_tiers, 192] fp32, the head-to-tier map tier [H] int32, eps.
+struct DecodeNormGate {
+  const void* g;
+  const float* w;
+  const int32_t* tier;
+  int n_tiers;
+  float eps;
+};
+
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 

@@ -11,6 +11,13 @@
 // stream): it is read and widened to fp32, updated and read out in fp32, and rounded to bf16 (to
 // nearest, ties to even) when it is written back.
 //
+// With the fused norm (NormGate given), the output row is not stored as o: it goes through the
+// per-tier Head RMSNorm and the SiLU(g) gate of the same section ("the per-head outputs pass
+// through a Head RMSNorm within each decay tier, then the SiLU(g) gate"), and y is stored:
+//     y = o / sqrt(mean_c o_c^2 + eps) * w_{tier(h)} * SiLU(g),
+// from the fp32 readout (before any rounding of o).  The CTA holds the head's whole 192-wide
+// row, so the mean square is a reduction over its first 48 threads.
+//
 // The step is a pure stream over the 72 KB state of each (sequence, head): read once, update,
 // write once.  One CTA of 576 threads owns one state; thread (r, c), r < 12, c < 48, holds
 // columns 4c..4c+3 (one 16-byte vector) of the 8 rows r, r+12, ..., r+84, so consecutive lanes
@@ -61,15 +68,37 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 x) {
   *reinterpret_cast<Bf16x4*>(p) = r;
 }
 
-template <class T, class ST>
+// The fused Head RMSNorm + SiLU gate's inputs: g [N, H, 192] (the gate stream, dtype of o),
+// weight [n_tiers, 192] fp32 (each tier's gain), tier [H] int32, eps.
+template <class T>
+struct NormGate {
+  const T* g;
+  const float* w;
+  const int32_t* tier;
+  int n_tiers;
+  float eps;
+};
+
+// SiLU(x) = x sigmoid(x) = x (1 + tanh(x / 2)) / 2: the hardware tanh approximation for bf16
+// data (relative error about 2^-11, inside a bf16 rounding), CUDA's tanhf for fp32 data.
+__device__ __forceinline__ float dec_tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float dec_silu(float g, __nv_bfloat16) { return g * fmaf(0.5f, dec_tanh_fast(0.5f * g), 0.5f); }
+__device__ __forceinline__ float dec_silu(float g, float) { return g * fmaf(0.5f, tanhf(0.5f * g), 0.5f); }
+
+template <class T, class ST, bool NG>
 __global__ void __launch_bounds__(DEC_THREADS, 2)
 decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    const float* __restrict__ log_lambda, float scale, ST* __restrict__ state,
                    const int32_t* __restrict__ slot, int pool_rows, T* __restrict__ o, int H,
-                   const float* __restrict__ aug, unsigned* err) {
+                   const float* __restrict__ aug, unsigned* err, const NormGate<T> ng) {
   __shared__ float s_q[DK];
   __shared__ float s_k[DK];
   __shared__ float s_gate;
+  __shared__ float s_ss[2];
   __shared__ float4 s_part[DEC_RGROUPS][DEC_COLS];
 
   const long long nh = blockIdx.x;  // n * H + h
@@ -96,6 +125,8 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     s_k[tid] = to_f(k[nh * DK + tid]);
   }
   const float4 vv = load4(v + nh * DV + 4 * c);
+  float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);  // the gate stream's 4 channels (fused norm)
+  if (NG && tid < DEC_COLS) gv = load4(ng.g + nh * DV + 4 * tid);
   const float lam = expf(log_lambda[h]);
   __syncthreads();
 
@@ -125,53 +156,89 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     if (tid == 0) s_gate = 1.f / (1.f + expf(-g));
   }
   __syncthreads();
-  if (tid < DEC_COLS) {
-    float4 t = s_part[0][tid];
+  if (tid < (NG ? 64 : DEC_COLS)) {  // (fused norm: warps 0 and 1 whole, for the reduction)
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid < DEC_COLS) {
+      t = s_part[0][tid];
 #pragma unroll
-    for (int g = 1; g < DEC_RGROUPS; ++g) {
-      const float4 p = s_part[g][tid];
-      t.x += p.x;
-      t.y += p.y;
-      t.z += p.z;
-      t.w += p.w;
+      for (int g = 1; g < DEC_RGROUPS; ++g) {
+        const float4 p = s_part[g][tid];
+        t.x += p.x;
+        t.y += p.y;
+        t.z += p.z;
+        t.w += p.w;
+      }
+      if (aug) {
+        const float gate = s_gate;
+        t.x = fmaf(gate, vv.x, t.x);
+        t.y = fmaf(gate, vv.y, t.y);
+        t.z = fmaf(gate, vv.z, t.z);
+        t.w = fmaf(gate, vv.w, t.w);
+      }
     }
-    if (aug) {
-      const float gate = s_gate;
-      t.x = fmaf(gate, vv.x, t.x);
-      t.y = fmaf(gate, vv.y, t.y);
-      t.z = fmaf(gate, vv.z, t.z);
-      t.w = fmaf(gate, vv.w, t.w);
+    if constexpr (NG) {
+      // mean square of the row's 192 channels: within warps 0 and 1, then across the two
+      float ss = t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      if ((tid & 31) == 0) s_ss[tid >> 5] = ss;
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+      const int tr = ng.tier[h];
+      if (tr < 0 || tr >= ng.n_tiers) {  // a tier outside the gains: y is left untouched
+        if (tid == 0) raise_error(err, ERR_SHAPE);
+        return;
+      }
+      if (tid < DEC_COLS) {
+        const float inv = rsqrtf((s_ss[0] + s_ss[1]) * (1.f / DV) + ng.eps);
+        const float4 w = *reinterpret_cast<const float4*>(ng.w + tr * DV + 4 * tid);
+        const T tag{};
+        t.x = (t.x * inv) * (w.x * dec_silu(gv.x, tag));
+        t.y = (t.y * inv) * (w.y * dec_silu(gv.y, tag));
+        t.z = (t.z * inv) * (w.z * dec_silu(gv.z, tag));
+        t.w = (t.w * inv) * (w.w * dec_silu(gv.w, tag));
+        store4(o + nh * DV + 4 * tid, t);
+      }
+    } else {
+      store4(o + nh * DV + 4 * tid, t);
     }
-    store4(o + nh * DV + 4 * tid, t);
+  }
+}
+
+template <class T, class ST>
+void launch_decode_t(long long blocks, const void* q, const void* k, const void* v, const float* log_lambda,
+                     float scale, void* state, const int32_t* slot, int pool_rows, void* o, int H,
+                     const float* aug, unsigned* err, const DecodeNormGate* ngp, cudaStream_t stream) {
+  if (ngp) {
+    const NormGate<T> ng = {(const T*)ngp->g, ngp->w, ngp->tier, ngp->n_tiers, ngp->eps};
+    decode_step_kernel<T, ST, true><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
+        (const T*)q, (const T*)k, (const T*)v, log_lambda, scale, (ST*)state, slot, pool_rows, (T*)o, H, aug,
+        err, ng);
+  } else {
+    decode_step_kernel<T, ST, false><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
+        (const T*)q, (const T*)k, (const T*)v, log_lambda, scale, (ST*)state, slot, pool_rows, (T*)o, H, aug,
+        err, NormGate<T>{});
   }
 }
 
 }  // namespace
 
+// ngp: the fused Head RMSNorm + SiLU gate (o then receives y), or null for the plain readout.
 cudaError_t launch_decode_step(int dtype_f32, int state_bf16, const void* q, const void* k, const void* v,
                                const float* log_lambda, float scale, void* state,
                                const int32_t* slot, int pool_rows, void* o, int N, int H,
-                               const float* aug, unsigned* err, cudaStream_t stream) {
+                               const float* aug, unsigned* err, cudaStream_t stream,
+                               const DecodeNormGate* ngp) {
   const long long blocks = (long long)N * H;
   if (blocks == 0) return cudaSuccess;
   using BF = __nv_bfloat16;
-  if (dtype_f32 && !state_bf16) {
-    decode_step_kernel<float, float><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
-        (const float*)q, (const float*)k, (const float*)v, log_lambda, scale, (float*)state, slot,
-        pool_rows, (float*)o, H, aug, err);
-  } else if (dtype_f32) {
-    decode_step_kernel<float, BF><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
-        (const float*)q, (const float*)k, (const float*)v, log_lambda, scale, (BF*)state, slot,
-        pool_rows, (float*)o, H, aug, err);
-  } else if (!state_bf16) {
-    decode_step_kernel<BF, float><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
-        (const BF*)q, (const BF*)k, (const BF*)v, log_lambda, scale, (float*)state, slot, pool_rows,
-        (BF*)o, H, aug, err);
-  } else {
-    decode_step_kernel<BF, BF><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
-        (const BF*)q, (const BF*)k, (const BF*)v, log_lambda, scale, (BF*)state, slot, pool_rows,
-        (BF*)o, H, aug, err);
-  }
+  if (dtype_f32 && !state_bf16)
+    launch_decode_t<float, float>(blocks, q, k, v, log_lambda, scale, state, slot, pool_rows, o, H, aug, err, ngp, stream);
+  else if (dtype_f32)
+    launch_decode_t<float, BF>(blocks, q, k, v, log_lambda, scale, state, slot, pool_rows, o, H, aug, err, ngp, stream);
+  else if (!state_bf16)
+    launch_decode_t<BF, float>(blocks, q, k, v, log_lambda, scale, state, slot, pool_rows, o, H, aug, err, ngp, stream);
+  else
+    launch_decode_t<BF, BF>(blocks, q, k, v, log_lambda, scale, state, slot, pool_rows, o, H, aug, err, ngp, stream);
   return cudaGetLastError();
 }
 
