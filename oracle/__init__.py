@@ -48,10 +48,14 @@ def _bind(path):
     lib.oracle_head_norm_gate.argtypes = [P, P, P, P, I, D, ctypes.c_longlong, I, I, P]
     lib.oracle_decode_step_bf16_state.argtypes = [P, P, P, P, D, P, P, I, I, I, I]
     lib.oracle_round_to_bf16.argtypes = [P, P, ctypes.c_longlong]
+    lib.oracle_mxfp8_quantize.argtypes = [P, ctypes.c_longlong, I, P, P]
+    lib.oracle_mxfp8_dequantize.argtypes = [P, P, ctypes.c_longlong, I, P]
+    lib.oracle_decode_step_mxfp8_state.argtypes = [P, P, P, P, D, P, P, P, I, I, I, I, P]
     lib.oracle_hardware_threads.argtypes = []
     for f in (lib.oracle_fwd, lib.oracle_fwd_chunked, lib.oracle_decode_step, lib.oracle_bwd,
               lib.oracle_self_aug, lib.oracle_head_norm_gate, lib.oracle_decode_step_bf16_state,
-              lib.oracle_round_to_bf16, lib.oracle_hardware_threads):
+              lib.oracle_round_to_bf16, lib.oracle_mxfp8_quantize, lib.oracle_mxfp8_dequantize,
+              lib.oracle_decode_step_mxfp8_state, lib.oracle_hardware_threads):
         f.restype = ctypes.c_int
     return lib
 
@@ -199,6 +203,55 @@ def decode_step_bf16_state(q, k, v, log_lambda, scale, state, _lib_override=None
     return o
 
 
+def mxfp8_quantize(x, _lib_override=None):
+    """MXFP8 (E4M3 elements, one E8M0 scale per 32 along the last axis) of fp32 values
+    ``x [..., 32 m]``: returns ``(codes uint8 [..., 32 m], scales uint8 [..., m])``."""
+    x = _f32(x)
+    cols = x.shape[-1]
+    rows = x.size // cols if cols else 0
+    codes = np.zeros(x.shape, np.uint8)
+    scales = np.zeros(x.shape[:-1] + (cols // 32,), np.uint8)
+    rc = (_lib_override or _load()).oracle_mxfp8_quantize(_ptr(x), rows, cols, _ptr(codes), _ptr(scales))
+    if rc:
+        raise ValueError(f"oracle_mxfp8_quantize rejected its arguments ({rc})")
+    return codes, scales
+
+
+def mxfp8_dequantize(codes, scales, _lib_override=None):
+    """The fp64 values of MXFP8 ``codes [..., 32 m]`` with ``scales [..., m]``."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    cols = codes.shape[-1]
+    if scales.shape != codes.shape[:-1] + (cols // 32,):
+        raise ValueError("scales must be [..., cols / 32]")
+    x = np.zeros(codes.shape, np.float64)
+    rc = (_lib_override or _load()).oracle_mxfp8_dequantize(_ptr(codes), _ptr(scales), codes.size // cols, cols,
+                                                            _ptr(x))
+    if rc:
+        raise ValueError(f"oracle_mxfp8_dequantize rejected its arguments ({rc})")
+    return x
+
+
+def decode_step_mxfp8_state(q, k, v, log_lambda, scale, codes, scales, return_pre=False, _lib_override=None):
+    """One decode step with an MXFP8-stored state (``codes`` uint8 ``[N, H, dk, dv]``, ``scales``
+    uint8 ``[N, H, dk, dv / 32]``, both updated in place); returns ``o`` (fp64, read out from the
+    update before it is stored), and with ``return_pre`` also the fp32 update that was quantised."""
+    q, k, v, ll = _f32(q), _f32(k), _f32(v), _f32(log_lambda)
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    for a, shape in ((codes, (N, H, dk, dv)), (scales, (N, H, dk, dv // 32))):
+        if a.dtype != np.uint8 or not a.flags.c_contiguous or a.shape != shape:
+            raise ValueError("codes / scales must be C-contiguous uint8 [N, H, dk, dv] / [N, H, dk, dv/32]")
+    o = np.zeros((N, H, dv), np.float64)
+    pre = np.zeros((N, H, dk, dv), np.float32) if return_pre else None
+    rc = (_lib_override or _load()).oracle_decode_step_mxfp8_state(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(ll), float(scale), _ptr(codes), _ptr(scales), _ptr(o), N, H, dk, dv,
+        _ptr(pre))
+    if rc:
+        raise ValueError(f"oracle_decode_step_mxfp8_state rejected its arguments ({rc})")
+    return (o, pre) if return_pre else o
+
+
 def bwd(q, k, v, log_lambda, scale, dO, h0=None, dhT=None, cu_seqlens=None, nthreads=0,
         _lib_override=None):
     """Adjoint of :func:`fwd`.  Returns ``(dq, dk, dv, dh0)`` in fp64."""
@@ -251,6 +304,15 @@ class Variant:
 
     def decode_step_bf16_state(self, *a, **kw):
         return decode_step_bf16_state(*a, _lib_override=self._lib, **kw)
+
+    def mxfp8_quantize(self, *a, **kw):
+        return mxfp8_quantize(*a, _lib_override=self._lib, **kw)
+
+    def mxfp8_dequantize(self, *a, **kw):
+        return mxfp8_dequantize(*a, _lib_override=self._lib, **kw)
+
+    def decode_step_mxfp8_state(self, *a, **kw):
+        return decode_step_mxfp8_state(*a, _lib_override=self._lib, **kw)
 
 
 def source_path() -> str:

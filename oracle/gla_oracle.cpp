@@ -30,6 +30,7 @@
 // log_lambda is the natural log of lambda_h, one fp32 per head; lambda_h = exp(log_lambda[h])
 // evaluated in double.
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -284,6 +285,116 @@ int oracle_decode_step_bf16_state(const float* q, const float* k, const float* v
 
 int oracle_round_to_bf16(const double* x, double* y, long long n) {
   for (long long i = 0; i < n; ++i) y[i] = round_to_bf16(x[i]);
+  return 0;
+}
+
+// ---- MXFP8 decode state (not on the pages: a storage variant that quarters the state stream) ----
+// Format: OCP "Microscaling Formats (MX) Specification" v1.0, MXFP8 with E4M3 elements: every
+// block of 32 consecutive elements of a state row shares one E8M0 scale X = 2^(byte - 127).
+// E4M3 (OCP "8-bit Floating Point Specification"): sign, 4 exponent bits (bias 7), 3 mantissa
+// bits; no infinities; S.1111.111 is NaN; the largest finite value is 0.1111.110 = 448;
+// exponent field 0 holds the subnormals m/8 * 2^-6.
+double e4m3_value(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return std::nan("");
+  const double mag = e == 0 ? std::ldexp((double)m, -9) : std::ldexp(8.0 + m, e - 10);
+  return sign ? -mag : mag;
+}
+
+// A finite value to E4M3: round to nearest, ties to even, magnitudes from 448 up saturate to 448
+// (the conversion with saturation of the MX specification).
+uint8_t e4m3_code(double y) {
+  const uint8_t sign = std::signbit(y) ? 0x80 : 0;
+  const double a = std::fabs(y);
+  if (a >= 448.0) return sign | 0x7E;
+  int ex = 0;
+  if (a > 0) std::frexp(a, &ex);
+  const int E = std::max(ex - 1, -6);                         // a in [2^E, 2^(E+1)), or subnormal
+  const double r = std::nearbyint(std::ldexp(a, 3 - E));      // multiples of 2^(E-3); default
+  const double val = std::ldexp(r, E - 3);                    // rounding: to nearest, ties to even
+  if (val == 0.0) return sign;
+  std::frexp(val, &ex);
+  const int Ev = ex - 1;                                      // (a carry may have raised it)
+  if (Ev < -6) return sign | (uint8_t)std::ldexp(val, 9);     // subnormal: m 2^-9
+  const int m = (int)std::ldexp(val, 3 - Ev) - 8;
+  return sign | (uint8_t)(((Ev + 7) << 3) | m);
+}
+
+// One block of n (32) values.  Shared exponent: the MX specification's floor(log2(max |x|)) - 8
+// (8 = the exponent of E4M3's largest power of two), raised by one when the block maximum
+// would then exceed 448 (the specification would saturate it to 448, an error of up to 12.5 %),
+// i.e. the smallest exponent at which the whole block is representable; clamped to E8M0's
+// [-127, 127] (-127 for an all-zero block).  Elements x / 2^shared_exp converted as above.
+void mxfp8_block(const float* x, int n, uint8_t* codes, uint8_t* scale_byte) {
+  double mx = 0.0;
+  for (int i = 0; i < n; ++i) mx = std::max(mx, std::fabs((double)x[i]));
+  int se = -127;
+  if (mx > 0) {
+    int ex;
+    std::frexp(mx, &ex);
+    se = ex - 1 - 8;
+    if (std::ldexp(mx, -se) > 448.0) se += 1;
+    se = std::min(std::max(se, -127), 127);
+  }
+  *scale_byte = (uint8_t)(se + 127);
+  for (int i = 0; i < n; ++i) codes[i] = e4m3_code(std::ldexp((double)x[i], -se));
+}
+
+double e8m0_value(uint8_t b) { return b == 255 ? std::nan("") : std::ldexp(1.0, (int)b - 127); }
+
+// rows x cols (cols a multiple of 32) fp32 values -> codes [rows, cols], scales [rows, cols/32].
+int oracle_mxfp8_quantize(const float* x, long long rows, int cols, uint8_t* codes, uint8_t* scales) {
+  if (rows < 0 || cols <= 0 || cols % 32) return -1;
+  for (long long r = 0; r < rows; ++r)
+    for (int b = 0; b < cols / 32; ++b)
+      mxfp8_block(x + r * cols + 32 * b, 32, codes + r * cols + 32 * b, scales + r * (cols / 32) + b);
+  return 0;
+}
+
+int oracle_mxfp8_dequantize(const uint8_t* codes, const uint8_t* scales, long long rows, int cols, double* x) {
+  if (rows < 0 || cols <= 0 || cols % 32) return -1;
+  for (long long r = 0; r < rows; ++r)
+    for (int c = 0; c < cols; ++c)
+      x[r * cols + c] = e4m3_value(codes[r * cols + c]) * e8m0_value(scales[r * (cols / 32) + c / 32]);
+  return 0;
+}
+
+// One decode step with an MXFP8-stored state [N, H, dk, dv] (codes) + [N, H, dk, dv/32]
+// (scales), in place.  The state is widened exactly, updated and read out in fp64 as in
+// oracle_decode_step (the readout from the update before any rounding); the update is then
+// rounded to fp32, the precision in which the GPU path takes its quantisation decisions, and
+// stored as MXFP8 row by row.  pre (optional, [N, H, dk, dv]) receives those fp32 values.
+int oracle_decode_step_mxfp8_state(const float* q, const float* k, const float* v, const float* log_lambda,
+                                   double scale, uint8_t* codes, uint8_t* scales, double* o, int N, int H,
+                                   int dk, int dv, float* pre) {
+  if (N < 0 || H <= 0 || dk <= 0 || dv <= 0 || dv % 32) return -1;
+  std::vector<double> S((size_t)dk * dv);
+  std::vector<float> X((size_t)dk * dv);
+  for (int n = 0; n < N; ++n)
+    for (int h = 0; h < H; ++h) {
+      const double lam = std::exp((double)log_lambda[h]);
+      uint8_t* Ct = codes + ((size_t)n * H + h) * dk * dv;
+      uint8_t* Bt = scales + ((size_t)n * H + h) * dk * (dv / 32);
+      const float* kt = k + ((size_t)n * H + h) * dk;
+      const float* vt = v + ((size_t)n * H + h) * dv;
+      const float* qt = q + ((size_t)n * H + h) * dk;
+      for (int a = 0; a < dk; ++a)
+        for (int b = 0; b < dv; ++b) {
+          const double s_ab = e4m3_value(Ct[(size_t)a * dv + b]) * e8m0_value(Bt[(size_t)a * (dv / 32) + b / 32]);
+          S[(size_t)a * dv + b] = lam * s_ab + (double)kt[a] * (double)vt[b];
+        }
+      double* ot = o + ((size_t)n * H + h) * dv;
+      for (int b = 0; b < dv; ++b) {
+        double acc = 0.0;
+        for (int a = 0; a < dk; ++a) acc += S[(size_t)a * dv + b] * (scale * (double)qt[a]);
+        ot[b] = acc;
+      }
+      for (size_t e = 0; e < S.size(); ++e) X[e] = (float)S[e];
+      for (int a = 0; a < dk; ++a)
+        for (int b = 0; b < dv / 32; ++b)
+          mxfp8_block(&X[(size_t)a * dv + 32 * b], 32, Ct + (size_t)a * dv + 32 * b, Bt + (size_t)a * (dv / 32) + b);
+      if (pre) std::memcpy(pre + ((size_t)n * H + h) * dk * dv, X.data(), X.size() * sizeof(float));
+    }
   return 0;
 }
 

@@ -76,6 +76,17 @@ MUTANTS = [
      "const double r = std::trunc(std::ldexp(m, 8));", 0),
     ("bf16 state: state stored unrounded", "for (size_t e = 0; e < S.size(); ++e) St[e] = round_to_bf16(S[e]);",
      "for (size_t e = 0; e < S.size(); ++e) St[e] = S[e];", 0),
+    ("mxfp8: E4M3 exponent bias 8", "std::ldexp(8.0 + m, e - 10)", "std::ldexp(8.0 + m, e - 11)", 0),
+    ("mxfp8: truncation instead of rounding", "const double r = std::nearbyint(std::ldexp(a, 3 - E));",
+     "const double r = std::trunc(std::ldexp(a, 3 - E));", 0),
+    ("mxfp8: subnormal range one binade too deep", "const int E = std::max(ex - 1, -6);",
+     "const int E = std::max(ex - 1, -7);", 0),
+    ("mxfp8: scale not raised for a block maximum above 448", "if (std::ldexp(mx, -se) > 448.0) se += 1;",
+     "", 0),
+    ("mxfp8: scale from the block's first element", "for (int i = 0; i < n; ++i) mx = std::max(mx, std::fabs((double)x[i]));",
+     "mx = std::fabs((double)x[0]);", 0),
+    ("mxfp8 step: decay dropped", "S[(size_t)a * dv + b] = lam * s_ab + (double)kt[a] * (double)vt[b];",
+     "S[(size_t)a * dv + b] = s_ab + (double)kt[a] * (double)vt[b];", 0),
     ("bwd: forward state missing its decay",
      "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];",
      "S[(size_t)a * dv + b] = S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];", 2),
@@ -101,6 +112,11 @@ PIN_TESTS = [
     pins.test_norm_gate_worked_example,
     pins.test_round_to_bf16_format_facts,
     pins.test_decode_bf16_state_is_rounded_fp32_step,
+    pins.test_e4m3_values_match_torch_float8,
+    pins.test_e4m3_conversion_is_round_to_nearest_even,
+    pins.test_mxfp8_scale_is_smallest_that_holds_the_block,
+    pins.test_mxfp8_round_trip_error_bound_and_idempotence,
+    pins.test_decode_mxfp8_state_is_quantised_fp32_step,
 ]
 
 

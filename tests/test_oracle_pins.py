@@ -500,3 +500,93 @@ def test_decode_bf16_state_is_rounded_fp32_step(oracle_mod):
     o_b = oracle_mod.decode_step_bf16_state(q, k, v, ll, 0.3, s_b)
     assert np.allclose(o_b, o_full, rtol=1e-14, atol=1e-15)
     assert np.array_equal(s_b, oracle_mod.round_to_bf16(s_full))
+
+
+# ------------------------------------------------------------------------------------------
+# MXFP8 decode state (OCP Microscaling MXFP8: E4M3 elements, one E8M0 scale per 32 elements)
+# ------------------------------------------------------------------------------------------
+def test_e4m3_values_match_torch_float8(oracle_mod):
+    """All 256 E4M3 codes at scale 2^0 against PyTorch's float8_e4m3fn (OCP E4M3: bias 7, no
+    infinities, S.1111.111 NaN, largest finite 448, subnormals m 2^-9)."""
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8).reshape(8, 32)
+    x = oracle_mod.mxfp8_dequantize(codes, np.full((8, 1), 127, np.uint8))
+    ref = torch.from_numpy(codes.reshape(-1).copy()).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(np.isnan(x.reshape(-1)), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(x.reshape(-1)[ok], ref[ok].astype(np.float64))
+    assert x.reshape(-1)[0x7E] == 448.0 and x.reshape(-1)[0x01] == 2.0 ** -9 and x.reshape(-1)[0x38] == 1.0
+
+
+def test_e4m3_conversion_is_round_to_nearest_even(oracle_mod):
+    """A block whose maximum sits in [256, 448] has scale 2^0, so its codes are plain E4M3
+    conversions: random values, and every midpoint between neighbouring positive values (the
+    ties, which go to the even mantissa), against PyTorch's float -> float8_e4m3fn."""
+    torch = pytest.importorskip("torch")
+    vals = torch.arange(0, 0x7F, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    mids = (vals[:-1] + vals[1:]) / 2
+    rng = np.random.default_rng(3)
+    pool = np.concatenate([mids, -mids, rng.uniform(-448, 448, 400), rng.normal(0, 1, 400) * 2.0 ** -7])
+    pool = pool.astype(np.float32)
+    n = (len(pool) + 30) // 31
+    blocks = np.zeros((n, 32), np.float32)
+    blocks[:, 0] = 300.0                           # sets the block's scale to 2^0
+    blocks[:, 1:].reshape(-1)[:len(pool)] = pool
+    codes, scales = oracle_mod.mxfp8_quantize(blocks)
+    assert np.all(scales == 127)
+    ref = torch.from_numpy(blocks).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    zero = blocks == 0                             # signed zeros may differ in the sign bit only
+    assert np.array_equal(codes[~zero], ref[~zero])
+    assert np.all((codes[zero] & 0x7F) == 0)
+
+
+def test_mxfp8_scale_is_smallest_that_holds_the_block(oracle_mod):
+    """The shared exponent is the smallest at which the block's largest magnitude fits E4M3's 448
+    (never saturating): max = 2^k gives 2^(k-8) (the max encodes to 256 = 0x78); max = 1.25 2^k
+    gives the same scale (320 = 0x7A); max = 1.9 2^k needs 2^(k-7) (243.2 -> 240 = 0x77).  An
+    all-zero block takes the smallest scale, 2^-127."""
+    for k in (-6, -1, 0, 3, 9):
+        for mant, want_se, want_code in ((1.0, k - 8, 0x78), (1.25, k - 8, 0x7A), (1.9, k - 7, 0x77)):
+            b = np.zeros((1, 32), np.float32)
+            b[0, 5] = -mant * 2.0 ** k
+            b[0, 9] = 2.0 ** (k - 3)
+            codes, scales = oracle_mod.mxfp8_quantize(b)
+            assert scales[0, 0] == want_se + 127, (k, mant)
+            assert codes[0, 5] == 0x80 | want_code, (k, mant, hex(codes[0, 5]))
+    codes, scales = oracle_mod.mxfp8_quantize(np.zeros((2, 64), np.float32))
+    assert np.all(scales == 0) and np.all(codes & 0x7F == 0)
+
+
+def test_mxfp8_round_trip_error_bound_and_idempotence(oracle_mod):
+    x = np.concatenate([gs.normal(71, 1, (64, 192), 0.1), gs.normal(71, 2, (64, 192), 30.0),
+                        gs.normal(71, 3, (64, 192), 1e-5)]).astype(np.float32)
+    codes, scales = oracle_mod.mxfp8_quantize(x)
+    y = oracle_mod.mxfp8_dequantize(codes, scales)
+    se = scales.astype(np.int64).repeat(32, axis=1) - 127
+    # half an E4M3 step: 2^-4 of the value in the normal range, 2^(se - 10) below 2^(se - 6)
+    bound = np.maximum(np.abs(x.astype(np.float64)) * 2.0 ** -4, np.ldexp(1.0, se - 10))
+    assert np.all(np.abs(y - x) <= bound)
+    assert np.max(np.abs(y) / np.ldexp(1.0, se)) <= 448.0
+    # quantising the dequantised values again reproduces them exactly (a block maximum that
+    # rounded down to 224 2^se is then held as 448 2^(se-1), the same value)
+    c2, s2 = oracle_mod.mxfp8_quantize(y.astype(np.float32))
+    assert np.array_equal(oracle_mod.mxfp8_dequantize(c2, s2), y)
+
+
+def test_decode_mxfp8_state_is_quantised_fp32_step(oracle_mod):
+    """The MXFP8 step reads out exactly what the fp64 step reads out from the widened state, and
+    stores the fp32-rounded update quantised block by block."""
+    N, H, dk, dv = 3, 2, 5, 64
+    q = _rand(62, 1, (N, H, dk))
+    k = _rand(62, 2, (N, H, dk))
+    v = _rand(62, 3, (N, H, dv))
+    ll = np.log(np.array([0.9, 0.5], np.float32))
+    codes, scales = oracle_mod.mxfp8_quantize(_rand(62, 4, (N, H, dk, dv), 0.5))
+    s_full = oracle_mod.mxfp8_dequantize(codes, scales)
+    o_full = oracle_mod.decode_step(q, k, v, ll, 0.3, s_full)
+    c, sc = codes.copy(), scales.copy()
+    o_m, pre = oracle_mod.decode_step_mxfp8_state(q, k, v, ll, 0.3, c, sc, return_pre=True)
+    assert np.allclose(o_m, o_full, rtol=1e-14, atol=1e-15)
+    assert np.array_equal(pre, s_full.astype(np.float32))
+    want_c, want_s = oracle_mod.mxfp8_quantize(s_full.astype(np.float32))
+    assert np.array_equal(c, want_c) and np.array_equal(sc, want_s)
