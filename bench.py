@@ -458,6 +458,44 @@ def bench_decode(torch, gla, wl, dist, args, peaks, aug=False, bf16_state=False,
     return res
 
 
+def bench_decode_mxfp8(torch, gla, wl, dist, args, peaks):
+    """The decode step on the same pool stored as MXFP8 (gla_decode_step_mxfp8_state: E4M3 codes
+    plus one E8M0 scale per 32 values, 19,008 bytes per state against 73,728 in fp32), built on
+    the device from the pool's fp32 states (2,048 pool rows at a time); 16 steps."""
+    from glasynth import TID
+    from glasynth.device import normal as dnormal
+    w = wl.DecodeWorkload(seqs=args.decode_seqs, layers=args.decode_layers)
+    codes = torch.empty((w.N, H, DK, DV), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((w.N, H, DK, DV // 32), dtype=torch.uint8, device="cuda")
+    for r0 in range(0, w.N, 2048):
+        r1 = min(w.N, r0 + 2048)
+        x = dnormal((r1 - r0, H, DK, DV), w.seed, TID["state"], w.state_sigma, torch.float32,
+                    start=r0 * H * DK * DV)
+        gla.gla_state_to_mxfp8(x, codes[r0:r1], scales[r0:r1])
+        del x
+    ll = torch.from_numpy(w.log_lambda).cuda()
+    steps = [w.device_step(s) for s in range(4)]
+    o = torch.empty((w.N, H, DV), dtype=torch.bfloat16, device="cuda")
+    it = [0]
+
+    def fn():
+        b = steps[it[0] % len(steps)]
+        it[0] += 1
+        gla.gla_decode_step_mxfp8_state(b["q"], b["k"], b["v"], ll, codes, scales, w.scale, o=o)
+    n = 16
+    region, per_call = timed(torch, dist, fn, n, max(args.warmup, 3))
+    region, per_call = dist.max(region), dist.max(per_call)
+    state_bytes = 2 * w.N * H * (DK * DV + DK * DV // 32)
+    res = {"workload": f"decode {w.seqs} seqs x {w.layers} layers H=16 MXFP8 state bf16 io", "steps": n,
+           "ms_per_step": region, "value": w.seqs * dist.world / (region / 1e3), "unit": "tokens/s",
+           "token": "one new token per sequence through all 24 layers",
+           "roofline": roofline(state_bytes, 2 * 2 * w.N * H * DK * DV, region / 1e3, peaks),
+           "io_bytes_outside_roofline": w.N * H * (2 * DK * 2 + 2 * DV * 2), "launches_per_step": 1}
+    res["roofline"]["algorithmic_bytes_note"] = "MXFP8 state (codes + scales) read + write per step"
+    del codes, scales, steps, o
+    return res
+
+
 def cpu_baseline_fwd(seconds_budget=10.0):
     """The oracle as it stands on the host cores: whole sequences of the B=8, T=2048, H=16
     workload (all 16 heads each), cycling over the 8 sequences until about `seconds_budget` of
@@ -578,7 +616,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--rows", default="fwd,bwd,varlen,decode,fwd_aug,norm_gate,decode_aug,decode_bf16_state,"
-                    "fwd_split,decode_norm_gate")
+                    "fwd_split,decode_norm_gate,decode_mxfp8_state")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-seqs", type=int, default=1280,
                     help="sequences in the decode pool (1280 = the measured workload)")
@@ -627,6 +665,8 @@ def main():
             out["decode_bf16_state"] = bench_decode(torch, gla, wl, dist, args, peaks, bf16_state=True)
         if "decode_norm_gate" in rows:
             out["decode_norm_gate"] = bench_decode(torch, gla, wl, dist, args, peaks, norm_gate=True)
+        if "decode_mxfp8_state" in rows:
+            out["decode_mxfp8_state"] = bench_decode_mxfp8(torch, gla, wl, dist, args, peaks)
     err = gla.gla_get_device_error()
     clocks = sampler.summary()
     cpu = None

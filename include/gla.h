@@ -207,6 +207,35 @@ int gla_decode_step_bf16_state(const void* q, const void* k, const void* v, cons
                                int pool_rows, void* o, int N, int H, int dk, int dv, int dtype,
                                gla_stream_t stream);
 
+/* Decode step on a state pool stored as MXFP8 (no counterpart in the paper: a storage variant
+ * that quarters the state stream; the pages keep fp32 states).  Format: OCP Microscaling (MX)
+ * v1.0 MXFP8, E4M3 elements (OCP 8-bit floating point: bias 7, largest finite 448) with one E8M0
+ * scale byte b (value 2^(b - 127)) per block of 32 consecutive values of a state row:
+ *   state_codes   [pool_rows, H, 96, 192] uint8 E4M3 codes, 16-byte aligned;
+ *   state_scales  [pool_rows, H, 96, 6] uint8 E8M0 scales of the blocks (columns 32j .. 32j+31),
+ *                 16-byte aligned.
+ * Each state is widened exactly to fp32, updated (S <- lambda S + k v^T) and read out
+ * (o = S^T (scale q), from the update before it is stored) in fp32, and written back quantised:
+ * per block, shared exponent se = floor(log2(max |x|)) - 8, plus one where the block maximum
+ * would otherwise exceed 448 (the MX rule alone saturates such maxima to 448; here nothing
+ * saturates), clamped to [-127, 127] (-127 for an all-zero block); codes = x 2^-se rounded to
+ * E4M3, to nearest, ties to even.  The quantisation error (up to 2^-4 relative per element per
+ * step, decayed by lambda) stays in the state, so long decodes drift from the fp32 result much
+ * more than with the bf16 pool; the fp32 pool is the reference path.  Every other argument as in
+ * gla_decode_step (aug NULL) or gla_decode_step_aug (aug non-NULL). */
+int gla_decode_step_mxfp8_state(const void* q, const void* k, const void* v, const float* log_lambda,
+                                float scale, const float* aug, uint8_t* state_codes, uint8_t* state_scales,
+                                const int32_t* slot, int pool_rows, void* o, int N, int H, int dk, int dv,
+                                int dtype, gla_stream_t stream);
+
+/* Conversions between fp32 state rows and MXFP8 (the format of gla_decode_step_mxfp8_state), for
+ * building a pool from fp32 states (a prefill's hT) and reading one back.  `rows` rows of 192
+ * values: x [rows, 192] fp32, codes [rows, 192] uint8, scales [rows, 6] uint8; all 16-byte
+ * aligned.  Quantisation as in gla_decode_step_mxfp8_state; dequantisation is exact. */
+int gla_state_to_mxfp8(const float* x, uint8_t* codes, uint8_t* scales, long long rows, gla_stream_t stream);
+int gla_state_from_mxfp8(const uint8_t* codes, const uint8_t* scales, float* x, long long rows,
+                         gla_stream_t stream);
+
 /* Sequence-split forward for long sequences (no counterpart in the paper).  A sequence's work
  * otherwise sits on one CTA per (head, 64-column tile of d_v), so one long sequence among few
  * keeps most SMs idle.  Here each sequence is cut into segments of at most seg_chunks chunks

@@ -30,7 +30,8 @@ GLA_BF16, GLA_F32 = 0, 1
 EXPORTS = ("gla_workspace_bytes", "gla_bwd_workspace_bytes", "gla_chunk_fwd", "gla_chunk_bwd",
            "gla_decode_step", "gla_chunk_fwd_aug", "gla_decode_step_aug", "gla_head_norm_gate",
            "gla_decode_step_bf16_state", "gla_split_workspace_bytes", "gla_chunk_fwd_split",
-           "gla_decode_step_norm_gate",
+           "gla_decode_step_norm_gate", "gla_decode_step_mxfp8_state", "gla_state_to_mxfp8",
+           "gla_state_from_mxfp8",
            "gla_split_choose_seg_chunks", "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
            "gla_status_string")
 NOALLOC_MAX_SEQS = 16384
@@ -87,6 +88,12 @@ def load_library(build: bool = True):
         lib.gla_decode_step_bf16_state.restype = I
         lib.gla_decode_step_norm_gate.argtypes = [P, P, P, P, F, P, P, P, I, P, P, P, I, F, P, I, I, I, I, I, P]
         lib.gla_decode_step_norm_gate.restype = I
+        lib.gla_decode_step_mxfp8_state.argtypes = [P, P, P, P, F, P, P, P, P, I, P, I, I, I, I, I, P]
+        lib.gla_decode_step_mxfp8_state.restype = I
+        lib.gla_state_to_mxfp8.argtypes = [P, P, P, ctypes.c_longlong, P]
+        lib.gla_state_to_mxfp8.restype = I
+        lib.gla_state_from_mxfp8.argtypes = [P, P, P, ctypes.c_longlong, P]
+        lib.gla_state_from_mxfp8.restype = I
         lib.gla_split_workspace_bytes.argtypes = [P, I, I, I]
         lib.gla_split_workspace_bytes.restype = Z
         lib.gla_chunk_fwd_split.argtypes = [P, P, P, P, P, F, P, P, P, P, I, I, I, I, I, I, I, P, Z, P]
@@ -397,6 +404,74 @@ def gla_decode_step_norm_gate(q, k, v, log_lambda, state, g, weight, tier, scale
                                            dt, _stream(dev))
     _check(rc, "gla_decode_step_norm_gate")
     return y
+
+
+def gla_state_to_mxfp8(x, codes=None, scales=None):
+    """fp32 state rows ``x [..., 192]`` to MXFP8: returns ``(codes uint8 [..., 192],
+    scales uint8 [..., 6])`` (the format of :func:`gla_decode_step_mxfp8_state`)."""
+    lib = load_library()
+    dev = x.device
+    _need(x, "x", torch.float32, dev)
+    if x.shape[-1] != DV:
+        raise ValueError("x must be [..., 192]")
+    rows = x.numel() // DV
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=dev) if codes is None else codes
+    scales = torch.empty(x.shape[:-1] + (DV // 32,), dtype=torch.uint8, device=dev) if scales is None else scales
+    _need(codes, "codes", torch.uint8, dev, x.numel())
+    _need(scales, "scales", torch.uint8, dev, rows * (DV // 32))
+    with torch.cuda.device(dev):
+        rc = lib.gla_state_to_mxfp8(_ptr(x), _ptr(codes), _ptr(scales), rows, _stream(dev))
+    _check(rc, "gla_state_to_mxfp8")
+    return codes, scales
+
+
+def gla_state_from_mxfp8(codes, scales, x=None):
+    """MXFP8 state rows back to fp32 (exact); returns ``x [..., 192]``."""
+    lib = load_library()
+    dev = codes.device
+    _need(codes, "codes", torch.uint8, dev)
+    if codes.shape[-1] != DV:
+        raise ValueError("codes must be [..., 192]")
+    rows = codes.numel() // DV
+    _need(scales, "scales", torch.uint8, dev, rows * (DV // 32))
+    x = torch.empty(codes.shape, dtype=torch.float32, device=dev) if x is None else x
+    _need(x, "x", torch.float32, dev, codes.numel())
+    with torch.cuda.device(dev):
+        rc = lib.gla_state_from_mxfp8(_ptr(codes), _ptr(scales), _ptr(x), rows, _stream(dev))
+    _check(rc, "gla_state_from_mxfp8")
+    return x
+
+
+def gla_decode_step_mxfp8_state(q, k, v, log_lambda, codes, scales, scale=None, slot=None, o=None, aug=None):
+    """One decode step on an MXFP8 state pool (``codes`` uint8 ``[P, H, 96, 192]``, ``scales``
+    uint8 ``[P, H, 96, 6]``, both updated in place).  Returns ``o [N, H, 192]``."""
+    lib = load_library()
+    dev = q.device
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, q.dtype, dev)
+    _need(log_lambda, "log_lambda", torch.float32, dev)
+    if q.dim() != 3 or q.shape[2] != DK or k.shape != q.shape or v.shape != (*q.shape[:2], DV):
+        raise ValueError("expected q, k [N, H, 96] and v [N, H, 192]")
+    N, H = q.shape[:2]
+    _need(codes, "codes", torch.uint8, dev)
+    if codes.dim() != 4 or codes.shape[1:] != (H, DK, DV):
+        raise ValueError("codes must be [P, H, 96, 192]")
+    _need(scales, "scales", torch.uint8, dev, codes.shape[0] * H * DK * (DV // 32))
+    if slot is not None:
+        _need(slot, "slot", torch.int32, dev, N)
+    if aug is not None:
+        _need(aug, "aug", torch.float32, dev, H * DK)
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, device=dev)
+    _need(o, "o", v.dtype, dev, v.numel())
+    s = float(DK ** -0.5) if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        rc = lib.gla_decode_step_mxfp8_state(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), s, _ptr(aug),
+                                             _ptr(codes), _ptr(scales), _ptr(slot), codes.shape[0], _ptr(o), N,
+                                             H, DK, DV, dt, _stream(dev))
+    _check(rc, "gla_decode_step_mxfp8_state")
+    return o
 
 
 def _host_offsets(lengths):

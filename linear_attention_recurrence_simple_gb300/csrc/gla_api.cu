@@ -19,6 +19,15 @@ size_t tc_bwd_acc_bytes(long long T_total, int H);
 cudaError_t tc_clear_handover(cudaStream_t stream);
 int check_chunk_sizes(int n_seq, int T, int H, int dk, int dv, int dtype, const int32_t* cu_seqlens,
                       long long* tokens);
+cudaError_t launch_mxfp8_quantise(const float* x, uint8_t* codes, uint8_t* scales, long long rows,
+                                  cudaStream_t stream);
+cudaError_t launch_mxfp8_dequantise(const uint8_t* codes, const uint8_t* scales, float* x, long long rows,
+                                    cudaStream_t stream);
+cudaError_t launch_decode_step_mxfp8(int dtype_f32, const void* q, const void* k, const void* v,
+                                     const float* log_lambda, float scale, uint8_t* codes, uint8_t* scales,
+                                     const int32_t* slot, int pool_rows, void* o, int N, int H,
+                                     const float* aug, unsigned* err, unsigned long long wait_ns,
+                                     cudaStream_t stream);
 cudaError_t launch_head_norm_gate(int dtype_f32, const void* o, const void* g, const float* w,
                                   const int32_t* tier, int n_tiers, float eps, void* y, long long rows,
                                   int H, unsigned* err, cudaStream_t stream);
@@ -333,6 +342,58 @@ int gla_decode_step_norm_gate(const void* q, const void* k, const void* v, const
   const gla::DecodeNormGate ng = {g, weight, tier, n_tiers, eps};
   return decode_step(q, k, v, log_lambda, scale, aug, state, 0, slot, pool_rows, y, N, H, dk, dv, dtype,
                      stream, &ng);
+}
+
+int gla_decode_step_mxfp8_state(const void* q, const void* k, const void* v, const float* log_lambda,
+                                float scale, const float* aug, uint8_t* state_codes, uint8_t* state_scales,
+                                const int32_t* slot, int pool_rows, void* o, int N, int H, int dk, int dv,
+                                int dtype, gla_stream_t stream) {
+  if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_DTYPE;
+  if (dk != GLA_DK || dv != GLA_DV) return GLA_ERR_UNSUPPORTED;
+  if (N < 0 || H < 1 || pool_rows < 0) return GLA_ERR_SHAPE;
+  if (!slot && pool_rows < N) return GLA_ERR_SHAPE;
+  if (N == 0) return GLA_OK;
+  if (!q || !k || !v || !log_lambda || !state_codes || !state_scales || !o) return GLA_ERR_NULL;
+  for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)o,
+                        (const void*)state_codes, (const void*)state_scales, (const void*)log_lambda})
+    if (!aligned16(p)) return GLA_ERR_ALIGN;
+  if (aug && !aligned16(aug)) return GLA_ERR_ALIGN;
+  if (slot && ((uintptr_t)slot & 3u)) return GLA_ERR_ALIGN;
+  int dev;
+  unsigned* err;
+  unsigned long long wait_ns;
+  int rc = device_state(&dev, &err, &wait_ns);
+  if (rc) return rc;
+  return to_status(gla::launch_decode_step_mxfp8(dtype == GLA_F32, q, k, v, log_lambda, scale, state_codes,
+                                                 state_scales, slot, pool_rows, o, N, H, aug, err, wait_ns,
+                                                 (cudaStream_t)stream));
+}
+
+int gla_state_to_mxfp8(const float* x, uint8_t* codes, uint8_t* scales, long long rows, gla_stream_t stream) {
+  if (rows < 0 || rows > (1ll << 40)) return GLA_ERR_SHAPE;
+  if (rows == 0) return GLA_OK;
+  if (!x || !codes || !scales) return GLA_ERR_NULL;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return GLA_ERR_ALIGN;
+  int dev;
+  unsigned* err;
+  unsigned long long wait_ns;
+  int rc = device_state(&dev, &err, &wait_ns);
+  if (rc) return rc;
+  return to_status(gla::launch_mxfp8_quantise(x, codes, scales, rows, (cudaStream_t)stream));
+}
+
+int gla_state_from_mxfp8(const uint8_t* codes, const uint8_t* scales, float* x, long long rows,
+                         gla_stream_t stream) {
+  if (rows < 0 || rows > (1ll << 40)) return GLA_ERR_SHAPE;
+  if (rows == 0) return GLA_OK;
+  if (!x || !codes || !scales) return GLA_ERR_NULL;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return GLA_ERR_ALIGN;
+  int dev;
+  unsigned* err;
+  unsigned long long wait_ns;
+  int rc = device_state(&dev, &err, &wait_ns);
+  if (rc) return rc;
+  return to_status(gla::launch_mxfp8_dequantise(codes, scales, x, rows, (cudaStream_t)stream));
 }
 
 int gla_head_norm_gate(const void* o, const void* g, const float* weight, const int32_t* tier,

@@ -61,3 +61,4 @@ def test_short_wait_limit_in_the_backward_reports_timeout():
     dq, dk, dv, dh0 = gla.gla_chunk_bwd(g["q"], g["k"], g["v"], g["log_lambda"], g["dO"], 0.1,
                                         h0=g["h0"], dhT=g["dhT"])
     assert gla.gla_get_device_error() == 0
+
