@@ -264,10 +264,12 @@ decode_step_mxfp8_kernel(const T* __restrict__ q, const T* __restrict__ k, const
   int it = 0;
   for (; j < total; j += stride, ++it) {
     const int s = it & 1;
-    const bool ok = mbar_wait(&full[s], (uint32_t)(it >> 1) & 1u, wait_ns, abort_flag);
-    if (__syncthreads_or(!ok)) break;  // (every thread leaves together)
+    // A thread whose wait gave up skips the state's work; the first barrier below is also the
+    // vote, so every thread of the CTA then leaves the loop together.
+    // (warp-uniform, so that the block's shuffles always see every lane)
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (uint32_t)(it >> 1) & 1u, wait_ns, abort_flag));
     uint8_t* sb = mx_smem + s * SL::BYTES;
-    const long long st = *reinterpret_cast<const long long*>(sb + SL::META);
+    const long long st = ok ? *reinterpret_cast<const long long*>(sb + SL::META) : -1;
     const T* sq = reinterpret_cast<const T*>(sb + SL::Q);
     const T* sk = reinterpret_cast<const T*>(sb + SL::K);
     const T* sv = reinterpret_cast<const T*>(sb + SL::V);
@@ -310,7 +312,7 @@ decode_step_mxfp8_kernel(const T* __restrict__ q, const T* __restrict__ k, const
       }
     }
     fence_async_smem_mx();  // the new codes and scales are read next by the bulk store
-    __syncthreads();
+    if (__syncthreads_or(!ok)) break;
     if (st >= 0) {
       if (tid == 0) {
         bulk_store(codes + st * (DK * DV), sb + SL::CODES, DK * DV);
