@@ -287,13 +287,23 @@ decode_step_mxfp8_kernel(const T* __restrict__ q, const T* __restrict__ k, const
         const float ka = to_f(sk[a]), qa = scale * to_f(sq[a]);
         uint4* cp = reinterpret_cast<uint4*>(sb + SL::CODES) + a * MX_PIECES + p;
         uint8_t* scp = sb + SL::SCALES + a * MX_BLOCKS + (p >> 1);
+        // x = fma(lambda, code * scale, k_a v) as in the fp32-state step.  The scale is a power
+        // of two, so lambda * scale is exact while it is a normal fp32 number (or lambda is 0),
+        // and fma(lambda * scale, code, k_a v) is then the same value with one multiply less.
+        const float sc = e8m0_to_f(*scp);
+        const float lsc = lam * sc;
         float x[16];
-        dequantise16(*cp, e8m0_to_f(*scp), x);
+        if (lsc >= 1.17549435e-38f || lam == 0.f) {
+          dequantise16(*cp, 1.f, x);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          x[e] = fmaf(lam, x[e], ka * vv[e]);  // as in the fp32-state step
-          acc[e] = fmaf(qa, x[e], acc[e]);
+          for (int e = 0; e < 16; ++e) x[e] = fmaf(lsc, x[e], ka * vv[e]);
+        } else {
+          dequantise16(*cp, sc, x);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) x[e] = fmaf(lam, x[e], ka * vv[e]);
         }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = fmaf(qa, x[e], acc[e]);
         const int se = mx_shared_exp(block_max(x));
         *cp = quantise16(x, se);  // in place: this thread's own 16 bytes
         // (both lanes of the block read this byte above, before the shuffle in block_max)
