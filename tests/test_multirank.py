@@ -74,3 +74,22 @@ def test_bench_refuses_disagreeing_world_size():
     env = dict(os.environ, WORLD_SIZE="3", RANK="0", LOCAL_RANK="0")
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=120, env=env, cwd=root)
     assert r.returncode != 0 and "disagree" in r.stderr
+
+
+def test_bench_reference_arm_prints_one_line():
+    """`bench.py --impl reference` times the oracle on the host cores (no GPU) and prints one JSON
+    line with the GPU arm's metric, the sample it ran, and an e2e entry with no copies."""
+    import json
+    import subprocess
+    cmd, root = _bench_cmd("--impl", "reference", "--steps", "1", "--warmup", "1")
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    rec = json.loads(lines[0])
+    import bench
+    assert rec["impl"] == "reference" and rec["metric"] == bench.METRIC and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["dtype"] == "f64"
+    assert rec["steps"] == 1 and rec["warmup"] >= 1
