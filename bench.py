@@ -38,6 +38,15 @@ PROFILED_TRAFFIC = {
     # 49,152-state pool: 3.661689 GB read + 3.583208 GB written; traffic scales with the pool
     "decode": ("linear_attention_recurrence_simple_gb300/csrc/gla_decode.cu", "98de2132efc39ffd",
                7244897000.0 / 49152, "per state per step"),
+    # the same pool in bf16: 1.849795 GB read + 1.770043 GB written
+    "decode_bf16_state": ("linear_attention_recurrence_simple_gb300/csrc/gla_decode.cu", "98de2132efc39ffd",
+                          3619838464.0 / 49152, "per state per step"),
+    # the fused norm-gate step on the fp32 pool: 3.680579 GB read + 3.583394 GB written
+    "decode_norm_gate": ("linear_attention_recurrence_simple_gb300/csrc/gla_decode.cu", "98de2132efc39ffd",
+                         7263972864.0 / 49152, "per state per step"),
+    # the MXFP8 pool: 972.098816 MB read + 892.308224 MB written
+    "decode_mxfp8_state": ("linear_attention_recurrence_simple_gb300/csrc/gla_mxfp8.cu", "03105fd25d81642d",
+                           1864407040.0 / 49152, "per state per step"),
 }
 
 
@@ -487,7 +496,8 @@ def bench_decode(torch, gla, wl, dist, args, peaks, aug=False, bf16_state=False,
     res["roofline"]["algorithmic_bytes_note"] = ("bf16" if bf16_state else "fp32") + " state read + write per step"
     if norm_gate:
         res["io_bytes_outside_roofline"] += w.N * H * DV * 2
-    res["roofline"]["traffic"] = None if (aug or bf16_state or norm_gate) else profiled_traffic("decode", w.N * H)
+    row = "decode_bf16_state" if bf16_state else "decode_norm_gate" if norm_gate else "decode"
+    res["roofline"]["traffic"] = None if aug else profiled_traffic(row, w.N * H)
     del state, steps, o, a
     return res
 
@@ -526,6 +536,7 @@ def bench_decode_mxfp8(torch, gla, wl, dist, args, peaks):
            "roofline": roofline(state_bytes, 2 * 2 * w.N * H * DK * DV, region / 1e3, peaks),
            "io_bytes_outside_roofline": w.N * H * (2 * DK * 2 + 2 * DV * 2), "launches_per_step": 1}
     res["roofline"]["algorithmic_bytes_note"] = "MXFP8 state (codes + scales) read + write per step"
+    res["roofline"]["traffic"] = profiled_traffic("decode_mxfp8_state", w.N * H)
     del codes, scales, steps, o
     return res
 
