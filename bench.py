@@ -44,6 +44,10 @@ PROFILED_TRAFFIC = {
     # the fused norm-gate step on the fp32 pool: 3.680579 GB read + 3.583394 GB written
     "decode_norm_gate": ("linear_attention_recurrence_simple_gb300/csrc/gla_decode.cu", "98de2132efc39ffd",
                          7263972864.0 / 49152, "per state per step"),
+    # head RMSNorm + gate, 16,384 x 16 rows: 201.355776 MB read + 70.854144 MB written (part of y
+    # is still in L2 when the kernel ends), one launch
+    "norm_gate": ("linear_attention_recurrence_simple_gb300/csrc/gla_norm.cu", "4987f08ea9f6d8e4",
+                  272209920.0, "per launch of the 16,384 x 16 rows"),
     # the MXFP8 pool: 972.098816 MB read + 892.308224 MB written
     "decode_mxfp8_state": ("linear_attention_recurrence_simple_gb300/csrc/gla_mxfp8.cu", "03105fd25d81642d",
                            1864407040.0 / 49152, "per state per step"),
@@ -371,6 +375,7 @@ def bench_norm_gate(torch, gla, wl, dist, args, peaks):
            "tokens": rows, "ms_per_step": region, "value": rows * dist.world / (region / 1e3),
            "unit": "tokens/s", "roofline": roofline(byts, rows * H * DV * 8, region / 1e3, peaks),
            "kernel_ms": per_call, "launches_per_step": 1}
+    res["roofline"]["traffic"] = profiled_traffic("norm_gate")
     del o, g, wt, tier, y
     return res
 

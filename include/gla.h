@@ -168,7 +168,7 @@ int gla_decode_step_aug(const void* q, const void* k, const void* v, const float
  *   tier         [H] int32 device: the tier of each head; a value outside [0, n_tiers) leaves
  *                that head's rows untouched and records GLA_ERR_SHAPE in the device error word.
  *   eps          >= 0, added to the mean square (not stated on the pages).
- * n_tiers <= 32 and H <= 4096 (else GLA_ERR_UNSUPPORTED).  Pointers 16-byte aligned (tier 4-byte).  Returns GLA_OK once the work is queued on `stream`. */
+ * H <= 4096 (else GLA_ERR_UNSUPPORTED).  Pointers 16-byte aligned (tier 4-byte).  Returns GLA_OK once the work is queued on `stream`. */
 int gla_head_norm_gate(const void* o, const void* g, const float* weight, const int32_t* tier,
                        int n_tiers, float eps, void* y, long long rows, int H, int dv, int dtype,
                        gla_stream_t stream);

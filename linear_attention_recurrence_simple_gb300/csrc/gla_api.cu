@@ -402,7 +402,7 @@ int gla_head_norm_gate(const void* o, const void* g, const float* weight, const 
   if (dtype != GLA_BF16 && dtype != GLA_F32) return GLA_ERR_DTYPE;
   if (dv != GLA_DV) return GLA_ERR_UNSUPPORTED;
   if (rows < 0 || H < 1 || n_tiers < 1 || !(eps >= 0.f) || rows > (1ll << 40)) return GLA_ERR_SHAPE;
-  if (n_tiers > 32 || H > 4096) return GLA_ERR_UNSUPPORTED;  // the kernel's shared-memory copies
+  if (H > 4096) return GLA_ERR_UNSUPPORTED;  // with rows <= 2^40, element offsets stay below 2^60
   if (rows == 0) return GLA_OK;
   if (!o || !g || !weight || !tier || !y) return GLA_ERR_NULL;
   for (const void* p : {o, g, (const void*)weight, (const void*)y})

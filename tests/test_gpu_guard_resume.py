@@ -161,6 +161,73 @@ def test_decode_writes_nothing_outside_pool_and_o(state_bf16):
     assert torch.equal(pool.t[[2, 4, 5, 6]], untouched)   # rows no slot names stay as they were
 
 
+def _decode_inputs(seed, N, H, dt):
+    q = torch.from_numpy(gs.normal(seed, 1, (N, H, 96), 0.1)).cuda().to(dt)
+    k = torch.from_numpy(gs.normal(seed, 2, (N, H, 96), 0.1)).cuda().to(dt)
+    v = torch.from_numpy(gs.normal(seed, 3, (N, H, 192))).cuda().to(dt)
+    return q, k, v, torch.from_numpy(gs.laplace_log_lambda(H)).cuda()
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_decode_norm_gate_writes_nothing_outside_pool_and_y(bf16):
+    N, H, P = 5, 6, 9
+    dt = torch.bfloat16 if bf16 else torch.float32
+    pool = Guarded((P, H, 96, 192), torch.float32)
+    pool.t.copy_(torch.from_numpy(gs.normal(96, 7, (P, H, 96, 192), 0.1)))
+    y = Guarded((N, H, 192), dt)
+    slot = torch.tensor([8, 0, 3, 7, 1], dtype=torch.int32, device="cuda")
+    q, k, v, ll = _decode_inputs(96, N, H, dt)
+    g = torch.from_numpy(gs.normal(96, 4, (N, H, 192), 2.0)).cuda().to(dt)
+    wt = (1.0 + torch.from_numpy(gs.normal(96, 5, (3, 192), 0.3))).cuda()
+    tier = torch.tensor([0, 0, 1, 1, 2, 2], dtype=torch.int32, device="cuda")
+    untouched = pool.t[[2, 4, 5, 6]].clone()
+    gla.gla_decode_step_norm_gate(q, k, v, ll, pool.t, g, wt, tier, scale=float(gs.SCALE), slot=slot, y=y.t)
+    assert pool.intact() and y.intact()
+    assert torch.equal(pool.t[[2, 4, 5, 6]], untouched)
+    assert bool(torch.isfinite(y.t.float()).all())
+
+
+def test_mxfp8_conversions_write_nothing_outside():
+    """Seven state rows (84 blocks of 16 codes, 42 scale bytes: the scale array ends off a
+    16-byte boundary) to MXFP8 and back."""
+    rows = 7
+    x = torch.from_numpy(gs.normal(97, 1, (rows, 192), 0.3)).cuda()
+    codes, scales = Guarded((rows, 192), torch.uint8), Guarded((rows, 6), torch.uint8)
+    back = Guarded((rows, 192), torch.float32)
+    gla.gla_state_to_mxfp8(x, codes.t, scales.t)
+    gla.gla_state_from_mxfp8(codes.t, scales.t, back.t)
+    assert codes.intact() and scales.intact() and back.intact()
+    assert bool(torch.isfinite(back.t).all())
+    assert float((back.t - x).abs().max()) <= float(x.abs().max()) * 2 ** -3
+
+
+def test_mxfp8_decode_writes_nothing_outside_pool_and_o():
+    N, H, P = 5, 3, 9
+    codes = Guarded((P, H, 96, 192), torch.uint8)
+    scales = Guarded((P, H, 96, 6), torch.uint8)
+    gla.gla_state_to_mxfp8(torch.from_numpy(gs.normal(98, 7, (P, H, 96, 192), 0.1)).cuda(), codes.t, scales.t)
+    o = Guarded((N, H, 192), torch.bfloat16)
+    slot = torch.tensor([8, 0, 3, 7, 1], dtype=torch.int32, device="cuda")
+    q, k, v, ll = _decode_inputs(98, N, H, torch.bfloat16)
+    keep_c, keep_s = codes.t[[2, 4, 5, 6]].clone(), scales.t[[2, 4, 5, 6]].clone()
+    gla.gla_decode_step_mxfp8_state(q, k, v, ll, codes.t, scales.t, float(gs.SCALE), slot=slot, o=o.t)
+    assert codes.intact() and scales.intact() and o.intact()
+    assert torch.equal(codes.t[[2, 4, 5, 6]], keep_c) and torch.equal(scales.t[[2, 4, 5, 6]], keep_s)
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_head_norm_gate_writes_nothing_outside_y(bf16):
+    rows, H = 3, 5
+    dt = torch.bfloat16 if bf16 else torch.float32
+    o = torch.from_numpy(gs.normal(99, 1, (rows, H, 192))).cuda().to(dt)
+    g = torch.from_numpy(gs.normal(99, 2, (rows, H, 192), 2.0)).cuda().to(dt)
+    wt = (1.0 + torch.from_numpy(gs.normal(99, 3, (2, 192), 0.3))).cuda()
+    tier = torch.tensor([0, 1, 1, 0, 1], dtype=torch.int32, device="cuda")
+    y = Guarded((rows, H, 192), dt)
+    gla.gla_head_norm_gate(o, g, wt, tier, y=y.t)
+    assert y.intact() and bool(torch.isfinite(y.t.float()).all())
+
+
 def test_decreasing_offsets_are_reported_and_stay_in_bounds():
     """cu_seqlens = [0, 200, 100, 300] (every offset inside [0, T = 300], the middle pair
     decreasing): the kernels clamp sequence 1 to an empty range, record GLA_ERR_SHAPE, and write
