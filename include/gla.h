@@ -67,7 +67,9 @@ typedef enum {
   GLA_ERR_UNSUPPORTED = -5, /* d_k != 96, d_v != 192, or no sm_103 device current */
   GLA_ERR_WORKSPACE = -6,   /* workspace missing or smaller than gla_workspace_bytes() */
   GLA_ERR_LAUNCH = -7,      /* the CUDA runtime refused a launch */
-  GLA_ERR_TIMEOUT = -8      /* a bounded device-side wait gave up (kernel returned early) */
+  GLA_ERR_TIMEOUT = -8,     /* a bounded device-side wait gave up (kernel returned early) */
+  GLA_ERR_BOUNDS = -9       /* debug-bounds build only: a device index fell outside its buffer
+                               (the access was skipped; see gla_debug_bounds) */
 } gla_status;
 
 typedef enum { GLA_BF16 = 0, GLA_F32 = 1 } gla_dtype;
@@ -291,10 +293,19 @@ int gla_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
                           int dtype, gla_stream_t stream);
 
 /* Synchronises `stream`, then returns and clears the current device's sticky error word:
- * GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_SHAPE; GLA_ERR_LAUNCH if the stream itself failed.
+ * GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_SHAPE (or, in the debug-bounds build, GLA_ERR_BOUNDS);
+ * GLA_ERR_LAUNCH if the stream itself failed.
  * There is one word per device, shared by every caller of the library on that device: the first
  * fault recorded since the last read is kept, and whichever caller reads next sees and clears it. */
 int gla_get_device_error(gla_stream_t stream);
+
+/* 1 in the library's debug-bounds build (libgla_debug.so, compiled with GLA_DEBUG_BOUNDS), 0 in
+ * the release build (libgla.so).  The debug-bounds build is the same library with device-side
+ * index checks at the kernels' computed global accesses (state rows, output and gradient rows,
+ * partial-sum rows, packed-order and segment lookups, hand-over flags, TMA coordinates): an index
+ * outside its buffer records GLA_ERR_BOUNDS in the device error word and the access is skipped.
+ * It stands in for a memory checker; its results equal the release build's. */
+int gla_debug_bounds(void);
 
 /* Upper bound, in nanoseconds, of every device-side wait on an mbarrier (default 2e9).  A wait
  * that exceeds it records GLA_ERR_TIMEOUT, drains the copies its CTA has in flight, releases

@@ -10,6 +10,7 @@ Layouts (see ``include/gla.h``): q, k ``[B, T, H, 96]``; v ``[B, T, H, 192]``; p
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -21,7 +22,7 @@ __all__ = [
     "gla_chunk_fwd",
     "gla_chunk_bwd", "gla_decode_step", "gla_chunk_fwd_noalloc", "gla_head_norm_gate", "gla_chunk_fwd_split",
     "gla_split_choose_seg_chunks", "gla_get_device_error",
-    "gla_set_wait_limit_ns",
+    "gla_set_wait_limit_ns", "gla_debug_bounds", "debug_bounds_library",
     "gla_status_string", "DK", "DV", "CHUNK", "EXPORTS",
 ]
 
@@ -33,13 +34,15 @@ EXPORTS = ("gla_workspace_bytes", "gla_bwd_workspace_bytes", "gla_chunk_fwd", "g
            "gla_decode_step_norm_gate", "gla_decode_step_mxfp8_state", "gla_state_to_mxfp8",
            "gla_state_from_mxfp8",
            "gla_split_choose_seg_chunks", "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
-           "gla_status_string")
+           "gla_debug_bounds", "gla_status_string")
 NOALLOC_MAX_SEQS = 16384
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libgla.so")
+_LIB_DEBUG_PATH = os.path.join(_PKG, "libgla_debug.so")  # the debug-bounds build
 _lock = threading.Lock()
-_lib = None
+_libs = {}          # False: release build, True: debug-bounds build
+_use_debug = False  # which one the calls go to (see debug_bounds_library)
 
 
 class GlaError(RuntimeError):
@@ -49,22 +52,26 @@ class GlaError(RuntimeError):
                          f"{gla_status_string(status)} ({status})")
 
 
-def library_path() -> str:
-    return _LIB_PATH
+def library_path(debug: bool = False) -> str:
+    return _LIB_DEBUG_PATH if debug else _LIB_PATH
 
 
-def load_library(build: bool = True):
-    """Loads libgla.so (building it first if missing and ``build``); raises if it cannot."""
-    global _lib
+def load_library(build: bool = True, debug: bool | None = None):
+    """Loads libgla.so, or with ``debug`` (default: inside :func:`debug_bounds_library`) its
+    debug-bounds build libgla_debug.so, building it first if missing and ``build``; raises if it
+    cannot."""
+    if debug is None:
+        debug = _use_debug
     with _lock:
-        if _lib is not None:
-            return _lib
+        if debug in _libs:
+            return _libs[debug]
+        path = library_path(debug)
         if build:
             from . import _build
-            _build.build()
-        if not os.path.exists(_LIB_PATH):
-            raise RuntimeError(f"libgla.so is missing ({_LIB_PATH}); run __graft_entry__.build()")
-        lib = ctypes.CDLL(_LIB_PATH)
+            _build.build(debug=debug)
+        if not os.path.exists(path):
+            raise RuntimeError(f"{os.path.basename(path)} is missing ({path}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
         P, I, F, Z, U = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
                          ctypes.c_ulonglong)
         lib.gla_workspace_bytes.argtypes = [I, I]
@@ -107,8 +114,29 @@ def load_library(build: bool = True):
         lib.gla_set_wait_limit_ns.restype = I
         lib.gla_status_string.argtypes = [I]
         lib.gla_status_string.restype = ctypes.c_char_p
-        _lib = lib
+        lib.gla_debug_bounds.argtypes = []
+        lib.gla_debug_bounds.restype = I
+        _libs[debug] = lib
         return lib
+
+
+@contextlib.contextmanager
+def debug_bounds_library():
+    """Within the block every call goes to the debug-bounds build (libgla_debug.so: device index
+    checks that record GLA_ERR_BOUNDS and skip the access).  Not for concurrent use from several
+    threads.  Each build keeps its own device error word."""
+    global _use_debug
+    lib = load_library(debug=True)
+    prev, _use_debug = _use_debug, True
+    try:
+        yield lib
+    finally:
+        _use_debug = prev
+
+
+def gla_debug_bounds() -> int:
+    """1 when calls go to the debug-bounds build, 0 for the release build."""
+    return int(load_library().gla_debug_bounds())
 
 
 def gla_status_string(status: int) -> str:

@@ -1,4 +1,6 @@
-"""Builds ``libgla.so`` in-tree from ``csrc/*.cu`` for sm_103a (nvcc; one -gencode; parallel)."""
+"""Builds ``libgla.so`` in-tree from ``csrc/*.cu`` for sm_103a (nvcc; one -gencode; parallel), and
+its debug-bounds build ``libgla_debug.so`` (the same sources with ``-DGLA_DEBUG_BOUNDS``: device
+index checks that record GLA_ERR_BOUNDS and skip the access)."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -13,6 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgla.so")
+BUILD_DIR_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libgla_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -39,16 +43,20 @@ def _stale(target, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Builds the release library, or with ``debug`` the debug-bounds one; returns its path."""
     srcs, deps = _inputs()
-    if not force and not _stale(LIB, deps + [__file__]):
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    lib_path, build_dir = (LIB_DEBUG, BUILD_DIR_DEBUG) if debug else (LIB, BUILD_DIR)
+    if debug:
+        extra_flags = tuple(extra_flags) + ("-DGLA_DEBUG_BOUNDS",)
+    if not force and not _stale(lib_path, deps + [__file__]):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     headers = [d for d in deps if not d.endswith(".cu")]
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         if force or _stale(obj, [src, __file__] + headers):
             cmd = [cc] + NVCC_FLAGS + list(extra_flags) + ["-c", src, "-o", obj]
             if verbose:
@@ -62,15 +70,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib_path + f".{os.getpid()}.tmp"
     cmd = [cc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"link of libgla.so failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link of {os.path.basename(lib_path)} failed:\n{r.stderr}")
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -447,6 +447,8 @@ int gla_set_wait_limit_ns(unsigned long long ns) {
   return GLA_OK;
 }
 
+int gla_debug_bounds(void) { return gla::kDebugBounds ? 1 : 0; }
+
 const char* gla_status_string(int status) {
   switch (status) {
     case GLA_OK: return "GLA_OK";
@@ -458,6 +460,7 @@ const char* gla_status_string(int status) {
     case GLA_ERR_WORKSPACE: return "GLA_ERR_WORKSPACE: workspace missing or too small";
     case GLA_ERR_LAUNCH: return "GLA_ERR_LAUNCH: the CUDA runtime refused a launch";
     case GLA_ERR_TIMEOUT: return "GLA_ERR_TIMEOUT: a bounded device wait gave up";
+    case GLA_ERR_BOUNDS: return "GLA_ERR_BOUNDS: a device index check of the debug-bounds build failed";
     default: return "unknown gla_status";
   }
 }

@@ -407,6 +407,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
   float* const pw_base = reinterpret_cast<float*>(sm + SMM::OFF_PW);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Extents of the caller's buffers, for the debug-bounds build's index checks: (token, head) rows
+  // of q, k, v, o and the gradients; rows of the [n_seq, H, 96, 192] states.
+  [[maybe_unused]] const long long tokens = a.cu_seqlens ? (long long)a.T : (long long)a.n_seq * a.T;
+  [[maybe_unused]] const long long rows_total = tokens * a.H, state_rows = (long long)a.n_seq * a.H * DK;
   // Persistent CTAs: this CTA runs work units blockIdx.x, blockIdx.x + gridDim.x, ... (a unit is a
   // (sequence, head, 64-column tile of d_v)); the chunk pipeline runs on across unit boundaries,
   // so a unit's first loads overlap the previous unit's last chunks.  Barrier phases count the
@@ -552,6 +556,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
         uint64_t* full = &bars[B_FULL + s];
         mbar_expect_tx(full, C::STATES ? C::SZ_STAGE - 24576u : C::SZ_STAGE);  // (no q: 24 KB)
         const int tok = (int)(w.tb + (long long)c * CHUNK);
+        (void)GLA_IN_BOUNDS(tok >= 0 && tok < tokens && h >= 0 && h < a.H, a.err);
         if (C::NARROW) {
           tma_load_3d(st + C::ST_X, &maps.x, full, col0, h, tok);
           tma_load_3d(st + C::ST_Y, &maps.y, full, col0, h, tok);
@@ -848,7 +853,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
      float* pw = pw_base + tbuf * PW_FLOATS;
      float* pws = pw + 129;
      if (ku >= 2 && !warp_wait(&bars[B_TBL_EMPTY + tbuf], (uint32_t)((ku - 2) >> 1) & 1u, a, abort_flag)) break;
-     {
+     if (GLA_IN_BOUNDS(w.h >= 0 && w.h < a.H, a.err)) {
        const float ll = a.log_lambda[w.h];
        for (int d = t; d <= 128; d += 128) {
          const float pv = d == 0 ? 1.f : expf((float)d * ll);
@@ -960,7 +965,12 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
              unsigned* flag = &g_handover[prm.flag_set * FLAG_MAX_CTAS + blockIdx.x - NTILE];
              unsigned long long t0 = ~0ull;
              bool seen = true;
-             while (ld_acquire_gpu(flag) != prm.epoch) {
+             if (!GLA_IN_BOUNDS(prm.flag_set < FLAG_SETS && blockIdx.x >= NTILE && blockIdx.x < FLAG_MAX_CTAS + NTILE,
+                                a.err)) {
+               *abort_flag = 1;
+               seen = false;
+             }
+             while (seen && ld_acquire_gpu(flag) != prm.epoch) {
                const unsigned long long tn = global_timer_ns();
                if (t0 == ~0ull) {
                  t0 = tn;
@@ -992,7 +1002,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
                S[4 * x + 3] = __uint_as_float(v.w);
              }
            }
-         } else if (prm.s0 && r_ < DK) {
+         } else if (prm.s0 && r_ < DK && GLA_IN_BOUNDS(srow0 + r_ < state_rows && col0 + TN <= DV, a.err)) {
            const float4* src = reinterpret_cast<const float4*>(prm.s0 + ((long long)srow0 + r_) * DV + col0);
 #pragma unroll
            for (int x = 0; x < TN / 4; ++x) {
@@ -1073,7 +1083,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
               if (staged) {  // 16-byte pieces 2qq, 2qq + 1 of the row, in the 128B-swizzled layout
                 st_shared_v4(srow + ((uint32_t)((2 * qq) ^ (r_ & 7)) << 4), ob[0], ob[1], ob[2], ob[3]);
                 st_shared_v4(srow + ((uint32_t)((2 * qq + 1) ^ (r_ & 7)) << 4), ob[4], ob[5], ob[6], ob[7]);
-              } else if (r_ < L) {
+              } else if (r_ < L && GLA_IN_BOUNDS(orow >= 0 && orow < rows_total, a.err)) {
                 if (out32) {  // one full 32-byte sector per store
                   st_global_v8(dst + 2 * qq, ob);
                 } else {
@@ -1085,7 +1095,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
             if (staged) {
               fence_async_smem();
               __syncwarp();
-              if (lane == 0)
+              if (lane == 0 && GLA_IN_BOUNDS(w.tb + (long long)c * CHUNK + 32 * (warp & 3) + 32 <= tokens, a.err))
                 tma_store_3d(&maps.o, sbase + SMM::OFF_OST + (uint32_t)(warp & 3) * 4096u, col0, h,
                              (int)(w.tb + (long long)c * CHUNK) + 32 * (warp & 3));
               ++nst;
@@ -1119,7 +1129,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
 #pragma unroll 2
               for (int k = 0; k < 12; ++k) {
                 const int pidx = k * 32 + lane, row = pidx / 12, pc = pidx - row * 12;
-                if (((warp & 3) << 5) + row < L) {
+                if (((warp & 3) << 5) + row < L && GLA_IN_BOUNDS(row0 + (long long)row * a.H < rows_total, a.err)) {
                   const uint4 v = ld_shared_v4(wreg + (uint32_t)row * RED_ROW + (uint32_t)pc * 16u);
                   red_add_v4(reinterpret_cast<float*>(prm.out) + (row0 + (long long)row * a.H) * DK + 48 * half + 4 * pc,
                              __uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
@@ -1136,7 +1146,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
          if (C::FWD && prm.s_out) {
            // Forward: each thread stores its final-state row straight from registers (no staging,
            // nothing to wait for); a tail piece raises its hand-over flag once every row is visible.
-           if (r_ < DK) {
+           if (r_ < DK && GLA_IN_BOUNDS(srow0 + r_ < state_rows, a.err)) {
              float* dst = prm.s_out + ((long long)srow0 + r_) * DV + col0;
              if ((reinterpret_cast<uintptr_t>(prm.s_out) & 31u) == 0) {
 #pragma unroll
@@ -1157,12 +1167,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
              __threadfence();
              mbar_arrive(&bars[B_ST_FULL]);
              if (r_ == 0) {
-               if (mbar_wait(&bars[B_ST_FULL], 0u, a.wait_ns, abort_flag))
+               if (mbar_wait(&bars[B_ST_FULL], 0u, a.wait_ns, abort_flag) &&
+                   GLA_IN_BOUNDS(prm.flag_set < FLAG_SETS && blockIdx.x < FLAG_MAX_CTAS, a.err))
                  st_release_gpu(&g_handover[prm.flag_set * FLAG_MAX_CTAS + blockIdx.x], prm.epoch);
              }
            }
          }
-         if (!C::FWD && prm.s_out && r_ < DK) {
+         if (!C::FWD && prm.s_out && r_ < DK && GLA_IN_BOUNDS(srow0 + r_ < state_rows, a.err)) {
            float4* dst = reinterpret_cast<float4*>(prm.s_out + ((long long)srow0 + r_) * DV + col0);
 #pragma unroll
            for (int x = 0; x < TN / 4; ++x) dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);

@@ -15,6 +15,7 @@ constexpr int CHUNK = 128;
 // Positive codes stored in the device error word (the host negates them into gla_status).
 constexpr unsigned ERR_SHAPE = 2;
 constexpr unsigned ERR_TIMEOUT = 8;
+constexpr unsigned ERR_BOUNDS = 9;
 
 // Everything a chunked forward or backward kernel needs; passed by value.
 struct ChunkArgs {
@@ -63,6 +64,22 @@ __device__ __forceinline__ void raise_error(unsigned* word, unsigned code) {
   atomicCAS(word, 0u, code);
 }
 
+// Index checks of the debug-bounds build (compiled with -DGLA_DEBUG_BOUNDS, a stand-in for a
+// memory checker): `ok` states that an access stays inside its buffer; when it does not, the
+// error word records ERR_BOUNDS and the caller skips the access.  In the release build the check
+// is the constant true and the condition is never evaluated.
+#ifdef GLA_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#define GLA_IN_BOUNDS(ok, err) (::gla::in_bounds_check((ok), (err)))
+__device__ __forceinline__ bool in_bounds_check(bool ok, unsigned* err) {
+  if (!ok) raise_error(err, ERR_BOUNDS);
+  return ok;
+}
+#else
+constexpr bool kDebugBounds = false;
+#define GLA_IN_BOUNDS(ok, err) true
+#endif
+
 // Token range [begin, end) of sequence n.  Packed offsets are read on the device, so they are
 // clamped here to 0 <= begin <= end <= T (the packed total), which keeps every access inside the
 // caller's buffers whatever the offsets hold; an offset that needed clamping (decreasing, negative
@@ -87,7 +104,19 @@ __device__ __forceinline__ void unit_of(const ChunkArgs& a, int tiles, int b, in
   const int rem = (int)((unsigned)b - (unsigned)rank * per_seq);
   h = rem / tiles;
   tile = rem % tiles;
-  n = a.order ? a.order[rank] : rank;
+  n = a.order && GLA_IN_BOUNDS(rank < a.n_seq, a.err) ? a.order[rank] : rank;
+  if (!GLA_IN_BOUNDS(n >= 0 && n < a.n_seq, a.err)) n = 0;
+}
+// Debug-bounds build: a unit's (sequence, head) and a chunk's rows [t0, t0 + L) lie inside the
+// caller's buffers (always true in the release build).
+__device__ __forceinline__ bool unit_in_bounds([[maybe_unused]] const ChunkArgs& a, [[maybe_unused]] int n,
+                                               [[maybe_unused]] int h) {
+  return GLA_IN_BOUNDS(n >= 0 && n < a.n_seq && h >= 0 && h < a.H, a.err);
+}
+__device__ __forceinline__ bool rows_in_bounds([[maybe_unused]] const ChunkArgs& a, [[maybe_unused]] long long t0,
+                                               [[maybe_unused]] int L) {
+  return GLA_IN_BOUNDS(t0 >= 0 && L >= 0 && t0 + L <= (a.cu_seqlens ? (long long)a.T : (long long)a.n_seq * a.T),
+                       a.err);
 }
 __device__ __forceinline__ void unit_of_block(const ChunkArgs& a, int tiles, int& n, int& h, int& tile) {
   unit_of(a, tiles, (int)blockIdx.x, n, h, tile);

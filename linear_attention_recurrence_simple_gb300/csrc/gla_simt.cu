@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(ChunkArgs a) {
   unit_of_block(a, FWD_TILES, n, h, tile);
   long long tb, te;
   seq_range(a, n, tb, te);
+  if (!unit_in_bounds(a, n, h)) return;  // (debug-bounds build; uniform over the CTA)
   const int col0 = tile * FWD_TILE;
   const T* q = (const T*)a.q;
   const T* k = (const T*)a.k;
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(ChunkArgs a) {
 
   for (long long t0 = tb; t0 < te; t0 += SC) {
     const int L = (int)(te - t0 < SC ? te - t0 : SC);
+    if (!rows_in_bounds(a, t0, L)) break;  // (debug-bounds build; uniform over the CTA)
     load_rows(Qs, PK, q, t0, L, a.H, h, DK, 0, DK);
     load_rows(Ks, PK, k, t0, L, a.H, h, DK, 0, DK);
     load_rows(Vs, PT, v, t0, L, a.H, h, DV, col0, FWD_TILE);
@@ -168,6 +170,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_dq_kernel(ChunkArgs a) {
   unit_of_block(a, BQ_TILES, n, h, tile);
   long long tb, te;
   seq_range(a, n, tb, te);
+  if (!unit_in_bounds(a, n, h)) return;  // (debug-bounds build; uniform over the CTA)
   const int row0 = tile * BQ_TILE;
   const T* k = (const T*)a.k;
   const T* v = (const T*)a.v;
@@ -183,6 +186,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_dq_kernel(ChunkArgs a) {
   __syncthreads();
   for (long long t0 = tb; t0 < te; t0 += SC) {
     const int L = (int)(te - t0 < SC ? te - t0 : SC);
+    if (!rows_in_bounds(a, t0, L)) break;  // (debug-bounds build; uniform over the CTA)
     load_rows(Vs, PV, v, t0, L, a.H, h, DV, 0, DV);
     load_rows(Gs, PV, dO, t0, L, a.H, h, DV, 0, DV);
     load_rows(Ks, PQ, k, t0, L, a.H, h, DK, row0, BQ_TILE);
@@ -251,6 +255,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_dk_kernel(ChunkArgs a) {
   unit_of_block(a, BQ_TILES, n, h, tile);
   long long tb, te;
   seq_range(a, n, tb, te);
+  if (!unit_in_bounds(a, n, h)) return;  // (debug-bounds build; uniform over the CTA)
   const int row0 = tile * BQ_TILE;
   const T* q = (const T*)a.q;
   const T* v = (const T*)a.v;
@@ -268,6 +273,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_dk_kernel(ChunkArgs a) {
   for (long long m0 = nchunks - 1; m0 >= 0; --m0) {
     const long long t0 = tb + m0 * SC;
     const int L = (int)(te - t0 < SC ? te - t0 : SC);
+    if (!rows_in_bounds(a, t0, L)) break;  // (debug-bounds build; uniform over the CTA)
     load_rows(Vs, PV, v, t0, L, a.H, h, DV, 0, DV);
     load_rows(Gs, PV, dO, t0, L, a.H, h, DV, 0, DV);
     load_rows(Qs, PQ, q, t0, L, a.H, h, DK, row0, BQ_TILE);
@@ -347,6 +353,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_dv_kernel(ChunkArgs a) {
   unit_of_block(a, BV_TILES, n, h, tile);
   long long tb, te;
   seq_range(a, n, tb, te);
+  if (!unit_in_bounds(a, n, h)) return;  // (debug-bounds build; uniform over the CTA)
   const int col0 = tile * BV_TILE;
   const T* q = (const T*)a.q;
   const T* k = (const T*)a.k;
@@ -364,6 +371,7 @@ __global__ void __launch_bounds__(NT) simt_bwd_dv_kernel(ChunkArgs a) {
   for (long long m0 = nchunks - 1; m0 >= 0; --m0) {
     const long long t0 = tb + m0 * SC;
     const int L = (int)(te - t0 < SC ? te - t0 : SC);
+    if (!rows_in_bounds(a, t0, L)) break;  // (debug-bounds build; uniform over the CTA)
     load_rows(Qs, PK, q, t0, L, a.H, h, DK, 0, DK);
     load_rows(Ks, PK, k, t0, L, a.H, h, DK, 0, DK);
     load_rows(Gs, PT, dO, t0, L, a.H, h, DV, col0, BV_TILE);

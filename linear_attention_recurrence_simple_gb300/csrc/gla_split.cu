@@ -40,12 +40,15 @@ constexpr int SCAN_AHEAD = 4;                  // segments whose loads are issue
 __global__ void __launch_bounds__(SPLIT_THREADS)
 split_scan_kernel(const float4* __restrict__ U, const float4* __restrict__ h0, const int32_t* __restrict__ seg_cu,
                   const int32_t* __restrict__ seg_first, const float* __restrict__ log_lambda,
-                  float4* __restrict__ S_in, float4* __restrict__ hT, int H) {
+                  float4* __restrict__ S_in, float4* __restrict__ hT, int H, [[maybe_unused]] int n_seq,
+                  [[maybe_unused]] int M, [[maybe_unused]] unsigned* err) {
   const long long nh = blockIdx.x / SCAN_CTAS_PER_STATE;
   const int e = (int)(blockIdx.x % SCAN_CTAS_PER_STATE) * SPLIT_THREADS + (int)threadIdx.x;
   const int n = (int)(nh / H), h = (int)(nh % H);
+  if (!GLA_IN_BOUNDS(n < n_seq && e < STATE4, err)) return;
   const float ll = log_lambda[h];
   const int i0 = seg_first[n], i1 = seg_first[n + 1];
+  if (!GLA_IN_BOUNDS(0 <= i0 && i0 <= i1 && i1 <= M, err)) return;  // sequence n's segments
   float4 s = h0 ? h0[nh * STATE4 + e] : make_float4(0.f, 0.f, 0.f, 0.f);
   for (int i = i0; i < i1; i += SCAN_AHEAD) {
     float4 u[SCAN_AHEAD];
@@ -295,9 +298,14 @@ int gla_chunk_fwd_split(const void* q, const void* k, const void* v, const float
     if (rc) return rc;
   }
   // 2. chain the segment states
+  unsigned* scan_err = nullptr;
+  {
+    unsigned long long wait_ns;
+    if ((rc = gla::current_device_state(&scan_err, &wait_ns)) != GLA_OK) return rc;
+  }
   gla::split_scan_kernel<<<(unsigned)((long long)n_seq * H * gla::SCAN_CTAS_PER_STATE), gla::SPLIT_THREADS, 0,
                            s>>>((const float4*)U, (const float4*)h0, seg_cu, seg_first, log_lambda,
-                                (float4*)S_in, (float4*)hT, H);
+                                (float4*)S_in, (float4*)hT, H, n_seq, plan.M, scan_err);
   if (cudaGetLastError() != cudaSuccess) return GLA_ERR_LAUNCH;
   // 3. the outputs, each segment from its starting state
   if (aug)

@@ -42,6 +42,21 @@ def test_library_exports_every_declared_symbol(lib):
     assert exported == set(_declared())
 
 
+def test_debug_bounds_build_exports_the_same_symbols_and_says_which_it_is(lib):
+    """libgla_debug.so (GLA_DEBUG_BOUNDS: device index checks) exports the same C ABI; the two
+    builds tell themselves apart without touching a GPU."""
+    dbg = gla.load_library(debug=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", gla.library_path(debug=True)], capture_output=True,
+                         text=True, check=True).stdout
+    assert set(re.findall(r"\bT (gla_[a-z_0-9]+)\b", out)) == set(_declared())
+    assert lib.gla_debug_bounds() == 0 and dbg.gla_debug_bounds() == 1
+    assert gla.gla_debug_bounds() == 0
+    with gla.debug_bounds_library():
+        assert gla.gla_debug_bounds() == 1
+        assert gla.gla_status_string(-9).startswith("GLA_ERR_BOUNDS")
+    assert gla.gla_debug_bounds() == 0
+
+
 def test_library_needs_no_cuda_runtime_soname():
     out = subprocess.run(["readelf", "-d", gla.library_path()], capture_output=True, text=True,
                          check=True).stdout
