@@ -277,59 +277,34 @@ def bench_fwd(torch, gla, wl, dist, args, peaks):
         "kernel_ms": per_call, "launches_per_step": 1,
     }
     res["roofline"]["traffic"] = profiled_traffic("fwd")
-    # e2e through the public call with host buffers: every step copies q, k, v from pinned host
-    # memory and reads o, hT back.  The batch's sequences are independent, so the step runs as a
-    # pipeline over sub-batches of whole sequences: the host-to-device copy of sub-batch i + 1 and
-    # the device-to-host copy of sub-batch i - 1 overlap the forward of sub-batch i, on three
-    # streams ordered by events; the step's region covers all of it.
+    # e2e through the C ABI with host buffers (gla_chunk_fwd_host): every step copies q, k, v in
+    # from pinned host memory and o, hT back out, inside the library, pipelined with the compute
+    # over pieces of the batch (sub-batches of whole sequences, or with more pieces than
+    # sequences, parts of each sequence cut at chunk boundaries and chained through the state);
+    # the step's region covers all of it.
     hq, hk, hv = (x.cpu().pin_memory() for x in (g["q"], g["k"], g["v"]))
     ho, hh = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(hT, device="cpu").pin_memory()
-    dq_, dk_, dv_ = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
-    parts = max(1, min(args.e2e_parts, w.n_seq))
-    bounds = [w.n_seq * i // parts for i in range(parts + 1)]
-    comp = torch.cuda.current_stream()
-    s_ins = [torch.cuda.Stream() for _ in range(max(1, args.e2e_copy_streams))]
-    s_out = torch.cuda.Stream()
+    B_, T_, H_ = g["q"].shape[:3]
+    ws_host = torch.empty(gla.gla_chunk_fwd_host_workspace_bytes(B_, T_, H_, 0), dtype=torch.uint8, device="cuda")
+    pieces = max(1, args.e2e_parts)
 
     def e2e():
-        start = torch.cuda.Event()
-        start.record(comp)
-        for st in s_ins:
-            st.wait_event(start)
-        for i in range(parts):
-            a, b = bounds[i], bounds[i + 1]
-            for j, (dst, src) in enumerate(((dq_, hq), (dk_, hk), (dv_, hv))):
-                st = s_ins[j % len(s_ins)]
-                with torch.cuda.stream(st):
-                    dst[a:b].copy_(src[a:b], non_blocking=True)
-            for st in s_ins:
-                landed = torch.cuda.Event()
-                landed.record(st)
-                comp.wait_event(landed)
-            gla.gla_chunk_fwd(dq_[a:b], dk_[a:b], dv_[a:b], g["log_lambda"], w.scale, o=o[a:b], hT=hT[a:b])
-            computed = torch.cuda.Event()
-            computed.record(comp)
-            s_out.wait_event(computed)
-            with torch.cuda.stream(s_out):
-                ho[a:b].copy_(o[a:b], non_blocking=True)
-                hh[a:b].copy_(hT[a:b], non_blocking=True)
-        finished = torch.cuda.Event()
-        finished.record(s_out)
-        comp.wait_event(finished)
+        gla.gla_chunk_fwd_host(hq, hk, hv, g["log_lambda"], w.scale, o=ho, hT=hh, pieces=pieces, workspace=ws_host)
     e_region, _ = timed(torch, dist, e2e, args.steps, args.warmup)
     e_region = dist.max(e_region)
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hh.numel() * hh.element_size()
     res["e2e"] = {"value": tokens * dist.world / (e_region / 1e3), "unit": "tokens/s",
                   "ms_per_step": e_region, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                  "pipeline": f"{parts} sub-batches of whole sequences: host-to-device copies "
-                              f"({len(s_ins)} streams), forward and device-to-host copies overlapped"}
+                  "call": "gla_chunk_fwd_host (pinned host q, k, v in; o, hT out)",
+                  "pipeline": f"{pieces} pieces: host-to-device copies, forward and device-to-host copies "
+                              f"overlapped on three streams inside the library"}
     # the pipelined results are the plain call's results
     ref_o, ref_h = o.clone(), hT.clone()
     gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], w.scale, o=ref_o, hT=ref_h)
     torch.cuda.synchronize()
     res["e2e"]["matches_device_call"] = bool(torch.equal(ho, ref_o.cpu()) and torch.equal(hh, ref_h.cpu()))
-    del g, o, hT, hq, hk, hv, ho, hh, dq_, dk_, dv_
+    del g, o, hT, hq, hk, hv, ho, hh, ws_host
     return res
 
 
@@ -672,9 +647,8 @@ def main():
                     help="sequences in the decode pool (1280 = the measured workload)")
     ap.add_argument("--decode-layers", type=int, default=24)
     ap.add_argument("--e2e-parts", type=int, default=8,
-                    help="sub-batches of the e2e pipeline (copies overlapped with compute)")
-    ap.add_argument("--e2e-copy-streams", type=int, default=1,
-                    help="streams sharing the e2e pipeline's host-to-device copies")
+                    help="pieces of the e2e pipeline (copies overlapped with compute); more pieces than "
+                         "sequences cut each sequence at chunk boundaries")
     ap.add_argument("--launcher-check", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -292,6 +292,36 @@ int gla_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
                           const int32_t* cu_seqlens, int n_seq, int T, int H, int dk, int dv,
                           int dtype, gla_stream_t stream);
 
+/* The chunked forward on HOST buffers ("Beyond the KV cache", section "Challenge 1: Using native
+ * PyTorch on Trainium for GLA": sequences are independent, and within one the scan carries only
+ * the state across a chunk boundary): q, k, v are read from host memory and o, hT written back
+ * to host memory, the copies pipelined with the compute inside the call.  The batch is cut into
+ * `pieces`: sub-batches of whole sequences (pieces <= n_seq), or, with pieces > n_seq, each
+ * sequence cut into pieces / n_seq parts of a whole number of 128-token chunks (fewer when T does
+ * not divide so), a part starting from the final state of the one before, which is the state the
+ * uncut scan carries across that boundary: the results equal gla_chunk_fwd's on the same values.
+ * Piece i is copied in on a library stream while piece i - 1 runs on `stream` and piece i - 2 is
+ * copied out on another library stream; `stream` completes after the last copy out, so the host
+ * outputs may be read once `stream` has been synchronised.
+ *   q, k, v      HOST [n_seq, T, H, 96 / 192] of dtype `dtype` (page-locked memory lets the copies
+ *                overlap the compute; pageable memory works, without the overlap).
+ *   h0           HOST [n_seq, H, 96, 192] fp32, or NULL for zeros.
+ *   o, hT        HOST outputs (o as v; hT [n_seq, H, 96, 192] fp32, or NULL to skip).
+ *   log_lambda   DEVICE [H] fp32, 16-byte aligned.
+ *   pieces       >= 1.
+ *   workspace    DEVICE, 256-byte aligned, >= gla_chunk_fwd_host_workspace_bytes(n_seq, T, H,
+ *                dtype) bytes: the staged batch (q, k, v, o) and three sets of states.
+ * Fixed-length batches only.  Returns GLA_OK once the work is queued; argument errors as in
+ * gla_chunk_fwd, GLA_ERR_WORKSPACE for a missing or short workspace, GLA_ERR_LAUNCH if a copy or
+ * an event could not be queued.  Calls on one device are issued one at a time (a library mutex);
+ * their work may still overlap on the GPU.
+ * gla_chunk_fwd_host_workspace_bytes returns 0 for n_seq < 0, T < 0, H < 1 or an unknown dtype. */
+size_t gla_chunk_fwd_host_workspace_bytes(int n_seq, int T, int H, int dtype);
+int gla_chunk_fwd_host(const void* q, const void* k, const void* v, const float* log_lambda,
+                       const float* h0, float scale, void* o, float* hT, int n_seq, int T, int H,
+                       int dk, int dv, int dtype, int pieces, void* workspace, size_t ws_bytes,
+                       gla_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the current device's sticky error word:
  * GLA_OK, GLA_ERR_TIMEOUT or GLA_ERR_SHAPE (or, in the debug-bounds build, GLA_ERR_BOUNDS);
  * GLA_ERR_LAUNCH if the stream itself failed.

@@ -22,7 +22,8 @@ __all__ = [
     "gla_chunk_fwd",
     "gla_chunk_bwd", "gla_decode_step", "gla_chunk_fwd_noalloc", "gla_head_norm_gate", "gla_chunk_fwd_split",
     "gla_split_choose_seg_chunks", "gla_get_device_error",
-    "gla_set_wait_limit_ns", "gla_debug_bounds", "debug_bounds_library",
+    "gla_set_wait_limit_ns", "gla_debug_bounds", "debug_bounds_library", "gla_chunk_fwd_host",
+    "gla_chunk_fwd_host_workspace_bytes",
     "gla_status_string", "DK", "DV", "CHUNK", "EXPORTS",
 ]
 
@@ -34,7 +35,7 @@ EXPORTS = ("gla_workspace_bytes", "gla_bwd_workspace_bytes", "gla_chunk_fwd", "g
            "gla_decode_step_norm_gate", "gla_decode_step_mxfp8_state", "gla_state_to_mxfp8",
            "gla_state_from_mxfp8",
            "gla_split_choose_seg_chunks", "gla_chunk_fwd_noalloc", "gla_get_device_error", "gla_set_wait_limit_ns",
-           "gla_debug_bounds", "gla_status_string")
+           "gla_debug_bounds", "gla_chunk_fwd_host", "gla_chunk_fwd_host_workspace_bytes", "gla_status_string")
 NOALLOC_MAX_SEQS = 16384
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -116,6 +117,10 @@ def load_library(build: bool = True, debug: bool | None = None):
         lib.gla_status_string.restype = ctypes.c_char_p
         lib.gla_debug_bounds.argtypes = []
         lib.gla_debug_bounds.restype = I
+        lib.gla_chunk_fwd_host_workspace_bytes.argtypes = [I, I, I, I]
+        lib.gla_chunk_fwd_host_workspace_bytes.restype = Z
+        lib.gla_chunk_fwd_host.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, P, Z, P]
+        lib.gla_chunk_fwd_host.restype = I
         _libs[debug] = lib
         return lib
 
@@ -296,6 +301,55 @@ def gla_chunk_fwd_noalloc(q, k, v, log_lambda, scale=None, h0=None, cu_seqlens=N
                                        _ptr(o), _ptr(hT), _ptr(cu_seqlens), n_seq, T, H, DK, DV, dt,
                                        _stream(dev))
     _check(rc, "gla_chunk_fwd_noalloc")
+    return o, hT
+
+
+def gla_chunk_fwd_host_workspace_bytes(n_seq: int, T: int, H: int, dtype_code: int) -> int:
+    return int(load_library().gla_chunk_fwd_host_workspace_bytes(n_seq, T, H, dtype_code))
+
+
+def gla_chunk_fwd_host(q, k, v, log_lambda, scale=None, h0=None, o=None, hT=None, pieces=16, workspace=None,
+                       output_final_state: bool = True):
+    """The forward on HOST tensors (``gla_chunk_fwd_host``): q, k ``[B, T, H, 96]``, v
+    ``[B, T, H, 192]`` and h0 (fp32, optional) on the CPU (page-locked for overlapped copies);
+    log_lambda on the device.  Returns host ``(o, hT)``, written once the current stream has run
+    (synchronise it before reading).  The library copies ``pieces`` pieces in, runs them and
+    copies them out, pipelined; ``workspace`` is a device buffer of at least
+    :func:`gla_chunk_fwd_host_workspace_bytes` bytes (allocated when not given)."""
+    lib = load_library()
+    dev = log_lambda.device
+    if dev.type != "cuda":
+        raise ValueError("log_lambda must be on the device")
+    dt = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.device.type != "cpu" or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor of q's dtype")
+    if q.dim() != 4 or q.shape[3] != DK or k.shape != q.shape or v.shape != (*q.shape[:3], DV):
+        raise ValueError("expected q, k [B, T, H, 96] and v [B, T, H, 192]")
+    B, T, H = q.shape[:3]
+    _need(log_lambda, "log_lambda", torch.float32, dev, H)
+    if h0 is not None and (h0.device.type != "cpu" or h0.dtype != torch.float32 or not h0.is_contiguous()
+                           or h0.shape != (B, H, DK, DV)):
+        raise ValueError("h0 must be a contiguous CPU fp32 tensor [B, H, 96, 192]")
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype).pin_memory()
+    if hT is None and output_final_state:
+        hT = torch.empty((B, H, DK, DV), dtype=torch.float32).pin_memory()
+    for name, t, shape, dtype in (("o", o, v.shape, v.dtype), ("hT", hT, (B, H, DK, DV), torch.float32)):
+        if t is not None and (t.device.type != "cpu" or t.dtype != dtype or t.shape != shape or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CPU tensor {tuple(shape)} of {dtype}")
+    need = gla_chunk_fwd_host_workspace_bytes(B, T, H, dt)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if workspace.numel() < need:
+        raise ValueError(f"workspace has {workspace.numel()} bytes, needs {need}")
+    s = float(DK ** -0.5) if scale is None else float(scale)
+    with torch.cuda.device(dev):
+        rc = lib.gla_chunk_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), s, _ptr(o), _ptr(hT),
+                                    B, T, H, DK, DV, dt, int(pieces), _ptr(workspace), workspace.numel(),
+                                    _stream(dev))
+    _check(rc, "gla_chunk_fwd_host")
     return o, hT
 
 

@@ -249,6 +249,41 @@ def test_bwd_argument_errors(lib):
     assert bwd(n=0) == OK
 
 
+def test_host_forward_argument_errors(lib):
+    """gla_chunk_fwd_host validates before touching a device: dtype, sizes, pointers, workspace."""
+    P = ctypes.c_void_p
+    need = lib.gla_chunk_fwd_host_workspace_bytes(2, 256, 4, 0)
+
+    def hf(q=A, k=A, v=A, ll=A, o=A, n=2, T=256, H=4, dk=96, dv=192, dt=0, pieces=4, ws=A, wsb=None):
+        return lib.gla_chunk_fwd_host(P(q), P(k), P(v), P(ll), None, ctypes.c_float(0.1), P(o), None, n, T, H,
+                                      dk, dv, dt, pieces, P(ws), need if wsb is None else wsb, None)
+    assert hf(dt=7) == DTYPE
+    assert hf(dk=64) == UNSUP
+    assert hf(n=-1) == SHAPE
+    assert hf(H=0) == SHAPE
+    assert hf(pieces=0) == SHAPE
+    assert hf(n=0, q=None, o=None) == OK
+    assert hf(ll=None) == NULL
+    assert hf(q=None) == NULL
+    assert hf(ws=None) == WS
+    assert hf(wsb=need - 1) == WS
+    assert hf(ws=A + 16) == ALIGN   # the workspace is 256-byte aligned
+    assert hf(ll=A + 4) == ALIGN
+
+
+def test_host_forward_workspace_bytes(lib):
+    """The staged batch (q, k, v, o, each rounded up to 256 bytes) and four state sets."""
+    def r(x):
+        return -(-x // 256) * 256
+    rows = 2 * 256 * 4
+    st = r(2 * 4 * 96 * 192 * 4)
+    for dt, el in ((0, 2), (1, 4)):
+        assert lib.gla_chunk_fwd_host_workspace_bytes(2, 256, 4, dt) == (
+            2 * r(rows * 96 * el) + 2 * r(rows * 192 * el) + 4 * st)
+    assert lib.gla_chunk_fwd_host_workspace_bytes(-1, 256, 4, 0) == 0
+    assert lib.gla_chunk_fwd_host_workspace_bytes(2, 256, 4, 9) == 0
+
+
 def test_bwd_workspace_bytes(lib):
     acc = 2 * 8 * 2048 * 16 * 96 * 4
     assert gla.gla_bwd_workspace_bytes(8, 2048, 16, False, 0) == 256 + acc
