@@ -314,7 +314,8 @@ int gla_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
  * Fixed-length batches only.  Returns GLA_OK once the work is queued; argument errors as in
  * gla_chunk_fwd, GLA_ERR_WORKSPACE for a missing or short workspace, GLA_ERR_LAUNCH if a copy or
  * an event could not be queued.  Calls on one device are issued one at a time (a library mutex);
- * their work may still overlap on the GPU.
+ * their work may still overlap on the GPU, so calls on streams that are not ordered with each
+ * other need workspaces of their own (calls on one stream may share one).
  * gla_chunk_fwd_host_workspace_bytes returns 0 for n_seq < 0, T < 0, H < 1 or an unknown dtype. */
 size_t gla_chunk_fwd_host_workspace_bytes(int n_seq, int T, int H, int dtype);
 int gla_chunk_fwd_host(const void* q, const void* k, const void* v, const float* log_lambda,
