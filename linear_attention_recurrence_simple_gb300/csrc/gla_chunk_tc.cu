@@ -118,7 +118,7 @@ constexpr uint32_t SZ_TILE64 = 128 * 128;       // one 128-row, 128-byte-row til
 constexpr uint32_t SZ_SPH = 96 * 128;           // bf16 state tile: 96 rows (d_k) x 64 columns
 constexpr uint32_t SZ_SP = 2 * SZ_SPH;          // hi then lo
 enum {
-  B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY, B_A_FULL, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
+  B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY = 6, B_A_FULL = 8, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
   B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY,
   B_ZR, B_P_HALF = B_ZR + 2, B_TBL_FULL, B_TBL_EMPTY = B_TBL_FULL + 2, B_ST_FULL = B_TBL_EMPTY + 2,
   B_HANDOVER, B_DRAIN, NBAR = B_DRAIN + 3
@@ -129,13 +129,17 @@ constexpr uint32_t RED_ROW = 208;                 // 192 bytes of fp32 + 16 (ban
 constexpr uint32_t RED_WARP_BYTES = 32 * RED_ROW;
 template <int MODE>
 struct Smem {
+  // weighted Z4 copies (hi and lo): two buffers in the states-only scan, whose next chunk's
+  // weighting then overlaps this chunk's MMA4 (it has no state copy and no output staging)
+  static constexpr uint32_t NVT = Cfg<MODE>::STATES ? 2 : 1;
   static constexpr uint32_t OFF_VT = 2 * Cfg<MODE>::SZ_STAGE;
-  static constexpr uint32_t OFF_SP = OFF_VT + 2 * SZ_TILE64;
+  static constexpr uint32_t OFF_SP = OFF_VT + NVT * 2 * SZ_TILE64;
   // output staging: wide, the bf16 output tile for the TMA store; narrow, one region per epilogue
   // warp (32 rows x 48 fp32, rows padded to 208 bytes) that turns row-wise sums into adds of
   // contiguous row segments
-  static constexpr uint32_t OFF_OST = OFF_SP + SZ_SP;
-  static constexpr uint32_t OFF_PW = OFF_OST + (Cfg<MODE>::NARROW ? 4u * RED_WARP_BYTES : SZ_TILE64);
+  static constexpr uint32_t OFF_OST = OFF_SP + (Cfg<MODE>::STATES ? 0 : SZ_SP);
+  static constexpr uint32_t OFF_PW =
+      OFF_OST + (Cfg<MODE>::STATES ? 0 : (Cfg<MODE>::NARROW ? 4u * RED_WARP_BYTES : SZ_TILE64));
   // two decay tables (per unit parity), then (self-augmentation) two copies of the head's aug_balance
   static constexpr uint32_t OFF_AUG = Cfg<MODE>::AUG ? (OFF_PW + 2 * PW_FLOATS * 4 + 8 + 15) / 16 * 16
                                                       : OFF_PW + 2 * PW_FLOATS * 4 + 8;
@@ -466,7 +470,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       if (i == B_TBL_EMPTY || i == B_TBL_EMPTY + 1) cnt = C::SPLIT ? 512 : (C::STATES ? 256 : 384);  // its readers
       if (i == B_O_FULL) cnt = 2;
       if (i == B_ST_FULL) cnt = 128;  // the epilogue threads' final-state rows are visible (tail piece)
-      if (i == B_VT_FULL || i == B_A_EMPTY || i == B_P_FULL || i == B_P_HALF || i == B_U_EMPTY || i == B_SP_FULL ||
+      if (i == B_VT_FULL || i == B_VT_FULL + 1 || i == B_A_EMPTY || i == B_P_FULL || i == B_P_HALF || i == B_U_EMPTY || i == B_SP_FULL ||
           i == B_O_EMPTY || i == B_ZR || i == B_ZR + 1)
         cnt = 128;
       mbar_init(&bars[i], cnt);
@@ -679,7 +683,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
           umma_commit(&bars[B_O_FULL]);
           umma_commit(&bars[B_EMPTY + s]);
         } else {
-          if (!mbar_wait(&bars[B_VT_FULL], pc, a.wait_ns, abort_flag)) { stop = true; break; }
+          const int vb = SMM::NVT == 2 ? (gk & 1) : 0;  // weighted Z4 buffer and its phase
+          const uint32_t vph = SMM::NVT == 2 ? (uint32_t)(gk >> 1) & 1u : pc;
+          if (!mbar_wait(&bars[B_VT_FULL + vb], vph, a.wait_ns, abort_flag)) { stop = true; break; }
           // states only: U accumulates over the unit's chunks, read once after the last
           const bool u_first = !C::STATES || it == wi.it0, u_last = !C::STATES || it + 1 == wi.it1;
           if (u_first && !mbar_wait(&bars[B_U_EMPTY], (C::STATES ? (uint32_t)nu & 1u : pc) ^ 1u, a.wait_ns,
@@ -688,9 +694,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma(tmem + C::TM_U, sdesc(st + C::ST_K4, 16384, 1024, LAYOUT_SW128) + (uint32_t)kk * 2048u,
-                 dvt + (uint32_t)kk * 2048u, ID_U, kk > 0 || !u_first);
+                 dvt + (uint32_t)vb * 2u * SZ_TILE64 + (uint32_t)kk * 2048u, ID_U, kk > 0 || !u_first);
           if (u_last) umma_commit(&bars[B_U_FULL]);
-          umma_commit(&bars[B_VT_EMPTY]);
+          umma_commit(&bars[B_VT_EMPTY + vb]);
           umma_commit(&bars[B_EMPTY + s]);
         }
        }
@@ -871,10 +877,12 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       const uint32_t ph = (uint32_t)(gk >> 1) & 1u, pc = (uint32_t)gk & 1u;
       const int L = min(CHUNK, w.len - c * CHUNK);
       if (!warp_wait(&bars[B_FULL + s], ph, a, abort_flag)) { stop = true; break; }
-      if (!warp_wait(&bars[B_VT_EMPTY], pc ^ 1u, a, abort_flag)) { stop = true; break; }
+      const int vb = SMM::NVT == 2 ? (gk & 1) : 0;  // weighted Z4 buffer and its phase
+      const uint32_t vph = SMM::NVT == 2 ? (uint32_t)(gk >> 1) & 1u : pc;
+      if (!warp_wait(&bars[B_VT_EMPTY + vb], vph ^ 1u, a, abort_flag)) { stop = true; break; }
       const uint8_t* zsrc = sm + s * C::SZ_STAGE + C::ST_Z4;
-      uint8_t* zhi = sm + SMM::OFF_VT;
-      uint8_t* zlo = sm + SMM::OFF_VT + SZ_TILE64;
+      uint8_t* zhi = sm + SMM::OFF_VT + vb * 2 * SZ_TILE64;
+      uint8_t* zlo = zhi + SZ_TILE64;
       {  // Z4t row j = w_j z_j; w_j = 0 past the sequence end
         const int j = t;
         float wj = j < L ? (C::REVERSE ? pws[j + 1] : pw[L - 1 - j]) : 0.f;
@@ -903,7 +911,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
         }
       }
       fence_async_smem();
-      mbar_arrive(&bars[B_VT_FULL]);
+      mbar_arrive(&bars[B_VT_FULL + vb]);
       if (C::REVERSE) mbar_arrive(&bars[B_ZR + s]);
      }
      mbar_arrive(&bars[B_TBL_EMPTY + tbuf]);
