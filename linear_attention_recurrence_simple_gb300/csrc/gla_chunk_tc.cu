@@ -101,13 +101,15 @@ struct Cfg {
   // shared memory of one stage (byte offsets; each tile 1024-aligned)
   //   wide:   X panel 0 (16 KB) | Y 2 panels (32 KB) | Z tile (16 KB) | X panel 1 (8 KB, 64B swizzle)
   //   narrow: X tile (16 KB) | Y tile (16 KB) | Z 2 panels (32 KB)
+  //   states only: Y 2 panels (32 KB) | Z tile (16 KB); no X, so three stages fit in the space of two
+  static constexpr int NSTAGE = STATES ? 3 : 2;  // depth of the TMA ring
   static constexpr uint32_t ST_X = 0;
   static constexpr uint32_t ST_X1 = NARROW ? 0 : 65536;
-  static constexpr uint32_t ST_Y = 16384;
-  static constexpr uint32_t ST_Z = NARROW ? 32768 : 49152;
+  static constexpr uint32_t ST_Y = STATES ? 0 : 16384;
+  static constexpr uint32_t ST_Z = NARROW || STATES ? 32768 : 49152;
   static constexpr uint32_t ST_K4 = NARROW ? ST_Z : ST_Y;
   static constexpr uint32_t ST_Z4 = NARROW ? ST_Y : ST_Z;
-  static constexpr uint32_t SZ_STAGE = NARROW ? 65536 : 73728;
+  static constexpr uint32_t SZ_STAGE = NARROW ? 65536 : (STATES ? 49152 : 73728);
   static constexpr int K1 = NARROW ? 4 : 6;       // K steps of MMA1 and MMA3 (d_v tile / d_k)
   static constexpr int OW = NARROW ? DK : TN;     // output columns per CTA
   // tensor memory columns
@@ -118,7 +120,7 @@ constexpr uint32_t SZ_TILE64 = 128 * 128;       // one 128-row, 128-byte-row til
 constexpr uint32_t SZ_SPH = 96 * 128;           // bf16 state tile: 96 rows (d_k) x 64 columns
 constexpr uint32_t SZ_SP = 2 * SZ_SPH;          // hi then lo
 enum {
-  B_FULL = 0, B_EMPTY = 2, B_VT_FULL = 4, B_VT_EMPTY = 6, B_A_FULL = 8, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
+  B_FULL = 0, B_EMPTY = 3, B_VT_FULL = 6, B_VT_EMPTY = 8, B_A_FULL = 10, B_A_EMPTY, B_P_FULL, B_P_EMPTY,
   B_U_FULL, B_U_EMPTY, B_SP_FULL, B_SP_EMPTY, B_O_FULL, B_O_EMPTY,
   B_ZR, B_P_HALF = B_ZR + 2, B_TBL_FULL, B_TBL_EMPTY = B_TBL_FULL + 2, B_ST_FULL = B_TBL_EMPTY + 2,
   B_HANDOVER, B_DRAIN, NBAR = B_DRAIN + 3
@@ -132,7 +134,7 @@ struct Smem {
   // weighted Z4 copies (hi and lo): two buffers in the states-only scan, whose next chunk's
   // weighting then overlaps this chunk's MMA4 (it has no state copy and no output staging)
   static constexpr uint32_t NVT = Cfg<MODE>::STATES ? 2 : 1;
-  static constexpr uint32_t OFF_VT = 2 * Cfg<MODE>::SZ_STAGE;
+  static constexpr uint32_t OFF_VT = Cfg<MODE>::NSTAGE * Cfg<MODE>::SZ_STAGE;
   static constexpr uint32_t OFF_SP = OFF_VT + NVT * 2 * SZ_TILE64;
   // output staging: wide, the bf16 output tile for the TMA store; narrow, one region per epilogue
   // warp (32 rows x 48 fp32, rows padded to 208 bytes) that turns row-wise sums into adds of
@@ -465,7 +467,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) {
       uint32_t cnt = 1;
-      if (i == B_EMPTY || i == B_EMPTY + 1) cnt = C::STATES ? 1 : 3;  // the MMA issuers that read a stage
+      if (i >= B_EMPTY && i < B_EMPTY + C::NSTAGE) cnt = C::STATES ? 1 : 3;  // the MMA issuers that read a stage
       if (i == B_TBL_FULL || i == B_TBL_FULL + 1) cnt = 128;   // the Z4 warps write a unit's table
       if (i == B_TBL_EMPTY || i == B_TBL_EMPTY + 1) cnt = C::SPLIT ? 512 : (C::STATES ? 256 : 384);  // its readers
       if (i == B_O_FULL) cnt = 2;
@@ -545,7 +547,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
     // ------------------------------------------------------------------ TMA producer
     setmaxnreg_dec<C::REG_CTRL>();
     if (lane == 0) {
-      int issued[2] = {0, 0};
+      int issued[C::NSTAGE] = {};
       int gk = 0;
       bool stop = false;
       for (int u = 0; u < n_items && !stop; ++u) {
@@ -553,12 +555,12 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
        const int h = w.h, col0 = w.tile * TN;
        for (int it = w.it0; it < w.it1; ++it, ++gk) {
         const int c = C::REVERSE ? w.nc - 1 - it : it;
-        const int s = gk & 1;
-        const uint32_t ph = (uint32_t)(gk >> 1) & 1u;
+        const int s = gk % C::NSTAGE;
+        const uint32_t ph = (uint32_t)(gk / C::NSTAGE) & 1u;
         if (!mbar_wait(&bars[B_EMPTY + s], ph ^ 1u, a.wait_ns, abort_flag)) { stop = true; break; }
         const uint32_t st = sbase + (uint32_t)s * C::SZ_STAGE;
         uint64_t* full = &bars[B_FULL + s];
-        mbar_expect_tx(full, C::STATES ? C::SZ_STAGE - 24576u : C::SZ_STAGE);  // (no q: 24 KB)
+        mbar_expect_tx(full, C::SZ_STAGE);
         const int tok = (int)(w.tb + (long long)c * CHUNK);
         (void)GLA_IN_BOUNDS(tok >= 0 && tok < tokens && h >= 0 && h < a.H, a.err);
         if (C::NARROW) {
@@ -598,7 +600,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
        }
       }
       // Never leave a copy in flight into shared memory that is about to be released.
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < C::NSTAGE; ++s)
         if (issued[s]) mbar_wait_drain(&bars[B_FULL + s], (uint32_t)(issued[s] - 1) & 1u, DRAIN_NS, a.err);
     }
     __syncwarp();
@@ -621,8 +623,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       for (int u = 0; u < n_items && !stop; ++u) {
        const Unit wi = unit_at(u);
        for (int it = wi.it0; it < wi.it1; ++it, ++gk) {
-        const int s = gk & 1;
-        const uint32_t ph = (uint32_t)(gk >> 1) & 1u, pc = (uint32_t)gk & 1u;
+        const int s = gk % C::NSTAGE;
+        const uint32_t ph = (uint32_t)(gk / C::NSTAGE) & 1u, pc = (uint32_t)gk & 1u;
         const uint32_t st = sbase + (uint32_t)s * C::SZ_STAGE;
         const SDesc dx = sdesc(st + C::ST_X, 16, 1024, LAYOUT_SW128);
         const SDesc dx1 = sdesc(st + C::ST_X1, 16, 512, LAYOUT_SW64);
@@ -749,8 +751,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
       // q and k rows (held until MMA2 is done), while MMA1 runs.
       float sig = 0.f;
       if constexpr (C::AUG) {
-        if (!warp_wait(&bars[B_FULL + (gk & 1)], (uint32_t)(gk >> 1) & 1u, a, abort_flag)) { stop = true; break; }
-        const uint32_t st = sbase + (uint32_t)(gk & 1) * C::SZ_STAGE;
+        if (!warp_wait(&bars[B_FULL + gk % C::NSTAGE], (uint32_t)(gk / C::NSTAGE) & 1u, a, abort_flag)) { stop = true; break; }
+        const uint32_t st = sbase + (uint32_t)(gk % C::NSTAGE) * C::SZ_STAGE;
         const uint32_t avs = sbase + SMM::OFF_AUG + (uint32_t)tbuf * DK * 4u;
         // q: columns 0..63 in a 128B-swizzled panel, 64..95 in a 64B-swizzled one; k: two
         // 128B-swizzled panels.  16-byte piece p of a row holds columns 8p .. 8p + 7.  The sum
@@ -873,8 +875,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
      if (!warp_wait(&bars[B_TBL_FULL + tbuf], (uint32_t)(ku >> 1) & 1u, a, abort_flag)) break;
      for (int it = w.it0; it < w.it1; ++it, ++gk) {
       const int c = C::REVERSE ? w.nc - 1 - it : it;
-      const int s = gk & 1;
-      const uint32_t ph = (uint32_t)(gk >> 1) & 1u, pc = (uint32_t)gk & 1u;
+      const int s = gk % C::NSTAGE;
+      const uint32_t ph = (uint32_t)(gk / C::NSTAGE) & 1u, pc = (uint32_t)gk & 1u;
       const int L = min(CHUNK, w.len - c * CHUNK);
       if (!warp_wait(&bars[B_FULL + s], ph, a, abort_flag)) { stop = true; break; }
       const int vb = SMM::NVT == 2 ? (gk & 1) : 0;  // weighted Z4 buffer and its phase
