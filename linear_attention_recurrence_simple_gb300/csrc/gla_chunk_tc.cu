@@ -892,8 +892,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
         // MMA4 accumulates the whole unit's update in tensor memory
         if constexpr (C::STATES) wj *= expf((float)(w.len - c * CHUNK - L) * a.log_lambda[w.h]);
         const float2 f = make_float2(wj, wj);
-#pragma unroll 1
-        for (int p = 0; p < 8; ++p) {
+        auto weigh = [&](int p) {
           const int off = j * 128 + ((p ^ (j & 7)) << 4);  // same permutation on both sides
           const uint4 x = *reinterpret_cast<const uint4*>(zsrc + off);
           const uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -902,6 +901,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_scan_kernel(const __
           for (int e = 0; e < 4; ++e) split_bf16x2(mul2(bf2_to_f2(w[e]), f), hi[e], lo[e]);
           *reinterpret_cast<uint4*>(zhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(zlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        };
+        if constexpr (C::STATES) {  // (its own code: unrolled, all loads in flight together)
+#pragma unroll
+          for (int p = 0; p < 8; ++p) weigh(p);
+        } else {
+#pragma unroll 1
+          for (int p = 0; p < 8; ++p) weigh(p);
         }
         if (C::REVERSE && j >= L) {
           // Reverse scans: rows of Z past the sequence end are zeroed, so MMA2 needs no column mask
