@@ -62,18 +62,37 @@ __device__ __forceinline__ int mx_shared_exp(float m) {
   const int se = E - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
   return max(se, -127);
 }
+// Pairs of fp32 values through the packed two-lane instructions (each lane rounded as its scalar
+// counterpart, so the results are those of the scalar code).
+__device__ __forceinline__ uint64_t f2b(float a, float b) { return ((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(a); }
+__device__ __forceinline__ void b2f(uint64_t r, float& a, float& b) {
+  a = __uint_as_float((uint32_t)r);
+  b = __uint_as_float((uint32_t)(r >> 32));
+}
+__device__ __forceinline__ uint64_t pmul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t pfma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
 // 2^-se as fp32 (se in [-127, 120]).
 __device__ __forceinline__ float pow2_neg(int se) { return __uint_as_float((uint32_t)(127 - se) << 23); }
 
 // 16 fp32 values -> 16 codes (one uint4), given the block's shared exponent.
 __device__ __forceinline__ uint4 quantise16(const float (&x)[16], int se) {
   const float inv = pow2_neg(se);
+  const uint64_t inv2 = f2b(inv, inv);
   uint32_t w[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint32_t a = f2_to_e4m3x2(x[4 * j] * inv, x[4 * j + 1] * inv);
-    const uint32_t b = f2_to_e4m3x2(x[4 * j + 2] * inv, x[4 * j + 3] * inv);
-    w[j] = a | (b << 16);
+    float y0, y1, y2, y3;
+    b2f(pmul(f2b(x[4 * j], x[4 * j + 1]), inv2), y0, y1);
+    b2f(pmul(f2b(x[4 * j + 2], x[4 * j + 3]), inv2), y2, y3);
+    w[j] = f2_to_e4m3x2(y0, y1) | (f2_to_e4m3x2(y2, y3) << 16);
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -293,17 +312,17 @@ decode_step_mxfp8_kernel(const T* __restrict__ q, const T* __restrict__ k, const
         const float sc = e8m0_to_f(*scp);
         const float lsc = lam * sc;
         float x[16];
-        if (lsc >= 1.17549435e-38f || lam == 0.f) {
-          dequantise16(*cp, 1.f, x);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) x[e] = fmaf(lsc, x[e], ka * vv[e]);
-        } else {
+        const bool fold = lsc >= 1.17549435e-38f || lam == 0.f;
+        if (fold)
+          dequantise16(*cp, 1.f, x);  // (no multiply: the scale rides in lambda)
+        else
           dequantise16(*cp, sc, x);
+        const uint64_t l2 = fold ? f2b(lsc, lsc) : f2b(lam, lam), k2 = f2b(ka, ka), q2 = f2b(qa, qa);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) x[e] = fmaf(lam, x[e], ka * vv[e]);
+        for (int e = 0; e < 16; e += 2) {
+          b2f(pfma(l2, f2b(x[e], x[e + 1]), pmul(k2, f2b(vv[e], vv[e + 1]))), x[e], x[e + 1]);
+          b2f(pfma(q2, f2b(x[e], x[e + 1]), f2b(acc[e], acc[e + 1])), acc[e], acc[e + 1]);
         }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] = fmaf(qa, x[e], acc[e]);
         const int se = mx_shared_exp(block_max(x));
         *cp = quantise16(x, se);  // in place: this thread's own 16 bytes
         // (both lanes of the block read this byte above, before the shuffle in block_max)
