@@ -93,3 +93,17 @@ def test_bench_reference_arm_prints_one_line():
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["cores"] >= 1
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["dtype"] == "f64"
     assert rec["steps"] == 1 and rec["warmup"] >= 1
+
+
+def test_bench_reference_arm_other_ranks_exit_without_work():
+    """Under a launcher with N > 1 only rank 0 runs the oracle arm; another rank exits 0 at once
+    and prints nothing."""
+    import subprocess
+    import time
+    cmd, root = _bench_cmd("--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1")
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1", LOCAL_RANK="1")
+    t = time.time()
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env=env, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert time.time() - t < 120
