@@ -19,20 +19,25 @@
 // row, so the mean square is a reduction over its first 48 threads.
 //
 // The step is a pure stream over the 72 KB state of each (sequence, head): read once, update,
-// write once.  One CTA of 576 threads owns one state; thread (r, c), r < 12, c < 48, holds
-// columns 4c..4c+3 (one 16-byte vector) of the 8 rows r, r+12, ..., r+84, so consecutive lanes
-// touch consecutive 16-byte pieces of a row.  All eight loads are issued before any arithmetic.  The readout's sum over d_k runs
-// in registers, then over the 12 row groups through shared memory.  Loads and stores carry
-// the streaming cache hint, since each state is touched once per step.
+// write once.  One CTA owns one state; thread (r, c), c < 48, holds columns 4c..4c+3 (one
+// vector) of the rows r, r + G, r + 2G, ... for G row groups, so consecutive lanes touch
+// consecutive pieces of a row: fp32 states with 576 threads (G = 12, 8 rows of 16-byte vectors
+// each, 2 CTAs per SM), bf16 states with 288 threads (G = 6, 16 rows of 8-byte vectors kept packed
+// until use, 4 CTAs per SM: twice the bytes in flight per SM of 576-thread CTAs).  All of a
+// thread's loads are issued before any arithmetic.  The readout's sum over d_k runs in
+// registers, then over the G row groups through shared memory.  Loads and stores carry the
+// streaming cache hint, since each state is touched once per step.
 #include "gla_common.cuh"
 
 namespace gla {
 namespace {
 
-constexpr int DEC_THREADS = 576;              // 48 column groups x 12 row groups
-constexpr int DEC_COLS = DV / 4;              // 48 float4 per state row
-constexpr int DEC_RGROUPS = DEC_THREADS / DEC_COLS;  // 12
-constexpr int DEC_ROWS = DK / DEC_RGROUPS;    // 8 rows per thread
+constexpr int DEC_COLS = DV / 4;              // 48 four-column vectors per state row
+// CTA shape per state storage type: threads (48 column groups x RGROUPS row groups), rows per
+// thread, CTAs per SM.
+template <class ST> struct DecCfg;
+template <> struct DecCfg<float> { static constexpr int THREADS = 576, MIN_BLOCKS = 2; };
+template <> struct DecCfg<__nv_bfloat16> { static constexpr int THREADS = 288, MIN_BLOCKS = 4; };
 
 struct Bf16x4 { __nv_bfloat162 a, b; };
 
@@ -49,9 +54,10 @@ __device__ __forceinline__ void store4(float* p, float4 x) { *reinterpret_cast<f
 template <class ST> struct StateVec;
 template <> struct StateVec<float> { using type = float4; };
 template <> struct StateVec<__nv_bfloat16> { using type = uint2; };
-__device__ __forceinline__ float4 load_state(const float4* p) { return __ldcs(p); }
-__device__ __forceinline__ float4 load_state(const uint2* p) {
-  const uint2 u = __ldcs(p);
+// A state vector as loaded, widened to fp32 at use (bf16 vectors stay packed in between, so the
+// loads in flight hold half the registers).
+__device__ __forceinline__ float4 widen_state(float4 x) { return x; }
+__device__ __forceinline__ float4 widen_state(uint2 u) {
   const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
   const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
   return make_float4(lo.x, lo.y, hi.x, hi.y);
@@ -90,7 +96,7 @@ __device__ __forceinline__ float dec_silu(float g, __nv_bfloat16) { return g * f
 __device__ __forceinline__ float dec_silu(float g, float) { return g * fmaf(0.5f, tanhf(0.5f * g), 0.5f); }
 
 template <class T, class ST, bool NG>
-__global__ void __launch_bounds__(DEC_THREADS, 2)
+__global__ void __launch_bounds__(DecCfg<ST>::THREADS, DecCfg<ST>::MIN_BLOCKS)
 decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                    const float* __restrict__ log_lambda, float scale, ST* __restrict__ state,
                    const int32_t* __restrict__ slot, int pool_rows, T* __restrict__ o, int H,
@@ -99,7 +105,8 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   __shared__ float s_k[DK];
   __shared__ float s_gate;
   __shared__ float s_ss[2];
-  __shared__ float4 s_part[DEC_RGROUPS][DEC_COLS];
+  constexpr int RG = DecCfg<ST>::THREADS / DEC_COLS, ROWS = DK / RG;
+  __shared__ float4 s_part[RG][DEC_COLS];
 
   const long long nh = blockIdx.x;  // n * H + h
   const int n = (int)(nh / H);
@@ -116,9 +123,9 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
   using SV = typename StateVec<ST>::type;
   SV* S = reinterpret_cast<SV*>(state + ((long long)row * H + h) * (DK * DV));
 
-  float4 s[DEC_ROWS];
+  SV s[ROWS];
 #pragma unroll
-  for (int i = 0; i < DEC_ROWS; ++i) s[i] = load_state(S + (r + DEC_RGROUPS * i) * DEC_COLS + c);
+  for (int i = 0; i < ROWS; ++i) s[i] = __ldcs(S + (r + RG * i) * DEC_COLS + c);
 
   if (tid < DK) {
     s_q[tid] = scale * to_f(q[nh * DK + tid]);
@@ -132,10 +139,10 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < DEC_ROWS; ++i) {
-    const int a = r + DEC_RGROUPS * i;
+  for (int i = 0; i < ROWS; ++i) {
+    const int a = r + RG * i;
     const float ka = s_k[a], qa = s_q[a];
-    float4 x = s[i];
+    float4 x = widen_state(s[i]);
     x.x = fmaf(lam, x.x, ka * vv.x);
     x.y = fmaf(lam, x.y, ka * vv.y);
     x.z = fmaf(lam, x.z, ka * vv.z);
@@ -161,7 +168,7 @@ decode_step_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     if (tid < DEC_COLS) {
       t = s_part[0][tid];
 #pragma unroll
-      for (int g = 1; g < DEC_RGROUPS; ++g) {
+      for (int g = 1; g < RG; ++g) {
         const float4 p = s_part[g][tid];
         t.x += p.x;
         t.y += p.y;
@@ -210,11 +217,11 @@ void launch_decode_t(long long blocks, const void* q, const void* k, const void*
                      const float* aug, unsigned* err, const DecodeNormGate* ngp, cudaStream_t stream) {
   if (ngp) {
     const NormGate<T> ng = {(const T*)ngp->g, ngp->w, ngp->tier, ngp->n_tiers, ngp->eps};
-    decode_step_kernel<T, ST, true><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
+    decode_step_kernel<T, ST, true><<<(unsigned)blocks, DecCfg<ST>::THREADS, 0, stream>>>(
         (const T*)q, (const T*)k, (const T*)v, log_lambda, scale, (ST*)state, slot, pool_rows, (T*)o, H, aug,
         err, ng);
   } else {
-    decode_step_kernel<T, ST, false><<<(unsigned)blocks, DEC_THREADS, 0, stream>>>(
+    decode_step_kernel<T, ST, false><<<(unsigned)blocks, DecCfg<ST>::THREADS, 0, stream>>>(
         (const T*)q, (const T*)k, (const T*)v, log_lambda, scale, (ST*)state, slot, pool_rows, (T*)o, H, aug,
         err, NormGate<T>{});
   }
