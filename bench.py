@@ -35,15 +35,15 @@ PROFILED_TRAFFIC = {
     # B=8 T=2048 H=16 forward: 245.515008 MB read + 81.780480 MB written, one launch
     "fwd": ("linear_attention_recurrence_simple_gb300/csrc/gla_chunk_tc.cu", "d75fb5f6c49d8cfb",
             327295488.0, "per launch of the B=8 T=2048 H=16 forward"),
-    # 49,152-state pool: 3.661689 GB read + 3.583208 GB written; traffic scales with the pool
-    "decode": ("linear_attention_recurrence_simple_gb300/csrc/gla_decode.cu", "98de2132efc39ffd",
-               7244897000.0 / 49152, "per state per step"),
-    # the same pool in bf16: 1.849795 GB read + 1.770043 GB written
-    "decode_bf16_state": ("linear_attention_recurrence_simple_gb300/csrc/gla_decode.cu", "98de2132efc39ffd",
-                          3619838464.0 / 49152, "per state per step"),
-    # the fused norm-gate step on the fp32 pool: 3.680579 GB read + 3.583394 GB written
-    "decode_norm_gate": ("linear_attention_recurrence_simple_gb300/csrc/gla_decode.cu", "98de2132efc39ffd",
-                         7263972864.0 / 49152, "per state per step"),
+    # 49,152-state pool: 3.662106 GB read + 3.583718 GB written; traffic scales with the pool
+    "decode": ("linear_attention_recurrence_simple_gb300/csrc/gla_decode.cu", "a4a26403a2ad2cf8",
+               7245823744.0 / 49152, "per state per step"),
+    # the same pool in bf16: 1.849750 GB read + 1.771710 GB written
+    "decode_bf16_state": ("linear_attention_recurrence_simple_gb300/csrc/gla_decode.cu", "a4a26403a2ad2cf8",
+                          3621459200.0 / 49152, "per state per step"),
+    # the fused norm-gate step on the fp32 pool: 3.680801 GB read + 3.583189 GB written
+    "decode_norm_gate": ("linear_attention_recurrence_simple_gb300/csrc/gla_decode.cu", "a4a26403a2ad2cf8",
+                         7263989504.0 / 49152, "per state per step"),
     # head RMSNorm + gate, 16,384 x 16 rows: 201.355776 MB read + 70.854144 MB written (part of y
     # is still in L2 when the kernel ends), one launch
     "norm_gate": ("linear_attention_recurrence_simple_gb300/csrc/gla_norm.cu", "4987f08ea9f6d8e4",
