@@ -44,6 +44,9 @@ PROFILED_TRAFFIC = {
     # the fused norm-gate step on the fp32 pool: 3.680801 GB read + 3.583189 GB written
     "decode_norm_gate": ("linear_attention_recurrence_simple_gb300/csrc/gla_decode.cu", "a4a26403a2ad2cf8",
                          7263989504.0 / 49152, "per state per step"),
+    # the same forward with the self-augmentation step: 244.934400 MB read + 82.883328 MB written
+    "fwd_aug": ("linear_attention_recurrence_simple_gb300/csrc/gla_chunk_tc.cu", "d75fb5f6c49d8cfb",
+                327817728.0, "per launch of the B=8 T=2048 H=16 augmented forward"),
     # head RMSNorm + gate, 16,384 x 16 rows: 201.355776 MB read + 70.854144 MB written (part of y
     # is still in L2 when the kernel ends), one launch
     "norm_gate": ("linear_attention_recurrence_simple_gb300/csrc/gla_norm.cu", "4987f08ea9f6d8e4",
@@ -327,6 +330,7 @@ def bench_fwd_aug(torch, gla, wl, dist, args, peaks):
            "roofline": roofline(fwd_bytes(tokens, w.n_seq, False) + H * DK * 4,
                                 fwd_flops(tokens) + tokens * H * 2 * (DK + DV), region / 1e3, peaks),
            "kernel_ms": per_call, "launches_per_step": 1}
+    res["roofline"]["traffic"] = profiled_traffic("fwd_aug")
     del g, o, hT, aug
     return res
 
