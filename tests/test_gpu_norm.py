@@ -32,7 +32,8 @@ def _inputs(seed, rows, H, n_tiers, bf16):
 
 
 @pytest.mark.parametrize("bf16", [True, False])
-@pytest.mark.parametrize("rows,H,n_tiers", [(1, 1, 1), (37, 16, 4), (300, 5, 3)])
+@pytest.mark.parametrize("rows,H,n_tiers", [(1, 1, 1), (37, 16, 4), (300, 5, 3), (7, 2, 2), (11, 3, 3),
+                                             (9, 40, 33)])
 def test_head_norm_gate_matches_oracle(bf16, rows, H, n_tiers):
     o, g, w, tier = _inputs(900 + rows + H, rows, H, n_tiers, bf16)
     dt = torch.bfloat16 if bf16 else torch.float32
