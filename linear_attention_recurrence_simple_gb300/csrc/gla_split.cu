@@ -82,11 +82,11 @@ struct SplitPlan {
 // Cost model of the automatic segment length (seg_chunks = 0).  The packed forward runs one CTA
 // per unit, (segment, head, d_v tile), one CTA per SM, longest units first; a unit takes its
 // chunk count plus a start-up cost, in chunk times.  The split runs two such passes (the
-// states-only pass at about three quarters of the full one), the plain forward one.  Costs are
+// states-only pass at about half the full one), the plain forward one.  Costs are
 // kept in quarter chunk times (integers).
 constexpr int PLAN_SMS = 152;             // SMs of a GB300
 constexpr long long UNIT_OVERHEAD = 12;   // 3 chunk times per unit: pipeline fill and drain
-constexpr long long SPLIT_PASSES_X4 = 7;  // both passes of the split: 7/4 of a full pass
+constexpr long long SPLIT_PASSES_X4 = 6;  // both passes of the split: 6/4 of a full pass
 
 using UnitGroups = std::vector<std::pair<int, long long>>;  // (chunks, units), any order
 

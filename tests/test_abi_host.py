@@ -209,8 +209,10 @@ def test_split_choice_of_segment_length(lib):
     L = choose([131072])              # 1,024 chunks on 48 units: cut
     assert 16 <= L <= 128
     assert choose([131072, 2048, 4096]) > 0   # one long sequence with short ones: cut
-    assert choose([131072] * 4) == 0  # 192 units of 1,024 chunks: two passes cost more than the
-                                      # plain forward's second wave
+    # 192 units of 1,024 chunks: the plain forward's second wave is 40 units long; the split's two
+    # passes (the states-only one about half a full pass) spread the work evenly instead (GB300:
+    # 3.52 ms at the chosen 147-chunk segments against 3.60 ms plain)
+    assert 64 <= choose([131072] * 4) <= 512
     assert choose([int(x) for x in varlen_lengths(3, 32, 128, 16384)]) == 0   # balanced by ordering
     assert choose([2048] * 8) == 0    # 384 units of 16 chunks
     assert choose([128]) == 0         # one chunk
