@@ -226,6 +226,8 @@ def timed(torch, dist, fn, steps, warmup):
 # The roofline's `frac` is against the measured copy bandwidth / cuBLAS throughput of
 # MEASURED_PEAKS.json; `frac_of_datasheet` is the same achieved figure against these.
 DATASHEET = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
+# fp32 FMA on the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops x 2,070 MHz (the maximum SM clock)
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
 
 
 def roofline(bytes_, flops, secs, peaks, bound="hbm"):
@@ -239,6 +241,12 @@ def roofline(bytes_, flops, secs, peaks, bound="hbm"):
                 "algorithmic_bytes": int(bytes_), "flops": int(flops),
                 "tensor_frac": round(flops / secs / 1e12 / peaks["bf16_tflops"], 4)}
     ach = flops / secs / 1e12
+    if bound == "alu":
+        return {"bound": "alu", "achieved": round(ach, 2), "peak": round(FP32_ALU_TFLOPS, 2), "unit": "TFLOP/s",
+                "frac": round(ach / FP32_ALU_TFLOPS, 4), "traffic": None,
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2,070 MHz",
+                "algorithmic_bytes": int(bytes_), "flops": int(flops),
+                "hbm_frac": round(bytes_ / secs / 1e9 / peaks["hbm_gbs"], 4)}
     return {"bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4), "traffic": None,
             "frac_of_datasheet": round(ach / DATASHEET["bf16_tflops"], 4),
@@ -308,6 +316,29 @@ def bench_fwd(torch, gla, wl, dist, args, peaks):
     torch.cuda.synchronize()
     res["e2e"]["matches_device_call"] = bool(torch.equal(ho, ref_o.cpu()) and torch.equal(hh, ref_h.cpu()))
     del g, o, hT, hq, hk, hv, ho, hh, ws_host
+    return res
+
+
+def bench_fwd_fp32(torch, gla, wl, dist, args, peaks):
+    """The all-fp32 mode's forward (fp32 q, k, v, o; the CUDA-core kernels that serve the 1e-4
+    accuracy bar) on the forward workload's shapes.  Its bytes: fp32 q, k, v in and o out (twice
+    the bf16 path's) plus hT."""
+    w = wl.layer()
+    g = w.device_inputs()
+    q, k, v = (g[x].float() for x in ("q", "k", "v"))
+    del g["q"], g["k"], g["v"]
+    o = torch.empty_like(v)
+    hT = torch.empty((w.n_seq, H, DK, DV), dtype=torch.float32, device="cuda")
+    fn = lambda: gla.gla_chunk_fwd(q, k, v, g["log_lambda"], w.scale, o=o, hT=hT)
+    region, per_call = timed(torch, dist, fn, max(3, args.steps // 4), args.warmup)
+    region, per_call = dist.max(region), dist.max(per_call)
+    tokens = w.tokens
+    byts = tokens * H * (2 * DK * 4 + 2 * DV * 4) + w.n_seq * H * DK * DV * 4
+    res = {"workload": w.name.replace("bf16", "fp32") + " (all-fp32 mode)", "tokens": tokens, "ms_per_step": region,
+           "value": tokens * dist.world / (region / 1e3), "unit": "tokens/s",
+           "roofline": roofline(byts, fwd_flops(tokens), region / 1e3, peaks, bound="alu"), "kernel_ms": per_call,
+           "launches_per_step": 1}
+    del g, q, k, v, o, hT
     return res
 
 
@@ -645,7 +676,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--rows", default="fwd,bwd,varlen,decode,fwd_aug,norm_gate,decode_aug,decode_bf16_state,"
-                    "fwd_split,decode_norm_gate,decode_mxfp8_state")
+                    "fwd_split,decode_norm_gate,decode_mxfp8_state,fwd_fp32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-seqs", type=int, default=1280,
                     help="sequences in the decode pool (1280 = the measured workload)")
@@ -687,6 +718,8 @@ def main():
             out["decode"] = bench_decode(torch, gla, wl, dist, args, peaks)
         if "fwd_aug" in rows:
             out["fwd_aug"] = bench_fwd_aug(torch, gla, wl, dist, args, peaks)
+        if "fwd_fp32" in rows:
+            out["fwd_fp32"] = bench_fwd_fp32(torch, gla, wl, dist, args, peaks)
         if "fwd_split" in rows:
             out["fwd_split"] = bench_fwd_split(torch, gla, wl, dist, args, peaks)
         if "norm_gate" in rows:
