@@ -463,6 +463,28 @@ def bench_bwd(torch, gla, wl, dist, args, peaks):
     return res
 
 
+def bench_bwd_fp32(torch, gla, wl, dist, args, peaks):
+    """The all-fp32 mode's backward (the CUDA-core scans) on the backward workload's shapes, with
+    fp32 q, k, v, dO and gradients."""
+    w = wl.layer(with_grad=True)
+    g = w.device_inputs()
+    q, k, v, dO = (g[x].float() for x in ("q", "k", "v", "dO"))
+    for x in ("q", "k", "v", "dO"):
+        del g[x]
+    fn = lambda: gla.gla_chunk_bwd(q, k, v, g["log_lambda"], dO, w.scale, dhT=g["dhT"])
+    region, per_call = timed(torch, dist, fn, max(3, args.steps // 4), args.warmup)
+    region, per_call = dist.max(region), dist.max(per_call)
+    tokens = w.tokens
+    byts = 2 * bwd_bytes(tokens, w.n_seq) - 2 * w.n_seq * H * DK * DV * 4  # fp32 rows, the states as before
+    flops = tokens * H * 2 * (128 * DV + 128 * DK + 2 * DK * DV + 128 * DV + 128 * DK + 128 * DK + 128 * DV
+                              + 4 * DK * DV)
+    res = {"workload": w.name.replace("bf16", "fp32") + " (all-fp32 mode)", "tokens": tokens, "ms_per_step": region,
+           "value": tokens * dist.world / (region / 1e3), "unit": "tokens/s",
+           "roofline": roofline(byts, flops, region / 1e3, peaks, bound="alu"), "launches_per_step": 3}
+    del g, q, k, v, dO
+    return res
+
+
 def bench_decode(torch, gla, wl, dist, args, peaks, aug=False, bf16_state=False, norm_gate=False):
     """``aug``: the step with the self-augmentation copy of v (gla_decode_step_aug), 16 steps;
     ``bf16_state``: the same pool stored in bf16 (gla_decode_step_bf16_state), 16 steps;
@@ -720,6 +742,8 @@ def main():
             out["fwd_aug"] = bench_fwd_aug(torch, gla, wl, dist, args, peaks)
         if "fwd_fp32" in rows:
             out["fwd_fp32"] = bench_fwd_fp32(torch, gla, wl, dist, args, peaks)
+        if "bwd_fp32" in rows:
+            out["bwd_fp32"] = bench_bwd_fp32(torch, gla, wl, dist, args, peaks)
         if "fwd_split" in rows:
             out["fwd_split"] = bench_fwd_split(torch, gla, wl, dist, args, peaks)
         if "norm_gate" in rows:
