@@ -29,9 +29,6 @@ namespace {
 
 constexpr int SC = 64;          // chunk length of these kernels
 constexpr int NT = 256;         // threads per CTA
-constexpr int PK = DK + 1;      // padded row pitches (bank-conflict-free column walks)
-constexpr int PV = DV + 1;
-constexpr int PT = 65;
 
 template <class T>
 __device__ __forceinline__ void load_rows(float* dst, int pitch, const T* src, long long t0, int L,
@@ -116,8 +113,12 @@ __device__ __forceinline__ void store4o(__nv_bfloat16* p, float4 x) {
   p[3] = __float2bfloat16_rn(x.w);
 }
 
-template <class T>
-__global__ void __launch_bounds__(NT, 2) simt_fwd_kernel(ChunkArgs a) {
+// REVERSE: the dv scan of the backward on the same tiles (reverse in time, carrying R = dL/dS):
+//   X = k, Y = q, Z = dO;  P[i][j] = scale lambda^(j-i) X_i . Y_j (j >= i);
+//   dv_i = sum_j P[i][j] Z_j + lambda^(L-1-i) R^T X_i;  R <- lambda^L R + scale sum_j lambda^(j+1) Y_j Z_j^T
+// (R starts from dhT; dh0 comes from the dk scan).
+template <class T, bool REVERSE>
+__global__ void __launch_bounds__(NT, 2) simt_wide_kernel(ChunkArgs a) {
   extern __shared__ __align__(16) float sm[];
   float* Qs = sm;                 // [SC][QP]
   float* Ks = Qs + SC * QP;       // [SC][QP]
@@ -133,20 +134,24 @@ __global__ void __launch_bounds__(NT, 2) simt_fwd_kernel(ChunkArgs a) {
   seq_range(a, n, tb, te);
   if (!unit_in_bounds(a, n, h)) return;  // (debug-bounds build; uniform over the CTA)
   const int col0 = tile * FWD_TILE;
-  const T* q = (const T*)a.q;
-  const T* k = (const T*)a.k;
-  const T* v = (const T*)a.v;
-  T* o = (T*)a.o;
+  const T* q = (const T*)(REVERSE ? a.k : a.q);   // X: the score's row operand (and the readout's)
+  const T* k = (const T*)(REVERSE ? a.q : a.k);   // Y: its column operand (and the state's row factor)
+  const T* v = (const T*)(REVERSE ? a.dO : a.v);  // Z: the tile's operand
+  T* o = (T*)(REVERSE ? a.dv : a.o);
+  const float* s0 = REVERSE ? a.dhT : a.h0;
+  const bool aug = !REVERSE && a.aug;
   const long long sbase = ((long long)n * a.H + h) * DK * DV;
 
   fill_powers(pw, a.log_lambda[h]);
   for (int e = tid; e < DK * FWD_TILE; e += NT) {
     const int r = e / FWD_TILE, c = e % FWD_TILE;
-    Ss[r * VP + c] = a.h0 ? a.h0[sbase + (long long)r * DV + col0 + c] : 0.f;
+    Ss[r * VP + c] = s0 ? s0[sbase + (long long)r * DV + col0 + c] : 0.f;
   }
   __syncthreads();
 
-  for (long long t0 = tb; t0 < te; t0 += SC) {
+  const long long nchunks = (te - tb + SC - 1) / SC;
+  for (long long m0 = 0; m0 < nchunks; ++m0) {
+    const long long t0 = tb + (REVERSE ? nchunks - 1 - m0 : m0) * SC;
     const int L = (int)(te - t0 < SC ? te - t0 : SC);
     if (!rows_in_bounds(a, t0, L)) break;  // (debug-bounds build; uniform over the CTA)
     if constexpr (std::is_same<T, float>::value) {
@@ -157,13 +162,14 @@ __global__ void __launch_bounds__(NT, 2) simt_fwd_kernel(ChunkArgs a) {
       load_rows(Vs, VP, v, t0, L, a.H, h, DV, col0, FWD_TILE);
     }
     __syncthreads();
-    if (t0 + SC < te) {  // the next chunk's rows into L2 during this chunk's arithmetic
-      const int Ln = (int)(te - t0 - SC < SC ? te - t0 - SC : SC);
-      prefetch_chunk(q, t0 + SC, Ln, a.H, h, DK, (int)sizeof(T), 0, DK);
-      prefetch_chunk(k, t0 + SC, Ln, a.H, h, DK, (int)sizeof(T), 0, DK);
-      prefetch_chunk(v, t0 + SC, Ln, a.H, h, DV, (int)sizeof(T), col0, FWD_TILE);
+    if (m0 + 1 < nchunks) {  // the next chunk's rows into L2 during this chunk's arithmetic
+      const long long tn = REVERSE ? t0 - SC : t0 + SC;
+      const int Ln = (int)(te - tn < SC ? te - tn : SC);
+      prefetch_chunk(q, tn, Ln, a.H, h, DK, (int)sizeof(T), 0, DK);
+      prefetch_chunk(k, tn, Ln, a.H, h, DK, (int)sizeof(T), 0, DK);
+      prefetch_chunk(v, tn, Ln, a.H, h, DV, (int)sizeof(T), col0, FWD_TILE);
     }
-    if (a.aug) {  // gate of row i: sigmoid(q_i . (a_h * k_i)), q unscaled; added to P[i][i] below
+    if (aug) {  // gate of row i: sigmoid(q_i . (a_h * k_i)), q unscaled; added to P[i][i] below
       if (tid < SC) {
         float g = 0.f;
         for (int c = 0; c < DK; ++c) g = fmaf(Qs[tid * QP + c] * a.aug[h * DK + c], Ks[tid * QP + c], g);
@@ -171,7 +177,7 @@ __global__ void __launch_bounds__(NT, 2) simt_fwd_kernel(ChunkArgs a) {
       }
       __syncthreads();
     }
-    {  // P[i][j] = scale lambda^(i-j) q_i . k_j for j <= i, else 0
+    {  // P[i][j] = scale lambda^|i-j| X_i . Y_j on the causal side (j <= i, or j >= i reversed)
       float acc[4][4];
 #pragma unroll
       for (int r = 0; r < 4; ++r)
@@ -199,8 +205,9 @@ __global__ void __launch_bounds__(NT, 2) simt_fwd_kernel(ChunkArgs a) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int i = ty + 16 * r, j = tx + 16 * c;
-          float p = j <= i ? acc[r][c] * (a.scale * pw[i - j]) : 0.f;
-          if (a.aug && j == i) p += gs[i];
+          const bool on = REVERSE ? j >= i : j <= i;
+          float p = on ? acc[r][c] * (a.scale * pw[REVERSE ? j - i : i - j]) : 0.f;
+          if (aug && j == i) p += gs[i];
           Ps[i * VP + j] = p;
         }
     }
@@ -245,7 +252,7 @@ __global__ void __launch_bounds__(NT, 2) simt_fwd_kernel(ChunkArgs a) {
       for (int r = 0; r < 4; ++r) {
         const int i = ty + 16 * r;
         if (i < L) {
-          const float f = a.scale * pw[i + 1];
+          const float f = REVERSE ? pw[L - 1 - i] : a.scale * pw[i + 1];
           store4o(o + ((t0 + i) * a.H + h) * (long long)DV + col0 + 4 * tx,
                   make_float4(fmaf(f, oe[r][0], oi[r][0]), fmaf(f, oe[r][1], oi[r][1]),
                               fmaf(f, oe[r][2], oi[r][2]), fmaf(f, oe[r][3], oi[r][3])));
@@ -265,7 +272,7 @@ __global__ void __launch_bounds__(NT, 2) simt_fwd_kernel(ChunkArgs a) {
         acc[r][3] = lamL * sv.w;
       }
       for (int j = 0; j < L; ++j) {
-        const float w = pw[L - 1 - j];
+        const float w = REVERSE ? a.scale * pw[j + 1] : pw[L - 1 - j];
         const float4 vv = ld4(Vs + j * VP + 4 * tx);
         const float4 wv = make_float4(w * vv.x, w * vv.y, w * vv.z, w * vv.w);
 #pragma unroll
@@ -282,7 +289,7 @@ __global__ void __launch_bounds__(NT, 2) simt_fwd_kernel(ChunkArgs a) {
     }
     __syncthreads();
   }
-  if (a.hT) {
+  if (!REVERSE && a.hT) {
     for (int e = tid; e < DK * FWD_TILE; e += NT) {
       const int r = e / FWD_TILE, c = e % FWD_TILE;
       a.hT[sbase + (long long)r * DV + col0 + c] = Ss[r * VP + c];
@@ -291,277 +298,207 @@ __global__ void __launch_bounds__(NT, 2) simt_fwd_kernel(ChunkArgs a) {
 }
 
 // ------------------------------------------------------------------------------------------
-// Backward, dq: forward-in-time scan.  Tile = 32 rows of d_k (3 tiles); needs all of d_v.
+// Backward, dq (forward in time) and dk with dh0 (reverse in time): one scan template over a tile
+// of 32 rows of d_k, carrying the matching 32 rows of a d_k x d_v state, with scores over all of
+// d_v.  With X the score's row operand, Y its column operand and Z the tile's operand:
+//   dq:  X = dO, Y = v, Z = k;   P[i][j] = scale lambda^(i-j) X_i . Y_j (j <= i);
+//        out_i = sum_j P[i][j] Z_j + scale lambda^(i+1) S X_i;  S <- lambda^L S + sum_j lambda^(L-1-j) Z_j Y_j^T
+//   dk:  X = v, Y = dO, Z = q;   P[i][j] = scale lambda^(j-i) X_i . Y_j (j >= i);
+//        out_i = sum_j P[i][j] Z_j + lambda^(L-1-i) R X_i;      R <- lambda^L R + scale sum_j lambda^(j+1) Z_j Y_j^T
+// (S, R: the tile's 32 rows; R starts from dhT and leaves as dh0.)  The chunk's products run on
+// register tiles as in the forward: thread (ty, tx) owns P rows ty + 16a, columns tx + 16b;
+// output rows ty + 16a, tile columns tx and tx + 16; state rows ty and ty + 16, columns
+// 4tx + 64m.
 // ------------------------------------------------------------------------------------------
 constexpr int BQ_TILE = 32;
 constexpr int BQ_TILES = DK / BQ_TILE;
-constexpr int PQ = BQ_TILE + 1;
-constexpr size_t BQ_SMEM = sizeof(float) * (2 * SC * PV + SC * PQ + BQ_TILE * PV + SC * PT + SC + 1);
+constexpr int XP = DV + 4;        // row pitch of X and Y (192 values) and of the state rows
+constexpr int ZP = BQ_TILE + 4;   // row pitch of the Z tile
+constexpr int PP = SC + 4;        // row pitch of P
+constexpr size_t BQ_SMEM = sizeof(float) * (2 * SC * XP + SC * ZP + BQ_TILE * XP + SC * PP + SC + 8);
 
-template <class T>
-__global__ void __launch_bounds__(NT) simt_bwd_dq_kernel(ChunkArgs a) {
-  extern __shared__ float sm[];
-  float* Vs = sm;                 // [SC][PV]
-  float* Gs = Vs + SC * PV;       // [SC][PV]   dO
-  float* Ks = Gs + SC * PV;       // [SC][PQ]   k, d_k tile
-  float* Ss = Ks + SC * PQ;       // [BQ_TILE][PV]  forward state rows of the tile
-  float* Ps = Ss + BQ_TILE * PV;  // [SC][PT]
-  float* pw = Ps + SC * PT;
-  const int tid = threadIdx.x;
+// A chunk's rows [t0, t0 + L) of columns [col0, col0 + NCOLS) of a [T, H, width] input into shared
+// memory rows of pitch `pitch`: fp32 inputs with 16-byte loads, all issued before the first store;
+// rows past the end as zeros.
+template <int NCOLS, class T>
+__device__ __forceinline__ void load_rows4(float* dst, int pitch, const T* src, long long t0, int L, int H, int h,
+                                           int width, int col0) {
+  if constexpr (std::is_same<T, float>::value) {
+    constexpr int PER = SC * NCOLS / 4 / NT;  // float4 per thread
+    static_assert(PER * NT * 4 == SC * NCOLS, "whole float4 per thread");
+    float4 r[PER];
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      const int e = threadIdx.x + NT * m, i = e / (NCOLS / 4), c = e % (NCOLS / 4);
+      const long long row = (t0 + (i < L ? i : 0)) * H + h;
+      r[m] = i < L ? ld4(src + row * width + col0 + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int m = 0; m < PER; ++m) {
+      const int e = threadIdx.x + NT * m, i = e / (NCOLS / 4), c = e % (NCOLS / 4);
+      st4(dst + i * pitch + 4 * c, r[m]);
+    }
+  } else {
+    load_rows(dst, pitch, src, t0, L, H, h, width, col0, NCOLS);
+  }
+}
+template <class T, bool REVERSE>
+__global__ void __launch_bounds__(NT, 1) simt_bwd_narrow_kernel(ChunkArgs a) {
+  extern __shared__ __align__(16) float sm[];
+  float* Xs = sm;                  // [SC][XP]
+  float* Ys = Xs + SC * XP;        // [SC][XP]
+  float* Zs = Ys + SC * XP;        // [SC][ZP]   the d_k tile of Z
+  float* Ss = Zs + SC * ZP;        // [BQ_TILE][XP]  the carried state's tile rows
+  float* Ps = Ss + BQ_TILE * XP;   // [SC][PP]
+  float* pw = Ps + SC * PP;        // [SC + 1]
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   int n, h, tile;
   unit_of_block(a, BQ_TILES, n, h, tile);
   long long tb, te;
   seq_range(a, n, tb, te);
   if (!unit_in_bounds(a, n, h)) return;  // (debug-bounds build; uniform over the CTA)
   const int row0 = tile * BQ_TILE;
-  const T* k = (const T*)a.k;
-  const T* v = (const T*)a.v;
-  const T* dO = (const T*)a.dO;
-  T* dq = (T*)a.o;
+  const T* X = (const T*)(REVERSE ? a.v : a.dO);
+  const T* Y = (const T*)(REVERSE ? a.dO : a.v);
+  const T* Z = (const T*)(REVERSE ? a.q : a.k);
+  T* out = (T*)(REVERSE ? a.dk : a.o);
+  const float* s0 = REVERSE ? a.dhT : a.h0;
   const long long sbase = ((long long)n * a.H + h) * DK * DV;
 
   fill_powers(pw, a.log_lambda[h]);
   for (int e = tid; e < BQ_TILE * DV; e += NT) {
     const int r = e / DV, c = e % DV;
-    Ss[r * PV + c] = a.h0 ? a.h0[sbase + (long long)(row0 + r) * DV + c] : 0.f;
-  }
-  __syncthreads();
-  for (long long t0 = tb; t0 < te; t0 += SC) {
-    const int L = (int)(te - t0 < SC ? te - t0 : SC);
-    if (!rows_in_bounds(a, t0, L)) break;  // (debug-bounds build; uniform over the CTA)
-    load_rows(Vs, PV, v, t0, L, a.H, h, DV, 0, DV);
-    load_rows(Gs, PV, dO, t0, L, a.H, h, DV, 0, DV);
-    load_rows(Ks, PQ, k, t0, L, a.H, h, DK, row0, BQ_TILE);
-    __syncthreads();
-    {  // P[i][j] = scale lambda^(i-j) dO_i.v_j, j <= i
-      const int i = tid / 4;
-      for (int m = 0; m < SC / 4; ++m) {
-        const int j = (tid % 4) + 4 * m;
-        float acc = 0.f;
-        if (j <= i) {
-#pragma unroll 8
-          for (int c = 0; c < DV; ++c) acc = fmaf(Gs[i * PV + c], Vs[j * PV + c], acc);
-          acc *= a.scale * pw[i - j];
-        }
-        Ps[i * PT + j] = acc;
-      }
-    }
-    __syncthreads();
-    {  // dq_i = sum_j P[i][j] k_j + scale lambda^(i+1) S dO_i     (8 outputs per thread)
-      const int i = tid / 4, cb = tid % 4;
-      float intra[8], inter[8];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) intra[m] = inter[m] = 0.f;
-      for (int j = 0; j <= i; ++j) {
-        const float p = Ps[i * PT + j];
-#pragma unroll
-        for (int m = 0; m < 8; ++m) intra[m] = fmaf(p, Ks[j * PQ + cb + 4 * m], intra[m]);
-      }
-      for (int c = 0; c < DV; ++c) {
-        const float g = Gs[i * PV + c];
-#pragma unroll
-        for (int m = 0; m < 8; ++m) inter[m] = fmaf(g, Ss[(cb + 4 * m) * PV + c], inter[m]);
-      }
-      if (i < L) {
-        const float f = a.scale * pw[i + 1];
-        T* row = dq + ((t0 + i) * a.H + h) * (long long)DK + row0;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) row[cb + 4 * m] = from_f<T>(fmaf(f, inter[m], intra[m]));
-      }
-    }
-    __syncthreads();
-    for (int e = tid; e < BQ_TILE * DV; e += NT) {
-      const int r = e / DV, c = e % DV;
-      float acc = pw[L] * Ss[r * PV + c];
-      for (int j = 0; j < L; ++j) acc = fmaf(pw[L - 1 - j] * Ks[j * PQ + r], Vs[j * PV + c], acc);
-      Ss[r * PV + c] = acc;
-    }
-    __syncthreads();
-  }
-}
-
-// ------------------------------------------------------------------------------------------
-// Backward, dk and dh0: reverse-in-time scan.  Tile = 32 rows of d_k; carry R[rows, all d_v].
-// ------------------------------------------------------------------------------------------
-template <class T>
-__global__ void __launch_bounds__(NT) simt_bwd_dk_kernel(ChunkArgs a) {
-  extern __shared__ float sm[];
-  float* Vs = sm;                 // [SC][PV]
-  float* Gs = Vs + SC * PV;       // [SC][PV]   dO
-  float* Qs = Gs + SC * PV;       // [SC][PQ]   q, d_k tile
-  float* Rs = Qs + SC * PQ;       // [BQ_TILE][PV]
-  float* Bs = Rs + BQ_TILE * PV;  // [SC][PT]   B[i][j] = scale lambda^(j-i) dO_j.v_i, j >= i
-  float* pw = Bs + SC * PT;
-  const int tid = threadIdx.x;
-  int n, h, tile;
-  unit_of_block(a, BQ_TILES, n, h, tile);
-  long long tb, te;
-  seq_range(a, n, tb, te);
-  if (!unit_in_bounds(a, n, h)) return;  // (debug-bounds build; uniform over the CTA)
-  const int row0 = tile * BQ_TILE;
-  const T* q = (const T*)a.q;
-  const T* v = (const T*)a.v;
-  const T* dO = (const T*)a.dO;
-  T* dk = (T*)a.dk;
-  const long long sbase = ((long long)n * a.H + h) * DK * DV;
-
-  fill_powers(pw, a.log_lambda[h]);
-  for (int e = tid; e < BQ_TILE * DV; e += NT) {
-    const int r = e / DV, c = e % DV;
-    Rs[r * PV + c] = a.dhT ? a.dhT[sbase + (long long)(row0 + r) * DV + c] : 0.f;
+    Ss[r * XP + c] = s0 ? s0[sbase + (long long)(row0 + r) * DV + c] : 0.f;
   }
   __syncthreads();
   const long long nchunks = (te - tb + SC - 1) / SC;
-  for (long long m0 = nchunks - 1; m0 >= 0; --m0) {
-    const long long t0 = tb + m0 * SC;
+  for (long long m0 = 0; m0 < nchunks; ++m0) {
+    const long long t0 = tb + (REVERSE ? nchunks - 1 - m0 : m0) * SC;
     const int L = (int)(te - t0 < SC ? te - t0 : SC);
     if (!rows_in_bounds(a, t0, L)) break;  // (debug-bounds build; uniform over the CTA)
-    load_rows(Vs, PV, v, t0, L, a.H, h, DV, 0, DV);
-    load_rows(Gs, PV, dO, t0, L, a.H, h, DV, 0, DV);
-    load_rows(Qs, PQ, q, t0, L, a.H, h, DK, row0, BQ_TILE);
+    load_rows4<DV>(Xs, XP, X, t0, L, a.H, h, DV, 0);
+    load_rows4<DV>(Ys, XP, Y, t0, L, a.H, h, DV, 0);
+    load_rows4<BQ_TILE>(Zs, ZP, Z, t0, L, a.H, h, DK, row0);
     __syncthreads();
-    {
-      const int i = tid / 4;
-      for (int m = 0; m < SC / 4; ++m) {
-        const int j = (tid % 4) + 4 * m;
-        float acc = 0.f;
-        if (j >= i) {
-#pragma unroll 8
-          for (int c = 0; c < DV; ++c) acc = fmaf(Gs[j * PV + c], Vs[i * PV + c], acc);
-          acc *= a.scale * pw[j - i];
+    if (m0 + 1 < nchunks) {  // the next chunk's rows into L2 during this chunk's arithmetic
+      const long long tn = REVERSE ? t0 - SC : t0 + SC;
+      const int Ln = (int)(te - tn < SC ? te - tn : SC);
+      prefetch_chunk(X, tn, Ln, a.H, h, DV, (int)sizeof(T), 0, DV);
+      prefetch_chunk(Y, tn, Ln, a.H, h, DV, (int)sizeof(T), 0, DV);
+      prefetch_chunk(Z, tn, Ln, a.H, h, DK, (int)sizeof(T), row0, BQ_TILE);
+    }
+    {  // P[i][j] = scale lambda^|i-j| X_i . Y_j on the causal side (j <= i, or j >= i reversed)
+      float acc[4][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+#pragma unroll 2
+      for (int kk = 0; kk < DV; kk += 4) {
+        float4 xv[4], yv[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) xv[r] = ld4(Xs + (ty + 16 * r) * XP + kk);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) yv[c] = ld4(Ys + (tx + 16 * c) * XP + kk);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            acc[r][c] = fmaf(xv[r].x, yv[c].x, acc[r][c]);
+            acc[r][c] = fmaf(xv[r].y, yv[c].y, acc[r][c]);
+            acc[r][c] = fmaf(xv[r].z, yv[c].z, acc[r][c]);
+            acc[r][c] = fmaf(xv[r].w, yv[c].w, acc[r][c]);
+          }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int i = ty + 16 * r, j = tx + 16 * c;
+          const bool on = REVERSE ? j >= i : j <= i;
+          Ps[i * PP + j] = on ? acc[r][c] * (a.scale * pw[REVERSE ? j - i : i - j]) : 0.f;
         }
-        Bs[i * PT + j] = acc;
+    }
+    __syncthreads();
+    {  // out_i = sum_j P[i][j] Z_j + g_i (state rows) . X_i for the tile's columns tx, tx + 16
+      float oi[4][2], oe[4][2];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) oi[r][0] = oi[r][1] = oe[r][0] = oe[r][1] = 0.f;
+      for (int j = 0; j < L; ++j) {
+        const float z0 = Zs[j * ZP + tx], z1 = Zs[j * ZP + tx + 16];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float p = Ps[(ty + 16 * r) * PP + j];
+          oi[r][0] = fmaf(p, z0, oi[r][0]);
+          oi[r][1] = fmaf(p, z1, oi[r][1]);
+        }
+      }
+#pragma unroll 2
+      for (int kk = 0; kk < DV; kk += 4) {
+        float4 xv[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) xv[r] = ld4(Xs + (ty + 16 * r) * XP + kk);
+        const float4 s0v = ld4(Ss + tx * XP + kk), s1v = ld4(Ss + (tx + 16) * XP + kk);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          oe[r][0] = fmaf(xv[r].x, s0v.x, fmaf(xv[r].y, s0v.y, fmaf(xv[r].z, s0v.z, fmaf(xv[r].w, s0v.w, oe[r][0]))));
+          oe[r][1] = fmaf(xv[r].x, s1v.x, fmaf(xv[r].y, s1v.y, fmaf(xv[r].z, s1v.z, fmaf(xv[r].w, s1v.w, oe[r][1]))));
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = ty + 16 * r;
+        if (i < L) {
+          const float f = REVERSE ? pw[L - 1 - i] : a.scale * pw[i + 1];
+          T* row = out + ((t0 + i) * a.H + h) * (long long)DK + row0;
+          row[tx] = from_f<T>(fmaf(f, oe[r][0], oi[r][0]));
+          row[tx + 16] = from_f<T>(fmaf(f, oe[r][1], oi[r][1]));
+        }
       }
     }
     __syncthreads();
-    {  // dk_i = sum_{j>=i} B[i][j] q_j + lambda^(L-1-i) R v_i
-      const int i = tid / 4, cb = tid % 4;
-      if (i < L) {
-        float intra[8], inter[8];
+    {  // state rows ty, ty + 16: lambda^L S + sum_j w_j Z_j[row] Y_j
+      float acc[2][3][4];
+      const float lamL = pw[L];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) intra[m] = inter[m] = 0.f;
-        for (int j = i; j < SC; ++j) {
-          const float b = Bs[i * PT + j];
+      for (int r = 0; r < 2; ++r)
 #pragma unroll
-          for (int m = 0; m < 8; ++m) intra[m] = fmaf(b, Qs[j * PQ + cb + 4 * m], intra[m]);
+        for (int m = 0; m < 3; ++m) {
+          const float4 sv = ld4(Ss + (ty + 16 * r) * XP + 4 * tx + 64 * m);
+          acc[r][m][0] = lamL * sv.x;
+          acc[r][m][1] = lamL * sv.y;
+          acc[r][m][2] = lamL * sv.z;
+          acc[r][m][3] = lamL * sv.w;
         }
-        for (int c = 0; c < DV; ++c) {
-          const float vc = Vs[i * PV + c];
+      for (int j = 0; j < L; ++j) {
+        const float w = REVERSE ? a.scale * pw[j + 1] : pw[L - 1 - j];
+        const float z0 = w * Zs[j * ZP + ty], z1 = w * Zs[j * ZP + ty + 16];
 #pragma unroll
-          for (int m = 0; m < 8; ++m) inter[m] = fmaf(vc, Rs[(cb + 4 * m) * PV + c], inter[m]);
+        for (int m = 0; m < 3; ++m) {
+          const float4 yv = ld4(Ys + j * XP + 4 * tx + 64 * m);
+          acc[0][m][0] = fmaf(z0, yv.x, acc[0][m][0]);
+          acc[0][m][1] = fmaf(z0, yv.y, acc[0][m][1]);
+          acc[0][m][2] = fmaf(z0, yv.z, acc[0][m][2]);
+          acc[0][m][3] = fmaf(z0, yv.w, acc[0][m][3]);
+          acc[1][m][0] = fmaf(z1, yv.x, acc[1][m][0]);
+          acc[1][m][1] = fmaf(z1, yv.y, acc[1][m][1]);
+          acc[1][m][2] = fmaf(z1, yv.z, acc[1][m][2]);
+          acc[1][m][3] = fmaf(z1, yv.w, acc[1][m][3]);
         }
-        const float f = pw[L - 1 - i];
-        T* row = dk + ((t0 + i) * a.H + h) * (long long)DK + row0;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) row[cb + 4 * m] = from_f<T>(fmaf(f, inter[m], intra[m]));
       }
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int m = 0; m < 3; ++m)
+          st4(Ss + (ty + 16 * r) * XP + 4 * tx + 64 * m, make_float4(acc[r][m][0], acc[r][m][1], acc[r][m][2], acc[r][m][3]));
     }
     __syncthreads();
-    // R <- lambda^L R + scale sum_j lambda^(j+1) q_j dO_j^T
+  }
+  if (REVERSE && a.hT) {  // dh0
     for (int e = tid; e < BQ_TILE * DV; e += NT) {
       const int r = e / DV, c = e % DV;
-      float acc = pw[L] * Rs[r * PV + c];
-      for (int j = 0; j < L; ++j) acc = fmaf(a.scale * pw[j + 1] * Qs[j * PQ + r], Gs[j * PV + c], acc);
-      Rs[r * PV + c] = acc;
+      a.hT[sbase + (long long)(row0 + r) * DV + c] = Ss[r * XP + c];
     }
-    __syncthreads();
-  }
-  if (a.hT) {  // dh0
-    for (int e = tid; e < BQ_TILE * DV; e += NT) {
-      const int r = e / DV, c = e % DV;
-      a.hT[sbase + (long long)(row0 + r) * DV + c] = Rs[r * PV + c];
-    }
-  }
-}
-
-// ------------------------------------------------------------------------------------------
-// Backward, dv: reverse-in-time scan.  Tile = 64 columns of d_v; carry R[all d_k, columns].
-// ------------------------------------------------------------------------------------------
-constexpr int BV_TILE = 64;
-constexpr int BV_TILES = DV / BV_TILE;
-constexpr size_t BV_SMEM = sizeof(float) * (2 * SC * PK + SC * PT + DK * PT + SC * PT + SC + 1);
-
-template <class T>
-__global__ void __launch_bounds__(NT) simt_bwd_dv_kernel(ChunkArgs a) {
-  extern __shared__ float sm[];
-  float* Qs = sm;                 // [SC][PK]
-  float* Ks = Qs + SC * PK;       // [SC][PK]
-  float* Gs = Ks + SC * PK;       // [SC][PT]  dO column tile
-  float* Rs = Gs + SC * PT;       // [DK][PT]
-  float* Bs = Rs + DK * PT;       // [SC][PT]  B[i][j] = scale lambda^(j-i) q_j.k_i, j >= i
-  float* pw = Bs + SC * PT;
-  const int tid = threadIdx.x;
-  int n, h, tile;
-  unit_of_block(a, BV_TILES, n, h, tile);
-  long long tb, te;
-  seq_range(a, n, tb, te);
-  if (!unit_in_bounds(a, n, h)) return;  // (debug-bounds build; uniform over the CTA)
-  const int col0 = tile * BV_TILE;
-  const T* q = (const T*)a.q;
-  const T* k = (const T*)a.k;
-  const T* dO = (const T*)a.dO;
-  T* dv = (T*)a.dv;
-  const long long sbase = ((long long)n * a.H + h) * DK * DV;
-
-  fill_powers(pw, a.log_lambda[h]);
-  for (int e = tid; e < DK * BV_TILE; e += NT) {
-    const int r = e / BV_TILE, c = e % BV_TILE;
-    Rs[r * PT + c] = a.dhT ? a.dhT[sbase + (long long)r * DV + col0 + c] : 0.f;
-  }
-  __syncthreads();
-  const long long nchunks = (te - tb + SC - 1) / SC;
-  for (long long m0 = nchunks - 1; m0 >= 0; --m0) {
-    const long long t0 = tb + m0 * SC;
-    const int L = (int)(te - t0 < SC ? te - t0 : SC);
-    if (!rows_in_bounds(a, t0, L)) break;  // (debug-bounds build; uniform over the CTA)
-    load_rows(Qs, PK, q, t0, L, a.H, h, DK, 0, DK);
-    load_rows(Ks, PK, k, t0, L, a.H, h, DK, 0, DK);
-    load_rows(Gs, PT, dO, t0, L, a.H, h, DV, col0, BV_TILE);
-    __syncthreads();
-    {
-      const int i = tid / 4;
-      for (int m = 0; m < SC / 4; ++m) {
-        const int j = (tid % 4) + 4 * m;
-        float acc = 0.f;
-        if (j >= i) {
-#pragma unroll 8
-          for (int c = 0; c < DK; ++c) acc = fmaf(Qs[j * PK + c], Ks[i * PK + c], acc);
-          acc *= a.scale * pw[j - i];
-        }
-        Bs[i * PT + j] = acc;
-      }
-    }
-    __syncthreads();
-    {  // dv_i = sum_{j>=i} B[i][j] dO_j + lambda^(L-1-i) R^T k_i
-      const int i = tid / 4, cb = tid % 4;
-      if (i < L) {
-        float intra[16], inter[16];
-#pragma unroll
-        for (int m = 0; m < 16; ++m) intra[m] = inter[m] = 0.f;
-        for (int j = i; j < SC; ++j) {
-          const float b = Bs[i * PT + j];
-#pragma unroll
-          for (int m = 0; m < 16; ++m) intra[m] = fmaf(b, Gs[j * PT + cb + 4 * m], intra[m]);
-        }
-        for (int c = 0; c < DK; ++c) {
-          const float kc = Ks[i * PK + c];
-#pragma unroll
-          for (int m = 0; m < 16; ++m) inter[m] = fmaf(kc, Rs[c * PT + cb + 4 * m], inter[m]);
-        }
-        const float f = pw[L - 1 - i];
-        T* row = dv + ((t0 + i) * a.H + h) * (long long)DV + col0;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) row[cb + 4 * m] = from_f<T>(fmaf(f, inter[m], intra[m]));
-      }
-    }
-    __syncthreads();
-    for (int e = tid; e < DK * BV_TILE; e += NT) {
-      const int r = e / BV_TILE, c = e % BV_TILE;
-      float acc = pw[L] * Rs[r * PT + c];
-      for (int j = 0; j < L; ++j) acc = fmaf(a.scale * pw[j + 1] * Qs[j * PK + r], Gs[j * PT + c], acc);
-      Rs[r * PT + c] = acc;
-    }
-    __syncthreads();
   }
 }
 
@@ -578,19 +515,19 @@ cudaError_t launch(K kernel, int tiles, size_t smem, const ChunkArgs& a, cudaStr
 }  // namespace
 
 cudaError_t launch_simt_fwd(const ChunkArgs& a, cudaStream_t stream) {
-  return launch(simt_fwd_kernel<float>, FWD_TILES, FWD_SMEM, a, stream);
+  return launch(simt_wide_kernel<float, false>, FWD_TILES, FWD_SMEM, a, stream);
 }
 
 cudaError_t launch_simt_bwd(int dtype_f32, const ChunkArgs& a, cudaStream_t stream) {
   cudaError_t e;
   if (dtype_f32) {
-    e = launch(simt_bwd_dq_kernel<float>, BQ_TILES, BQ_SMEM, a, stream);
-    if (e == cudaSuccess) e = launch(simt_bwd_dk_kernel<float>, BQ_TILES, BQ_SMEM, a, stream);
-    if (e == cudaSuccess) e = launch(simt_bwd_dv_kernel<float>, BV_TILES, BV_SMEM, a, stream);
+    e = launch(simt_bwd_narrow_kernel<float, false>, BQ_TILES, BQ_SMEM, a, stream);
+    if (e == cudaSuccess) e = launch(simt_bwd_narrow_kernel<float, true>, BQ_TILES, BQ_SMEM, a, stream);
+    if (e == cudaSuccess) e = launch(simt_wide_kernel<float, true>, FWD_TILES, FWD_SMEM, a, stream);
   } else {
-    e = launch(simt_bwd_dq_kernel<__nv_bfloat16>, BQ_TILES, BQ_SMEM, a, stream);
-    if (e == cudaSuccess) e = launch(simt_bwd_dk_kernel<__nv_bfloat16>, BQ_TILES, BQ_SMEM, a, stream);
-    if (e == cudaSuccess) e = launch(simt_bwd_dv_kernel<__nv_bfloat16>, BV_TILES, BV_SMEM, a, stream);
+    e = launch(simt_bwd_narrow_kernel<__nv_bfloat16, false>, BQ_TILES, BQ_SMEM, a, stream);
+    if (e == cudaSuccess) e = launch(simt_bwd_narrow_kernel<__nv_bfloat16, true>, BQ_TILES, BQ_SMEM, a, stream);
+    if (e == cudaSuccess) e = launch(simt_wide_kernel<__nv_bfloat16, true>, FWD_TILES, FWD_SMEM, a, stream);
   }
   return e;
 }
