@@ -518,17 +518,12 @@ cudaError_t launch_simt_fwd(const ChunkArgs& a, cudaStream_t stream) {
   return launch(simt_wide_kernel<float, false>, FWD_TILES, FWD_SMEM, a, stream);
 }
 
+// The fp32 mode's backward (bf16 inputs go through the tensor-core scans).
 cudaError_t launch_simt_bwd(int dtype_f32, const ChunkArgs& a, cudaStream_t stream) {
-  cudaError_t e;
-  if (dtype_f32) {
-    e = launch(simt_bwd_narrow_kernel<float, false>, BQ_TILES, BQ_SMEM, a, stream);
-    if (e == cudaSuccess) e = launch(simt_bwd_narrow_kernel<float, true>, BQ_TILES, BQ_SMEM, a, stream);
-    if (e == cudaSuccess) e = launch(simt_wide_kernel<float, true>, FWD_TILES, FWD_SMEM, a, stream);
-  } else {
-    e = launch(simt_bwd_narrow_kernel<__nv_bfloat16, false>, BQ_TILES, BQ_SMEM, a, stream);
-    if (e == cudaSuccess) e = launch(simt_bwd_narrow_kernel<__nv_bfloat16, true>, BQ_TILES, BQ_SMEM, a, stream);
-    if (e == cudaSuccess) e = launch(simt_wide_kernel<__nv_bfloat16, true>, FWD_TILES, FWD_SMEM, a, stream);
-  }
+  if (!dtype_f32) return cudaErrorInvalidValue;
+  cudaError_t e = launch(simt_bwd_narrow_kernel<float, false>, BQ_TILES, BQ_SMEM, a, stream);
+  if (e == cudaSuccess) e = launch(simt_bwd_narrow_kernel<float, true>, BQ_TILES, BQ_SMEM, a, stream);
+  if (e == cudaSuccess) e = launch(simt_wide_kernel<float, true>, FWD_TILES, FWD_SMEM, a, stream);
   return e;
 }
 
