@@ -54,6 +54,14 @@ PROFILED_TRAFFIC = {
     # the MXFP8 pool: 972.095744 MB read + 892.485120 MB written
     "decode_mxfp8_state": ("linear_attention_recurrence_simple_gb300/csrc/gla_mxfp8.cu", "158873036f51e740",
                            1864580864.0 / 49152, "per state per step"),
+    # the all-fp32 mode's forward: 404.469504 MB read + 183.305728 MB written (part of o is still
+    # in L2 when the kernel ends), one launch
+    "fwd_fp32": ("linear_attention_recurrence_simple_gb300/csrc/gla_simt.cu", "f1b9f51523b1e5ae",
+                 587775232.0, "per launch of the B=8 T=2048 H=16 fp32 forward"),
+    # the all-fp32 mode's backward, its three launches per call: dq 509.635328 + 91.569152 MB,
+    # dk 519.081984 + 97.524480 MB, dv 414.296064 + 177.118720 MB (read + written)
+    "bwd_fp32": ("linear_attention_recurrence_simple_gb300/csrc/gla_simt.cu", "f1b9f51523b1e5ae",
+                 1809225728.0, "per call (three launches) of the B=8 T=2048 H=16 fp32 backward"),
 }
 
 
@@ -338,6 +346,7 @@ def bench_fwd_fp32(torch, gla, wl, dist, args, peaks):
            "value": tokens * dist.world / (region / 1e3), "unit": "tokens/s",
            "roofline": roofline(byts, fwd_flops(tokens), region / 1e3, peaks, bound="alu"), "kernel_ms": per_call,
            "launches_per_step": 1}
+    res["roofline"]["traffic"] = profiled_traffic("fwd_fp32")
     del g, q, k, v, o, hT
     return res
 
@@ -481,6 +490,7 @@ def bench_bwd_fp32(torch, gla, wl, dist, args, peaks):
     res = {"workload": w.name.replace("bf16", "fp32") + " (all-fp32 mode)", "tokens": tokens, "ms_per_step": region,
            "value": tokens * dist.world / (region / 1e3), "unit": "tokens/s",
            "roofline": roofline(byts, flops, region / 1e3, peaks, bound="alu"), "launches_per_step": 3}
+    res["roofline"]["traffic"] = profiled_traffic("bwd_fp32")
     del g, q, k, v, dO
     return res
 
@@ -698,7 +708,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--rows", default="fwd,bwd,varlen,decode,fwd_aug,norm_gate,decode_aug,decode_bf16_state,"
-                    "fwd_split,decode_norm_gate,decode_mxfp8_state,fwd_fp32")
+                    "fwd_split,decode_norm_gate,decode_mxfp8_state,fwd_fp32,bwd_fp32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-seqs", type=int, default=1280,
                     help="sequences in the decode pool (1280 = the measured workload)")
