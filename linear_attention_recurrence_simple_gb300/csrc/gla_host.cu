@@ -121,14 +121,17 @@ int gla_chunk_fwd_host(const void* q, const void* k, const void* v, const float*
     const bool last = t1 == T;
     // copy in: rows (n, t) of sequences a..b-1 at tokens t0..t1-1 (contiguous for one sequence,
     // or for whole sequences)
+    // (no rows at all when T = 0: then q, k, v and o may be NULL and nothing is copied)
     const size_t row0 = ((size_t)a * T + t0) * H, nrows = (size_t)(b - a) * len * H;
-    ok = cudaMemcpyAsync(ws + l.q + row0 * GLA_DK * el, (const char*)q + row0 * GLA_DK * el, nrows * GLA_DK * el,
-                         cudaMemcpyDefault, pp.in) == cudaSuccess &&
-         cudaMemcpyAsync(ws + l.k + row0 * GLA_DK * el, (const char*)k + row0 * GLA_DK * el, nrows * GLA_DK * el,
-                         cudaMemcpyDefault, pp.in) == cudaSuccess &&
-         cudaMemcpyAsync(ws + l.v + row0 * GLA_DV * el, (const char*)v + row0 * GLA_DV * el, nrows * GLA_DV * el,
-                         cudaMemcpyDefault, pp.in) == cudaSuccess &&
-         cudaEventRecord(ev[1 + 2 * p], pp.in) == cudaSuccess && cudaStreamWaitEvent(comp, ev[1 + 2 * p], 0) == cudaSuccess;
+    if (nrows > 0)
+      ok = cudaMemcpyAsync(ws + l.q + row0 * GLA_DK * el, (const char*)q + row0 * GLA_DK * el, nrows * GLA_DK * el,
+                           cudaMemcpyDefault, pp.in) == cudaSuccess &&
+           cudaMemcpyAsync(ws + l.k + row0 * GLA_DK * el, (const char*)k + row0 * GLA_DK * el, nrows * GLA_DK * el,
+                           cudaMemcpyDefault, pp.in) == cudaSuccess &&
+           cudaMemcpyAsync(ws + l.v + row0 * GLA_DV * el, (const char*)v + row0 * GLA_DV * el, nrows * GLA_DV * el,
+                           cudaMemcpyDefault, pp.in) == cudaSuccess;
+    ok = ok && cudaEventRecord(ev[1 + 2 * p], pp.in) == cudaSuccess &&
+         cudaStreamWaitEvent(comp, ev[1 + 2 * p], 0) == cudaSuccess;
     if (!ok) break;
     // compute: the piece as a fixed-length batch of b - a sequences of len tokens
     const float* p_h0 = j > 0 ? d_mid[(j - 1) & 1] + (size_t)a * (st_bytes / 4) : (h0 ? d_h0 + (size_t)a * (st_bytes / 4) : nullptr);
@@ -145,9 +148,10 @@ int gla_chunk_fwd_host(const void* q, const void* k, const void* v, const float*
     }
     if (rc != GLA_OK) break;
     // copy out: the piece's o rows, and the final states once a sequence is done
-    ok = cudaEventRecord(ev[2 + 2 * p], comp) == cudaSuccess && cudaStreamWaitEvent(pp.out, ev[2 + 2 * p], 0) == cudaSuccess &&
-         cudaMemcpyAsync((char*)o + row0 * GLA_DV * el, ws + l.o + row0 * GLA_DV * el, nrows * GLA_DV * el,
-                         cudaMemcpyDefault, pp.out) == cudaSuccess;
+    ok = cudaEventRecord(ev[2 + 2 * p], comp) == cudaSuccess && cudaStreamWaitEvent(pp.out, ev[2 + 2 * p], 0) == cudaSuccess;
+    if (ok && nrows > 0)
+      ok = cudaMemcpyAsync((char*)o + row0 * GLA_DV * el, ws + l.o + row0 * GLA_DV * el, nrows * GLA_DV * el,
+                           cudaMemcpyDefault, pp.out) == cudaSuccess;
     if (ok && last && hT)
       ok = cudaMemcpyAsync(hT + (size_t)a * (st_bytes / 4), p_hT, (size_t)(b - a) * st_bytes, cudaMemcpyDefault,
                            pp.out) == cudaSuccess;

@@ -92,3 +92,13 @@ def test_back_to_back_calls_reuse_the_pipeline():
         o_ref, hT_ref = _device_call(x[0], x[1], x[2], x[3], x[4])
         assert torch.equal(o, o_ref) and torch.equal(hT, hT_ref)
     assert np.isfinite(ra[0].float().numpy()).all()
+
+
+def test_zero_length_passes_h0_through():
+    """T = 0: no rows to copy (the empty host tensors may have no storage at all); each final
+    state is its initial state."""
+    q, k, v, h0, ll = _inputs(37, 3, 0, 2, True)
+    o, hT = gla.gla_chunk_fwd_host(q, k, v, ll, float(gs.SCALE), h0=h0, pieces=4)
+    torch.cuda.synchronize()
+    assert o.shape == (3, 0, 2, 192)
+    assert torch.equal(hT, h0)
