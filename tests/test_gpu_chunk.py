@@ -204,6 +204,23 @@ def test_fwd_layer_workload_sampled():
     _sampled_units(w, [(0, 0), (7, 15), (3, 5), (5, 10), (1, 1), (6, 14)], o, hT, BF16_TOL)
 
 
+def test_fwd_layer_workload_sampled_fp32_mode():
+    """The all-fp32 mode at the benchmark's shapes (its fwd_fp32 launch: the layer workload's values
+    in fp32), 4 sampled units at the fp32 bar."""
+    w = wl.layer()
+    g = w.device_inputs()
+    q, k, v = (g[x].float() for x in ("q", "k", "v"))
+    o, hT = gla.gla_chunk_fwd(q, k, v, g["log_lambda"], w.scale)
+    torch.cuda.synchronize()
+    for n, h in [(0, 0), (7, 15), (2, 9), (5, 4)]:
+        u = w.host_unit(n, h)
+        o_ref, hT_ref = oracle.fwd(u["q"], u["k"], u["v"], u["log_lambda"], w.scale, h0=u["h0"])
+        og = o[n, :, h].cpu().numpy()
+        assert np.all(np.isfinite(og))
+        assert rel_err(og, o_ref[:, 0]) <= F32_TOL, (n, h)
+        assert rel_err(hT[n, h].cpu().numpy(), hT_ref[0, 0]) <= F32_TOL, (n, h)
+
+
 def test_fwd_varlen_workload_sampled():
     """32 packed sequences, lengths U[128, 16384], h0 ~ N(0, 0.1): longest, shortest, others."""
     w = wl.varlen()
@@ -276,6 +293,24 @@ def test_bwd_layer_workload_sampled():
             assert np.all(np.isfinite(xs))
             assert rel_err(xs, r[:, 0], bf16_out=True) <= BF16_TOL, (n, h)
         assert rel_err(dh0[n, h].cpu().numpy(), ref[3][0, 0]) <= BF16_TOL, (n, h)
+
+
+def test_bwd_layer_workload_sampled_fp32_mode():
+    """The all-fp32 mode's backward at the benchmark's shapes (its bwd_fp32 launch), sampled units
+    at the fp32 bar."""
+    w = wl.layer(with_grad=True)
+    g = w.device_inputs()
+    q, k, v, dO = (g[x].float() for x in ("q", "k", "v", "dO"))
+    dq, dk, dv, dh0 = gla.gla_chunk_bwd(q, k, v, g["log_lambda"], dO, w.scale, dhT=g["dhT"])
+    torch.cuda.synchronize()
+    for n, h in [(0, 0), (7, 15), (3, 6)]:
+        u = w.host_unit(n, h)
+        ref = oracle.bwd(u["q"], u["k"], u["v"], u["log_lambda"], w.scale, u["dO"], dhT=u["dhT"])
+        for name, x, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref[:3]):
+            xs = x[n, :, h].cpu().numpy()
+            assert np.all(np.isfinite(xs))
+            assert rel_err(xs, r[:, 0]) <= F32_TOL, (name, n, h)
+        assert rel_err(dh0[n, h].cpu().numpy(), ref[3][0, 0]) <= F32_TOL, (n, h)
 
 
 @pytest.mark.parametrize("bf16", [True, False])
