@@ -42,8 +42,11 @@
  *   - Empty work is valid: n_seq = 0, T = 0 or sequences of length 0 launch nothing for them;
  *     a length-0 sequence gives hT = h0 (zeros if h0 is NULL) and dh0 = dhT.
  *   - The library looks up the device addresses of its own device variables (the error word,
- *     the hand-over flags, the array of gla_chunk_fwd_noalloc) once per device and keeps them, so
- *     resetting a device (cudaDeviceReset) after the library's first call on it is not supported.
+ *     the hand-over flags, the array of gla_chunk_fwd_noalloc) once per device and keeps them,
+ *     and creates a few CUDA objects per device that live until the process exits (the
+ *     backward's two side streams; the host-buffer forward's two copy streams and its events),
+ *     so resetting a device (cudaDeviceReset) after the library's first call on it is not
+ *     supported.
  */
 #ifndef GLA_H_
 #define GLA_H_
