@@ -42,6 +42,12 @@ MUTANTS = [
      "const double inter = scale * std::pow(lam, i);", 0),
     ("chunked: state decay uses L-j", "acc += std::pow(lam, L - 1 - j) * K(j, a) * V(j, b);",
      "acc += std::pow(lam, L - j) * K(j, a) * V(j, b);", 0),
+    ("chunked: intra-chunk mask lets a row see the next token", "for (int j = 0; j <= i; ++j) {",
+     "for (int j = 0; j <= i + 1 && j < L; ++j) {", 0),
+    ("chunked: intra-chunk mask drops the diagonal", "for (int j = 0; j <= i; ++j) {",
+     "for (int j = 0; j < i; ++j) {", 0),
+    ("chunked: state not decayed across the chunk", "double acc = lamL * S[(size_t)a * dv + b];",
+     "double acc = S[(size_t)a * dv + b];", 0),
     ("decode: decay dropped",
      "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];",
      "S[(size_t)a * dv + b] = S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];", 1),
@@ -87,6 +93,17 @@ MUTANTS = [
      "mx = std::fabs((double)x[0]);", 0),
     ("mxfp8 step: decay dropped", "S[(size_t)a * dv + b] = lam * s_ab + (double)kt[a] * (double)vt[b];",
      "S[(size_t)a * dv + b] = s_ab + (double)kt[a] * (double)vt[b];", 0),
+    ("bwd: dv contracts with q instead of k",
+     "for (int a = 0; a < dk; ++a) acc += G[(size_t)a * dv + b] * (double)kt[a];",
+     "for (int a = 0; a < dk; ++a) acc += G[(size_t)a * dv + b] * (double)qt[a];", 0),
+    ("bwd: dq read off the state before its token's write",
+     "for (int b = 0; b < dv; ++b) acc += S[(size_t)a * dv + b] * (double)gt[b];",
+     "for (int b = 0; b < dv; ++b) acc += (S[(size_t)a * dv + b] - (double)kt[a] * (double)vt[b]) * (double)gt[b];", 0),
+    ("bwd: adjoint seed without the scale",
+     "G[(size_t)a * dv + b] = R[(size_t)a * dv + b] + scale * (double)qt[a] * (double)gt[b];",
+     "G[(size_t)a * dv + b] = R[(size_t)a * dv + b] + (double)qt[a] * (double)gt[b];", 0),
+    ("bwd: carry decayed twice", "for (size_t e = 0; e < DS; ++e) R[e] = lam * G[e];",
+     "for (size_t e = 0; e < DS; ++e) R[e] = lam * lam * G[e];", 0),
     ("bwd: forward state missing its decay",
      "S[(size_t)a * dv + b] = lam * S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];",
      "S[(size_t)a * dv + b] = S[(size_t)a * dv + b] + (double)kt[a] * (double)vt[b];", 2),
