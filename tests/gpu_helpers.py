@@ -49,6 +49,17 @@ def rel_err(x, ref, bf16_out=False):
     return RelErr(float(np.max(d) / rms), raw)
 
 
+def within_one_bf16_rounding(x, y):
+    """True when two bf16 results of the same fp32 sum, added up in different orders, differ
+    element by element by at most one bf16 ulp of the larger (2^-7 of its magnitude: adjacent
+    bf16 values), plus 1e-5 of the RMS for values near zero, where a reordered fp32 sum can
+    change sign."""
+    x = np.asarray(x, np.float64)
+    y = np.asarray(y, np.float64)
+    rms = float(np.sqrt(np.mean(y ** 2))) if y.size else 0.0
+    return bool(np.all(np.abs(x - y) <= np.exp2(-7) * np.maximum(np.abs(x), np.abs(y)) + 1e-5 * rms))
+
+
 def host_chunk_inputs(seed, lengths, H, bf16, with_h0, packed, log_lambda=None, grad=False,
                       qk_sigma=1 / np.sqrt(96), v_sigma=1.0):
     """Numpy inputs in oracle layout ([T_total, H, d], cu_seqlens) plus the GPU layout shape."""

@@ -12,7 +12,8 @@ import glasynth as gs
 import linear_attention_recurrence_simple_gb300 as gla
 import oracle
 from glasynth import workloads as wl
-from tests.gpu_helpers import BF16_TOL, F32_TOL, flat, host_chunk_inputs, rel_err, to_device
+from tests.gpu_helpers import (BF16_TOL, F32_TOL, flat, host_chunk_inputs, rel_err, to_device,
+                               within_one_bf16_rounding)
 
 pytestmark = pytest.mark.gpu
 
@@ -325,3 +326,35 @@ def test_bwd_pages_decay_schedule(bf16):
     res = gla.gla_chunk_bwd(g["q"], g["k"], g["v"], g["log_lambda"], g["dO"], d["scale"], h0=g["h0"],
                             dhT=g["dhT"], cu_seqlens=g["cu_seqlens"])
     _check_bwd(d, res, True, BF16_TOL if bf16 else F32_TOL)
+
+
+def test_run_to_run_reproducibility():
+    """The forward (balanced persistent launch with hand-overs, and packed varlen), dv and dh0 of
+    the backward, and the decode step give the same bits on every run; dq and dk (fp32 partial sums
+    added in arrival order) differ by at most one bf16 rounding, element by element."""
+    d = host_chunk_inputs(901, [300] * 12, 16, True, with_h0=True, packed=False, grad=True)
+    g = to_device(d, True, packed=False)
+    s = float(gs.SCALE)
+    runs = [gla.gla_chunk_fwd(g["q"], g["k"], g["v"], g["log_lambda"], s, h0=g["h0"]) for _ in range(3)]
+    for o, hT in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(hT, runs[0][1])
+    dv_ = host_chunk_inputs(902, [5, 0, 200, 1, 128, 129, 77], 3, True, with_h0=True, packed=True)
+    gv = to_device(dv_, True, packed=True)
+    runs = [gla.gla_chunk_fwd(gv["q"], gv["k"], gv["v"], gv["log_lambda"], s, h0=gv["h0"],
+                              cu_seqlens=gv["cu_seqlens"]) for _ in range(3)]
+    for o, hT in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(hT, runs[0][1])
+    grads = [gla.gla_chunk_bwd(g["q"], g["k"], g["v"], g["log_lambda"], g["dO"], s, h0=g["h0"], dhT=g["dhT"])
+             for _ in range(3)]
+    for r in grads[1:]:
+        assert torch.equal(r[2], grads[0][2]) and torch.equal(r[3], grads[0][3])
+        for x, y in zip(r[:2], grads[0][:2]):
+            assert within_one_bf16_rounding(x.float().cpu().numpy(), y.float().cpu().numpy())
+    pool0 = torch.from_numpy(gs.normal(903, 7, (5, 16, 96, 192), 0.1)).cuda()
+    q1, k1 = (torch.from_numpy(gs.normal(903, i, (5, 16, 96), 0.1)).cuda().to(torch.bfloat16) for i in (1, 2))
+    v1 = torch.from_numpy(gs.normal(903, 3, (5, 16, 192))).cuda().to(torch.bfloat16)
+    outs = []
+    for _ in range(2):
+        pool = pool0.clone()
+        outs.append((gla.gla_decode_step(q1, k1, v1, g["log_lambda"], pool, s), pool))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
